@@ -1,0 +1,409 @@
+// ds41_attn.cu - step 3 of the forward: sparse attention of every head over
+// the gathered window + compressed rows, with a per-head sink logit.
+//
+// metrale_model_arch/deepseek_v41_ref/compress.rs, attention_any: sparse_attn
+// (q, kv_rows, sink, idx, m, nh, hd, topk, scale) with scale = head_dim^-0.5;
+// metrale_model_arch/attn_v41/forward.rs passes rows_a, rows_b and the merged
+// idx to attend_and_project.  One row per position is both key and value.
+//
+//   o[t,h] = sum_v e^{s_v} row_v / (e^{sink_h} + sum_v e^{s_v}),
+//   s_v = scale * <q[t,h], row_v>
+//
+// One CTA handles one query token, 64 heads, and a contiguous range of its
+// index row (a split).  Eight warps: warp w owns heads 16*(w%4).. and half
+// w/4 of the head dim.  Per chunk of 32 gathered rows the two warps of a head
+// group each form the partial scores of their half, exchange them through
+// shared memory, and both run the same online softmax on the full scores;
+// each then accumulates P*V for its half of the output columns.  Rows are
+// gathered with cp.async (double-buffered); tensor-core MMAs are bf16 with f32
+// accumulation.  With several splits the unnormalised (m, l, O) of each split
+// goes to the workspace and a merge kernel adds the sink once.
+#include "ds41_common.cuh"
+
+namespace ds41 {
+
+constexpr int ATT_NC = 32;       // gathered rows per chunk
+constexpr int ATT_HEADS = 64;    // heads per CTA
+constexpr int ATT_THREADS = 256;
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int HD>
+struct AttnSmem {
+    static constexpr int CPR = HD / 8;  // 16-byte chunks per row
+    static constexpr size_t q_bytes = (size_t)ATT_HEADS * HD * 2;
+    static constexpr size_t kv_bytes = (size_t)ATT_NC * HD * 2;
+    static constexpr size_t sx_bytes = (size_t)2 * ATT_HEADS * ATT_NC * 4;
+    static constexpr size_t total = q_bytes + 2 * kv_bytes + sx_bytes + 2 * ATT_NC * 4;
+};
+
+__device__ __forceinline__ int aswz(int row, int c) { return c ^ (row & 7); }
+
+template <int HD>
+__global__ void __launch_bounds__(ATT_THREADS, 1) sparse_attn_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ rows_a, int64_t n_a,
+    const uint16_t* __restrict__ rows_b, int64_t n_c, const int32_t* __restrict__ idx, int K,
+    const float* __restrict__ sink, float scale_log2, uint16_t* __restrict__ o,
+    float* __restrict__ lse, int nh, int chunks_per_split, float* __restrict__ part_o,
+    float2* __restrict__ part_ml, unsigned int* status) {
+    using SM = AttnSmem<HD>;
+    constexpr int CPR = SM::CPR;
+    constexpr int HALF = HD / 2;
+    constexpr int NT = HALF / 8;  // output n-tiles per warp
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint16_t* qs = reinterpret_cast<uint16_t*>(smem);
+    uint16_t* kvs = reinterpret_cast<uint16_t*>(smem + SM::q_bytes);
+    float* sx = reinterpret_cast<float*>(smem + SM::q_bytes + 2 * SM::kv_bytes);
+    int* vflag = reinterpret_cast<int*>(smem + SM::q_bytes + 2 * SM::kv_bytes + SM::sx_bytes);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = warp & 3, half = warp >> 2;
+    const int64_t t = blockIdx.x;
+    const int split = blockIdx.y;
+    const int splits = gridDim.y;
+    const int h0 = blockIdx.z * ATT_HEADS;
+    const int64_t n_rows = n_a + n_c;
+
+    const int nchunks_total = (K + ATT_NC - 1) / ATT_NC;
+    const int c_begin = split * chunks_per_split;
+    int c_end = c_begin + chunks_per_split;
+    if (c_end > nchunks_total) c_end = nchunks_total;
+    const int32_t* irow = idx + t * (int64_t)K;
+
+    // Q of 64 heads (rows beyond nh are zero).
+    for (int id = tid; id < ATT_HEADS * CPR; id += ATT_THREADS) {
+        const int r = id / CPR, c = id % CPR;
+        const int h = h0 + r;
+        const bool live = h < nh;
+        const uint16_t* src = q + ((t * nh + (live ? h : 0)) * (int64_t)HD) + c * 8;
+        cp_async16(smem_u32(qs + r * HD + aswz(r, c) * 8), src, live);
+    }
+    auto load_chunk = [&](int chunk, int buf) {
+        uint16_t* dst = kvs + buf * (ATT_NC * HD);
+        for (int id = tid; id < ATT_NC * CPR; id += ATT_THREADS) {
+            const int r = id / CPR, c = id % CPR;
+            const int j = chunk * ATT_NC + r;
+            int64_t v = -1;
+            if (j < K) v = irow[j];
+            bool ok = v >= 0 && v < n_rows;
+            if (c == 0) {
+                if (j < K && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
+                vflag[buf * ATT_NC + r] = ok ? 1 : 0;
+            }
+            const uint16_t* src = rows_a;
+            if (ok) src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
+            cp_async16(smem_u32(dst + r * HD + aswz(r, c) * 8), src + c * 8, ok);
+        }
+    };
+
+    float oacc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; j++) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.0f;
+    float mrow[2] = {-INFINITY, -INFINITY};  // running max (log2 units) of rows lane/4, +8
+    float lrow[2] = {0.0f, 0.0f};            // this thread's partial denominators
+
+    if (c_begin < c_end) load_chunk(c_begin, 0);
+    cp_async_commit();
+
+    for (int chunk = c_begin; chunk < c_end; chunk++) {
+        const int buf = (chunk - c_begin) & 1;
+        if (chunk + 1 < c_end) load_chunk(chunk + 1, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const uint16_t* kv = kvs + buf * (ATT_NC * HD);
+
+        // partial scores of this half: [16 heads] x [32 rows]
+        float sacc[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
+#pragma unroll 4
+        for (int kk = 0; kk < HALF / 16; kk++) {
+            uint32_t a0, a1, a2, a3;
+            {
+                const int r = g * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int c = half * (HALF / 8) + kk * 2 + (lane >> 4);
+                ldsm_x4(smem_u32(qs + r * HD + aswz(r, c) * 8), a0, a1, a2, a3);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; jj++) {
+                uint32_t b0, b1, b2, b3;
+                const int r = jj * 16 + (lane & 7) + (lane >> 4) * 8;
+                const int c = half * (HALF / 8) + kk * 2 + ((lane >> 3) & 1);
+                ldsm_x4(smem_u32(kv + r * HD + aswz(r, c) * 8), b0, b1, b2, b3);
+                mma_bf16(sacc[2 * jj], a0, a1, a2, a3, b0, b1);
+                mma_bf16(sacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        // exchange halves
+        float* mine = sx + half * (ATT_HEADS * ATT_NC);
+        const float* other = sx + (half ^ 1) * (ATT_HEADS * ATT_NC);
+        const int ra = g * 16 + (lane >> 2), rb = ra + 8;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int col = j * 8 + 2 * (lane & 3);
+            *reinterpret_cast<float2*>(mine + ra * ATT_NC + col) = make_float2(sacc[j][0], sacc[j][1]);
+            *reinterpret_cast<float2*>(mine + rb * ATT_NC + col) = make_float2(sacc[j][2], sacc[j][3]);
+        }
+        asm volatile("bar.sync %0, 64;\n" ::"r"(1 + g));
+        float sv[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int col = j * 8 + 2 * (lane & 3);
+            const float2 xa = *reinterpret_cast<const float2*>(other + ra * ATT_NC + col);
+            const float2 xb = *reinterpret_cast<const float2*>(other + rb * ATT_NC + col);
+            // the same sum, in the same order, in both warps of the pair
+            const float s0 = half ? xa.x + sacc[j][0] : sacc[j][0] + xa.x;
+            const float s1 = half ? xa.y + sacc[j][1] : sacc[j][1] + xa.y;
+            const float s2 = half ? xb.x + sacc[j][2] : sacc[j][2] + xb.x;
+            const float s3 = half ? xb.y + sacc[j][3] : sacc[j][3] + xb.y;
+            const bool v0 = vflag[buf * ATT_NC + col] != 0;
+            const bool v1 = vflag[buf * ATT_NC + col + 1] != 0;
+            sv[j][0] = v0 ? s0 * scale_log2 : -INFINITY;
+            sv[j][1] = v1 ? s1 * scale_log2 : -INFINITY;
+            sv[j][2] = v0 ? s2 * scale_log2 : -INFINITY;
+            sv[j][3] = v1 ? s3 * scale_log2 : -INFINITY;
+        }
+        // online softmax on rows ra (sv[.][0..1]) and rb (sv[.][2..3])
+        float mx[2] = {mrow[0], mrow[1]};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            mx[0] = fmaxf(mx[0], fmaxf(sv[j][0], sv[j][1]));
+            mx[1] = fmaxf(mx[1], fmaxf(sv[j][2], sv[j][3]));
+        }
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+        }
+        float corr[2], muse[2];
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            muse[i] = (mx[i] == -INFINITY) ? 0.0f : mx[i];
+            corr[i] = exp2f(mrow[i] - muse[i]);
+            mrow[i] = mx[i];
+            lrow[i] *= corr[i];
+        }
+        uint32_t pa[2][4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float p0 = exp2f(sv[j][0] - muse[0]), p1 = exp2f(sv[j][1] - muse[0]);
+            const float p2 = exp2f(sv[j][2] - muse[1]), p3 = exp2f(sv[j][3] - muse[1]);
+            lrow[0] += p0 + p1;
+            lrow[1] += p2 + p3;
+            // C fragment of n-tile j -> A fragment of k-step j/2
+            pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
+            pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; j++) {
+            oacc[j][0] *= corr[0];
+            oacc[j][1] *= corr[0];
+            oacc[j][2] *= corr[1];
+            oacc[j][3] *= corr[1];
+        }
+        // O += P * V over this half's columns
+#pragma unroll
+        for (int ks = 0; ks < 2; ks++) {
+            // A fragment order: a0 (row ra, k 0-7), a1 (row rb, k 0-7),
+            // a2 (row ra, k 8-15), a3 (row rb, k 8-15)
+            const uint32_t a0 = pa[ks][0], a1 = pa[ks][1], a2 = pa[ks][2], a3 = pa[ks][3];
+#pragma unroll
+            for (int jj = 0; jj < NT / 2; jj++) {
+                uint32_t b0, b1, b2, b3;
+                const int r = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int c = half * (HALF / 8) + jj * 2 + (lane >> 4);
+                ldsm_x4_t(smem_u32(kv + r * HD + aswz(r, c) * 8), b0, b1, b2, b3);
+                mma_bf16(oacc[2 * jj], a0, a1, a2, a3, b0, b1);
+                mma_bf16(oacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        __syncthreads();  // buffer and exchange area are reused next chunk
+    }
+    cp_async_wait<0>();
+
+    // reduce the per-thread denominators over the quad
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        lrow[i] += __shfl_xor_sync(0xffffffffu, lrow[i], 1);
+        lrow[i] += __shfl_xor_sync(0xffffffffu, lrow[i], 2);
+    }
+    const int rows[2] = {g * 16 + (lane >> 2), g * 16 + (lane >> 2) + 8};
+    if (splits == 1) {
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int h = h0 + rows[i];
+            if (h >= nh) continue;
+            const float sk = sink[h] * LOG2E;
+            const float mfin = fmaxf(mrow[i], sk);
+            const float mref = (mfin == -INFINITY) ? 0.0f : mfin;
+            const float a = exp2f(mrow[i] - mref);
+            const float L = lrow[i] * a + exp2f(sk - mref);
+            const float inv = (L > 0.0f) ? a / L : 0.0f;
+            uint16_t* orow = o + (t * nh + h) * (int64_t)HD + half * HALF;
+#pragma unroll
+            for (int j = 0; j < NT; j++) {
+                const int col = j * 8 + 2 * (lane & 3);
+                const float x0 = oacc[j][2 * i] * inv, x1 = oacc[j][2 * i + 1] * inv;
+                *reinterpret_cast<uint32_t*>(orow + col) = pack_bf16x2(x0, x1);
+            }
+            if (lse && half == 0 && (lane & 3) == 0) lse[t * nh + h] = (mref + log2f(L)) / LOG2E;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int h = h0 + rows[i];
+            if (h >= nh) continue;
+            const int64_t pidx = (t * splits + split) * (int64_t)nh + h;
+            float* prow = part_o + pidx * HD + half * HALF;
+#pragma unroll
+            for (int j = 0; j < NT; j++) {
+                const int col = j * 8 + 2 * (lane & 3);
+                *reinterpret_cast<float2*>(prow + col) = make_float2(oacc[j][2 * i], oacc[j][2 * i + 1]);
+            }
+            if (half == 0 && (lane & 3) == 0) part_ml[pidx] = make_float2(mrow[i], lrow[i]);
+        }
+    }
+}
+
+// Merge the splits of one (token, head): M = max(sink, m_s),
+// L = e^{sink - M} + sum_s l_s e^{m_s - M}, o = sum_s O_s e^{m_s - M} / L.
+template <int HD>
+__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ part_o,
+                                                         const float2* __restrict__ part_ml,
+                                                         const float* __restrict__ sink,
+                                                         uint16_t* __restrict__ o,
+                                                         float* __restrict__ lse, int nh,
+                                                         int splits) {
+    const int64_t t = blockIdx.x;
+    const int h = blockIdx.y;
+    const float sk = sink[h] * LOG2E;
+    float M = sk;
+    for (int s = 0; s < splits; s++) M = fmaxf(M, part_ml[(t * splits + s) * nh + h].x);
+    const float Mref = (M == -INFINITY) ? 0.0f : M;
+    float L = exp2f(sk - Mref);
+    for (int s = 0; s < splits; s++) {
+        const float2 ml = part_ml[(t * splits + s) * nh + h];
+        L += ml.y * exp2f(ml.x - Mref);
+    }
+    const float invL = (L > 0.0f) ? 1.0f / L : 0.0f;
+    for (int d = threadIdx.x * 2; d < HD; d += blockDim.x * 2) {
+        float a0 = 0.0f, a1 = 0.0f;
+        for (int s = 0; s < splits; s++) {
+            const int64_t pidx = (t * splits + s) * (int64_t)nh + h;
+            const float wgt = exp2f(part_ml[pidx].x - Mref);
+            const float2 v = *reinterpret_cast<const float2*>(part_o + pidx * HD + d);
+            a0 += v.x * wgt;
+            a1 += v.y * wgt;
+        }
+        *reinterpret_cast<uint32_t*>(o + (t * nh + h) * (int64_t)HD + d) =
+            pack_bf16x2(a0 * invL, a1 * invL);
+    }
+    if (lse && threadIdx.x == 0) lse[t * nh + h] = (Mref + log2f(L)) / LOG2E;
+}
+
+struct AttnPlan {
+    int splits, chunks_per_split, head_groups;
+    size_t part_o_bytes, part_ml_bytes;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static AttnPlan plan_attn(int64_t m, int64_t nh, int64_t hd, int64_t K, int sms) {
+    AttnPlan p;
+    p.head_groups = (int)((nh + ATT_HEADS - 1) / ATT_HEADS);
+    const int chunks = (int)((K + ATT_NC - 1) / ATT_NC);
+    const int64_t ctas = m * p.head_groups;
+    int splits = 1;
+    if (ctas < sms) {
+        splits = (int)((sms + ctas - 1) / ctas);
+        if (splits > chunks) splits = chunks;
+    }
+    p.chunks_per_split = (chunks + splits - 1) / splits;
+    p.splits = (chunks + p.chunks_per_split - 1) / p.chunks_per_split;
+    if (p.splits > 1) {
+        p.part_o_bytes = align256((size_t)m * p.splits * nh * hd * 4);
+        p.part_ml_bytes = align256((size_t)m * p.splits * nh * 8);
+    } else {
+        p.part_o_bytes = p.part_ml_bytes = 0;
+    }
+    return p;
+}
+
+static int device_sms() {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+template <int HD>
+static int launch_attn(const AttnPlan& p, const uint16_t* q, const uint16_t* rows_a, int64_t n_a,
+                       const uint16_t* rows_b, int64_t n_c, const int32_t* idx, int64_t K,
+                       const float* sink, float scale, uint16_t* o, float* lse, int64_t m,
+                       int64_t nh, uint8_t* ws, unsigned int* status, cudaStream_t st) {
+    const size_t smem = AttnSmem<HD>::total;
+    auto kern = sparse_attn_kernel<HD>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    float* part_o = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+    float2* part_ml = p.splits > 1 ? reinterpret_cast<float2*>(ws + p.part_o_bytes) : nullptr;
+    dim3 grid((unsigned)m, (unsigned)p.splits, (unsigned)p.head_groups);
+    kern<<<grid, ATT_THREADS, smem, st>>>(q, rows_a, n_a, rows_b, n_c, idx, (int)K, sink,
+                                          scale * LOG2E, o, lse, (int)nh, p.chunks_per_split,
+                                          part_o, part_ml, status);
+    int rc = launch_check("ds41_sparse_attn_sink_fwd: attention kernel");
+    if (rc || p.splits == 1) return rc;
+    attn_merge_kernel<HD><<<dim3((unsigned)m, (unsigned)nh), 128, 0, st>>>(
+        part_o, part_ml, sink, o, lse, (int)nh, p.splits);
+    return launch_check("ds41_sparse_attn_sink_fwd: merge kernel");
+}
+
+}  // namespace ds41
+
+using namespace ds41;
+
+extern "C" size_t ds41_sparse_attn_workspace_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K) {
+    if (m < 1 || nh < 1 || hd < 1 || K < 1) return 0;
+    AttnPlan p = plan_attn(m, nh, hd, K, device_sms());
+    return p.part_o_bytes + p.part_ml_bytes;
+}
+
+extern "C" int ds41_sparse_attn_sink_fwd(const ds41_bf16* q, const ds41_bf16* rows_a,
+                                         int64_t n_a, const ds41_bf16* rows_b, int64_t n_c,
+                                         const int32_t* idx, int64_t K, const float* sink,
+                                         float scale, ds41_bf16* o, float* lse, int64_t m,
+                                         int64_t nh, int64_t hd, void* ws, size_t ws_bytes,
+                                         ds41_stream_t stream) {
+    const char* name = "ds41_sparse_attn_sink_fwd";
+    DS41_REQUIRE(m >= 1 && m < (int64_t(1) << 31), DS41_E_RANGE, "%s: m=%lld", name,
+                 (long long)m);
+    DS41_REQUIRE(nh >= 1 && nh <= 65535 * ATT_HEADS, DS41_E_ARG, "%s: nh=%lld", name,
+                 (long long)nh);
+    DS41_REQUIRE(hd == 64 || hd == 128 || hd == 256 || hd == 512, DS41_E_ARG,
+                 "%s: hd=%lld must be 64, 128, 256 or 512", name, (long long)hd);
+    DS41_REQUIRE(K >= 1 && K < (int64_t(1) << 30), DS41_E_ARG, "%s: K=%lld", name, (long long)K);
+    DS41_REQUIRE(n_a >= 0 && n_c >= 0 && n_a + n_c >= 1, DS41_E_ARG, "%s: n_a=%lld n_c=%lld",
+                 name, (long long)n_a, (long long)n_c);
+    DS41_REQUIRE(q && idx && sink && o && (n_a == 0 || rows_a) && (n_c == 0 || rows_b),
+                 DS41_E_ARG, "%s: null tensor pointer", name);
+    DS41_REQUIRE(aligned16(q) && aligned16(o) && (n_a == 0 || aligned16(rows_a)) &&
+                     (n_c == 0 || aligned16(rows_b)),
+                 DS41_E_ARG, "%s: q/o/rows must be 16-byte aligned", name);
+    unsigned int* status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    AttnPlan p = plan_attn(m, nh, hd, K, device_sms());
+    const size_t need = p.part_o_bytes + p.part_ml_bytes;
+    DS41_REQUIRE(need == 0 || (ws && ws_bytes >= need), DS41_E_WORKSPACE,
+                 "%s: workspace of %zu bytes needed, %zu given", name, need, ws ? ws_bytes : 0);
+    DS41_REQUIRE(need == 0 || aligned16(ws), DS41_E_ARG, "%s: ws must be 16-byte aligned", name);
+    const uint16_t* ra = n_a ? rows_a : rows_b;
+    const uint16_t* rb = n_c ? rows_b : rows_a;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    switch (hd) {
+        case 64: return launch_attn<64>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, wsb, status, st);
+        case 128: return launch_attn<128>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, wsb, status, st);
+        case 256: return launch_attn<256>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, wsb, status, st);
+        default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, wsb, status, st);
+    }
+}

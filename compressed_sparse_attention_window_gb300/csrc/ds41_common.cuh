@@ -1,0 +1,159 @@
+// ds41_common.cuh - shared device helpers and host-side error handling of
+// libds41 (the CUDA path).  Nothing here is shared with the CPU oracle.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ds41.h"
+
+namespace ds41 {
+
+// ---------------------------------------------------------------------------
+// Host-side error handling (ds41_common.cu)
+// ---------------------------------------------------------------------------
+int fail(int code, const char* fmt, ...);
+int cuda_check(cudaError_t e, const char* what);
+int launch_check(const char* what);
+// Device address of the status word of the current device (set-up per device).
+int status_word(unsigned int** out);
+bool aligned16(const void* p);
+
+#define DS41_REQUIRE(cond, code, ...)              \
+    do {                                           \
+        if (!(cond)) return ::ds41::fail((code), __VA_ARGS__); \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// bf16 bit helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ uint16_t f2bf(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));  // round to nearest even
+}
+
+// ---------------------------------------------------------------------------
+// fp4 (e2m1) rounding, e8m0 and e4m3 scales
+// ---------------------------------------------------------------------------
+// Grid index 0..7 of {0,.5,1,1.5,2,3,4,6} nearest |t| (|t| <= 6 after the
+// clamp).  A value on a midpoint goes to the neighbour with the even index, so
+// each interval is closed on its even-index end.
+__device__ __forceinline__ int e2m1_idx(float t) {
+    const float a = fabsf(t);
+    int i = 7;
+    i = (a <= 5.0f) ? 6 : i;
+    i = (a < 3.5f) ? 5 : i;
+    i = (a <= 2.5f) ? 4 : i;
+    i = (a < 1.75f) ? 3 : i;
+    i = (a <= 1.25f) ? 2 : i;
+    i = (a < 0.75f) ? 1 : i;
+    i = (a <= 0.25f) ? 0 : i;
+    return i;
+}
+
+// Magnitude of grid index i, as a float (exact): 0 and 0.5 below index 2,
+// then (1 or 1.5) * 2^(i/2 - 1).
+__device__ __forceinline__ float e2m1_mag(int i) {
+    if (i < 2) return 0.5f * (float)i;
+    const float m = (i & 1) ? 1.5f : 1.0f;
+    return m * __uint_as_float((uint32_t)((i >> 1) + 126) << 23);
+}
+
+// 4-bit code: sign in bit 3 (taken from t, so a negative value that rounds to
+// zero keeps its sign), index in bits 0..2.
+__device__ __forceinline__ uint32_t e2m1_code(float t) {
+    return ((__float_as_uint(t) >> 28) & 8u) | (uint32_t)e2m1_idx(t);
+}
+
+// Value of a code (signed, -0 preserved).
+__device__ __forceinline__ float e2m1_val(uint32_t c) {
+    const float m = e2m1_mag((int)(c & 7u));
+    return (c & 8u) ? -m : m;
+}
+
+// Smallest power of two >= x, x a positive normal float.
+__device__ __forceinline__ float pow2_ceil_pos(float x) {
+    const uint32_t u = __float_as_uint(x);
+    if ((u & 0x007fffffu) == 0u) return x;
+    return __uint_as_float((u & 0x7f800000u) + 0x00800000u);
+}
+
+// f32 -> e4m3 (OCP "fn") with round-to-nearest-even and saturation at the
+// largest finite value (448), via the hardware conversion.  Returns the byte.
+__device__ __forceinline__ uint32_t f32_to_e4m3_sat(float x) {
+    uint16_t r;
+    // cvt packs two inputs: the first operand lands in the upper byte.
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+    return (uint32_t)(r & 0xffu);
+}
+
+// e4m3 byte -> f32 (exact), via the hardware conversion to f16.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+    uint32_t h2;
+    const uint16_t in = (uint16_t)(c & 0xffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    return __half2float(__ushort_as_half((uint16_t)(h2 & 0xffffu)));
+}
+
+// One element of the fp4 round trip with scale s: clamp(v/s) -> e2m1 -> * s.
+// Division and product are single IEEE operations (never contracted).
+__device__ __forceinline__ float fp4_elem(float v, float s, uint32_t* code) {
+    float t = __fdiv_rn(v, s);
+    t = fminf(fmaxf(t, -6.0f), 6.0f);
+    const uint32_t c = e2m1_code(t);
+    *code = c;
+    return __fmul_rn(e2m1_val(c), s);
+}
+
+// ---------------------------------------------------------------------------
+// Vector loads / stores and async copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    const int n = valid ? 16 : 0;  // 0 source bytes: the 16 bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level bf16 tensor-core helpers (m16n8k16, f32 accumulate)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const uint32_t l = f2bf(lo), h = f2bf(hi);
+    return l | (h << 16);
+}
+
+// Raise a DS41_E_* code in the device status word (first error wins).
+__device__ __forceinline__ void raise_status(unsigned int* status, unsigned int code) {
+    if (status) atomicCAS(status, 0u, code);
+}
+
+}  // namespace ds41

@@ -1,0 +1,255 @@
+"""Thin ctypes binding of ``libds41.so`` (declared in ``include/ds41.h``).
+
+Every function here only checks and marshals torch tensors (device, dtype,
+contiguity) into the C ABI and passes the current CUDA stream; all arithmetic
+runs in the library's CUDA kernels.  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libds41.so")
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+ERRORS = {1: "DS41_E_ARG", 2: "DS41_E_RANGE", 3: "DS41_E_CUDA", 4: "DS41_E_INDEX",
+          5: "DS41_E_WORKSPACE"}
+
+#: Exported symbols of include/ds41.h and their (restype, argtypes).
+SIGNATURES = {
+    "ds41_last_error": (ctypes.c_char_p, []),
+    "ds41_device_status": (ctypes.c_int, [_P, ctypes.c_int]),
+    "ds41_fp4_quant_e8m0": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _P]),
+    "ds41_fp4_quant_e4m3": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _P]),
+    "ds41_yarn_freqs_cis": (ctypes.c_int, [_P, _I64, _I64, _I64, _F, _F, _F, _F, _P]),
+    "ds41_rows_a_len": (_I64, [_I64, _I64, _I64]),
+    "ds41_window_ring_write": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "ds41_compress_latent_write": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64,
+                                                  _I64, _I64, _I64, _P]),
+    "ds41_indexer_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64, ctypes.c_int]),
+    "ds41_indexer_topk": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                         _I64, _I64, _I64, _P, _SZ, _P]),
+    "ds41_sparse_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
+    "ds41_sparse_attn_sink_fwd": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F, _P, _P,
+                                                 _I64, _I64, _I64, _P, _SZ, _P]),
+}
+
+
+class DS41Error(RuntimeError):
+    """A libds41 entry point returned an error code."""
+
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed with {ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def load(path: Optional[str] = None):
+    """Load libds41.so (built by ``build.py``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with "
+                           "`python -m compressed_sparse_attention_window_gb300.build`")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _call(name: str, *args) -> None:
+    lib = load()
+    rc = getattr(lib, name)(*args)
+    if rc != 0:
+        raise DS41Error(name, rc, lib.ds41_last_error().decode(errors="replace"))
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    return t.data_ptr()
+
+
+_BF = torch.bfloat16
+
+
+def device_status(reset: bool = True) -> int:
+    """The device status word (0 or a DS41_E_* code); synchronises."""
+    v = ctypes.c_int32(0)
+    _call("ds41_device_status", ctypes.addressof(v), 1 if reset else 0)
+    return int(v.value)
+
+
+def fp4_quant(x: torch.Tensor, e4m3: bool, want_codes: bool = False):
+    """ds41_fp4_quant_e8m0 (block 32) / ds41_fp4_quant_e4m3 (block 16) on the
+    rows of a 2-D bf16 tensor.  Returns y, or (y, codes, scales)."""
+    rows, cols = x.shape
+    block = 16 if e4m3 else 32
+    y = torch.empty_like(x)
+    codes = scales = None
+    if want_codes:
+        codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=x.device)
+        scales = torch.empty(rows, cols // block, dtype=torch.uint8, device=x.device)
+    fn = "ds41_fp4_quant_e4m3" if e4m3 else "ds41_fp4_quant_e8m0"
+    _call(fn, _ptr(x, _BF, "x"), _ptr(y, _BF, "y"), _ptr(codes), _ptr(scales), rows, cols, _stream())
+    return (y, codes, scales) if want_codes else y
+
+
+def yarn_freqs_cis(dim: int, seqlen: int, original_seq_len: int = 65536, base: float = 160000.0,
+                   factor: float = 16.0, beta_fast: float = 32.0, beta_slow: float = 1.0,
+                   device="cuda") -> torch.Tensor:
+    """ds41_yarn_freqs_cis: f32 [seqlen, dim/2, 2] of (cos, sin)."""
+    out = torch.empty(seqlen, dim // 2, 2, dtype=torch.float32, device=device)
+    _call("ds41_yarn_freqs_cis", _ptr(out, torch.float32, "out"), dim, seqlen, original_seq_len,
+          base, factor, beta_fast, beta_slow, _stream())
+    return out
+
+
+def rows_a_len(m: int, win: int, start_pos: int) -> int:
+    return int(load().ds41_rows_a_len(m, win, start_pos))
+
+
+def window_ring_write(kv: torch.Tensor, ring: torch.Tensor, win_idx: torch.Tensor, start_pos: int,
+                      rows_a: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """ds41_window_ring_write: updates ``ring`` in place, fills ``win_idx``
+    [m, win] and returns the rows the window indices point into (kv, the
+    ring, or ``rows_a`` [win + m, hd] for a chunk past position 0)."""
+    m, hd = kv.shape
+    win = ring.shape[0]
+    chunk = start_pos > 0 and m > 1
+    if chunk and rows_a is None:
+        rows_a = torch.empty(win + m, hd, dtype=kv.dtype, device=kv.device)
+    n_a = ctypes.c_int64(0)
+    _call("ds41_window_ring_write", _ptr(kv, _BF, "kv"), _ptr(ring, _BF, "ring"),
+          _ptr(rows_a if chunk else None), _ptr(win_idx, torch.int32, "win_idx"),
+          ctypes.addressof(n_a), m, hd, win, start_pos, _stream())
+    if start_pos == 0:
+        return kv
+    if m == 1:
+        return ring
+    return rows_a[: n_a.value]
+
+
+def compress_latent_write(latent: torch.Tensor, freqs_cis: torch.Tensor, cache: torch.Tensor,
+                          rd: int, ratio: int, start_pos: int, m: int,
+                          codes: Optional[torch.Tensor] = None,
+                          scales: Optional[torch.Tensor] = None) -> None:
+    """ds41_compress_latent_write: RoPE + bf16 + e4m3 fp4 round trip of the G
+    new groups into ``cache`` rows start_pos/ratio ...; optional packed codes
+    [rows, hd/2] and scale codes [rows, hd/16]."""
+    G, hd = latent.shape
+    _call("ds41_compress_latent_write", _ptr(latent, _BF, "latent"),
+          _ptr(freqs_cis, torch.float32, "freqs_cis"), freqs_cis.shape[0],
+          _ptr(cache, _BF, "cache"), cache.shape[0], _ptr(codes, torch.uint8, "codes"),
+          _ptr(scales, torch.uint8, "scales"), G, hd, rd, ratio, start_pos, m, _stream())
+
+
+def indexer_workspace_bytes(m, Hi, Di, n_c, scores_given) -> int:
+    return int(load().ds41_indexer_workspace_bytes(m, Hi, Di, n_c, 1 if scores_given else 0))
+
+
+def indexer_topk(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor,
+                 win_idx: torch.Tensor, ratio: int, start_pos: int, topk: int, offset: int,
+                 idx: Optional[torch.Tensor] = None, scores: Optional[torch.Tensor] = None,
+                 ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """ds41_indexer_topk: merged index rows [m, win + min(topk, n_c)] int32."""
+    m, Hi, Di = q_idx.shape
+    n_c = k_idx.shape[0]
+    win = win_idx.shape[1]
+    ctopk = min(topk, n_c)
+    if idx is None:
+        idx = torch.empty(m, win + ctopk, dtype=torch.int32, device=q_idx.device)
+    need = indexer_workspace_bytes(m, Hi, Di, n_c, scores is not None)
+    if need and (ws is None or ws.numel() < need):
+        ws = torch.empty(need, dtype=torch.uint8, device=q_idx.device)
+    _call("ds41_indexer_topk", _ptr(q_idx, _BF, "q_idx"), _ptr(k_idx, _BF, "k_idx"),
+          _ptr(w, torch.float32, "w"), _ptr(win_idx, torch.int32, "win_idx"),
+          _ptr(idx, torch.int32, "idx"), _ptr(scores, _BF, "scores"), m, Hi, Di, n_c, win, ratio,
+          start_pos, topk, offset, _ptr(ws) if need else None, need, _stream())
+    return idx
+
+
+def sparse_attn_workspace_bytes(m, nh, hd, K) -> int:
+    return int(load().ds41_sparse_attn_workspace_bytes(m, nh, hd, K))
+
+
+def sparse_attn_sink_fwd(q: torch.Tensor, rows_a: torch.Tensor, rows_b: Optional[torch.Tensor],
+                         idx: torch.Tensor, sink: torch.Tensor, scale: float,
+                         o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                         ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """ds41_sparse_attn_sink_fwd: o [m, nh, hd] bf16 (lse [m, nh] f32 if given)."""
+    m, nh, hd = q.shape
+    K = idx.shape[1]
+    n_a = rows_a.shape[0]
+    n_c = 0 if rows_b is None else rows_b.shape[0]
+    if o is None:
+        o = torch.empty_like(q)
+    need = sparse_attn_workspace_bytes(m, nh, hd, K)
+    if need and (ws is None or ws.numel() < need):
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _call("ds41_sparse_attn_sink_fwd", _ptr(q, _BF, "q"), _ptr(rows_a, _BF, "rows_a"), n_a,
+          _ptr(rows_b, _BF, "rows_b"), n_c, _ptr(idx, torch.int32, "idx"), K,
+          _ptr(sink, torch.float32, "sink"), float(scale), _ptr(o, _BF, "o"),
+          _ptr(lse, torch.float32, "lse"), m, nh, hd, _ptr(ws) if need else None, need, _stream())
+    return o
+
+
+def forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
+            out: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
+    """One layer's compressed sparse attention forward for a workload ``wl``
+    (see workloads.Workload) on device tensors ``inp`` (kv, ring, latent,
+    cache, q_idx, k_idx, w, q, sink): ring write + window indices, latent
+    write, indexer top-k + merge, sparse attention.  ``out`` may hold
+    preallocated win_idx / idx / o / rows_a / workspaces, reused across calls.
+    Returns the dict of outputs."""
+    out = {} if out is None else out
+    dev = inp["q"].device
+    m, win = wl.m, wl.win
+    if "win_idx" not in out:
+        out["win_idx"] = torch.empty(m, win, dtype=torch.int32, device=dev)
+    rows_a = window_ring_write(inp["kv"], inp["ring"], out["win_idx"], wl.start_pos,
+                               rows_a=out.get("rows_a"))
+    if wl.start_pos > 0 and m > 1:
+        out["rows_a"] = rows_a
+    if wl.G > 0:
+        compress_latent_write(inp["latent"], freqs_cis, inp["cache"], wl.rd, wl.ratio,
+                              wl.start_pos, m)
+    n_a = rows_a.shape[0]
+    if wl.n_c > 0:
+        idx = indexer_topk(inp["q_idx"], inp["k_idx"][: wl.n_c], inp["w"], out["win_idx"],
+                           wl.ratio, wl.start_pos, wl.topk, n_a, idx=out.get("idx"),
+                           ws=out.get("ws_idx"))
+        rows_b = inp["cache"][: wl.n_c]
+    else:
+        idx = out["win_idx"]
+        rows_b = None
+    out["idx"] = idx
+    out["o"] = sparse_attn_sink_fwd(inp["q"], rows_a, rows_b, idx, inp["sink"], wl.scale,
+                                    o=out.get("o"), lse=out.get("lse"), ws=out.get("ws_attn"))
+    return out

@@ -1,0 +1,211 @@
+/*
+ * ds41.h - C ABI of libds41: one layer's compressed sparse attention forward
+ * (DeepSeek-V4.1 style) for m tokens at start_pos, as hand-written CUDA for
+ * GB300 (sm_103a).
+ *
+ * The operations follow three pages of the metrale_model_arch crate:
+ *   forward.rs  = metrale_model_arch/attn_v41/forward.rs, AttnV41::forward
+ *   compress.rs = metrale_model_arch/deepseek_v41_ref/compress.rs, the CPU
+ *                 reference (attention_any and its helpers)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensor pointers are DEVICE pointers owned by the caller (for example
+ *   torch allocations).  Nothing here allocates device memory.  Entry points
+ *   that need scratch memory take (ws, ws_bytes); the matching
+ *   *_workspace_bytes function says how much.  Host pointers are marked
+ *   "host".
+ * - bf16 tensors are passed as uint16_t bit patterns (ds41_bf16).
+ * - Layouts are row-major and contiguous; every device pointer must be 16-byte
+ *   aligned.
+ * - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and runs asynchronously; no entry point synchronises the host.
+ * - Every entry point returns DS41_OK (0) or an error code.  On DS41_E_ARG and
+ *   DS41_E_RANGE nothing was enqueued.  ds41_last_error() gives the message of
+ *   the calling thread's last failure.
+ * - Kernels that read indices check them; an out-of-range index is skipped
+ *   (never dereferenced) and raises DS41_E_INDEX in the device status word,
+ *   read with ds41_device_status().
+ */
+#ifndef DS41_H_
+#define DS41_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t ds41_bf16;               /* bfloat16 bit pattern */
+typedef struct CUstream_st* ds41_stream_t; /* same type as cudaStream_t */
+
+enum {
+    DS41_OK = 0,
+    DS41_E_ARG = 1,       /* null / misaligned pointer, unsupported size */
+    DS41_E_RANGE = 2,     /* a limit of the forward: token count, position, top-k */
+    DS41_E_CUDA = 3,      /* a CUDA call or launch failed */
+    DS41_E_INDEX = 4,     /* a device-side index check tripped (device status) */
+    DS41_E_WORKSPACE = 5  /* ws is NULL or smaller than *_workspace_bytes */
+};
+
+/* Message of the calling thread's last error ("" if none).  The pointer stays
+ * valid until the thread's next failing call. */
+const char* ds41_last_error(void);
+
+/* Reads (and with reset != 0 clears) the device status word of the current
+ * device: 0, or the DS41_E_* code a kernel raised.  Synchronises the device. */
+int ds41_device_status(int32_t* status /* host */, int reset);
+
+/* ------------------------------------------------------------------------ */
+/* fp4 block quantisers                                                      */
+/* ------------------------------------------------------------------------ */
+/* compress.rs, fp4_quant_e8m0_inplace (the indexer's q and k): per block of
+ * 32 values along a row, amax (floored at 6*2^-126), scale s = the power of
+ * two at or above amax/6, each value v -> bf16(e2m1(clamp(v/s, -6, 6)) * s),
+ * where e2m1 rounds to the grid {0,.5,1,1.5,2,3,4,6} with ties to the even
+ * code.
+ *   x      [rows, cols] bf16 input;  y [rows, cols] bf16 output (may equal x)
+ *   codes  nullable [rows, cols/2] uint8: e2m1 codes, element 2j in the low
+ *          nibble of byte j; bit 3 of a code is the sign
+ *   scales nullable [rows, cols/32] uint8: the biased exponent of s (e8m0)
+ *   cols % 32 == 0.  rows * cols < 2^31. */
+int ds41_fp4_quant_e8m0(const ds41_bf16* x, ds41_bf16* y, uint8_t* codes, uint8_t* scales,
+                        int64_t rows, int64_t cols, ds41_stream_t stream);
+
+/* compress.rs, fp4_quant_e4m3_inplace (the compressed KV latent): per block
+ * of 16, amax floored at 6*2^-9, s = e4m3(amax/6) (round to nearest even,
+ * saturating at 448), then the same element path as above.
+ *   scales nullable [rows, cols/16] uint8: the e4m3 code of s.  cols % 16 == 0. */
+int ds41_fp4_quant_e4m3(const ds41_bf16* x, ds41_bf16* y, uint8_t* codes, uint8_t* scales,
+                        int64_t rows, int64_t cols, ds41_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* RoPE table                                                                 */
+/* ------------------------------------------------------------------------ */
+/* compress.rs, yarn_freqs_cis: out [seqlen, dim/2, 2] f32 of (cos, sin) of
+ * p * f_i, where f_i = base^(-2i/dim) blended towards f_i / factor by the YaRN
+ * ramp between floor(corr(beta_fast)) and ceil(corr(beta_slow)),
+ * corr(r) = dim * ln(original_seq_len / (2 pi r)) / (2 ln base).  Built once
+ * per model; the latent write reads it.  dim even, >= 2. */
+int ds41_yarn_freqs_cis(float* out, int64_t dim, int64_t seqlen, int64_t original_seq_len,
+                        float base, float factor, float beta_fast, float beta_slow,
+                        ds41_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step 1a: window ring and window indices                                    */
+/* ------------------------------------------------------------------------ */
+/* Rows the window indices point into (rows_a): m at start_pos 0, win for a
+ * single-token step past position 0, win + m for a chunk of m > 1 tokens past
+ * position 0.  Host function, no device work. */
+int64_t ds41_rows_a_len(int64_t m, int64_t win, int64_t start_pos);
+
+/* forward.rs, "the window ring" block, and compress.rs attention_any's ring
+ * update: the row of position q goes to ring slot q mod win; when m > win
+ * only the newest row of each slot is kept.  Also writes the window indices
+ * (forward.rs calls window_topk_idxs): win_idx[t][j] is the rows_a index of
+ * position p - win + 1 + j (p = start_pos + t), or -1 when that position is
+ * negative.  rows_a is
+ *   start_pos == 0        : kv itself (index = position);
+ *   start_pos > 0, m == 1 : the ring after this write (index = q mod win);
+ *   start_pos > 0, m > 1  : the ring as it was before this call, then kv
+ *                           (q < start_pos -> q mod win, else
+ *                           win + q - start_pos); this function writes it.
+ *   kv      [m, hd] bf16 new rows;     ring [win, hd] bf16, updated in place
+ *   rows_a  [win + m, hd] bf16 output, required only when start_pos > 0 and
+ *           m > 1 (ignored otherwise, may be NULL)
+ *   win_idx [m, win] int32 output
+ *   n_a     nullable host int64 output: ds41_rows_a_len(m, win, start_pos)
+ *   m >= 1, hd % 8 == 0, win >= 1. */
+int ds41_window_ring_write(const ds41_bf16* kv, ds41_bf16* ring, ds41_bf16* rows_a,
+                           int32_t* win_idx, int64_t* n_a, int64_t m, int64_t hd, int64_t win,
+                           int64_t start_pos, ds41_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step 1b: compressed latent rows                                            */
+/* ------------------------------------------------------------------------ */
+/* forward.rs, "if let Some(groups) = latent_groups" (rope, fp4_quant with
+ * LATENT_BLOCK, copy into the cache at row start_pos/ratio) and the same
+ * branch of compress.rs attention_any.  The call completes
+ * G = (start_pos + m)/ratio - start_pos/ratio groups; group g becomes cache
+ * row c = start_pos/ratio + g.  Its RoPE position is c * ratio (g*ratio at
+ * start_pos 0, start_pos + 1 - ratio for the single decode group).  The row
+ * is rotated (last rd dims, adjacent pairs, table row c * ratio), rounded to
+ * bf16, then sent through the e4m3 fp4 round trip (block 16).
+ *   latent     [G, hd] bf16, before RoPE
+ *   freqs_cis  [max_pos, rd/2, 2] f32 (cos, sin), from ds41_yarn_freqs_cis
+ *   cache      [cache_rows, hd] bf16, rows c written
+ *   cache_codes  nullable [cache_rows, hd/2] uint8 e2m1 codes of row c
+ *   cache_scales nullable [cache_rows, hd/16] uint8 e4m3 scale codes of row c
+ *   G must equal (start_pos + m)/ratio - start_pos/ratio (G == 0 is a no-op);
+ *   hd % 16 == 0, rd even, 0 < rd <= hd, (start_pos + m)/ratio <= cache_rows,
+ *   start_pos + m <= max_pos. */
+int ds41_compress_latent_write(const ds41_bf16* latent, const float* freqs_cis, int64_t max_pos,
+                               ds41_bf16* cache, int64_t cache_rows, uint8_t* cache_codes,
+                               uint8_t* cache_scales, int64_t G, int64_t hd, int64_t rd,
+                               int64_t ratio, int64_t start_pos, int64_t m, ds41_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Steps 2a + 2b: fp4 indexer scores, per-query top-k, index merge            */
+/* ------------------------------------------------------------------------ */
+/* Scratch bytes ds41_indexer_topk needs (scores_out given or not). */
+size_t ds41_indexer_workspace_bytes(int64_t m, int64_t Hi, int64_t Di, int64_t n_c,
+                                    int scores_out_given);
+
+/* forward.rs / compress.rs call the indexer (its body is not on the pages)
+ * and then merge: idx row t = the window indices of t, then the indexer's
+ * ctopk = min(topk, n_c) picks, already offset by n_a (= offset).  The
+ * compress.rs header fixes the precision: q and k take the e2m1 round trip
+ * with power-of-two scales per block of 32 and the scores are bf16 values.
+ * This library computes, for query t at p = start_pos + t and every
+ * compressed row s < (p + 1)/ratio (rows that are complete at p):
+ *   qh = Q8(q_idx[t, h, :]), kh = Q8(k_idx[s, :])       (as ds41_fp4_quant_e8m0)
+ *   dot = sum_d qh[d] * kh[d]                             (exact for fp4 values
+ *                                                          of moderate range)
+ *   acc = 0; for h = 0 .. Hi-1: acc = fma(w[t, h], max(dot, 0), acc)   (f32)
+ *   score[t, s] = bf16(acc)  (-0 stored as +0; rows not yet visible: -inf)
+ * then keeps the min(topk, visible) highest scores, ties to the lower row, as
+ * offset + s, and pads with -1.  The picks of a row are in ascending s.
+ *   q_idx  [m, Hi, Di] bf16;  k_idx [n_c, Di] bf16;  w [m, Hi] f32
+ *   win_idx [m, win] int32 (from ds41_window_ring_write)
+ *   idx    [m, win + ctopk] int32 output
+ *   scores nullable [m, n_c] bf16 output
+ *   Di % 32 == 0, Di <= 256, 1 <= Hi <= 128, n_c >= 1 (with n_c == 0 call
+ *   nothing: the merged row is the window row alone), 1 <= topk. */
+int ds41_indexer_topk(const ds41_bf16* q_idx, const ds41_bf16* k_idx, const float* w,
+                      const int32_t* win_idx, int32_t* idx, ds41_bf16* scores, int64_t m,
+                      int64_t Hi, int64_t Di, int64_t n_c, int64_t win, int64_t ratio,
+                      int64_t start_pos, int64_t topk, int64_t offset, void* ws, size_t ws_bytes,
+                      ds41_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step 3: sparse attention with a per-head sink                              */
+/* ------------------------------------------------------------------------ */
+/* Scratch bytes ds41_sparse_attn_sink_fwd needs. */
+size_t ds41_sparse_attn_workspace_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K);
+
+/* compress.rs attention_any: sparse_attn(q, kv_rows, sink, idx, ...) with
+ * scale = head_dim^-0.5 (the body of sparse_attn is not on the pages), and
+ * forward.rs attend_and_project's rows_a / rows_b / idx / topk arguments.
+ * For every query t and head h, over the valid entries v of idx row t
+ * (v < n_a -> rows_a[v], n_a <= v < n_a + n_c -> rows_b[v - n_a], -1 skipped):
+ *   s_v = scale * <q[t, h], row_v>
+ *   o[t, h] = sum_v e^{s_v} row_v / (e^{sink[h]} + sum_v e^{s_v})
+ * One row serves as key and value.  The sink is a logit in the denominator
+ * only (-inf gives a plain softmax).  f32 accumulation, bf16 output.
+ *   q [m, nh, hd] bf16;  rows_a [n_a, hd];  rows_b [n_c, hd] (NULL if n_c == 0)
+ *   idx [m, K] int32;  sink [nh] f32
+ *   o [m, nh, hd] bf16 output;  lse nullable [m, nh] f32 output: the natural
+ *   log of the denominator above, e^{lse} = e^{sink} + sum_v e^{s_v}
+ *   hd % 64 == 0, hd <= 512, nh >= 1, K >= 1. */
+int ds41_sparse_attn_sink_fwd(const ds41_bf16* q, const ds41_bf16* rows_a, int64_t n_a,
+                              const ds41_bf16* rows_b, int64_t n_c, const int32_t* idx, int64_t K,
+                              const float* sink, float scale, ds41_bf16* o, float* lse, int64_t m,
+                              int64_t nh, int64_t hd, void* ws, size_t ws_bytes,
+                              ds41_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS41_H_ */

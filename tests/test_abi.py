@@ -1,0 +1,92 @@
+"""The C ABI library: it builds for sm_103a, loads, exports every entry point
+include/ds41.h declares, and rejects bad arguments on the host before any
+device work (no GPU needed for these)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from compressed_sparse_attention_window_gb300 import build as ds41_build
+from compressed_sparse_attention_window_gb300 import ds41
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ds41.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ds41_build.build()
+    return ds41.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds41_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    names = _declared()
+    for n in ("ds41_fp4_quant_e8m0", "ds41_fp4_quant_e4m3", "ds41_window_ring_write",
+              "ds41_compress_latent_write", "ds41_indexer_topk", "ds41_sparse_attn_sink_fwd"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert set(_declared()) == set(ds41.SIGNATURES), "binding signatures out of date"
+
+
+def test_rows_a_len(lib):
+    assert lib.ds41_rows_a_len(64, 16, 0) == 64
+    assert lib.ds41_rows_a_len(1, 128, 8191) == 128
+    assert lib.ds41_rows_a_len(1024, 128, 65536) == 1152
+
+
+def _err(lib):
+    return lib.ds41_last_error().decode()
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+
+
+def test_host_argument_checks(lib):
+    # the forward's own limits: at least one token
+    assert lib.ds41_window_ring_write(FAKE, FAKE, None, FAKE, None, 0, 64, 16, 0, None) == 2
+    assert "m=0" in _err(lib)
+    # a chunk past position 0 needs rows_a
+    assert lib.ds41_window_ring_write(FAKE, FAKE, None, FAKE, None, 4, 64, 16, 8, None) == 1
+    # hd not a multiple of 8
+    assert lib.ds41_window_ring_write(FAKE, FAKE, None, FAKE, None, 4, 60, 16, 0, None) == 1
+    # misaligned pointer
+    bad = ctypes.c_void_p((1 << 20) + 2)
+    assert lib.ds41_fp4_quant_e8m0(bad, FAKE, None, None, 1, 32, None) == 1
+    # cols not a multiple of the block
+    assert lib.ds41_fp4_quant_e8m0(FAKE, FAKE, None, None, 1, 48, None) == 1
+    assert lib.ds41_fp4_quant_e4m3(FAKE, FAKE, None, None, 1, 24, None) == 1
+    # wrong group count for the latent write
+    assert lib.ds41_compress_latent_write(FAKE, FAKE, 100, FAKE, 100, None, None, 3, 64, 16, 4,
+                                          0, 8, None) == 1
+    # cache too small
+    assert lib.ds41_compress_latent_write(FAKE, FAKE, 100, FAKE, 1, None, None, 2, 64, 16, 4, 0,
+                                          8, None) == 2
+    # indexer: unsupported Di, topk < 1
+    assert lib.ds41_indexer_topk(FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 2, 48, 4, 16, 4, 0, 8, 16,
+                                 None, 0, None) == 1
+    assert lib.ds41_indexer_topk(FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 2, 32, 4, 16, 4, 0, 0, 16,
+                                 None, 0, None) == 2
+    # attention: unsupported head dim, no tokens
+    assert lib.ds41_sparse_attn_sink_fwd(FAKE, FAKE, 4, None, 0, FAKE, 4, FAKE,
+                                         ctypes.c_float(0.1), FAKE, None, 1, 4, 96, None, 0,
+                                         None) == 1
+    assert lib.ds41_sparse_attn_sink_fwd(FAKE, FAKE, 4, None, 0, FAKE, 4, FAKE,
+                                         ctypes.c_float(0.1), FAKE, None, 0, 4, 64, None, 0,
+                                         None) == 2
+
+
+def test_workspace_sizes_are_host_only(lib):
+    # the indexer needs scratch for its scores unless the caller takes them
+    assert lib.ds41_indexer_workspace_bytes(4096, 64, 128, 1024, 0) >= 4096 * 1024 * 2
+    assert lib.ds41_indexer_workspace_bytes(1, 64, 128, 2048, 1) == 0

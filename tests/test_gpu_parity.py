@@ -1,0 +1,287 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: fp4 quantisers (values, codes, scales), ring / window indices /
+rows_a, latent cache rows (values, codes, scales), indexer scores, top-k index
+sets.  Attention: |gpu - oracle| <= 2e-2 + 1e-2 |oracle| (f64 oracle).
+"""
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_attention_window_gb300 import ds41
+from compressed_sparse_attention_window_gb300.workloads import (CHUNKED, DECODE, LONG_DECODE,
+                                                                 PREFILL, TINY_PREFILL, WORKLOADS,
+                                                                 bf16_bits, from_bits,
+                                                                 make_inputs)
+from helpers import (assert_idx_sets_equal, attn_close, oracle_forward, sample_tokens, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ds41.load()
+    yield
+    assert ds41.device_status() == 0
+
+
+def _special_rows(cols, block, rng):
+    """Rows that hit the corners of the fp4 round trip: zero blocks, blocks at
+    exactly 6*2^k, values on e2m1 midpoints, tiny and huge values, negatives."""
+    rows = []
+    z = np.zeros(cols, np.float32)
+    rows.append(z)
+    r = rng.standard_normal(cols).astype(np.float32)
+    r[:block] = 0.0
+    r[block: 2 * block] = -1e-30
+    rows.append(r)
+    e = np.zeros(cols, np.float32)
+    for b in range(cols // block):
+        k = (b % 20) - 10
+        e[b * block] = 6.0 * 2.0 ** k
+        mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -2.5, -5.0]) * 2.0 ** k
+        e[b * block + 1: b * block + 1 + min(len(mids), block - 1)] = mids[: block - 1]
+    rows.append(e)
+    rows.append(rng.standard_normal(cols).astype(np.float32) * 1e4)
+    rows.append(rng.standard_normal(cols).astype(np.float32) * 1e-6)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("e4m3", [False, True])
+@pytest.mark.parametrize("rows,cols", [(1, 32), (37, 128), (300, 512), (3, 4096)])
+def test_fp4_quant_bit_exact(orc, e4m3, rows, cols):
+    block = 16 if e4m3 else 32
+    rng = np.random.default_rng(rows * 7 + cols)
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    x[rng.random(x.shape) < 0.01] *= 20
+    x = np.concatenate([x, _special_rows(cols, block, rng)])
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    y, codes, scales = ds41.fp4_quant(xb.cuda(), e4m3, want_codes=True)
+    oy, ocodes, oscales = orc.fp4_quant(bf16_bits(xb), block, e4m3)
+    assert np.array_equal(bf16_bits(y), oy)
+    assert np.array_equal(codes.cpu().numpy(), ocodes)
+    assert np.array_equal(scales.cpu().numpy(), oscales)
+
+
+def test_fp4_quant_all_bf16_values(orc):
+    """Every finite bf16 bit pattern through both quantisers, each inside a
+    block whose scale is fixed by a planted maximum."""
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = (allb.astype(np.uint32) << 16).view(np.float32)
+    allb = allb[np.isfinite(vals)]
+    for e4m3, block in ((False, 32), (True, 16)):
+        per = block - 1
+        n = (allb.size + per - 1) // per
+        rows_per = 512 // block
+        n = (n + rows_per - 1) // rows_per * rows_per
+        pad = np.zeros(n * per, np.uint16)
+        pad[: allb.size] = allb
+        blocks = pad.reshape(n, per)
+        for amax_bits in (0x3F80, 0x4300, 0x0000):  # 1.0, 128.0, none
+            col0 = np.full((n, 1), amax_bits, np.uint16)
+            x = np.ascontiguousarray(np.concatenate([col0, blocks], axis=1).reshape(-1, 512))
+            xt = from_bits(x)
+            y, codes, scales = ds41.fp4_quant(xt.cuda(), e4m3, want_codes=True)
+            oy, ocodes, oscales = orc.fp4_quant(x, block, e4m3)
+            assert np.array_equal(bf16_bits(y), oy)
+            assert np.array_equal(codes.cpu().numpy(), ocodes)
+            assert np.array_equal(scales.cpu().numpy(), oscales)
+
+
+def test_yarn_table_matches_oracle(orc):
+    rd, seqlen = 64, 140000
+    fc_gpu = ds41.yarn_freqs_cis(rd, seqlen).cpu().numpy().astype(np.float64)
+    fc_ora = orc.yarn_freqs_cis(rd, seqlen).astype(np.float64)
+    f = orc.yarn_inv_freqs(rd, 65536, 160000.0, 16.0, 32.0, 1.0).astype(np.float64)
+    p = np.arange(seqlen, dtype=np.float64)[:, None]
+    # cos/sin of the same f32 angle agree to a few ulp; one ulp of difference in
+    # a frequency moves the angle by p * ulp(f), which bounds the rest.
+    ulp_f = np.spacing(f.astype(np.float32)).astype(np.float64)
+    tol = 4e-7 + p * ulp_f[None, :]
+    err = np.abs(fc_gpu - fc_ora).max(axis=2)
+    assert np.all(err <= tol), float(err.max())
+    # the frequencies themselves: identical in nearly every entry
+    assert np.mean(err[:2000] <= 4e-7) == 1.0
+
+
+RING_CASES = [(1, 0, 16), (16, 0, 16), (64, 0, 16), (70, 0, 16), (1, 3, 16), (1, 17, 16),
+              (1, 8191, 128), (5, 40, 16), (24, 37, 16), (300, 1000, 128), (1024, 65536, 128)]
+
+
+@pytest.mark.parametrize("m,sp,win", RING_CASES)
+def test_window_ring_bit_exact(orc, m, sp, win):
+    hd = 64
+    wl = TINY_PREFILL.replace(m=m, start_pos=sp, win=win, hd=hd, rd=16)
+    inp = make_inputs(wl, seed=m + sp)
+    ring_d = inp["ring"].cuda()
+    win_idx = torch.empty(m, win, dtype=torch.int32, device="cuda")
+    rows_a = ds41.window_ring_write(inp["kv"].cuda(), ring_d, win_idx, sp)
+    oring, orows = orc.window_ring_write(bf16_bits(inp["kv"]), bf16_bits(inp["ring"]), win, sp)
+    assert np.array_equal(bf16_bits(ring_d), oring)
+    assert np.array_equal(bf16_bits(rows_a), orows)
+    assert np.array_equal(win_idx.cpu().numpy(), orc.window_topk_idxs(win, m, sp))
+    assert ds41.rows_a_len(m, win, sp) == orc.rows_a_len(m, win, sp)
+
+
+LATENT_CASES = [(TINY_PREFILL, None), (DECODE, None), (PREFILL, None), (LONG_DECODE, None),
+                (CHUNKED, None), (TINY_PREFILL.replace(m=3, start_pos=9), None),
+                (TINY_PREFILL.replace(m=1, start_pos=10), None)]
+
+
+@pytest.mark.parametrize("wl", [c[0] for c in LATENT_CASES], ids=lambda w: f"{w.name}-{w.m}-{w.start_pos}")
+def test_latent_write_bit_exact(orc, wl):
+    inp = make_inputs(wl)
+    fc = orc.yarn_freqs_cis(wl.rd, wl.max_pos)  # the table is an input of the write
+    cache_d = inp["cache"].cuda()
+    rows = cache_d.shape[0]
+    codes = torch.zeros(rows, wl.hd // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(rows, wl.hd // 16, dtype=torch.uint8, device="cuda")
+    if wl.G > 0:
+        ds41.compress_latent_write(inp["latent"].cuda(), torch.from_numpy(fc).cuda(), cache_d,
+                                   wl.rd, wl.ratio, wl.start_pos, wl.m, codes, scales)
+    ocache, ocodes, oscales = orc.compress_latent_write(bf16_bits(inp["latent"]), fc,
+                                                        bf16_bits(inp["cache"]), wl.rd, wl.ratio,
+                                                        wl.start_pos)
+    assert np.array_equal(bf16_bits(cache_d), ocache)
+    first = wl.start_pos // wl.ratio
+    sl = slice(first, first + wl.G)
+    assert np.array_equal(codes.cpu().numpy()[sl], ocodes[sl])
+    assert np.array_equal(scales.cpu().numpy()[sl], oscales[sl])
+
+
+def _gpu_indexer(wl, inp, with_scores=True):
+    dev = to_dev(inp)
+    win_idx = torch.from_numpy(
+        np.ascontiguousarray(np.zeros((wl.m, wl.win), np.int32))).cuda()
+    from oracle import window_topk_idxs
+    win_idx.copy_(torch.from_numpy(window_topk_idxs(wl.win, wl.m, wl.start_pos)))
+    scores = torch.empty(wl.m, wl.n_c, dtype=torch.bfloat16, device="cuda") if with_scores else None
+    idx = ds41.indexer_topk(dev["q_idx"], dev["k_idx"][: wl.n_c], dev["w"], win_idx, wl.ratio,
+                            wl.start_pos, wl.topk, wl.n_a, scores=scores)
+    return idx, scores
+
+
+INDEXER_CASES = [TINY_PREFILL, TINY_PREFILL.replace(topk=64), DECODE, LONG_DECODE, CHUNKED,
+                 PREFILL, TINY_PREFILL.replace(m=37, start_pos=5, Hi=5, Di=64),
+                 DECODE.replace(start_pos=8191 + 9, m=1, topk=4000)]
+
+
+@pytest.mark.parametrize("wl", INDEXER_CASES, ids=lambda w: f"{w.name}-{w.m}-{w.start_pos}-{w.topk}-{w.Hi}")
+def test_indexer_scores_and_topk(orc, wl):
+    inp = make_inputs(wl)
+    idx, scores = _gpu_indexer(wl, inp)
+    toks = sample_tokens(wl) if wl.m > 128 else list(range(wl.m))
+    sc, bad = orc.indexer_scores(bf16_bits(inp["q_idx"]), bf16_bits(inp["k_idx"])[: wl.n_c],
+                                 inp["w"].numpy(), wl.ratio, wl.start_pos, tokens=toks)
+    assert bad == 0
+    gsc = bf16_bits(scores)[toks]
+    assert np.array_equal(gsc, sc), np.argwhere(gsc != sc)[:5]
+    win_idx = orc.window_topk_idxs(wl.win, wl.m, wl.start_pos)
+    oidx = orc.topk_merge(sc, win_idx[toks], wl.n_c, wl.win, wl.ratio, wl.start_pos, wl.topk,
+                          wl.n_a, tokens=toks)
+    assert_idx_sets_equal(idx.cpu().numpy()[toks], oidx, wl.win)
+    # the picks of a row come in ascending row order, -1 padding last
+    g = idx.cpu().numpy()[:, wl.win:]
+    for r in g[:: max(1, wl.m // 64)]:
+        v = r[r >= 0]
+        assert np.all(np.diff(v) > 0) and np.all(r[len(v):] == -1)
+
+
+@pytest.mark.parametrize("sink_kind", ["normal", "minus_inf", "large"])
+def test_sparse_attn_given_indices(orc, sink_kind):
+    wl = TINY_PREFILL.replace(m=40, start_pos=0, topk=12, nh=20, hd=128)
+    inp = make_inputs(wl, seed=5)
+    if sink_kind == "minus_inf":
+        inp["sink"][:] = -float("inf")
+    elif sink_kind == "large":
+        inp["sink"] *= 30
+    rng = np.random.default_rng(3)
+    n_a, n_c, K = 40, 17, 45
+    rows_a = torch.randn(n_a, wl.hd).to(torch.bfloat16)
+    rows_b = torch.randn(n_c, wl.hd).to(torch.bfloat16)
+    idx = rng.integers(-1, n_a + n_c, (wl.m, K)).astype(np.int32)
+    idx[3, :] = -1          # a row with no valid index
+    idx[4, 1:] = -1         # a single valid index
+    o = ds41.sparse_attn_sink_fwd(inp["q"].cuda(), rows_a.cuda(), rows_b.cuda(),
+                                  torch.from_numpy(idx).cuda(), inp["sink"].cuda(), wl.scale)
+    oo, _, bad = orc.sparse_attn(bf16_bits(inp["q"]), bf16_bits(rows_a), bf16_bits(rows_b), idx,
+                                 inp["sink"].numpy(), wl.scale)
+    assert bad == 0
+    ok, err, worst = attn_close(o.float().cpu().numpy(), oo)
+    assert ok, (err, worst)
+
+
+@pytest.mark.parametrize("K", [1, 31, 33, 640, 2176])
+def test_sparse_attn_split_paths(orc, K):
+    """Decode-sized m exercises the split-K partials and the merge."""
+    nh, hd = 64, 512
+    n_a, n_c = 128, 2500
+    g = torch.Generator().manual_seed(K)
+    q = torch.randn(2, nh, hd, generator=g).to(torch.bfloat16)
+    rows_a = torch.randn(n_a, hd, generator=g).to(torch.bfloat16)
+    rows_b = torch.randn(n_c, hd, generator=g).to(torch.bfloat16)
+    sink = torch.randn(nh, generator=g)
+    rng = np.random.default_rng(K)
+    idx = np.stack([rng.permutation(n_a + n_c)[:K] for _ in range(2)]).astype(np.int32)
+    lse = torch.empty(2, nh, device="cuda")
+    o = ds41.sparse_attn_sink_fwd(q.cuda(), rows_a.cuda(), rows_b.cuda(),
+                                  torch.from_numpy(idx).cuda(), sink.cuda(), hd ** -0.5, lse=lse)
+    oo, olse, _ = orc.sparse_attn(bf16_bits(q), bf16_bits(rows_a), bf16_bits(rows_b), idx,
+                                  sink.numpy(), np.float32(hd ** -0.5))
+    ok, err, worst = attn_close(o.float().cpu().numpy(), oo)
+    assert ok, (err, worst)
+    assert np.allclose(lse.cpu().numpy(), olse, atol=1e-3, rtol=1e-4)
+
+
+def test_sparse_attn_bad_index_sets_status(orc):
+    nh, hd = 4, 64
+    q = torch.randn(1, nh, hd).to(torch.bfloat16).cuda()
+    rows = torch.randn(8, hd).to(torch.bfloat16).cuda()
+    idx = torch.tensor([[0, 1, 99, 2]], dtype=torch.int32).cuda()  # 99 is out of range
+    sink = torch.zeros(nh).cuda()
+    assert ds41.device_status(reset=True) == 0
+    o = ds41.sparse_attn_sink_fwd(q, rows, None, idx, sink, 0.125)
+    assert ds41.device_status(reset=True) == 4  # DS41_E_INDEX; the row was skipped
+    ok_idx = np.array([[0, 1, -1, 2]], np.int32)
+    oo, _, _ = orc.sparse_attn(bf16_bits(q), bf16_bits(rows), None, ok_idx,
+                               np.zeros(nh, np.float32), 0.125)
+    assert attn_close(o.float().cpu().numpy(), oo)[0]
+
+
+FORWARD_CASES = ["tiny_prefill", "decode", "long_decode", "chunked_prefill", "prefill"]
+
+
+@pytest.mark.parametrize("name", FORWARD_CASES)
+def test_forward_end_to_end(orc, name):
+    """All steps through the C ABI, launched as bench.py launches them,
+    against the oracle on sampled tokens (every token for small m)."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    dev = to_dev(inp)
+    fc = ds41.yarn_freqs_cis(wl.rd, wl.max_pos)
+    ora_fc = orc.yarn_freqs_cis(wl.rd, wl.max_pos)
+    out = ds41.forward(dev, wl, torch.from_numpy(ora_fc).cuda())
+    toks = sample_tokens(wl) if wl.m > 128 else list(range(wl.m))
+    ref = oracle_forward(orc, wl, inp, tokens=toks, fc=ora_fc)
+    assert np.array_equal(bf16_bits(dev["ring"]), ref["ring"])
+    assert np.array_equal(bf16_bits(dev["cache"]), ref["cache"])
+    assert_idx_sets_equal(out["idx"].cpu().numpy()[toks], ref["idx"], wl.win)
+    ok, err, worst = attn_close(out["o"].float().cpu().numpy()[toks], ref["o"])
+    assert ok, (name, err, worst)
+    assert fc.shape == (wl.max_pos, wl.rd // 2, 2)
+
+
+def test_forward_no_compressed_rows_yet(orc):
+    """start_pos + m < ratio: no compressed row exists, the merged rows are the
+    window rows alone."""
+    wl = TINY_PREFILL.replace(m=3, start_pos=0, ratio=4)
+    assert wl.n_c == 0
+    inp = make_inputs(wl)
+    dev = to_dev(inp)
+    fc = torch.from_numpy(orc.yarn_freqs_cis(wl.rd, wl.max_pos)).cuda()
+    out = ds41.forward(dev, wl, fc)
+    ref = oracle_forward(orc, wl, inp, fc=fc.cpu().numpy())
+    assert np.array_equal(out["idx"].cpu().numpy(), ref["idx"])
+    assert attn_close(out["o"].float().cpu().numpy(), ref["o"])[0]
