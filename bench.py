@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of one layer's compressed sparse attention forward on GB300.
+
+One step = the whole hot path for one batch of synthetic input: window ring
+write + window indices, compressed latent write, fp4 indexer scores + top-k +
+merge, sparse attention with the sink.  The default workload is single-token
+decode (m=1 at start_pos 8191, 64 heads x 512, window 128, ratio 4 -> 2048
+compressed rows, top-k 512, indexer 64 x 128); ``--workload`` picks another.
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier +
+synchronize on both sides, CUDA events on the launching stream, each step a
+CUDA-graph replay of the four C-ABI calls.  Steps rotate over independent
+layer states whose total size exceeds twice the L2 cache, so every step reads
+its window ring, latent cache and indexer keys from HBM.  The JSON line adds
+the roofline of the dominant kernel (timed again with events around it), the
+end-to-end rate through the public API with host buffers, the SM clocks seen
+during the timed region, and the CPU oracle timed on a bounded sample.
+
+``--impl reference`` times the CPU oracle itself on the same workload.
+Multi-GPU (torchrun): every rank runs independent replicas of the step on its
+own GPU; no data-path collective; value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from compressed_sparse_attention_window_gb300 import ds41  # noqa: E402
+from compressed_sparse_attention_window_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "query-tokens/s of compressed sparse attn fwd (decode, prefill); % HBM/TC roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (host float)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of one step (bytes / flops the method itself must move)
+# ---------------------------------------------------------------------------
+def attn_valid_rows(wl) -> int:
+    """Valid gathered rows summed over the tokens: window positions that exist
+    plus the visible compressed rows the top-k keeps."""
+    tot = 0
+    for t in range(wl.m):
+        p = wl.start_pos + t
+        vis = min(wl.n_c, (p + 1) // wl.ratio)
+        tot += min(p + 1, wl.win) + min(wl.topk, vis)
+    return tot
+
+
+def algorithmic(wl):
+    """Per-op algorithmic bytes and flops of one step."""
+    bf, m = 2, wl.m
+    rows = attn_valid_rows(wl)
+    pairs = sum(min(wl.n_c, (wl.start_pos + t + 1) // wl.ratio) for t in range(wl.m))
+    K = wl.K
+    ops = {
+        "window_ring_write": {"bytes": 2 * min(m, wl.win) * wl.hd * bf + m * wl.win * 4},
+        "compress_latent_write": {"bytes": 2 * wl.G * wl.hd * bf + wl.G * (wl.rd // 2) * 8},
+        "indexer_topk": {
+            "bytes": (m * wl.Hi * wl.Di * bf + wl.n_c * wl.Di * bf + m * wl.Hi * 4
+                      + m * wl.win * 4 + m * K * 4),
+            "flops": 2 * wl.Hi * wl.Di * pairs},
+        "sparse_attn_sink_fwd": {
+            "bytes": rows * wl.hd * bf + 2 * m * wl.nh * wl.hd * bf + m * K * 4 + wl.nh * 4,
+            "flops": 4 * wl.nh * wl.hd * rows},
+    }
+    return ops
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler
+# ---------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ds41_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait(timeout=5)
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.remove(self.path)
+        # median over the samples taken under load (the top half by clock)
+        load = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def build_slots(wl, n_slots, device, seed0=1000):
+    """Independent layer states (inputs + outputs + workspaces) for rotation."""
+    slots = []
+    for s in range(n_slots):
+        inp = make_inputs(wl, device=device, seed=seed0 + s)
+        out = {"win_idx": torch.empty(wl.m, wl.win, dtype=torch.int32, device=device)}
+        if wl.start_pos > 0 and wl.m > 1:
+            out["rows_a"] = torch.empty(wl.win + wl.m, wl.hd, dtype=torch.bfloat16, device=device)
+        if wl.n_c > 0:
+            out["idx"] = torch.empty(wl.m, wl.K, dtype=torch.int32, device=device)
+            nb = ds41.indexer_workspace_bytes(wl.m, wl.Hi, wl.Di, wl.n_c, False)
+            if nb:
+                out["ws_idx"] = torch.empty(nb, dtype=torch.uint8, device=device)
+        out["o"] = torch.empty(wl.m, wl.nh, wl.hd, dtype=torch.bfloat16, device=device)
+        nb = ds41.sparse_attn_workspace_bytes(wl.m, wl.nh, wl.hd, wl.K)
+        if nb:
+            out["ws_attn"] = torch.empty(nb, dtype=torch.uint8, device=device)
+        slots.append((inp, out))
+    return slots
+
+
+def slot_bytes(slot) -> int:
+    inp, out = slot
+    return sum(v.numel() * v.element_size() for d in (inp, out) for v in d.values())
+
+
+def launches_per_step(wl) -> int:
+    n = 1  # ring write
+    if wl.G > 0:
+        n += 1
+    if wl.n_c > 0:
+        hpad = (wl.Hi + 7) // 8 * 8
+        tt = max(1, 128 // hpad)
+        groups = (wl.m + tt - 1) // tt
+        n += 2 + (1 if groups > 4 else 0)
+    heads_groups = (wl.nh + 63) // 64
+    chunks = (wl.K + 31) // 32
+    ctas = wl.m * heads_groups
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    splits = 1
+    if ctas < sms:
+        splits = min(chunks, (sms + ctas - 1) // ctas)
+        cps = (chunks + splits - 1) // splits
+        splits = (chunks + cps - 1) // cps
+    n += 1 + (1 if splits > 1 else 0)
+    return n
+
+
+def run_ours(args, world, rank, local):
+    wl = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    ds41.load()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    fc = ds41.yarn_freqs_cis(wl.rd, wl.max_pos, device=dev)
+
+    one = build_slots(wl, 1, dev)
+    per = slot_bytes(one[0])
+    n_slots = max(1, min(256, math.ceil(2.2 * l2 / per)))
+    slots = one + (build_slots(wl, n_slots - 1, dev, seed0=2000) if n_slots > 1 else [])
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    # eager warm-up of every slot (sets kernel attributes, status word)
+    with torch.cuda.stream(stream):
+        for inp, out in slots:
+            ds41.forward(inp, wl, fc, out)
+    stream.synchronize()
+
+    graphs = []
+    for inp, out in slots:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            ds41.forward(inp, wl, fc, out)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            graphs[i % n_slots].replay()
+    stream.synchronize()
+
+    clocks = Clocks(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(K):
+            graphs[(W + i) % n_slots].replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop()
+    t_ms = e0.elapsed_time(e1)
+    t_max_ms = max_over_ranks(t_ms, world)
+    value = wl.m * K * world / (t_max_ms / 1e3)
+
+    # ---- per-op timing (events around each op; the GPU is kept behind the CPU
+    # by a sleep kernel so no launch gap enters the measured intervals)
+    ops = ["window_ring_write", "compress_latent_write", "indexer_topk", "sparse_attn_sink_fwd"]
+    op_ms = {k: 0.0 for k in ops}
+    evs = []
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(2e9 * (0.05 + 5e-4 * K)))
+        for i in range(K):
+            inp, out = slots[(W + i) % n_slots]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record(stream)
+            win_idx = out["win_idx"]
+            rows_a = ds41.window_ring_write(inp["kv"], inp["ring"], win_idx, wl.start_pos,
+                                            rows_a=out.get("rows_a"))
+            ev[1].record(stream)
+            if wl.G > 0:
+                ds41.compress_latent_write(inp["latent"], fc, inp["cache"], wl.rd, wl.ratio,
+                                           wl.start_pos, wl.m)
+            ev[2].record(stream)
+            if wl.n_c > 0:
+                idx = ds41.indexer_topk(inp["q_idx"], inp["k_idx"][: wl.n_c], inp["w"], win_idx,
+                                        wl.ratio, wl.start_pos, wl.topk, rows_a.shape[0],
+                                        idx=out["idx"], ws=out.get("ws_idx"))
+                rows_b = inp["cache"][: wl.n_c]
+            else:
+                idx, rows_b = win_idx, None
+            ev[3].record(stream)
+            ds41.sparse_attn_sink_fwd(inp["q"], rows_a, rows_b, idx, inp["sink"], wl.scale,
+                                      o=out["o"], ws=out.get("ws_attn"))
+            ev[4].record(stream)
+            evs.append(ev)
+    stream.synchronize()
+    for ev in evs:
+        for j, k in enumerate(ops):
+            op_ms[k] += ev[j].elapsed_time(ev[j + 1]) / K
+    alg = algorithmic(wl)
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    dom = max(ops, key=lambda k: op_ms[k])
+    d_ms = op_ms[dom]
+    if wl.m >= 256 and dom == "sparse_attn_sink_fwd":
+        achieved = alg[dom]["flops"] / (d_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                "frac": achieved / bf16}
+    else:
+        achieved = alg[dom]["bytes"] / (d_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm}
+    roof.update({"kernel": dom, "ms_per_launch": d_ms, "algorithmic_bytes": alg[dom]["bytes"],
+                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
+                 else "fallback", "traffic": args.traffic})
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(wl, slots, fc, stream, K, W, n_slots)
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": t_max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: m={wl.m} start_pos={wl.start_pos} heads={wl.nh}x{wl.hd}"
+                               f" rope={wl.rd} window={wl.win} ratio={wl.ratio} compressed_rows="
+                               f"{wl.n_c} topk={wl.topk} indexer={wl.Hi}x{wl.Di}",
+                   "global_batch": wl.m * world, "parallelism": f"replicas{world}",
+                   "l2": f"inputs larger than L2: {n_slots} rotating layer states x "
+                         f"{per / 2**20:.2f} MiB = {n_slots * per / 2**20:.0f} MiB "
+                         f"(L2 {l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA-graph replay per step, CUDA events on the launching stream"},
+        "roofline": roof,
+        "per_op_ms": op_ms,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(wl) * K,
+        "clocks": ck,
+    }
+    return res, wl
+
+
+def run_e2e(wl, slots, fc, stream, K, W, n_slots):
+    """The same metric through ds41.forward (eager, the call a user makes), with
+    each step's inputs copied from pinned host memory and the output read back."""
+    names = ["q", "kv", "latent", "q_idx", "w"]
+    host = []
+    for s in range(min(n_slots, 8)):
+        inp, _ = slots[s]
+        host.append({k: inp[k].cpu().pin_memory() for k in names})
+    o_host = torch.empty(slots[0][1]["o"].shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = o_host.numel() * o_host.element_size()
+
+    def step(i):
+        inp, out = slots[i % n_slots]
+        hs = host[i % len(host)]
+        for k in names:
+            inp[k].copy_(hs[k], non_blocking=True)
+        ds41.forward(inp, wl, fc, out)
+        o_host.copy_(out["o"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    stream.synchronize()
+    t0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(K):
+            step(W + i)
+        e1.record(stream)
+    stream.synchronize()
+    wall = time.perf_counter() - t0
+    ms = max(e0.elapsed_time(e1), wall * 1e3)
+    return {"value": wl.m * K / (ms / 1e3), "unit": "query-tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "how": "ds41.forward eager per step; pinned H2D of q/kv/latent/q_idx/w, D2H of o"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_rate(wl, steps=None, budget_s=None):
+    """Time the oracle's whole forward on a bounded sample of the workload:
+    ``steps`` forwards (or as many as fit in ``budget_s``), each over at most
+    8 query tokens (ring and latent writes run whole every time)."""
+    import numpy as np
+
+    import oracle
+    from compressed_sparse_attention_window_gb300.workloads import bf16_bits
+    inp = make_inputs(wl)
+    b = {k: bf16_bits(inp[k]) for k in ("q", "kv", "latent", "q_idx", "ring", "cache", "k_idx")}
+    sink, w = inp["sink"].numpy(), inp["w"].numpy()
+    fc = oracle.yarn_freqs_cis(wl.rd, wl.max_pos)
+    toks_per = min(wl.m, 8)
+    rng = np.random.default_rng(0)
+    done_tokens, n = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        if steps is not None and n >= steps:
+            break
+        if budget_s is not None and time.perf_counter() - t0 >= budget_s:
+            break
+        toks = sorted(rng.choice(wl.m, toks_per, replace=False).tolist()) if wl.m > 1 else [0]
+        ring, rows_a = oracle.window_ring_write(b["kv"], b["ring"], wl.win, wl.start_pos)
+        win_idx = oracle.window_topk_idxs(wl.win, wl.m, wl.start_pos)
+        cache, _, _ = oracle.compress_latent_write(b["latent"], fc, b["cache"], wl.rd, wl.ratio,
+                                                   wl.start_pos)
+        if wl.n_c > 0:
+            sc, _ = oracle.indexer_scores(b["q_idx"], b["k_idx"][: wl.n_c], w, wl.ratio,
+                                          wl.start_pos, tokens=toks)
+            idx = oracle.topk_merge(sc, win_idx[toks], wl.n_c, wl.win, wl.ratio, wl.start_pos,
+                                    wl.topk, wl.n_a, tokens=toks)
+            rows_b = cache[: wl.n_c]
+        else:
+            idx, rows_b = win_idx[toks], None
+        oracle.sparse_attn(b["q"], rows_a, rows_b, idx, sink, wl.scale, tokens=toks)
+        done_tokens += len(toks)
+        n += 1
+    el = time.perf_counter() - t0
+    return {"value": done_tokens / el, "unit": "query-tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": el,
+            "sample": f"{n} oracle forwards of {toks_per} query token(s) each "
+                      f"({done_tokens} tokens, {el:.1f} s) on the {wl.name} workload; the ring "
+                      f"and latent writes run whole every time"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    wl = WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    oracle_rate(wl, steps=W)                       # warm-up
+    cb = oracle_rate(wl, steps=K)
+    return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": cb["unit"],
+            "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": 1e3 * cb["seconds"] / max(1, K), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "global_batch": min(wl.m, 8), "parallelism": "cpu"},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of CPU oracle work for the cpu_baseline field")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the dominant kernel, if known")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, wl = run_ours(args, world, rank, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            cb = oracle_rate(wl, budget_s=args.cpu_budget)
+            res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
