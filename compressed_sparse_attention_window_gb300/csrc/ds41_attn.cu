@@ -18,6 +18,8 @@
 // gathered with cp.async (double-buffered); tensor-core MMAs are bf16 with f32
 // accumulation.  With several splits the unnormalised (m, l, O) of each split
 // goes to the workspace and a merge kernel adds the sink once.
+#include <mutex>
+
 #include "ds41_common.cuh"
 
 namespace ds41 {
@@ -405,5 +407,87 @@ extern "C" int ds41_sparse_attn_sink_fwd(const ds41_bf16* q, const ds41_bf16* ro
         case 128: return launch_attn<128>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, wsb, status, st);
         case 256: return launch_attn<256>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, wsb, status, st);
         default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, wsb, status, st);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The same attention for callers that cannot allocate device memory.  The
+// split partials live in one file-scope device array instead of a
+// caller-provided workspace.
+// ---------------------------------------------------------------------------
+namespace ds41 {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+static constexpr int kNoAllocMaxDevices = 64;
+static uint8_t* g_noalloc_ptr[kNoAllocMaxDevices];
+static std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device.  The array's
+// name is only a host-side stand-in in host code, so its address is looked
+// up once per device, with that device current, and cached.
+static int noalloc_scratch(uint8_t** out) {
+    int dev = 0;
+    int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+    if (rc) return rc;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(DS41_E_CUDA, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        rc = cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch),
+                        "cudaGetSymbolAddress(no-alloc scratch)");
+        if (rc) return rc;
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return DS41_OK;
+}
+
+}  // namespace ds41
+
+extern "C" size_t ds41_sparse_attn_noalloc_capacity(void) { return ds41::kNoAllocScratchBytes; }
+
+extern "C" int ds41_sparse_attn_sink_fwd_noalloc(const ds41_bf16* q, const ds41_bf16* rows_a,
+                                                 int64_t n_a, const ds41_bf16* rows_b,
+                                                 int64_t n_c, const int32_t* idx, int64_t K,
+                                                 const float* sink, float scale, ds41_bf16* o,
+                                                 float* lse, int64_t m, int64_t nh, int64_t hd,
+                                                 ds41_stream_t stream) {
+    const char* name = "ds41_sparse_attn_sink_fwd_noalloc";
+    DS41_REQUIRE(m >= 1 && m < (int64_t(1) << 31), DS41_E_RANGE, "%s: m=%lld", name,
+                 (long long)m);
+    DS41_REQUIRE(nh >= 1 && nh <= 65535 * ATT_HEADS, DS41_E_ARG, "%s: nh=%lld", name,
+                 (long long)nh);
+    DS41_REQUIRE(hd == 64 || hd == 128 || hd == 256 || hd == 512, DS41_E_ARG,
+                 "%s: hd=%lld must be 64, 128, 256 or 512", name, (long long)hd);
+    DS41_REQUIRE(K >= 1 && K < (int64_t(1) << 30), DS41_E_ARG, "%s: K=%lld", name, (long long)K);
+    DS41_REQUIRE(n_a >= 0 && n_c >= 0 && n_a + n_c >= 1, DS41_E_ARG, "%s: n_a=%lld n_c=%lld",
+                 name, (long long)n_a, (long long)n_c);
+    DS41_REQUIRE(q && idx && sink && o && (n_a == 0 || rows_a) && (n_c == 0 || rows_b),
+                 DS41_E_ARG, "%s: null tensor pointer", name);
+    DS41_REQUIRE(aligned16(q) && aligned16(o) && (n_a == 0 || aligned16(rows_a)) &&
+                     (n_c == 0 || aligned16(rows_b)),
+                 DS41_E_ARG, "%s: q/o/rows must be 16-byte aligned", name);
+    AttnPlan p = plan_attn(m, nh, hd, K, device_sms());
+    const size_t need = p.part_o_bytes + p.part_ml_bytes;
+    DS41_REQUIRE(need <= kNoAllocScratchBytes, DS41_E_WORKSPACE,
+                 "%s: these sizes need %zu bytes of scratch, more than the %zu bytes of the "
+                 "static scratch array; use ds41_sparse_attn_sink_fwd with a workspace",
+                 name, need, kNoAllocScratchBytes);
+    unsigned int* status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    uint8_t* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    const uint16_t* ra = n_a ? rows_a : rows_b;
+    const uint16_t* rb = n_c ? rows_b : rows_a;
+    cudaStream_t st = (cudaStream_t)stream;
+    switch (hd) {
+        case 64: return launch_attn<64>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, scratch, status, st);
+        case 128: return launch_attn<128>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, scratch, status, st);
+        case 256: return launch_attn<256>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, scratch, status, st);
+        default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, scratch, status, st);
     }
 }

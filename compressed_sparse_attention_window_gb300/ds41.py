@@ -43,6 +43,9 @@ SIGNATURES = {
     "ds41_sparse_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
     "ds41_sparse_attn_sink_fwd": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F, _P, _P,
                                                  _I64, _I64, _I64, _P, _SZ, _P]),
+    "ds41_sparse_attn_noalloc_capacity": (_SZ, []),
+    "ds41_sparse_attn_sink_fwd_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F,
+                                                         _P, _P, _I64, _I64, _I64, _P]),
 }
 
 
@@ -217,6 +220,28 @@ def sparse_attn_sink_fwd(q: torch.Tensor, rows_a: torch.Tensor, rows_b: Optional
           _ptr(rows_b, _BF, "rows_b"), n_c, _ptr(idx, torch.int32, "idx"), K,
           _ptr(sink, torch.float32, "sink"), float(scale), _ptr(o, _BF, "o"),
           _ptr(lse, torch.float32, "lse"), m, nh, hd, _ptr(ws) if need else None, need, _stream())
+    return o
+
+
+def sparse_attn_noalloc_capacity() -> int:
+    """Bytes of the static scratch array behind sparse_attn_sink_fwd_noalloc."""
+    return int(load().ds41_sparse_attn_noalloc_capacity())
+
+
+def sparse_attn_sink_fwd_noalloc(q: torch.Tensor, rows_a: torch.Tensor,
+                                 rows_b: Optional[torch.Tensor], idx: torch.Tensor,
+                                 sink: torch.Tensor, scale: float, o: torch.Tensor,
+                                 lse: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """ds41_sparse_attn_sink_fwd_noalloc: the attention for callers that cannot
+    allocate device memory; the library's static scratch holds the split
+    partials.  ``o`` (and ``lse``) must be provided by the caller."""
+    m, nh, hd = q.shape
+    K = idx.shape[1]
+    n_c = 0 if rows_b is None else rows_b.shape[0]
+    _call("ds41_sparse_attn_sink_fwd_noalloc", _ptr(q, _BF, "q"), _ptr(rows_a, _BF, "rows_a"),
+          rows_a.shape[0], _ptr(rows_b, _BF, "rows_b"), n_c, _ptr(idx, torch.int32, "idx"), K,
+          _ptr(sink, torch.float32, "sink"), float(scale), _ptr(o, _BF, "o"),
+          _ptr(lse, torch.float32, "lse"), m, nh, hd, _stream())
     return o
 
 

@@ -204,6 +204,41 @@ int ds41_sparse_attn_sink_fwd(const ds41_bf16* q, const ds41_bf16* rows_a, int64
                               int64_t nh, int64_t hd, void* ws, size_t ws_bytes,
                               ds41_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Step 3 without caller-provided scratch                                     */
+/* ------------------------------------------------------------------------ */
+/* No counterpart in the paper: this entry point exists for callers that
+ * cannot allocate device memory.  Examples are serving runtimes that reserve
+ * all device memory when they start and forbid any allocation afterwards
+ * (cudaMalloc can synchronise the device and fragment a carefully packed
+ * pool), and plugin hosts that hand a kernel its input and output buffers and
+ * no allocator.  Such callers can still run the split (flash-decoding) path
+ * of ds41_sparse_attn_sink_fwd, whose partial results need scratch memory.
+ *
+ * Same arguments, same computation and same results as
+ * ds41_sparse_attn_sink_fwd, minus ws / ws_bytes.  The split partials go to
+ * one static device array of ds41_sparse_attn_noalloc_capacity() bytes
+ * (16 MiB) that every GPU loading this library holds until the process
+ * exits.  Sizes whose partials need more (ds41_sparse_attn_workspace_bytes
+ * larger than the capacity) are rejected with DS41_E_WORKSPACE and nothing is
+ * enqueued.  The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call shares the one array and it keeps the last call's
+ * contents; nothing in it has to start at zero, because each split writes its
+ * partial before the merge reads it.  Calls whose work overlaps on the GPU
+ * (on different streams, or on different host threads) race on the array:
+ * order them on one stream. */
+size_t ds41_sparse_attn_noalloc_capacity(void);
+
+int ds41_sparse_attn_sink_fwd_noalloc(const ds41_bf16* q, const ds41_bf16* rows_a, int64_t n_a,
+                                      const ds41_bf16* rows_b, int64_t n_c, const int32_t* idx,
+                                      int64_t K, const float* sink, float scale, ds41_bf16* o,
+                                      float* lse, int64_t m, int64_t nh, int64_t hd,
+                                      ds41_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
