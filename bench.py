@@ -197,6 +197,9 @@ def build_slots(wl, n_slots, device, seed0=1000):
         nb = ds41.sparse_attn_workspace_bytes(wl.m, wl.nh, wl.hd, wl.K)
         if nb:
             out["ws_attn"] = torch.empty(nb, dtype=torch.uint8, device=device)
+        nb = ds41.csa_workspace_bytes(wl)
+        if nb:
+            out["ws_csa"] = torch.empty(nb, dtype=torch.uint8, device=device)
         slots.append((inp, out))
     return slots
 
@@ -207,6 +210,12 @@ def slot_bytes(slot) -> int:
 
 
 def launches_per_step(wl) -> int:
+    """Kernels one ds41_csa_forward launches for this workload."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    hpad = (wl.Hi + 7) // 8 * 8
+    groups = (wl.m + max(1, 128 // hpad) - 1) // max(1, 128 // hpad)
+    if wl.n_c > 0 and groups <= 4 and wl.m * ((wl.nh + 15) // 16) * 4 <= sms:
+        return 3  # fused front (scores + ring + latent), top-k, cluster attention
     n = 1  # ring write
     if wl.G > 0:
         n += 1
@@ -215,10 +224,12 @@ def launches_per_step(wl) -> int:
         tt = max(1, 128 // hpad)
         groups = (wl.m + tt - 1) // tt
         n += 2 + (1 if groups > 4 else 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if wl.m * ((wl.nh + 15) // 16) * 4 <= sms:
+        return n + 1  # few-token cluster kernel
     heads_groups = (wl.nh + 63) // 64
     chunks = (wl.K + 31) // 32
     ctas = wl.m * heads_groups
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
     splits = 1
     if ctas < sms:
         splits = min(chunks, (sms + ctas - 1) // ctas)
@@ -246,14 +257,14 @@ def run_ours(args, world, rank, local):
     # eager warm-up of every slot (sets kernel attributes, status word)
     with torch.cuda.stream(stream):
         for inp, out in slots:
-            ds41.forward(inp, wl, fc, out)
+            ds41.csa_forward(inp, wl, fc, out)
     stream.synchronize()
 
     graphs = []
     for inp, out in slots:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            ds41.forward(inp, wl, fc, out)
+            ds41.csa_forward(inp, wl, fc, out)
         graphs.append(g)
     torch.cuda.synchronize()
 
@@ -357,6 +368,53 @@ def run_ours(args, world, rank, local):
     return res, wl
 
 
+def run_only(args, local):
+    """Profiling mode: W + K eager calls of the whole step (``--only step``) or
+    of one op over rotating layer states; prints the average time per call."""
+    wl = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    ds41.load()
+    fc = ds41.yarn_freqs_cis(wl.rd, wl.max_pos, device=dev)
+    slots = build_slots(wl, args.slots, dev)
+    for inp, out in slots:
+        ds41.forward(inp, wl, fc, out)  # fills win_idx / idx for the later ops
+    torch.cuda.synchronize()
+
+    def op(i):
+        inp, out = slots[i % len(slots)]
+        if args.only == "step":
+            ds41.csa_forward(inp, wl, fc, out)
+        elif args.only == "window_ring_write":
+            ds41.window_ring_write(inp["kv"], inp["ring"], out["win_idx"], wl.start_pos,
+                                   rows_a=out.get("rows_a"))
+        elif args.only == "compress_latent_write":
+            ds41.compress_latent_write(inp["latent"], fc, inp["cache"], wl.rd, wl.ratio,
+                                       wl.start_pos, wl.m)
+        elif args.only == "indexer_topk":
+            ds41.indexer_topk(inp["q_idx"], inp["k_idx"][: wl.n_c], inp["w"], out["win_idx"],
+                              wl.ratio, wl.start_pos, wl.topk, wl.n_a, idx=out["idx"],
+                              ws=out.get("ws_idx"))
+        elif args.only == "sparse_attn_sink_fwd":
+            rows_a = {0: inp["kv"]}.get(wl.start_pos, inp["ring"] if wl.m == 1 else out.get("rows_a"))
+            ds41.sparse_attn_sink_fwd(inp["q"], rows_a, inp["cache"][: wl.n_c], out["idx"],
+                                      inp["sink"], wl.scale, o=out["o"], ws=out.get("ws_attn"))
+        else:
+            raise SystemExit(f"unknown op {args.only}")
+
+    for i in range(args.warmup):
+        op(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        op(args.warmup + i)
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"only": args.only, "workload": wl.name, "calls": args.steps,
+                      "ms_per_call": e0.elapsed_time(e1) / args.steps, "slots": len(slots)}))
+
+
 def run_e2e(wl, slots, fc, stream, K, W, n_slots):
     """The same metric through ds41.forward (eager, the call a user makes), with
     each step's inputs copied from pinned host memory and the output read back."""
@@ -374,7 +432,7 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots):
         hs = host[i % len(host)]
         for k in names:
             inp[k].copy_(hs[k], non_blocking=True)
-        ds41.forward(inp, wl, fc, out)
+        ds41.csa_forward(inp, wl, fc, out)
         o_host.copy_(out["o"], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -394,7 +452,7 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots):
     ms = max(e0.elapsed_time(e1), wall * 1e3)
     return {"value": wl.m * K / (ms / 1e3), "unit": "query-tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "how": "ds41.forward eager per step; pinned H2D of q/kv/latent/q_idx/w, D2H of o"}
+            "how": "ds41.csa_forward eager per step; pinned H2D of q/kv/latent/q_idx/w, D2H of o"}
 
 
 # ---------------------------------------------------------------------------
@@ -474,10 +532,16 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if known")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="profiling mode: time eager calls of one op (or 'step') and exit")
+    ap.add_argument("--slots", type=int, default=4, help="layer states rotated in --only mode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     world, rank, local = dist_setup()
+    if args.only:
+        run_only(args, local)
+        return
     if args.impl == "reference":
         res = run_reference(args, world, rank)
         if res is not None:

@@ -18,13 +18,16 @@
 // gathered with cp.async (double-buffered); tensor-core MMAs are bf16 with f32
 // accumulation.  With several splits the unnormalised (m, l, O) of each split
 // goes to the workspace and a merge kernel adds the sink once.
+#include <cooperative_groups.h>
+
 #include <mutex>
 
-#include "ds41_common.cuh"
+#include "ds41_internal.cuh"
 
 namespace ds41 {
 
 constexpr int ATT_NC = 32;       // gathered rows per chunk
+constexpr int ATT_STAGE = 4096;  // indices of a CTA's range staged in shared memory
 constexpr int ATT_HEADS = 64;    // heads per CTA
 constexpr int ATT_THREADS = 256;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -35,7 +38,8 @@ struct AttnSmem {
     static constexpr size_t q_bytes = (size_t)ATT_HEADS * HD * 2;
     static constexpr size_t kv_bytes = (size_t)ATT_NC * HD * 2;
     static constexpr size_t sx_bytes = (size_t)2 * ATT_HEADS * ATT_NC * 4;
-    static constexpr size_t total = q_bytes + 2 * kv_bytes + sx_bytes + 2 * ATT_NC * 4;
+    static constexpr size_t total =
+        q_bytes + 2 * kv_bytes + sx_bytes + 2 * ATT_NC * 4 + (size_t)ATT_STAGE * 4;
 };
 
 __device__ __forceinline__ int aswz(int row, int c) { return c ^ (row & 7); }
@@ -56,6 +60,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) sparse_attn_kernel(
     uint16_t* kvs = reinterpret_cast<uint16_t*>(smem + SM::q_bytes);
     float* sx = reinterpret_cast<float*>(smem + SM::q_bytes + 2 * SM::kv_bytes);
     int* vflag = reinterpret_cast<int*>(smem + SM::q_bytes + 2 * SM::kv_bytes + SM::sx_bytes);
+    int* sidx = vflag + 2 * ATT_NC;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = warp & 3, half = warp >> 2;
@@ -79,13 +84,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) sparse_attn_kernel(
         const uint16_t* src = q + ((t * nh + (live ? h : 0)) * (int64_t)HD) + c * 8;
         cp_async16(smem_u32(qs + r * HD + aswz(r, c) * 8), src, live);
     }
+    // The indices of this CTA's range go to shared memory in one coalesced
+    // pass, so the gathers below do not wait on a global load per row.
+    const int jr0 = c_begin * ATT_NC;
+    const int nst = max(0, min(min(K, c_end * ATT_NC) - jr0, ATT_STAGE));
+    for (int j = tid; j < nst; j += ATT_THREADS) sidx[j] = irow[jr0 + j];
+    __syncthreads();
     auto load_chunk = [&](int chunk, int buf) {
         uint16_t* dst = kvs + buf * (ATT_NC * HD);
         for (int id = tid; id < ATT_NC * CPR; id += ATT_THREADS) {
             const int r = id / CPR, c = id % CPR;
             const int j = chunk * ATT_NC + r;
             int64_t v = -1;
-            if (j < K) v = irow[j];
+            if (j - jr0 < nst) v = sidx[j - jr0];
+            else if (j < K) v = irow[j];
             bool ok = v >= 0 && v < n_rows;
             if (c == 0) {
                 if (j < K && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
@@ -303,8 +315,296 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
     if (lse && threadIdx.x == 0) lse[t * nh + h] = (Mref + log2f(L)) / LOG2E;
 }
 
+// ---------------------------------------------------------------------------
+// Few-token (decode) path.  A cluster of CL CTAs shares one (token, group of
+// 16 heads); CTA r of the cluster takes slice r of the index row.  Four warps
+// split the head dim: for S each warp reduces over its quarter of hd and the
+// four partials are summed in a fixed order by every warp, so all warps hold
+// bit-identical scores and softmax statistics; for P*V each warp owns a
+// quarter of the output columns.  At the end the CTAs exchange (m, l) and
+// their unnormalised O through distributed shared memory; CTA r reduces the
+// r-th slice of the columns over the cluster, adds the sink and writes o.
+// No scratch memory and no second launch.
+// ---------------------------------------------------------------------------
+constexpr int DEC_HEADS = 16;
+constexpr int DEC_NC = 32;
+constexpr int DEC_SPS = DEC_NC + 8;  // padded row stride of the partial scores (no bank conflicts)
+// warps per CTA: 8 when the head dim gives every warp at least two n-tiles
+template <int HD>
+__host__ __device__ constexpr int dec_warps() { return HD >= 128 ? 8 : 4; }
+constexpr int DEC_STAGE = 2048;  // indices of a CTA's slice staged in shared memory
+
+template <int HD>
+struct DecSmem {
+    static constexpr int OSTR = HD + 8;  // padded row stride of the staged O
+    static constexpr size_t q_bytes = (size_t)DEC_HEADS * HD * 2;
+    static constexpr size_t kv_bytes = (size_t)DEC_NC * HD * 2;   // one buffer
+    static constexpr size_t sp_bytes = (size_t)dec_warps<HD>() * DEC_HEADS * DEC_SPS * 4;
+    static constexpr size_t o_bytes = (size_t)DEC_HEADS * OSTR * 4;  // reuses the kv buffers
+    static constexpr size_t total = q_bytes + 2 * kv_bytes + sp_bytes + 2 * DEC_NC * 4 +
+                                    2 * DEC_HEADS * 4 + (size_t)DEC_STAGE * 4;
+    static_assert(o_bytes <= 2 * kv_bytes, "O staging must fit in the kv buffers");
+};
+
+template <int HD>
+__global__ void __launch_bounds__(32 * dec_warps<HD>()) sparse_attn_decode_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ rows_a, int64_t n_a,
+    const uint16_t* __restrict__ rows_b, int64_t n_c, const int32_t* __restrict__ idx, int K,
+    const float* __restrict__ sink, float scale_log2, uint16_t* __restrict__ o,
+    float* __restrict__ lse, int nh, unsigned int* status) {
+    namespace cg = cooperative_groups;
+    using SM = DecSmem<HD>;
+    constexpr int NW = dec_warps<HD>();
+    constexpr int DEC_THREADS = 32 * NW;
+    constexpr int CPR = HD / 8;
+    constexpr int QW = HD / NW;      // head-dim columns per warp
+    constexpr int NT = QW / 8;       // output n-tiles per warp
+    constexpr int OSTR = SM::OSTR;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint16_t* qs = reinterpret_cast<uint16_t*>(smem);
+    uint16_t* kvs = reinterpret_cast<uint16_t*>(smem + SM::q_bytes);
+    float* sp = reinterpret_cast<float*>(smem + SM::q_bytes + 2 * SM::kv_bytes);
+    int* vflag = reinterpret_cast<int*>(smem + SM::q_bytes + 2 * SM::kv_bytes + SM::sp_bytes);
+    float* stat = reinterpret_cast<float*>(vflag + 2 * DEC_NC);  // [2][16]: m then l
+    int* sidx = reinterpret_cast<int*>(stat + 2 * DEC_HEADS);      // [DEC_STAGE]
+    float* ostage = reinterpret_cast<float*>(kvs);                // [16][HD] after the loop
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t t = blockIdx.z;
+    const int h0 = blockIdx.y * DEC_HEADS;
+    const int64_t n_rows = n_a + n_c;
+    const int32_t* irow = idx + t * (int64_t)K;
+
+    // this CTA's slice of the index row
+    const int per = (K + CL - 1) / CL;
+    const int j0 = rank * per;
+    const int j1 = min(K, j0 + per);
+    const int nchunks = j1 > j0 ? (j1 - j0 + DEC_NC - 1) / DEC_NC : 0;
+
+    for (int id = tid; id < DEC_HEADS * CPR; id += DEC_THREADS) {
+        const int r = id / CPR, c = id % CPR;
+        const int h = h0 + r;
+        const bool live = h < nh;
+        const uint16_t* src = q + ((t * nh + (live ? h : 0)) * (int64_t)HD) + c * 8;
+        cp_async16(smem_u32(qs + r * HD + aswz(r, c) * 8), src, live);
+    }
+    // Everything above reads only q; the indices, the ring and the cache may
+    // come from the kernels just before this one.
+    pdl_wait();
+    // this slice's indices to shared memory first (one coalesced pass)
+    const int nst = max(0, min(j1 - j0, DEC_STAGE));
+    for (int j = tid; j < nst; j += DEC_THREADS) sidx[j] = irow[j0 + j];
+    __syncthreads();
+    auto load_chunk = [&](int chunk, int buf) {
+        uint16_t* dst = kvs + buf * (DEC_NC * HD);
+        for (int id = tid; id < DEC_NC * CPR; id += DEC_THREADS) {
+            const int r = id / CPR, c = id % CPR;
+            const int j = j0 + chunk * DEC_NC + r;
+            int64_t v = -1;
+            if (j - j0 < nst) v = sidx[j - j0];
+            else if (j < j1) v = irow[j];
+            const bool ok = v >= 0 && v < n_rows;
+            if (c == 0) {
+                if (j < j1 && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
+                vflag[buf * DEC_NC + r] = ok ? 1 : 0;
+            }
+            const uint16_t* src = rows_a;
+            if (ok) src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
+            cp_async16(smem_u32(dst + r * HD + aswz(r, c) * 8), src + c * 8, ok);
+        }
+    };
+
+    float oacc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; j++) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.0f;
+    float mrow[2] = {-INFINITY, -INFINITY};
+    float lrow[2] = {0.0f, 0.0f};
+    const int ra = lane >> 2, rb = ra + 8;
+
+    if (nchunks > 0) load_chunk(0, 0);
+    cp_async_commit();
+    for (int chunk = 0; chunk < nchunks; chunk++) {
+        const int buf = chunk & 1;
+        if (chunk + 1 < nchunks) load_chunk(chunk + 1, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const uint16_t* kv = kvs + buf * (DEC_NC * HD);
+        float sacc[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
+#pragma unroll 1
+        for (int kk = 0; kk < QW / 16; kk++) {
+            uint32_t a0, a1, a2, a3;
+            {
+                const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int c = warp * (QW / 8) + kk * 2 + (lane >> 4);
+                ldsm_x4(smem_u32(qs + r * HD + aswz(r, c) * 8), a0, a1, a2, a3);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; jj++) {
+                uint32_t b0, b1, b2, b3;
+                const int r = jj * 16 + (lane & 7) + (lane >> 4) * 8;
+                const int c = warp * (QW / 8) + kk * 2 + ((lane >> 3) & 1);
+                ldsm_x4(smem_u32(kv + r * HD + aswz(r, c) * 8), b0, b1, b2, b3);
+                mma_bf16(sacc[2 * jj], a0, a1, a2, a3, b0, b1);
+                mma_bf16(sacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        // partial scores of the NW slices of hd, summed in a fixed order by all
+        float* mine = sp + warp * (DEC_HEADS * DEC_SPS);
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int col = j * 8 + 2 * (lane & 3);
+            *reinterpret_cast<float2*>(mine + ra * DEC_SPS + col) = make_float2(sacc[j][0], sacc[j][1]);
+            *reinterpret_cast<float2*>(mine + rb * DEC_SPS + col) = make_float2(sacc[j][2], sacc[j][3]);
+        }
+        __syncthreads();
+        float sv[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int col = j * 8 + 2 * (lane & 3);
+            float2 xa = *reinterpret_cast<const float2*>(sp + ra * DEC_SPS + col);
+            float2 xb = *reinterpret_cast<const float2*>(sp + rb * DEC_SPS + col);
+#pragma unroll
+            for (int w = 1; w < NW; w++) {
+                const float2 ya = *reinterpret_cast<const float2*>(sp + w * DEC_HEADS * DEC_SPS + ra * DEC_SPS + col);
+                const float2 yb = *reinterpret_cast<const float2*>(sp + w * DEC_HEADS * DEC_SPS + rb * DEC_SPS + col);
+                xa.x += ya.x; xa.y += ya.y; xb.x += yb.x; xb.y += yb.y;
+            }
+            const bool v0 = vflag[buf * DEC_NC + col] != 0;
+            const bool v1 = vflag[buf * DEC_NC + col + 1] != 0;
+            sv[j][0] = v0 ? xa.x * scale_log2 : -INFINITY;
+            sv[j][1] = v1 ? xa.y * scale_log2 : -INFINITY;
+            sv[j][2] = v0 ? xb.x * scale_log2 : -INFINITY;
+            sv[j][3] = v1 ? xb.y * scale_log2 : -INFINITY;
+        }
+        float mx[2] = {mrow[0], mrow[1]};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            mx[0] = fmaxf(mx[0], fmaxf(sv[j][0], sv[j][1]));
+            mx[1] = fmaxf(mx[1], fmaxf(sv[j][2], sv[j][3]));
+        }
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+        }
+        float corr[2], muse[2];
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            muse[i] = (mx[i] == -INFINITY) ? 0.0f : mx[i];
+            corr[i] = exp2f(mrow[i] - muse[i]);
+            mrow[i] = mx[i];
+            lrow[i] *= corr[i];
+        }
+        uint32_t pa[2][4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float p0 = exp2f(sv[j][0] - muse[0]), p1 = exp2f(sv[j][1] - muse[0]);
+            const float p2 = exp2f(sv[j][2] - muse[1]), p3 = exp2f(sv[j][3] - muse[1]);
+            lrow[0] += p0 + p1;
+            lrow[1] += p2 + p3;
+            pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
+            pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; j++) {
+            oacc[j][0] *= corr[0];
+            oacc[j][1] *= corr[0];
+            oacc[j][2] *= corr[1];
+            oacc[j][3] *= corr[1];
+        }
+#pragma unroll
+        for (int ks = 0; ks < 2; ks++) {
+#pragma unroll
+            for (int jj = 0; jj < NT / 2; jj++) {
+                uint32_t b0, b1, b2, b3;
+                const int r = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int c = warp * (QW / 8) + jj * 2 + (lane >> 4);
+                ldsm_x4_t(smem_u32(kv + r * HD + aswz(r, c) * 8), b0, b1, b2, b3);
+                mma_bf16(oacc[2 * jj], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b0, b1);
+                mma_bf16(oacc[2 * jj + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b2, b3);
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        lrow[i] += __shfl_xor_sync(0xffffffffu, lrow[i], 1);
+        lrow[i] += __shfl_xor_sync(0xffffffffu, lrow[i], 2);
+    }
+    // stage (m, l) and the unnormalised O of this CTA
+    if (warp == 0 && (lane & 3) == 0) {
+        stat[ra] = mrow[0];
+        stat[rb] = mrow[1];
+        stat[DEC_HEADS + ra] = lrow[0];
+        stat[DEC_HEADS + rb] = lrow[1];
+    }
+#pragma unroll
+    for (int j = 0; j < NT; j++) {
+        const int col = warp * QW + j * 8 + 2 * (lane & 3);
+        *reinterpret_cast<float2*>(ostage + ra * OSTR + col) = make_float2(oacc[j][0], oacc[j][1]);
+        *reinterpret_cast<float2*>(ostage + rb * OSTR + col) = make_float2(oacc[j][2], oacc[j][3]);
+    }
+    cluster.sync();
+
+    // Every CTA gathers the cluster's (m, l) into its own shared memory and
+    // forms the per-(rank, head) weights e^{m_r - M} / L with the sink in L.
+    float* allst = sp;                        // [CL][32]
+    float* wts = sp + 16 * 2 * DEC_HEADS;     // [CL][16]
+    for (int i = tid; i < CL * 2 * DEC_HEADS; i += DEC_THREADS)
+        allst[i] = cluster.map_shared_rank(stat, i / (2 * DEC_HEADS))[i % (2 * DEC_HEADS)];
+    __syncthreads();
+    if (tid < DEC_HEADS) {
+        const int h = h0 + tid;
+        const float sk = (h < nh) ? sink[h] * LOG2E : -INFINITY;
+        float M = sk;
+        for (int r = 0; r < CL; r++) M = fmaxf(M, allst[r * 2 * DEC_HEADS + tid]);
+        const float Mref = (M == -INFINITY) ? 0.0f : M;
+        float L = exp2f(sk - Mref);
+        for (int r = 0; r < CL; r++)
+            L += allst[r * 2 * DEC_HEADS + DEC_HEADS + tid] *
+                 exp2f(allst[r * 2 * DEC_HEADS + tid] - Mref);
+        const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+        for (int r = 0; r < CL; r++)
+            wts[r * DEC_HEADS + tid] = exp2f(allst[r * 2 * DEC_HEADS + tid] - Mref) * inv;
+        if (lse && rank == 0 && h < nh) lse[t * nh + h] = (Mref + log2f(L)) / LOG2E;
+    }
+    __syncthreads();
+    // CTA `rank` reduces columns [c0, c0 + cols) of the 16 heads, 4 at a time.
+    const int cols = HD / CL;
+    const int c0 = rank * cols;
+    for (int e = tid; e < DEC_HEADS * (cols / 4); e += DEC_THREADS) {
+        const int hh = e / (cols / 4), c = c0 + 4 * (e % (cols / 4));
+        const int h = h0 + hh;
+        if (h >= nh) continue;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+        for (int r = 0; r < CL; r++) {
+            const float4 v = *reinterpret_cast<const float4*>(
+                cluster.map_shared_rank(ostage, r) + hh * OSTR + c);
+            const float wgt = wts[r * DEC_HEADS + hh];
+            acc.x += v.x * wgt;
+            acc.y += v.y * wgt;
+            acc.z += v.z * wgt;
+            acc.w += v.w * wgt;
+        }
+        uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        *reinterpret_cast<uint2*>(o + (t * nh + h) * (int64_t)HD + c) = packed;
+    }
+    cluster.sync();  // keep this CTA's shared memory alive until all readers are done
+}
+
 struct AttnPlan {
     int splits, chunks_per_split, head_groups;
+    int cluster;  // > 0: the few-token path with this many CTAs per cluster
     size_t part_o_bytes, part_ml_bytes;
 };
 
@@ -312,6 +612,20 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static AttnPlan plan_attn(int64_t m, int64_t nh, int64_t hd, int64_t K, int sms) {
     AttnPlan p;
+    p.cluster = 0;
+    // Few tokens: one cluster per (token, 16 heads) when that leaves most SMs
+    // to the row slices; no scratch, no merge launch.
+    const int64_t dec_groups = m * ((nh + DEC_HEADS - 1) / DEC_HEADS);
+    if (dec_groups * 4 <= sms) {
+        int cl = 16;
+        while (cl > 1 && (dec_groups * cl > 2 * sms || (K + cl - 1) / cl < 8)) cl >>= 1;
+        p.cluster = cl;
+        p.splits = 1;
+        p.chunks_per_split = 0;
+        p.head_groups = (int)((nh + DEC_HEADS - 1) / DEC_HEADS);
+        p.part_o_bytes = p.part_ml_bytes = 0;
+        return p;
+    }
     p.head_groups = (int)((nh + ATT_HEADS - 1) / ATT_HEADS);
     const int chunks = (int)((K + ATT_NC - 1) / ATT_NC);
     const int64_t ctas = m * p.head_groups;
@@ -339,10 +653,45 @@ static int device_sms() {
 }
 
 template <int HD>
+static int launch_attn_decode(const AttnPlan& p, const uint16_t* q, const uint16_t* rows_a,
+                              int64_t n_a, const uint16_t* rows_b, int64_t n_c,
+                              const int32_t* idx, int64_t K, const float* sink, float scale,
+                              uint16_t* o, float* lse, int64_t m, int64_t nh,
+                              unsigned int* status, cudaStream_t st, bool pdl) {
+    const size_t smem = DecSmem<HD>::total;
+    auto kern = sparse_attn_decode_kernel<HD>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (p.cluster > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.cluster, (unsigned)p.head_groups, (unsigned)m);
+    cfg.blockDim = dim3(32 * dec_warps<HD>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    int rc = cuda_check(cudaLaunchKernelEx(&cfg, kern, q, rows_a, n_a, rows_b, n_c, idx, (int)K,
+                                           sink, scale * LOG2E, o, lse, (int)nh, status),
+                        "ds41_sparse_attn_sink_fwd: decode kernel");
+    if (rc) return rc;
+    return launch_check("ds41_sparse_attn_sink_fwd: decode kernel");
+}
+
+template <int HD>
 static int launch_attn(const AttnPlan& p, const uint16_t* q, const uint16_t* rows_a, int64_t n_a,
                        const uint16_t* rows_b, int64_t n_c, const int32_t* idx, int64_t K,
                        const float* sink, float scale, uint16_t* o, float* lse, int64_t m,
-                       int64_t nh, uint8_t* ws, unsigned int* status, cudaStream_t st) {
+                       int64_t nh, uint8_t* ws, unsigned int* status, cudaStream_t st,
+                       bool pdl = false) {
+    if (p.cluster > 0)
+        return launch_attn_decode<HD>(p, q, rows_a, n_a, rows_b, n_c, idx, K, sink, scale, o, lse,
+                                      m, nh, status, st, pdl);
     const size_t smem = AttnSmem<HD>::total;
     auto kern = sparse_attn_kernel<HD>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -409,6 +758,45 @@ extern "C" int ds41_sparse_attn_sink_fwd(const ds41_bf16* q, const ds41_bf16* ro
         default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, wsb, status, st);
     }
 }
+
+// ---------------------------------------------------------------------------
+// Internal entry for the fused step (ds41_forward.cu): arguments already
+// checked by the caller.
+// ---------------------------------------------------------------------------
+namespace ds41 {
+
+size_t attn_ws_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K) {
+    if (m < 1 || nh < 1 || hd < 1 || K < 1) return 0;
+    AttnPlan p = plan_attn(m, nh, hd, K, device_sms());
+    return p.part_o_bytes + p.part_ml_bytes;
+}
+
+int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint16_t* rows_b,
+             int64_t n_c, const int32_t* idx, int64_t K, const float* sink, float scale,
+             uint16_t* o, float* lse, int64_t m, int64_t nh, int64_t hd, uint8_t* ws,
+             size_t ws_bytes, bool pdl, cudaStream_t st, const char* name) {
+    unsigned int* status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    AttnPlan p = plan_attn(m, nh, hd, K, device_sms());
+    const size_t need = p.part_o_bytes + p.part_ml_bytes;
+    DS41_REQUIRE(need == 0 || (ws && ws_bytes >= need), DS41_E_WORKSPACE,
+                 "%s: workspace of %zu bytes needed, %zu given", name, need, ws ? ws_bytes : 0);
+    const uint16_t* ra = n_a ? rows_a : rows_b;
+    const uint16_t* rb = n_c ? rows_b : rows_a;
+    switch (hd) {
+        case 64: return launch_attn<64>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl);
+        case 128: return launch_attn<128>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl);
+        case 256: return launch_attn<256>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl);
+        default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl);
+    }
+}
+
+bool attn_is_cluster_path(int64_t m, int64_t nh, int64_t hd, int64_t K) {
+    return plan_attn(m, nh, hd, K, device_sms()).cluster > 0;
+}
+
+}  // namespace ds41
 
 // ---------------------------------------------------------------------------
 // The same attention for callers that cannot allocate device memory.  The

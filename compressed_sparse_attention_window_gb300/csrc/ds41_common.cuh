@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -106,6 +107,56 @@ __device__ __forceinline__ float fp4_elem(float v, float s, uint32_t* code) {
     return __fmul_rn(e2m1_val(c), s);
 }
 
+// The same element path for a power-of-two scale s with rs = 1/s (exact for
+// a power of two, subnormal results included): v * rs rounds exactly as v / s.
+__device__ __forceinline__ float fp4_elem_pow2(float v, float s, float rs, uint32_t* code) {
+    float t = __fmul_rn(v, rs);
+    t = fminf(fmaxf(t, -6.0f), 6.0f);
+    const uint32_t c = e2m1_code(t);
+    *code = c;
+    return __fmul_rn(e2m1_val(c), s);
+}
+
+// Hardware e2m1 conversion: two f32 values -> two 4-bit codes (round to
+// nearest, ties to the even code, saturating at +-6; a negative value that
+// rounds to zero keeps its sign).  The first value lands in the low nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+    uint16_t r;
+    asm("{\n.reg .b8 b0;\ncvt.rn.satfinite.e2m1x2.f32 b0, %1, %2;\nmov.b16 %0, {b0, b0};\n}"
+        : "=h"(r)
+        : "f"(hi), "f"(lo));
+    return (uint32_t)(r & 0xffu);
+}
+
+// Two e2m1 codes (one byte, first element in the low nibble) -> their exact
+// values as two floats.
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
+    uint32_t h2;
+    const uint16_t in = (uint16_t)(byte & 0xffu);
+    asm("{\n.reg .b8 b0, b1;\nmov.b16 {b0, b1}, %1;\ncvt.rn.f16x2.e2m1x2 %0, b0;\n}"
+        : "=r"(h2)
+        : "h"(in));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// The fp4 round trip of 8 values t[] already divided by their block scale s:
+// codes (element k in nibble k) and bf16(e2m1(t) * s) packed in a uint4.
+// |t| > 6 saturates to 6, which is what clamping first and rounding gives.
+__device__ __forceinline__ uint4 e2m1_round8(const float t[8], float s, uint32_t* codes) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) c |= cvt_e2m1x2(t[k], t[k + 1]) << (4 * k);
+    uint4 out;
+    uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+        const float2 g = e2m1x2_to_float2(c >> (4 * k));
+        o[k / 2] = (uint32_t)f2bf(__fmul_rn(g.x, s)) | ((uint32_t)f2bf(__fmul_rn(g.y, s)) << 16);
+    }
+    *codes = c;
+    return out;
+}
+
 // ---------------------------------------------------------------------------
 // Vector loads / stores and async copies
 // ---------------------------------------------------------------------------
@@ -149,6 +200,16 @@ __device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uin
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const uint32_t l = f2bf(lo), h = f2bf(hi);
     return l | (h << 16);
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor on the stream finishes;
+// pdl_wait() blocks until the predecessor has completed and its writes are
+// visible (a no-op without such a predecessor), pdl_trigger() lets the next
+// kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Raise a DS41_E_* code in the device status word (first error wins).

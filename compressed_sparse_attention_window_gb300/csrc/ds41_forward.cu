@@ -1,0 +1,127 @@
+// ds41_forward.cu - the whole step of one layer's compressed sparse attention
+// forward in one call: window ring + window indices, latent write, indexer
+// scores + top-k + merge, sparse attention with the sink.
+//
+// metrale_model_arch/attn_v41/forward.rs, AttnV41::forward runs these steps
+// in this order for m tokens at start_pos; metrale_model_arch/
+// deepseek_v41_ref/compress.rs, attention_any does the same on the CPU.
+//
+// Few-token calls (decode) take three launches: (1) one grid whose CTAs
+// compute the indexer scores while its last CTA writes the ring, the window
+// indices and the latent rows (these are independent of each other); (2)
+// the top-k + merge; (3) the cluster attention.  (2) and (3) are launched
+// with programmatic stream serialization, so each starts while its
+// predecessor finishes and waits on the device (griddepcontrol) only where it
+// reads the predecessor's output.  Larger calls run the four entry points in
+// sequence.
+#include "ds41_internal.cuh"
+#include "ds41_step1.cuh"
+
+using namespace ds41;
+
+static int64_t ctopk_of(int64_t topk, int64_t n_c) { return n_c == 0 ? 0 : (topk < n_c ? topk : n_c); }
+
+static bool use_fused(int64_t m, int64_t start_pos, int64_t nh, int64_t hd, int64_t win,
+                      int64_t ratio, int64_t topk, int64_t Hi, int64_t Di) {
+    const int64_t n_c = (start_pos + m) / ratio;
+    if (n_c < 1) return false;
+    const int64_t K = win + ctopk_of(topk, n_c);
+    return front_fusable(m, Hi, Di, n_c) && attn_is_cluster_path(m, nh, hd, K);
+}
+
+extern "C" size_t ds41_csa_workspace_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_t hd,
+                                           int64_t win, int64_t ratio, int64_t topk, int64_t Hi,
+                                           int64_t Di) {
+    if (m < 1 || ratio < 1 || win < 1) return 0;
+    const int64_t n_c = (start_pos + m) / ratio;
+    const int64_t K = win + ctopk_of(topk, n_c);
+    size_t a = 0;
+    if (n_c > 0) {
+        a = use_fused(m, start_pos, nh, hd, win, ratio, topk, Hi, Di)
+                ? front_scores_bytes(m, n_c)
+                : ds41_indexer_workspace_bytes(m, Hi, Di, n_c, 0);
+    }
+    const size_t b = attn_ws_bytes(m, nh, hd, K);
+    return a > b ? a : b;
+}
+
+extern "C" int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring,
+                                ds41_bf16* rows_a, const ds41_bf16* latent,
+                                const float* freqs_cis, int64_t max_pos, ds41_bf16* cache,
+                                int64_t cache_rows, const ds41_bf16* q_idx,
+                                const ds41_bf16* k_idx, const float* w, const float* sink,
+                                float scale, int32_t* win_idx, int32_t* idx, ds41_bf16* o,
+                                float* lse, int64_t m, int64_t start_pos, int64_t nh, int64_t hd,
+                                int64_t rd, int64_t win, int64_t ratio, int64_t topk, int64_t Hi,
+                                int64_t Di, void* ws, size_t ws_bytes, ds41_stream_t stream) {
+    const char* name = "ds41_csa_forward";
+    DS41_REQUIRE(m >= 1 && m < (int64_t(1) << 31), DS41_E_RANGE, "%s: m=%lld", name,
+                 (long long)m);
+    DS41_REQUIRE(start_pos >= 0 && start_pos + m < (int64_t(1) << 31), DS41_E_RANGE,
+                 "%s: start_pos=%lld", name, (long long)start_pos);
+    DS41_REQUIRE(ratio >= 1 && win >= 1 && topk >= 1, DS41_E_ARG,
+                 "%s: ratio=%lld win=%lld topk=%lld", name, (long long)ratio, (long long)win,
+                 (long long)topk);
+    const int64_t n_c = (start_pos + m) / ratio;
+    const int64_t G = n_c - start_pos / ratio;
+    const int64_t ctopk = ctopk_of(topk, n_c);
+    const int64_t K = win + ctopk;
+    const int64_t n_a = ds41_rows_a_len(m, win, start_pos);
+    const size_t need = ds41_csa_workspace_bytes(m, start_pos, nh, hd, win, ratio, topk, Hi, Di);
+    DS41_REQUIRE(need == 0 || (ws && ws_bytes >= need), DS41_E_WORKSPACE,
+                 "%s: workspace of %zu bytes needed, %zu given", name, need, ws ? ws_bytes : 0);
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool chunk = start_pos > 0 && m > 1;
+    const ds41_bf16* rows_a_used = start_pos == 0 ? kv : (m == 1 ? ring : rows_a);
+
+    if (!use_fused(m, start_pos, nh, hd, win, ratio, topk, Hi, Di)) {
+        int rc = ds41_window_ring_write(kv, ring, rows_a, win_idx, nullptr, m, hd, win, start_pos,
+                                        stream);
+        if (rc) return rc;
+        if (G > 0) {
+            rc = ds41_compress_latent_write(latent, freqs_cis, max_pos, cache, cache_rows, nullptr,
+                                            nullptr, G, hd, rd, ratio, start_pos, m, stream);
+            if (rc) return rc;
+        }
+        const int32_t* att_idx = win_idx;
+        if (n_c > 0) {
+            rc = ds41_indexer_topk(q_idx, k_idx, w, win_idx, idx, nullptr, m, Hi, Di, n_c, win,
+                                   ratio, start_pos, topk, n_a, ws, ws_bytes, stream);
+            if (rc) return rc;
+            att_idx = idx;
+        }
+        return ds41_sparse_attn_sink_fwd(q, rows_a_used, n_a, n_c ? cache : nullptr, n_c, att_idx,
+                                         K, sink, scale, o, lse, m, nh, hd, ws, ws_bytes, stream);
+    }
+
+    // ---- few-token fused path: the same checks the separate entry points make
+    DS41_REQUIRE(hd >= 64 && hd <= 512 && (hd & (hd - 1)) == 0, DS41_E_ARG,
+                 "%s: hd=%lld must be 64, 128, 256 or 512", name, (long long)hd);
+    DS41_REQUIRE(nh >= 1 && rd > 0 && rd % 2 == 0 && rd <= hd, DS41_E_ARG, "%s: nh=%lld rd=%lld",
+                 name, (long long)nh, (long long)rd);
+    DS41_REQUIRE(n_c <= cache_rows, DS41_E_RANGE, "%s: cache holds %lld rows, need %lld", name,
+                 (long long)cache_rows, (long long)n_c);
+    DS41_REQUIRE(G == 0 || start_pos + m <= max_pos, DS41_E_RANGE,
+                 "%s: RoPE table has %lld rows, need %lld", name, (long long)max_pos,
+                 (long long)(start_pos + m));
+    DS41_REQUIRE(q && kv && ring && cache && q_idx && k_idx && w && sink && win_idx && idx && o &&
+                     (G == 0 || (latent && freqs_cis)) && (!chunk || rows_a),
+                 DS41_E_ARG, "%s: null tensor pointer", name);
+    DS41_REQUIRE(aligned16(q) && aligned16(kv) && aligned16(ring) && aligned16(cache) &&
+                     aligned16(q_idx) && aligned16(k_idx) && aligned16(o) &&
+                     (G == 0 || (aligned16(latent) && aligned16(freqs_cis))) &&
+                     (!chunk || aligned16(rows_a)) && aligned16(ws),
+                 DS41_E_ARG, "%s: pointers must be 16-byte aligned", name);
+    RingArgs ra{reinterpret_cast<const uint4*>(kv), reinterpret_cast<uint4*>(ring),
+                reinterpret_cast<uint4*>(rows_a), win_idx, m, hd / 8, win, start_pos, chunk};
+    LatentArgs la{reinterpret_cast<const uint4*>(latent),
+                  reinterpret_cast<const float2*>(freqs_cis), reinterpret_cast<uint4*>(cache),
+                  nullptr, nullptr, (int)hd, (int)rd, (int)G, start_pos / ratio, ratio};
+    uint16_t* scores = static_cast<uint16_t*>(ws);
+    int rc = launch_front(q_idx, k_idx, w, scores, m, Hi, Di, n_c, ratio, start_pos, ra, la, st);
+    if (rc) return rc;
+    rc = launch_topk(scores, win_idx, idx, m, n_c, win, ctopk, ratio, start_pos, n_a, true, st);
+    if (rc) return rc;
+    return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
+                    nullptr, 0, true, st, name);
+}

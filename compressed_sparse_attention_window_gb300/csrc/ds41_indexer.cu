@@ -14,13 +14,14 @@
 // scales stay within a moderate range, so the tensor-core sum equals the
 // ordered sum bit for bit; the head sum is an explicit fma chain in head
 // order, identical on every architecture.
-#include "ds41_common.cuh"
+#include "ds41_internal.cuh"
+#include "ds41_step1.cuh"
 
 namespace ds41 {
 
 constexpr int IDX_ROWS = 64;     // compressed rows per tile (16 per warp)
 constexpr int IDX_N = 128;       // (token, head) columns per CTA
-constexpr int IDX_THREADS = 128;
+constexpr int IDX_THREADS = 256;
 
 template <int CPR>
 __device__ __forceinline__ int swz(int n, int c) {
@@ -44,14 +45,11 @@ __device__ __forceinline__ uint4 q8_chunk(uint4 raw, bool live) {
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
     const float s = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
-    uint4 out;
-    uint16_t* o = reinterpret_cast<uint16_t*>(&out);
+    const float rs = __frcp_rn(s);  // exact: s is a power of two
 #pragma unroll
-    for (int k = 0; k < 8; k++) {
-        uint32_t c;
-        o[k] = f2bf(fp4_elem(v[k], s, &c));
-    }
-    return out;
+    for (int k = 0; k < 8; k++) v[k] = __fmul_rn(v[k], rs);
+    uint32_t codes;
+    return e2m1_round8(v, s, &codes);
 }
 
 __device__ __forceinline__ int64_t visible_rows(int64_t t, int64_t start_pos, int64_t ratio,
@@ -70,8 +68,21 @@ template <int DI, bool KQ_INLINE>
 __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_src,
     const float* __restrict__ w, uint16_t* __restrict__ scores, int m, int Hi, int hpad, int TT,
-    int64_t n_c, int64_t ratio, int64_t start_pos, bool fill_hidden) {
+    int64_t n_c, int64_t ratio, int64_t start_pos, bool fill_hidden, int ymain, RingArgs ring,
+    LatentArgs lat) {
     constexpr int CPR = DI / 8;  // 16-byte chunks per row
+    pdl_trigger();  // the next kernel may start launching (it waits for this one)
+    if ((int)blockIdx.y >= ymain) {
+        // Fused front of a few-token step: the CTAs past the score grid do
+        // step 1 (ring write + window indices, then the latent groups).
+        const int side = (int)(blockIdx.y - ymain) * gridDim.x + blockIdx.x;
+        const int nside = (int)(gridDim.y - ymain) * gridDim.x;
+        if (side == 0) ring_write_cta(ring);
+        const int hd8 = lat.hd / 8;
+        for (int g = side; g < lat.G; g += nside)
+            for (int k0 = 0; k0 < hd8; k0 += IDX_THREADS) latent_write_item(lat, g, k0 + threadIdx.x);
+        return;
+    }
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* qs = reinterpret_cast<uint16_t*>(smem);                 // [IDX_N][DI]
     uint16_t* ks = qs + IDX_N * DI;                                    // [IDX_ROWS][DI]
@@ -82,21 +93,29 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     const int t0 = blockIdx.x * TT;
     const int tcount = min(TT, m - t0);
 
-    // q of this CTA's tokens, quantised, as rows n = tt * hpad + h.
+    // q of this CTA's tokens as rows n = tt * hpad + h: staged raw with
+    // cp.async (padding rows zero-filled), then quantised in place.  The
+    // quantisation loop stays rolled: a decode call runs this code once per
+    // SM, so compact code (fewer instruction-cache misses) beats unrolling.
     for (int id = tid; id < IDX_N * CPR; id += IDX_THREADS) {
         const int n = id / CPR, c = id % CPR;
         const int tt = n / hpad, h = n % hpad;
         const bool live = tt < tcount && h < Hi;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (live)
-            raw = reinterpret_cast<const uint4*>(q_idx + ((int64_t)(t0 + tt) * Hi + h) * DI)[c];
-        uint4 qv = q8_chunk(raw, live);
-        if (!live) qv = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qs + n * DI + swz<CPR>(n, c) * 8) = qv;
+        const uint16_t* src = q_idx + ((int64_t)(t0 + (live ? tt : 0)) * Hi + (live ? h : 0)) * DI;
+        cp_async16(smem_u32(qs + n * DI + swz<CPR>(n, c) * 8), src + c * 8, live);
     }
+    cp_async_commit();
     for (int n = tid; n < IDX_N; n += IDX_THREADS) {
         const int tt = n / hpad, h = n % hpad;
         wsm[n] = (tt < tcount && h < Hi) ? w[(int64_t)(t0 + tt) * Hi + h] : 0.0f;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+#pragma unroll 1
+    for (int id = tid; id < IDX_N * CPR; id += IDX_THREADS) {
+        const int n = id / CPR, c = id % CPR;
+        uint4* p = reinterpret_cast<uint4*>(qs + n * DI + swz<CPR>(n, c) * 8);
+        *p = q8_chunk(*p, true);
     }
 
     const int64_t vis_last = visible_rows(t0 + tcount - 1, start_pos, ratio, n_c);
@@ -105,7 +124,7 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     // group can see yet are written as -inf too.
     const int64_t tiles = fill_hidden ? (n_c + IDX_ROWS - 1) / IDX_ROWS : tiles_vis;
 
-    for (int64_t tile = blockIdx.y; tile < tiles; tile += gridDim.y) {
+    for (int64_t tile = blockIdx.y; tile < tiles; tile += ymain) {
         const int64_t r0 = tile * IDX_ROWS;
         if (tile >= tiles_vis) {
             for (int p = tid; p < IDX_ROWS * tcount; p += IDX_THREADS) {
@@ -119,39 +138,42 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             const int r = id / CPR, c = id % CPR;
             const int64_t row = r0 + r;
             const bool live = row < n_c;
-            uint16_t* dst = ks + r * DI + swz<CPR>(r, c) * 8;
-            if (KQ_INLINE) {
-                uint4 raw = make_uint4(0, 0, 0, 0);
-                if (live) raw = reinterpret_cast<const uint4*>(k_src + row * DI)[c];
-                uint4 kv = q8_chunk(raw, live);
-                if (!live) kv = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(dst) = kv;
-            } else {
-                cp_async16(smem_u32(dst), k_src + (live ? row : 0) * DI + c * 8, live);
-            }
+            cp_async16(smem_u32(ks + r * DI + swz<CPR>(r, c) * 8),
+                       k_src + (live ? row : 0) * DI + c * 8, live);
         }
-        if (!KQ_INLINE) {
-            cp_async_commit();
-            cp_async_wait<0>();
-        }
+        cp_async_commit();
+        cp_async_wait<0>();
         __syncthreads();
+        if (KQ_INLINE) {
+            // raw keys -> fp4 round trip, in place (rows past n_c are zero)
+#pragma unroll 1
+            for (int id = tid; id < IDX_ROWS * CPR; id += IDX_THREADS) {
+                const int r = id / CPR, c = id % CPR;
+                uint4* p = reinterpret_cast<uint4*>(ks + r * DI + swz<CPR>(r, c) * 8);
+                *p = q8_chunk(*p, true);
+            }
+            __syncthreads();
+        }
 
-        float acc[IDX_N / 8][4];
+        // 8 warps: warp w owns rows 16*(w%4).. and columns 64*(w/4)..
+        constexpr int WN = IDX_N / 2;  // columns per warp
+        const int wr = (warp & 3) * 16, wc = (warp >> 2) * WN;
+        float acc[WN / 8][4];
 #pragma unroll
-        for (int j = 0; j < IDX_N / 8; j++)
+        for (int j = 0; j < WN / 8; j++)
             acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < DI / 16; kk++) {
             uint32_t a0, a1, a2, a3;
             {
-                const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int r = wr + (lane & 7) + ((lane >> 3) & 1) * 8;
                 const int c = kk * 2 + (lane >> 4);
                 ldsm_x4(smem_u32(ks + r * DI + swz<CPR>(r, c) * 8), a0, a1, a2, a3);
             }
 #pragma unroll
-            for (int jj = 0; jj < IDX_N / 16; jj++) {
+            for (int jj = 0; jj < WN / 16; jj++) {
                 uint32_t b0, b1, b2, b3;
-                const int n = jj * 16 + (lane & 7) + (lane >> 4) * 8;
+                const int n = wc + jj * 16 + (lane & 7) + (lane >> 4) * 8;
                 const int c = kk * 2 + ((lane >> 3) & 1);
                 ldsm_x4(smem_u32(qs + n * DI + swz<CPR>(n, c) * 8), b0, b1, b2, b3);
                 mma_bf16(acc[2 * jj], a0, a1, a2, a3, b0, b1);
@@ -159,9 +181,9 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             }
         }
 #pragma unroll
-        for (int j = 0; j < IDX_N / 8; j++) {
-            const int r = warp * 16 + (lane >> 2);
-            const int col = j * 8 + 2 * (lane & 3);
+        for (int j = 0; j < WN / 8; j++) {
+            const int r = wr + (lane >> 2);
+            const int col = wc + j * 8 + 2 * (lane & 3);
             cs[r * (IDX_N + 1) + col] = acc[j][0];
             cs[r * (IDX_N + 1) + col + 1] = acc[j][1];
             cs[(r + 8) * (IDX_N + 1) + col] = acc[j][2];
@@ -200,38 +222,102 @@ __device__ __forceinline__ uint32_t order_key(uint16_t b) {
     return (b & 0x8000u) ? (uint32_t)(~b & 0xffffu) : (uint32_t)(b | 0x8000u);
 }
 
-// Block-wide exclusive prefix count of a per-thread flag (blockDim multiple of
-// 32, <= 1024).  Returns this thread's rank; *total gets the block total.
-__device__ __forceinline__ int block_rank(bool flag, int* wsum, int* total) {
+// Block-wide exclusive prefix sums of two per-thread counts (blockDim a
+// multiple of 32, <= 1024).  wsum needs 2 * 32 ints.
+__device__ __forceinline__ void block_scan2(int a, int b, int* a_before, int* b_before,
+                                            int* wsum) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const unsigned bal = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    __syncthreads();
-    if (lane == 0) wsum[warp] = __popc(bal);
-    __syncthreads();
-    if (warp == 0) {
-        int v = lane < nw ? wsum[lane] : 0;
-        int incl = v;
+    int ia = a, ib = b;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int oa = __shfl_up_sync(0xffffffffu, ia, off);
+        const int ob = __shfl_up_sync(0xffffffffu, ib, off);
+        if (lane >= off) {
+            ia += oa;
+            ib += ob;
         }
-        if (lane < nw) wsum[lane] = incl - v;
-        if (lane == 31) wsum[32] = incl;
+    }
+    if (lane == 31) {
+        wsum[warp] = ia;
+        wsum[32 + warp] = ib;
     }
     __syncthreads();
-    *total = wsum[32];
-    return wsum[warp] + in_warp;
+    if (warp == 0) {
+        const int va = lane < nw ? wsum[lane] : 0;
+        const int vb = lane < nw ? wsum[32 + lane] : 0;
+        int xa = va, xb = vb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int oa = __shfl_up_sync(0xffffffffu, xa, off);
+            const int ob = __shfl_up_sync(0xffffffffu, xb, off);
+            if (lane >= off) {
+                xa += oa;
+                xb += ob;
+            }
+        }
+        if (lane < nw) {
+            wsum[lane] = xa - va;
+            wsum[32 + lane] = xb - vb;
+        }
+    }
+    __syncthreads();
+    *a_before = wsum[warp] + ia - a;
+    *b_before = wsum[32 + warp] + ib - b;
 }
+
+// Warp 0: the bucket b (of 256) holding the kk-th largest key, counting
+// `above` keys already known to be larger; *bucket = b, *cum = above + keys
+// in buckets above b.  Lane l owns buckets 8l .. 8l+7.
+__device__ __forceinline__ void find_bucket(const int* hist, int kk, int above, int* bucket,
+                                            int* cum) {
+    const int lane = threadIdx.x & 31;
+    int v[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        v[i] = hist[8 * lane + i];
+        sum += v[i];
+    }
+    // keys in the buckets of lanes l .. 31
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32) incl += o;
+    }
+    int c = above + incl - sum;  // keys in buckets of higher lanes
+    const bool mine = (c < kk && c + sum >= kk) || (lane == 0 && c + sum < kk);
+    if (mine) {
+        int b = 8 * lane + 7;
+#pragma unroll
+        for (int i = 7; i > 0; i--, b--) {
+            if (c + v[i] >= kk) break;
+            c += v[i];
+        }
+        *bucket = b;
+        *cum = c;
+    }
+}
+
+// Keys of the visible scores, staged in shared memory when they fit
+// (keys_cap entries), read from global memory otherwise.
+struct KeySrc {
+    const uint16_t* g;
+    const uint16_t* s;
+    __device__ __forceinline__ uint32_t operator()(int64_t i) const {
+        return s ? (uint32_t)s[i] : order_key(g[i]);
+    }
+};
 
 __global__ void __launch_bounds__(1024) topk_merge_kernel(
     const uint16_t* __restrict__ scores, const int32_t* __restrict__ win_idx,
     int32_t* __restrict__ idx, int64_t n_c, int win, int ctopk, int64_t ratio, int64_t start_pos,
-    int64_t offset) {
+    int64_t offset, int keys_cap) {
+    extern __shared__ __align__(16) uint16_t skeys[];
     __shared__ int hist[256];
-    __shared__ int wsum[33];
+    __shared__ int wsum[64];
     __shared__ int sel[4];
+    pdl_wait();     // the scores (and window indices) come from the previous kernel
+    pdl_trigger();
     const int t = blockIdx.x;
     const int K = win + ctopk;
     int32_t* out = idx + (int64_t)t * K;
@@ -244,21 +330,28 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(
             out[win + j] = (j < vis) ? (int32_t)(offset + j) : -1;
         return;
     }
+    KeySrc key{sc, nullptr};
+    if (vis <= keys_cap) {
+        // 8 scores per 16-byte load when the row is aligned, else one by one
+        const bool vec = ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0);
+        const int64_t n8 = vec ? vis / 8 : 0;
+        for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) {
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(sc) + i);
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+            for (int e = 0; e < 8; e++) skeys[i * 8 + e] = (uint16_t)order_key(h[e]);
+        }
+        for (int64_t i = n8 * 8 + threadIdx.x; i < vis; i += blockDim.x)
+            skeys[i] = (uint16_t)order_key(sc[i]);
+        __syncthreads();
+        key.s = skeys;
+    }
     // pass 1: high byte
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int64_t s = threadIdx.x; s < vis; s += blockDim.x)
-        atomicAdd(&hist[order_key(sc[s]) >> 8], 1);
+    for (int64_t s = threadIdx.x; s < vis; s += blockDim.x) atomicAdd(&hist[key(s) >> 8], 1);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int cum = 0, b = 255;
-        for (; b > 0; b--) {
-            if (cum + hist[b] >= kk) break;
-            cum += hist[b];
-        }
-        sel[0] = b;
-        sel[1] = cum;  // keys in higher buckets
-    }
+    if (threadIdx.x < 32) find_bucket(hist, kk, 0, &sel[0], &sel[1]);
     __syncthreads();
     const uint32_t hb = (uint32_t)sel[0];
     const int above1 = sel[1];
@@ -267,37 +360,36 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     for (int64_t s = threadIdx.x; s < vis; s += blockDim.x) {
-        const uint32_t k = order_key(sc[s]);
+        const uint32_t k = key(s);
         if ((k >> 8) == hb) atomicAdd(&hist[k & 0xffu], 1);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int cum = above1, b = 255;
-        for (; b > 0; b--) {
-            if (cum + hist[b] >= kk) break;
-            cum += hist[b];
-        }
-        sel[2] = b;
-        sel[3] = cum;  // keys strictly above T
-    }
+    if (threadIdx.x < 32) find_bucket(hist, kk, above1, &sel[2], &sel[3]);
     __syncthreads();
     const uint32_t T = (hb << 8) | (uint32_t)sel[2];
     const int need_eq = kk - sel[3];
-    // pass 3: ordered selection
-    int base_out = 0, base_eq = 0;
-    for (int64_t s0 = 0; s0 < vis; s0 += blockDim.x) {
-        const int64_t s = s0 + threadIdx.x;
-        const uint32_t k = (s < vis) ? order_key(sc[s]) : 0u;
-        const bool gt = (s < vis) && k > T;
-        const bool eq = (s < vis) && k == T;
-        int n_eq;
-        const int r_eq = block_rank(eq, wsum, &n_eq);
-        const bool take = gt || (eq && base_eq + r_eq < need_eq);
-        int n_take;
-        const int r_take = block_rank(take, wsum, &n_take);
-        if (take && base_out + r_take < kk) out[win + base_out + r_take] = (int32_t)(offset + s);
-        base_out += n_take;
-        base_eq += n_eq;
+    // pass 3: each thread takes a contiguous segment of the visible keys and
+    // counts the keys above T and equal to T; one block scan turns the counts
+    // into output offsets (the equal keys taken are the lowest-numbered
+    // need_eq of them), and every segment is written in ascending row order.
+    const int64_t seg = (vis + blockDim.x - 1) / blockDim.x;
+    const int64_t s_lo = min(vis, (int64_t)threadIdx.x * seg);
+    const int64_t s_hi = min(vis, s_lo + seg);
+    int n_gt = 0, n_eq = 0;
+    for (int64_t s = s_lo; s < s_hi; s++) {
+        const uint32_t k = key(s);
+        n_gt += k > T;
+        n_eq += k == T;
+    }
+    int gt_before, eq_before;
+    block_scan2(n_gt, n_eq, &gt_before, &eq_before, wsum);
+    int pos = gt_before + min(eq_before, need_eq);
+    int eq_rank = eq_before;
+    for (int64_t s = s_lo; s < s_hi; s++) {
+        const uint32_t k = key(s);
+        bool take = k > T;
+        if (k == T) take = eq_rank++ < need_eq;
+        if (take && pos < kk) out[win + pos++] = (int32_t)(offset + s);
     }
     for (int j = kk + threadIdx.x; j < ctopk; j += blockDim.x) out[win + j] = -1;
 }
@@ -325,7 +417,8 @@ static IndexerPlan plan_indexer(int64_t m, int64_t Hi, int64_t Di, int64_t n_c, 
 template <int DI>
 static int launch_scores(const IndexerPlan& p, const uint16_t* q, const uint16_t* k, const float* w,
                          uint16_t* scores, int64_t m, int64_t Hi, int64_t n_c, int64_t ratio,
-                         int64_t start_pos, bool fill_hidden, cudaStream_t st) {
+                         int64_t start_pos, bool fill_hidden, cudaStream_t st,
+                         const RingArgs* ring = nullptr, const LatentArgs* lat = nullptr) {
     const size_t smem = (size_t)IDX_N * DI * 2 + (size_t)IDX_ROWS * DI * 2 +
                         (size_t)IDX_ROWS * (IDX_N + 1) * 4 + IDX_N * 4;
     // Row-tile splits: enough CTAs to cover the GPU when there are few tokens.
@@ -336,17 +429,20 @@ static int launch_scores(const IndexerPlan& p, const uint16_t* q, const uint16_t
     int64_t ysplit = (2 * (int64_t)sms + p.groups - 1) / p.groups;
     if (ysplit > tiles) ysplit = tiles;
     if (ysplit < 1) ysplit = 1;
-    dim3 grid((unsigned)p.groups, (unsigned)ysplit);
+    const bool side = ring != nullptr;
+    const RingArgs ra = side ? *ring : RingArgs{};
+    const LatentArgs la = side ? *lat : LatentArgs{};
+    dim3 grid((unsigned)p.groups, (unsigned)(ysplit + (side ? 1 : 0)));
     if (p.prequant) {
         auto kern = indexer_scores_kernel<DI, false>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         kern<<<grid, IDX_THREADS, smem, st>>>(q, k, w, scores, (int)m, (int)Hi, p.hpad, p.TT, n_c,
-                                              ratio, start_pos, fill_hidden);
+                                              ratio, start_pos, fill_hidden, (int)ysplit, ra, la);
     } else {
         auto kern = indexer_scores_kernel<DI, true>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         kern<<<grid, IDX_THREADS, smem, st>>>(q, k, w, scores, (int)m, (int)Hi, p.hpad, p.TT, n_c,
-                                              ratio, start_pos, fill_hidden);
+                                              ratio, start_pos, fill_hidden, (int)ysplit, ra, la);
     }
     return launch_check("ds41_indexer_topk: scores kernel");
 }
@@ -411,7 +507,69 @@ extern "C" int ds41_indexer_topk(const ds41_bf16* q_idx, const ds41_bf16* k_idx,
     }
     if (rc) return rc;
     int threads = n_c >= 8192 ? 1024 : (n_c >= 1024 ? 512 : 256);
-    topk_merge_kernel<<<(unsigned)m, threads, 0, st>>>(sc, win_idx, idx, n_c, (int)win, (int)ctopk,
-                                                        ratio, start_pos, offset);
+    const int keys_cap = (int)(n_c < 49152 ? n_c : 49152);  // up to 96 KiB of staged keys
+    const size_t ksm = ((size_t)keys_cap * 2 + 15) & ~size_t(15);
+    if (ksm > 48 * 1024)
+        cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ksm);
+    topk_merge_kernel<<<(unsigned)m, threads, ksm, st>>>(sc, win_idx, idx, n_c, (int)win,
+                                                          (int)ctopk, ratio, start_pos, offset,
+                                                          keys_cap);
     return launch_check("ds41_indexer_topk: top-k kernel");
 }
+
+// ---------------------------------------------------------------------------
+// Pieces of the fused step (ds41_forward.cu).
+// ---------------------------------------------------------------------------
+namespace ds41 {
+
+size_t front_scores_bytes(int64_t m, int64_t n_c) { return align256((size_t)m * n_c * 2); }
+
+bool front_fusable(int64_t m, int64_t Hi, int64_t Di, int64_t n_c) {
+    if (n_c < 1 || Hi < 1 || Hi > 128) return false;
+    if (!(Di == 32 || Di == 64 || Di == 128 || Di == 256)) return false;
+    IndexerPlan p = plan_indexer(m, Hi, Di, n_c, false);
+    return !p.prequant;
+}
+
+int launch_front(const uint16_t* q_idx, const uint16_t* k_idx, const float* w, uint16_t* scores,
+                 int64_t m, int64_t Hi, int64_t Di, int64_t n_c, int64_t ratio,
+                 int64_t start_pos, const RingArgs& ring, const LatentArgs& lat,
+                 cudaStream_t st) {
+    IndexerPlan p = plan_indexer(m, Hi, Di, n_c, true);
+    switch (Di) {
+        case 32: return launch_scores<32>(p, q_idx, k_idx, w, scores, m, Hi, n_c, ratio, start_pos, false, st, &ring, &lat);
+        case 64: return launch_scores<64>(p, q_idx, k_idx, w, scores, m, Hi, n_c, ratio, start_pos, false, st, &ring, &lat);
+        case 128: return launch_scores<128>(p, q_idx, k_idx, w, scores, m, Hi, n_c, ratio, start_pos, false, st, &ring, &lat);
+        default: return launch_scores<256>(p, q_idx, k_idx, w, scores, m, Hi, n_c, ratio, start_pos, false, st, &ring, &lat);
+    }
+}
+
+int launch_topk(const uint16_t* scores, const int32_t* win_idx, int32_t* idx, int64_t m,
+                int64_t n_c, int64_t win, int64_t ctopk, int64_t ratio, int64_t start_pos,
+                int64_t offset, bool pdl, cudaStream_t st) {
+    const int threads = n_c >= 8192 ? 1024 : (n_c >= 1024 ? 512 : 256);
+    const int keys_cap = (int)(n_c < 49152 ? n_c : 49152);
+    const size_t ksm = ((size_t)keys_cap * 2 + 15) & ~size_t(15);
+    if (ksm > 48 * 1024)
+        cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ksm);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)m);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = ksm;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    int rc = cuda_check(cudaLaunchKernelEx(&cfg, topk_merge_kernel, scores, win_idx, idx, n_c,
+                                           (int)win, (int)ctopk, ratio, start_pos, offset,
+                                           keys_cap),
+                        "top-k kernel");
+    if (rc) return rc;
+    return launch_check("top-k kernel");
+}
+
+}  // namespace ds41

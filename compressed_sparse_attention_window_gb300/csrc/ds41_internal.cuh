@@ -1,0 +1,32 @@
+// ds41_internal.cuh - host-side pieces shared between translation units of
+// libds41 (not part of the C ABI).
+#pragma once
+
+#include "ds41_common.cuh"
+
+namespace ds41 {
+
+struct RingArgs;
+struct LatentArgs;
+
+// few-token fused front: step 1 + indexer scores in one launch
+bool front_fusable(int64_t m, int64_t Hi, int64_t Di, int64_t n_c);
+size_t front_scores_bytes(int64_t m, int64_t n_c);
+int launch_front(const uint16_t* q_idx, const uint16_t* k_idx, const float* w, uint16_t* scores,
+                 int64_t m, int64_t Hi, int64_t Di, int64_t n_c, int64_t ratio,
+                 int64_t start_pos, const RingArgs& ring, const LatentArgs& lat,
+                 cudaStream_t st);
+int launch_topk(const uint16_t* scores, const int32_t* win_idx, int32_t* idx, int64_t m,
+                int64_t n_c, int64_t win, int64_t ctopk, int64_t ratio, int64_t start_pos,
+                int64_t offset, bool pdl, cudaStream_t st);
+
+// sparse attention with an explicit plan choice; pdl launches the few-token
+// kernel with programmatic stream serialization
+int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint16_t* rows_b,
+             int64_t n_c, const int32_t* idx, int64_t K, const float* sink, float scale,
+             uint16_t* o, float* lse, int64_t m, int64_t nh, int64_t hd, uint8_t* ws,
+             size_t ws_bytes, bool pdl, cudaStream_t st, const char* name);
+size_t attn_ws_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K);
+bool attn_is_cluster_path(int64_t m, int64_t nh, int64_t hd, int64_t K);
+
+}  // namespace ds41

@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(256) fp4_quant_kernel(const uint4* __restrict_
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     float s;
     uint32_t sbyte;
+    float rs = 0.0f;
     if (E4M3) {
         amax = fmaxf(amax, 0.01171875f);  // 6 * 2^-9
         sbyte = f32_to_e4m3_sat(__fdiv_rn(amax, 6.0f));
@@ -43,18 +44,15 @@ __global__ void __launch_bounds__(256) fp4_quant_kernel(const uint4* __restrict_
     } else {
         amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
         s = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
+        rs = __frcp_rn(s);
         sbyte = (__float_as_uint(s) >> 23) & 0xffu;  // biased exponent = e8m0
     }
     if (!live) return;
-    uint4 out;
-    uint16_t* o = reinterpret_cast<uint16_t*>(&out);
-    uint32_t packed = 0;
+    float tq[8];
 #pragma unroll
-    for (int k = 0; k < 8; k++) {
-        uint32_t c;
-        o[k] = f2bf(fp4_elem(v[k], s, &c));
-        packed |= c << (4 * k);
-    }
+    for (int k = 0; k < 8; k++) tq[k] = E4M3 ? __fdiv_rn(v[k], s) : __fmul_rn(v[k], rs);
+    uint32_t packed;
+    const uint4 out = e2m1_round8(tq, s, &packed);
     y[i] = out;
     if (codes) codes[i] = packed;
     if (scales && (threadIdx.x % LANES) == 0) scales[i / LANES] = (uint8_t)sbyte;

@@ -5,117 +5,19 @@
 // copies, window_topk_idxs, and the latent branch (rope, fp4_quant with
 // LATENT_BLOCK, copy to cache row start_pos / ratio).  The same steps appear
 // in attention_any of metrale_model_arch/deepseek_v41_ref/compress.rs.
-#include "ds41_common.cuh"
+#include "ds41_step1.cuh"
 
 namespace ds41 {
 
-// Non-negative remainder.
-__device__ __forceinline__ int64_t pmod(int64_t a, int64_t b) {
-    const int64_t r = a % b;
-    return r < 0 ? r + b : r;
+// One thread per work item (see ring_write_item).
+__global__ void __launch_bounds__(256) ring_write_kernel(RingArgs a) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < a.total()) ring_write_item(a, i);
 }
 
-// One flat launch over three independent parts:
-//   A  win * hd/8 vectors: ring slot j takes the newest of this call's
-//      positions q with q mod win == j (if any).  In chunk mode the slot's
-//      old contents are first copied to rows_a[j] by the same thread, so the
-//      read happens before the overwrite.
-//   B  (chunk mode) m * hd/8 vectors: rows_a[win + t] = kv[t].
-//   C  m * win window indices.
-__global__ void __launch_bounds__(256) ring_write_kernel(const uint4* __restrict__ kv,
-                                                         uint4* __restrict__ ring,
-                                                         uint4* __restrict__ rows_a,
-                                                         int32_t* __restrict__ win_idx, int64_t m,
-                                                         int64_t hd8, int64_t win,
-                                                         int64_t start_pos, bool chunk) {
-    const int64_t nA = win * hd8;
-    const int64_t nB = chunk ? m * hd8 : 0;
-    const int64_t nC = m * win;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < nA) {
-        const int64_t j = i / hd8, v = i % hd8;
-        if (chunk) rows_a[j * hd8 + v] = ring[j * hd8 + v];
-        const int64_t last = start_pos + m - 1;
-        const int64_t q = last - pmod(last - j, win);
-        if (q >= start_pos) ring[j * hd8 + v] = kv[(q - start_pos) * hd8 + v];
-        return;
-    }
-    i -= nA;
-    if (i < nB) {
-        rows_a[win * hd8 + i] = kv[i];
-        return;
-    }
-    i -= nB;
-    if (i < nC) {
-        const int64_t t = i / win, j = i % win;
-        const int64_t p = start_pos + t;
-        const int64_t q = p - win + 1 + j;
-        int64_t v;
-        if (q < 0) v = -1;
-        else if (start_pos == 0) v = q;
-        else if (m == 1) v = q % win;
-        else if (q < start_pos) v = q % win;
-        else v = win + (q - start_pos);
-        win_idx[i] = (int32_t)v;
-    }
-}
-
-// One CTA per completed group.  Thread k owns dims 8k..8k+7 of the row; a
-// rotary pair (2i, 2i+1) never straddles two threads because the rotary part
-// starts at an even dim.  Blocks of 16 dims span two neighbouring lanes.
-__global__ void latent_write_kernel(const uint4* __restrict__ latent,
-                                    const float2* __restrict__ freqs, uint4* __restrict__ cache,
-                                    uint32_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                    int hd, int rd, int64_t first_row, int64_t ratio) {
-    const int g = blockIdx.x;
-    const int k = threadIdx.x;
-    const int hd8 = hd / 8;
-    const bool live = k < hd8;
-    const int64_t row = first_row + g;
-    const int64_t lpos = row * ratio;  // first position of the group
-    float x[8];
-    if (live) {
-        uint4 raw = latent[(int64_t)g * hd8 + k];
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(&raw);
-#pragma unroll
-        for (int e = 0; e < 8; e++) x[e] = bf2f(h[e]);
-        const int rope0 = hd - rd;
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const int d = 8 * k + e;
-            if (d >= rope0) {
-                const float2 cs = freqs[lpos * (rd / 2) + (d - rope0) / 2];
-                const float x0 = x[e], x1 = x[e + 1];
-                const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
-                const float y1 = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
-                x[e] = bf2f(f2bf(y0));  // the rotated row is a bf16 buffer
-                x[e + 1] = bf2f(f2bf(y1));
-            }
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; e++) x[e] = 0.0f;
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 8; e++) amax = fmaxf(amax, fabsf(x[e]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, 0.01171875f);  // 6 * 2^-9
-    const uint32_t sbyte = f32_to_e4m3_sat(__fdiv_rn(amax, 6.0f));
-    const float s = e4m3_to_f32(sbyte);
-    if (!live) return;
-    uint4 out;
-    uint16_t* o = reinterpret_cast<uint16_t*>(&out);
-    uint32_t packed = 0;
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-        uint32_t c;
-        o[e] = f2bf(fp4_elem(x[e], s, &c));
-        packed |= c << (4 * e);
-    }
-    cache[row * hd8 + k] = out;
-    if (codes) codes[row * hd8 + k] = packed;
-    if (scales && (k & 1) == 0) scales[row * (hd / 16) + k / 2] = (uint8_t)sbyte;
+// One CTA per completed group, one lane per 8 dims (whole warps).
+__global__ void latent_write_kernel(LatentArgs a) {
+    latent_write_item(a, blockIdx.x, threadIdx.x);
 }
 
 }  // namespace ds41
@@ -147,13 +49,12 @@ extern "C" int ds41_window_ring_write(const ds41_bf16* kv, ds41_bf16* ring, ds41
     DS41_REQUIRE(aligned16(kv) && aligned16(ring) && (!chunk || aligned16(rows_a)), DS41_E_ARG,
                  "%s: kv/ring/rows_a must be 16-byte aligned", name);
     if (n_a) *n_a = ds41_rows_a_len(m, win, start_pos);
-    const int64_t hd8 = hd / 8;
-    const int64_t total = win * hd8 + (chunk ? m * hd8 : 0) + m * win;
+    RingArgs ra{reinterpret_cast<const uint4*>(kv), reinterpret_cast<uint4*>(ring),
+                reinterpret_cast<uint4*>(rows_a), win_idx, m, hd / 8, win, start_pos, chunk};
+    const int64_t total = ra.total();
     const int threads = 256;
     ring_write_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0,
-                        (cudaStream_t)stream>>>(
-        reinterpret_cast<const uint4*>(kv), reinterpret_cast<uint4*>(ring),
-        reinterpret_cast<uint4*>(rows_a), win_idx, m, hd8, win, start_pos, chunk);
+                        (cudaStream_t)stream>>>(ra);
     return launch_check(name);
 }
 
@@ -188,9 +89,9 @@ extern "C" int ds41_compress_latent_write(const ds41_bf16* latent, const float* 
     DS41_REQUIRE(!cache_codes || (reinterpret_cast<uintptr_t>(cache_codes) & 3u) == 0, DS41_E_ARG,
                  "%s: cache_codes must be 4-byte aligned", name);
     const int threads = (int)(((hd / 8) + 31) / 32 * 32);
-    latent_write_kernel<<<(unsigned)G, threads, 0, (cudaStream_t)stream>>>(
-        reinterpret_cast<const uint4*>(latent), reinterpret_cast<const float2*>(freqs_cis),
-        reinterpret_cast<uint4*>(cache), reinterpret_cast<uint32_t*>(cache_codes), cache_scales,
-        (int)hd, (int)rd, start_pos / ratio, ratio);
+    LatentArgs la{reinterpret_cast<const uint4*>(latent), reinterpret_cast<const float2*>(freqs_cis),
+                  reinterpret_cast<uint4*>(cache), reinterpret_cast<uint32_t*>(cache_codes),
+                  cache_scales, (int)hd, (int)rd, (int)G, start_pos / ratio, ratio};
+    latent_write_kernel<<<(unsigned)G, threads, 0, (cudaStream_t)stream>>>(la);
     return launch_check(name);
 }

@@ -43,6 +43,9 @@ SIGNATURES = {
     "ds41_sparse_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
     "ds41_sparse_attn_sink_fwd": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F, _P, _P,
                                                  _I64, _I64, _I64, _P, _SZ, _P]),
+    "ds41_csa_workspace_bytes": (_SZ, [_I64] * 9),
+    "ds41_csa_forward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _P, _P, _F,
+                                        _P, _P, _P, _P] + [_I64] * 10 + [_P, _SZ, _P]),
     "ds41_sparse_attn_noalloc_capacity": (_SZ, []),
     "ds41_sparse_attn_sink_fwd_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F,
                                                          _P, _P, _I64, _I64, _I64, _P]),
@@ -243,6 +246,47 @@ def sparse_attn_sink_fwd_noalloc(q: torch.Tensor, rows_a: torch.Tensor,
           _ptr(sink, torch.float32, "sink"), float(scale), _ptr(o, _BF, "o"),
           _ptr(lse, torch.float32, "lse"), m, nh, hd, _stream())
     return o
+
+
+def csa_workspace_bytes(wl) -> int:
+    return int(load().ds41_csa_workspace_bytes(wl.m, wl.start_pos, wl.nh, wl.hd, wl.win, wl.ratio,
+                                               wl.topk, wl.Hi, wl.Di))
+
+
+def csa_forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
+                out: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
+    """ds41_csa_forward: the whole step in one call (same inputs and outputs as
+    :func:`forward`)."""
+    out = {} if out is None else out
+    dev = inp["q"].device
+    m, win = wl.m, wl.win
+    if "win_idx" not in out:
+        out["win_idx"] = torch.empty(m, win, dtype=torch.int32, device=dev)
+    if "idx" not in out:
+        out["idx"] = torch.empty(m, wl.K, dtype=torch.int32, device=dev)
+    if "o" not in out:
+        out["o"] = torch.empty_like(inp["q"])
+    chunk = wl.start_pos > 0 and m > 1
+    if chunk and "rows_a" not in out:
+        out["rows_a"] = torch.empty(win + m, wl.hd, dtype=torch.bfloat16, device=dev)
+    need = csa_workspace_bytes(wl)
+    ws = out.get("ws_csa")
+    if need and (ws is None or ws.numel() < need):
+        ws = out["ws_csa"] = torch.empty(need, dtype=torch.uint8, device=dev)
+    _call("ds41_csa_forward", _ptr(inp["q"], _BF, "q"), _ptr(inp["kv"], _BF, "kv"),
+          _ptr(inp["ring"], _BF, "ring"), _ptr(out.get("rows_a") if chunk else None),
+          _ptr(inp["latent"], _BF, "latent") if wl.G > 0 else None,
+          _ptr(freqs_cis, torch.float32, "freqs_cis"), freqs_cis.shape[0],
+          _ptr(inp["cache"], _BF, "cache"), inp["cache"].shape[0], _ptr(inp["q_idx"], _BF, "q_idx"),
+          _ptr(inp["k_idx"], _BF, "k_idx"), _ptr(inp["w"], torch.float32, "w"),
+          _ptr(inp["sink"], torch.float32, "sink"), float(wl.scale),
+          _ptr(out["win_idx"], torch.int32, "win_idx"), _ptr(out["idx"], torch.int32, "idx"),
+          _ptr(out["o"], _BF, "o"), _ptr(out.get("lse"), torch.float32, "lse"), m, wl.start_pos,
+          wl.nh, wl.hd, wl.rd, win, wl.ratio, wl.topk, wl.Hi, wl.Di, _ptr(ws) if need else None,
+          need, _stream())
+    if wl.n_c == 0:
+        out["idx"] = out["win_idx"]
+    return out
 
 
 def forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,

@@ -205,6 +205,35 @@ int ds41_sparse_attn_sink_fwd(const ds41_bf16* q, const ds41_bf16* rows_a, int64
                               ds41_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* The whole step                                                             */
+/* ------------------------------------------------------------------------ */
+/* Scratch bytes ds41_csa_forward needs for these sizes. */
+size_t ds41_csa_workspace_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_t hd, int64_t win,
+                                int64_t ratio, int64_t topk, int64_t Hi, int64_t Di);
+
+/* forward.rs, AttnV41::forward (and compress.rs attention_any): the whole
+ * compressed sparse attention step of one layer for m tokens at start_pos, in
+ * the pages' order: the window ring write and window indices
+ * (ds41_window_ring_write), the latent write of the groups this call
+ * completes (ds41_compress_latent_write), the indexer top-k and merge
+ * (ds41_indexer_topk, offset = ds41_rows_a_len), and sparse attention with
+ * the sink (ds41_sparse_attn_sink_fwd).  Arguments and layouts are those of
+ * the four calls; the results are the same.  rows_a ([win + m, hd]) is
+ * needed only for a chunk of m > 1 tokens past position 0; latent /
+ * freqs_cis only when the call completes a group; lse is nullable.  idx is
+ * [m, win + min(topk, n_c)] with n_c = (start_pos + m)/ratio (unused when
+ * n_c == 0).  Few-token calls run in three launches chained on the device
+ * (programmatic dependent launch), larger ones as the four calls. */
+int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring, ds41_bf16* rows_a,
+                     const ds41_bf16* latent, const float* freqs_cis, int64_t max_pos,
+                     ds41_bf16* cache, int64_t cache_rows, const ds41_bf16* q_idx,
+                     const ds41_bf16* k_idx, const float* w, const float* sink, float scale,
+                     int32_t* win_idx, int32_t* idx, ds41_bf16* o, float* lse, int64_t m,
+                     int64_t start_pos, int64_t nh, int64_t hd, int64_t rd, int64_t win,
+                     int64_t ratio, int64_t topk, int64_t Hi, int64_t Di, void* ws,
+                     size_t ws_bytes, ds41_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Step 3 without caller-provided scratch                                     */
 /* ------------------------------------------------------------------------ */
 /* No counterpart in the paper: this entry point exists for callers that

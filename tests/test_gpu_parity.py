@@ -213,19 +213,23 @@ def test_sparse_attn_given_indices(orc, sink_kind):
     assert ok, (err, worst)
 
 
+@pytest.mark.parametrize("m,nh", [(1, 64), (2, 64), (3, 20), (12, 64), (40, 16)])
 @pytest.mark.parametrize("K", [1, 31, 33, 640, 2176])
-def test_sparse_attn_split_paths(orc, K):
-    """Decode-sized m exercises the split-K partials and the merge."""
-    nh, hd = 64, 512
+def test_sparse_attn_few_token_paths(orc, K, m, nh):
+    """Few tokens take the cluster path (m * heads/16 small) or the split-K
+    partials + merge (larger m); both against the oracle."""
+    hd = 512
     n_a, n_c = 128, 2500
-    g = torch.Generator().manual_seed(K)
-    q = torch.randn(2, nh, hd, generator=g).to(torch.bfloat16)
+    g = torch.Generator().manual_seed(K + 7 * m)
+    q = torch.randn(m, nh, hd, generator=g).to(torch.bfloat16)
     rows_a = torch.randn(n_a, hd, generator=g).to(torch.bfloat16)
     rows_b = torch.randn(n_c, hd, generator=g).to(torch.bfloat16)
     sink = torch.randn(nh, generator=g)
     rng = np.random.default_rng(K)
-    idx = np.stack([rng.permutation(n_a + n_c)[:K] for _ in range(2)]).astype(np.int32)
-    lse = torch.empty(2, nh, device="cuda")
+    idx = np.stack([rng.permutation(n_a + n_c)[:K] for _ in range(m)]).astype(np.int32)
+    if K > 40:
+        idx[0, 5:9] = -1
+    lse = torch.empty(m, nh, device="cuda")
     o = ds41.sparse_attn_sink_fwd(q.cuda(), rows_a.cuda(), rows_b.cuda(),
                                   torch.from_numpy(idx).cuda(), sink.cuda(), hd ** -0.5, lse=lse)
     oo, olse, _ = orc.sparse_attn(bf16_bits(q), bf16_bits(rows_a), bf16_bits(rows_b), idx,
@@ -285,3 +289,33 @@ def test_forward_no_compressed_rows_yet(orc):
     ref = oracle_forward(orc, wl, inp, fc=fc.cpu().numpy())
     assert np.array_equal(out["idx"].cpu().numpy(), ref["idx"])
     assert attn_close(out["o"].float().cpu().numpy(), ref["o"])[0]
+
+
+CSA_CASES = ["tiny_prefill", "decode", "long_decode", "chunked_prefill", "prefill"]
+CSA_EXTRA = [TINY_PREFILL.replace(m=1, start_pos=43), TINY_PREFILL.replace(m=3, start_pos=37),
+             TINY_PREFILL.replace(m=1, start_pos=2), DECODE.replace(start_pos=8190),
+             DECODE.replace(m=2, start_pos=5000), TINY_PREFILL.replace(m=2, start_pos=0)]
+
+
+@pytest.mark.parametrize("wl", [WORKLOADS[n] for n in CSA_CASES] + CSA_EXTRA,
+                         ids=lambda w: f"{w.name}-{w.m}-{w.start_pos}")
+def test_csa_forward_matches_oracle_and_the_four_calls(orc, wl):
+    """ds41_csa_forward (fused few-token path or the four calls) against the
+    oracle, and bit-for-bit against running the four entry points."""
+    inp = make_inputs(wl)
+    ora_fc = orc.yarn_freqs_cis(wl.rd, max(wl.max_pos, 1))
+    fc = torch.from_numpy(ora_fc).cuda()
+    dev1, dev2 = to_dev(inp), to_dev(inp)
+    out1 = ds41.csa_forward(dev1, wl, fc)
+    out2 = ds41.forward(dev2, wl, fc)
+    torch.cuda.synchronize()
+    assert torch.equal(dev1["ring"], dev2["ring"]) and torch.equal(dev1["cache"], dev2["cache"])
+    assert torch.equal(out1["idx"], out2["idx"])
+    assert torch.equal(out1["o"], out2["o"])
+    toks = sample_tokens(wl) if wl.m > 128 else list(range(wl.m))
+    ref = oracle_forward(orc, wl, inp, tokens=toks, fc=ora_fc)
+    assert np.array_equal(bf16_bits(dev1["ring"]), ref["ring"])
+    assert np.array_equal(bf16_bits(dev1["cache"]), ref["cache"])
+    assert_idx_sets_equal(out1["idx"].cpu().numpy()[toks], ref["idx"], wl.win)
+    ok, err, worst = attn_close(out1["o"].float().cpu().numpy()[toks], ref["o"])
+    assert ok, (wl.name, err, worst)
