@@ -329,25 +329,43 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
 constexpr int DEC_HEADS = 16;
 constexpr int DEC_NC = 32;
 constexpr int DEC_SPS = DEC_NC + 8;  // padded row stride of the partial scores (no bank conflicts)
+constexpr int DEC_STAGE = 2048;      // indices of a CTA's slice staged in shared memory
 // warps per CTA: 8 when the head dim gives every warp at least two n-tiles
 template <int HD>
 __host__ __device__ constexpr int dec_warps() { return HD >= 128 ? 8 : 4; }
-constexpr int DEC_STAGE = 2048;  // indices of a CTA's slice staged in shared memory
 
 template <int HD>
 struct DecSmem {
-    static constexpr int OSTR = HD + 8;  // padded row stride of the staged O
-    static constexpr size_t q_bytes = (size_t)DEC_HEADS * HD * 2;
-    static constexpr size_t kv_bytes = (size_t)DEC_NC * HD * 2;   // one buffer
+    // Rows of q and of the gathered kv are padded to HD + 8 bf16 (a 16-byte
+    // multiple): eight consecutive rows then start on eight different 4-bank
+    // groups, so ldmatrix reads them without conflicts, and every row can be
+    // the destination of one contiguous bulk copy.
+    static constexpr int RS = HD + 8;
+    static constexpr int OSTR = HD + 8;  // padded row stride of the staged O (f32)
+    static constexpr size_t q_bytes = (size_t)DEC_HEADS * RS * 2;
+    static constexpr size_t kv_bytes = (size_t)DEC_NC * RS * 2;  // one buffer
     static constexpr size_t sp_bytes = (size_t)dec_warps<HD>() * DEC_HEADS * DEC_SPS * 4;
     static constexpr size_t o_bytes = (size_t)DEC_HEADS * OSTR * 4;  // reuses the kv buffers
-    static constexpr size_t total = q_bytes + 2 * kv_bytes + sp_bytes + 2 * DEC_NC * 4 +
-                                    2 * DEC_HEADS * 4 + (size_t)DEC_STAGE * 4;
+    static constexpr size_t bar_off = q_bytes + 2 * kv_bytes + sp_bytes;
+    static constexpr size_t total = bar_off + 4 * 8 + 2 * DEC_NC * 4 + 2 * DEC_HEADS * 4 +
+                                    (size_t)DEC_STAGE * 4;
     static_assert(o_bytes <= 2 * kv_bytes, "O staging must fit in the kv buffers");
+    static_assert(q_bytes % 16 == 0 && kv_bytes % 16 == 0 && sp_bytes % 16 == 0, "alignment");
 };
 
+// Few-token (decode) path.  A cluster of CL CTAs shares one (token, group of
+// 16 heads); CTA r of the cluster takes slice r of the index row.  Warp 0
+// moves data with TMA bulk copies (one per 1 KiB row) completing on
+// mbarriers: the 16 q rows, then chunks of 32 gathered rows, double-buffered.
+// The warps split the head dim: for S each warp reduces over its slice and the
+// partials are summed in a fixed order by every warp, so all warps hold
+// bit-identical scores and softmax statistics; for P*V each warp owns a slice
+// of the output columns.  At the end the CTAs exchange (m, l) and their
+// unnormalised O through distributed shared memory; CTA r reduces the r-th
+// slice of the columns over the cluster, adds the sink and writes o.  No
+// scratch memory and no second launch.
 template <int HD>
-__global__ void __launch_bounds__(32 * dec_warps<HD>()) sparse_attn_decode_kernel(
+__global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ rows_a, int64_t n_a,
     const uint16_t* __restrict__ rows_b, int64_t n_c, const int32_t* __restrict__ idx, int K,
     const float* __restrict__ sink, float scale_log2, uint16_t* __restrict__ o,
@@ -355,19 +373,21 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>()) sparse_attn_decode_kerne
     namespace cg = cooperative_groups;
     using SM = DecSmem<HD>;
     constexpr int NW = dec_warps<HD>();
-    constexpr int DEC_THREADS = 32 * NW;
-    constexpr int CPR = HD / 8;
+    constexpr int NTH = 32 * NW;
+    constexpr int RS = SM::RS;
     constexpr int QW = HD / NW;      // head-dim columns per warp
     constexpr int NT = QW / 8;       // output n-tiles per warp
     constexpr int OSTR = SM::OSTR;
+    constexpr uint32_t ROWB = HD * 2;  // bytes of one row
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* qs = reinterpret_cast<uint16_t*>(smem);
     uint16_t* kvs = reinterpret_cast<uint16_t*>(smem + SM::q_bytes);
     float* sp = reinterpret_cast<float*>(smem + SM::q_bytes + 2 * SM::kv_bytes);
-    int* vflag = reinterpret_cast<int*>(smem + SM::q_bytes + 2 * SM::kv_bytes + SM::sp_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bar_off);  // q, kv0, kv1
+    int* vflag = reinterpret_cast<int*>(smem + SM::bar_off + 4 * 8);
     float* stat = reinterpret_cast<float*>(vflag + 2 * DEC_NC);  // [2][16]: m then l
     int* sidx = reinterpret_cast<int*>(stat + 2 * DEC_HEADS);      // [DEC_STAGE]
-    float* ostage = reinterpret_cast<float*>(kvs);                // [16][HD] after the loop
+    float* ostage = reinterpret_cast<float*>(kvs);                // [16][OSTR] after the loop
 
     cg::cluster_group cluster = cg::this_cluster();
     const int CL = (int)cluster.num_blocks();
@@ -384,37 +404,53 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>()) sparse_attn_decode_kerne
     const int j1 = min(K, j0 + per);
     const int nchunks = j1 > j0 ? (j1 - j0 + DEC_NC - 1) / DEC_NC : 0;
 
-    for (int id = tid; id < DEC_HEADS * CPR; id += DEC_THREADS) {
-        const int r = id / CPR, c = id % CPR;
-        const int h = h0 + r;
-        const bool live = h < nh;
-        const uint16_t* src = q + ((t * nh + (live ? h : 0)) * (int64_t)HD) + c * 8;
-        cp_async16(smem_u32(qs + r * HD + aswz(r, c) * 8), src, live);
+    if (tid == 0) {
+        for (int i = 0; i < 3; i++) mbar_init(&bars[i], 1);
+        mbar_init_fence();
     }
-    // Everything above reads only q; the indices, the ring and the cache may
-    // come from the kernels just before this one.
-    pdl_wait();
-    // this slice's indices to shared memory first (one coalesced pass)
-    const int nst = max(0, min(j1 - j0, DEC_STAGE));
-    for (int j = tid; j < nst; j += DEC_THREADS) sidx[j] = irow[j0 + j];
     __syncthreads();
-    auto load_chunk = [&](int chunk, int buf) {
-        uint16_t* dst = kvs + buf * (DEC_NC * HD);
-        for (int id = tid; id < DEC_NC * CPR; id += DEC_THREADS) {
-            const int r = id / CPR, c = id % CPR;
-            const int j = j0 + chunk * DEC_NC + r;
-            int64_t v = -1;
-            if (j - j0 < nst) v = sidx[j - j0];
-            else if (j < j1) v = irow[j];
-            const bool ok = v >= 0 && v < n_rows;
-            if (c == 0) {
-                if (j < j1 && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
-                vflag[buf * DEC_NC + r] = ok ? 1 : 0;
+    // q rows of this head group (rows past nh are zero); q is an input, so it
+    // is read before waiting for the previous kernel.
+    if (warp == 0) {
+        const int hv = max(0, min(DEC_HEADS, nh - h0));
+        if (lane == 0) mbar_arrive_expect_tx(&bars[0], (uint32_t)hv * ROWB);
+        __syncwarp();
+        if (lane < DEC_HEADS) {
+            uint16_t* dst = qs + lane * RS;
+            if (lane < hv) {
+                bulk_g2s(dst, q + (t * nh + h0 + lane) * (int64_t)HD, ROWB, &bars[0]);
+            } else {
+                for (int c = 0; c < HD / 8; c++) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
             }
-            const uint16_t* src = rows_a;
-            if (ok) src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
-            cp_async16(smem_u32(dst + r * HD + aswz(r, c) * 8), src + c * 8, ok);
         }
+    }
+    // The indices, the ring and the cache may come from the kernels just
+    // before this one.
+    pdl_wait();
+    const int nst = max(0, min(j1 - j0, DEC_STAGE));
+    for (int j = tid; j < nst; j += NTH) sidx[j] = irow[j0 + j];
+    __syncthreads();
+    // warp 0: one bulk copy per valid row of the chunk; invalid rows are zeroed
+    // (their scores are masked, and 0 * row must stay finite in P*V)
+    auto load_chunk = [&](int chunk, int buf) {
+        const int j = j0 + chunk * DEC_NC + lane;
+        int64_t v = -1;
+        if (j < j1) v = (j - j0 < nst) ? sidx[j - j0] : irow[j];
+        const bool ok = v >= 0 && v < n_rows;
+        if (j < j1 && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
+        const unsigned bal = __ballot_sync(0xffffffffu, ok);
+        // order this buffer's earlier generic-proxy writes before the copies
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        if (lane == 0) mbar_arrive_expect_tx(&bars[1 + buf], (uint32_t)__popc(bal) * ROWB);
+        __syncwarp();
+        uint16_t* dst = kvs + buf * (DEC_NC * RS) + lane * RS;
+        if (ok) {
+            const uint16_t* src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
+            bulk_g2s(dst, src, ROWB, &bars[1 + buf]);
+        } else {
+            for (int c = 0; c < HD / 8; c++) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+        }
+        vflag[buf * DEC_NC + lane] = ok ? 1 : 0;
     };
 
     float oacc[NT][4];
@@ -423,16 +459,16 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>()) sparse_attn_decode_kerne
     float mrow[2] = {-INFINITY, -INFINITY};
     float lrow[2] = {0.0f, 0.0f};
     const int ra = lane >> 2, rb = ra + 8;
+    bool failed = false;
 
-    if (nchunks > 0) load_chunk(0, 0);
-    cp_async_commit();
+    if (warp == 0 && nchunks > 0) load_chunk(0, 0);
     for (int chunk = 0; chunk < nchunks; chunk++) {
         const int buf = chunk & 1;
-        if (chunk + 1 < nchunks) load_chunk(chunk + 1, buf ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const uint16_t* kv = kvs + buf * (DEC_NC * HD);
+        if (warp == 0 && chunk + 1 < nchunks) load_chunk(chunk + 1, buf ^ 1);
+        if (chunk == 0 && !mbar_wait(&bars[0], 0, kWaitPolls)) failed = true;
+        if (!mbar_wait(&bars[1 + buf], (chunk >> 1) & 1, kWaitPolls)) failed = true;
+        __syncthreads();  // zero-filled rows and flags of warp 0 are visible
+        const uint16_t* kv = kvs + buf * (DEC_NC * RS);
         float sacc[4][4];
 #pragma unroll
         for (int j = 0; j < 4; j++) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
@@ -442,14 +478,14 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>()) sparse_attn_decode_kerne
             {
                 const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
                 const int c = warp * (QW / 8) + kk * 2 + (lane >> 4);
-                ldsm_x4(smem_u32(qs + r * HD + aswz(r, c) * 8), a0, a1, a2, a3);
+                ldsm_x4(smem_u32(qs + r * RS + c * 8), a0, a1, a2, a3);
             }
 #pragma unroll
             for (int jj = 0; jj < 2; jj++) {
                 uint32_t b0, b1, b2, b3;
                 const int r = jj * 16 + (lane & 7) + (lane >> 4) * 8;
                 const int c = warp * (QW / 8) + kk * 2 + ((lane >> 3) & 1);
-                ldsm_x4(smem_u32(kv + r * HD + aswz(r, c) * 8), b0, b1, b2, b3);
+                ldsm_x4(smem_u32(kv + r * RS + c * 8), b0, b1, b2, b3);
                 mma_bf16(sacc[2 * jj], a0, a1, a2, a3, b0, b1);
                 mma_bf16(sacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
             }
@@ -525,15 +561,23 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>()) sparse_attn_decode_kerne
                 uint32_t b0, b1, b2, b3;
                 const int r = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
                 const int c = warp * (QW / 8) + jj * 2 + (lane >> 4);
-                ldsm_x4_t(smem_u32(kv + r * HD + aswz(r, c) * 8), b0, b1, b2, b3);
+                ldsm_x4_t(smem_u32(kv + r * RS + c * 8), b0, b1, b2, b3);
                 mma_bf16(oacc[2 * jj], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b0, b1);
                 mma_bf16(oacc[2 * jj + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b2, b3);
             }
         }
-        __syncthreads();
+        __syncthreads();  // this buffer is refilled two chunks later
     }
-    cp_async_wait<0>();
-    __syncthreads();
+    if (failed) {
+        // a copy never completed (only a broken index or address could do
+        // this): report it and leave this CTA's contribution empty
+        raise_status(status, DS41_E_TIMEOUT);
+        mrow[0] = mrow[1] = -INFINITY;
+        lrow[0] = lrow[1] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NT; j++) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.0f;
+    }
+    if (nchunks == 0 && !mbar_wait(&bars[0], 0, kWaitPolls)) raise_status(status, DS41_E_TIMEOUT);
 
 #pragma unroll
     for (int i = 0; i < 2; i++) {
@@ -555,49 +599,60 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>()) sparse_attn_decode_kerne
     }
     cluster.sync();
 
-    // Every CTA gathers the cluster's (m, l) into its own shared memory and
-    // forms the per-(rank, head) weights e^{m_r - M} / L with the sink in L.
-    float* allst = sp;                        // [CL][32]
-    float* wts = sp + 16 * 2 * DEC_HEADS;     // [CL][16]
-    for (int i = tid; i < CL * 2 * DEC_HEADS; i += DEC_THREADS)
-        allst[i] = cluster.map_shared_rank(stat, i / (2 * DEC_HEADS))[i % (2 * DEC_HEADS)];
-    __syncthreads();
-    if (tid < DEC_HEADS) {
-        const int h = h0 + tid;
+    // Weights e^{m_r - M} / L for every (head, rank): one thread per pair,
+    // the max and the sum over the ranks by shuffles within 16-lane groups.
+    float* wts = sp;  // [16 ranks][16 heads]
+    for (int pidx = tid; pidx < DEC_HEADS * 16; pidx += NTH) {
+        const int hh = pidx >> 4, r = pidx & 15;
+        const int h = h0 + hh;
+        float mr = -INFINITY, lr = 0.0f;
+        if (r < CL) {
+            const float* st = cluster.map_shared_rank(stat, r);
+            mr = st[hh];
+            lr = st[DEC_HEADS + hh];
+        }
         const float sk = (h < nh) ? sink[h] * LOG2E : -INFINITY;
-        float M = sk;
-        for (int r = 0; r < CL; r++) M = fmaxf(M, allst[r * 2 * DEC_HEADS + tid]);
+        float M = fmaxf(mr, sk);
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         const float Mref = (M == -INFINITY) ? 0.0f : M;
-        float L = exp2f(sk - Mref);
-        for (int r = 0; r < CL; r++)
-            L += allst[r * 2 * DEC_HEADS + DEC_HEADS + tid] *
-                 exp2f(allst[r * 2 * DEC_HEADS + tid] - Mref);
+        const float e = exp2f(mr - Mref);
+        float L = lr * e;
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        L += exp2f(sk - Mref);
         const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-        for (int r = 0; r < CL; r++)
-            wts[r * DEC_HEADS + tid] = exp2f(allst[r * 2 * DEC_HEADS + tid] - Mref) * inv;
-        if (lse && rank == 0 && h < nh) lse[t * nh + h] = (Mref + log2f(L)) / LOG2E;
+        wts[r * DEC_HEADS + hh] = e * inv;
+        if (lse && rank == 0 && r == 0 && h < nh) lse[t * nh + h] = (Mref + log2f(L)) / LOG2E;
     }
     __syncthreads();
-    // CTA `rank` reduces columns [c0, c0 + cols) of the 16 heads, 4 at a time.
+    // CTA `rank` reduces columns [c0, c0 + cols) of the 16 heads, 4 at a time,
+    // with the loads from all ranks issued before the sums.
     const int cols = HD / CL;
     const int c0 = rank * cols;
-    for (int e = tid; e < DEC_HEADS * (cols / 4); e += DEC_THREADS) {
+    for (int e = tid; e < DEC_HEADS * (cols / 4); e += NTH) {
         const int hh = e / (cols / 4), c = c0 + 4 * (e % (cols / 4));
         const int h = h0 + hh;
-        if (h >= nh) continue;
+        float4 v[16];
+#pragma unroll
+        for (int r = 0; r < 16; r++)
+            if (r < CL)
+                v[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(ostage, r) + hh * OSTR + c);
         float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 4
-        for (int r = 0; r < CL; r++) {
-            const float4 v = *reinterpret_cast<const float4*>(
-                cluster.map_shared_rank(ostage, r) + hh * OSTR + c);
-            const float wgt = wts[r * DEC_HEADS + hh];
-            acc.x += v.x * wgt;
-            acc.y += v.y * wgt;
-            acc.z += v.z * wgt;
-            acc.w += v.w * wgt;
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            if (r < CL) {
+                const float wgt = wts[r * DEC_HEADS + hh];
+                acc.x += v[r].x * wgt;
+                acc.y += v[r].y * wgt;
+                acc.z += v[r].z * wgt;
+                acc.w += v[r].w * wgt;
+            }
         }
-        uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-        *reinterpret_cast<uint2*>(o + (t * nh + h) * (int64_t)HD + c) = packed;
+        if (h < nh) {
+            const uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+            *reinterpret_cast<uint2*>(o + (t * nh + h) * (int64_t)HD + c) = packed;
+        }
     }
     cluster.sync();  // keep this CTA's shared memory alive until all readers are done
 }
@@ -664,7 +719,7 @@ static int launch_attn_decode(const AttnPlan& p, const uint16_t* q, const uint16
     if (p.cluster > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.cluster, (unsigned)p.head_groups, (unsigned)m);
-    cfg.blockDim = dim3(32 * dec_warps<HD>());
+    cfg.blockDim = dim3(32 * dec_warps<HD>());  // NOLINT
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];

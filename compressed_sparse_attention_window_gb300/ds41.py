@@ -24,7 +24,7 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 
 ERRORS = {1: "DS41_E_ARG", 2: "DS41_E_RANGE", 3: "DS41_E_CUDA", 4: "DS41_E_INDEX",
-          5: "DS41_E_WORKSPACE"}
+          5: "DS41_E_WORKSPACE", 6: "DS41_E_TIMEOUT"}
 
 #: Exported symbols of include/ds41.h and their (restype, argtypes).
 SIGNATURES = {

@@ -46,7 +46,8 @@ enum {
     DS41_E_RANGE = 2,     /* a limit of the forward: token count, position, top-k */
     DS41_E_CUDA = 3,      /* a CUDA call or launch failed */
     DS41_E_INDEX = 4,     /* a device-side index check tripped (device status) */
-    DS41_E_WORKSPACE = 5  /* ws is NULL or smaller than *_workspace_bytes */
+    DS41_E_WORKSPACE = 5, /* ws is NULL or smaller than *_workspace_bytes */
+    DS41_E_TIMEOUT = 6    /* a bounded device-side wait gave up (device status) */
 };
 
 /* Message of the calling thread's last error ("" if none).  The pointer stays
