@@ -660,6 +660,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
 struct AttnPlan {
     int splits, chunks_per_split, head_groups;
     int cluster;  // > 0: the few-token path with this many CTAs per cluster
+    int tc;       // > 0: the tensor-core path on this many SMs
     size_t part_o_bytes, part_ml_bytes;
 };
 
@@ -668,6 +669,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static AttnPlan plan_attn(int64_t m, int64_t nh, int64_t hd, int64_t K, int sms) {
     AttnPlan p;
     p.cluster = 0;
+    p.tc = 0;
     // Few tokens: one cluster per (token, 16 heads) when that leaves most SMs
     // to the row slices; no scratch, no merge launch.
     const int64_t dec_groups = m * ((nh + DEC_HEADS - 1) / DEC_HEADS);
@@ -682,6 +684,14 @@ static AttnPlan plan_attn(int64_t m, int64_t nh, int64_t hd, int64_t K, int sms)
         return p;
     }
     p.head_groups = (int)((nh + ATT_HEADS - 1) / ATT_HEADS);
+    // Many tokens, hd 512, whole 64-head groups: persistent tcgen05 kernel.
+    if (attn_tc_supported(m, nh, hd, K, sms)) {
+        p.tc = sms;
+        p.splits = 1;
+        p.chunks_per_split = 0;
+        p.part_o_bytes = p.part_ml_bytes = 0;
+        return p;
+    }
     const int chunks = (int)((K + ATT_NC - 1) / ATT_NC);
     const int64_t ctas = m * p.head_groups;
     int splits = 1;
@@ -747,6 +757,11 @@ static int launch_attn(const AttnPlan& p, const uint16_t* q, const uint16_t* row
     if (p.cluster > 0)
         return launch_attn_decode<HD>(p, q, rows_a, n_a, rows_b, n_c, idx, K, sink, scale, o, lse,
                                       m, nh, status, st, pdl);
+    if constexpr (HD == 512) {
+        if (p.tc > 0)
+            return attn_tc_launch(q, rows_a, n_a, rows_b, n_c, idx, K, sink, scale, o, lse, m, nh,
+                                  status, p.tc, st);
+    }
     const size_t smem = AttnSmem<HD>::total;
     auto kern = sparse_attn_kernel<HD>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -29,4 +29,11 @@ int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint1
 size_t attn_ws_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K);
 bool attn_is_cluster_path(int64_t m, int64_t nh, int64_t hd, int64_t K);
 
+// many-token attention on the tcgen05 tensor cores (ds41_attn_tc.cu)
+bool attn_tc_supported(int64_t m, int64_t nh, int64_t hd, int64_t K, int sms);
+int attn_tc_launch(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint16_t* rows_b,
+                   int64_t n_c, const int32_t* idx, int64_t K, const float* sink, float scale,
+                   uint16_t* o, float* lse, int64_t m, int64_t nh, unsigned int* status,
+                   int sms, cudaStream_t st);
+
 }  // namespace ds41

@@ -239,6 +239,82 @@ def test_sparse_attn_few_token_paths(orc, K, m, nh):
     assert np.allclose(lse.cpu().numpy(), olse, atol=1e-3, rtol=1e-4)
 
 
+def _tc_index_rows(m, n_a, n_c, K, rng):
+    """Index rows that exercise every chunk form of the many-token kernel:
+    compact ranges of both sources (consecutive-row chunks with masks),
+    scattered rows (listed rows), repeated rows, rows with no or one valid
+    index, and padding with -1."""
+    idx = np.full((m, K), -1, np.int32)
+    for t in range(m):
+        kind = t % 5
+        if kind == 0:   # a window-like run of rows_a + half of a range of rows_b
+            w = min(K // 3, n_a)
+            a0 = rng.integers(0, n_a - w + 1)
+            nb = min(K - w, n_c // 2)
+            b0 = rng.integers(0, n_c - 2 * nb + 1)
+            picks = b0 + rng.permutation(2 * nb)[:nb]
+            row = np.concatenate([np.arange(a0, a0 + w), n_a + picks])
+        elif kind == 1:  # scattered over everything
+            row = rng.permutation(n_a + n_c)[:K]
+        elif kind == 2:  # a compact range with repeated rows
+            n = K - 3
+            b0 = rng.integers(0, n_c - n + 1)
+            row = n_a + b0 + rng.integers(0, n, n)
+        elif kind == 3:  # a few valid rows among -1
+            row = rng.permutation(n_a + n_c)[: max(1, K // 9)]
+        else:            # rows_b only, ascending, every third row
+            n = min(K, n_c // 3)
+            b0 = rng.integers(0, n_c - 3 * n + 1)
+            row = n_a + b0 + 3 * np.arange(n)
+        row = row[:K]
+        rng.shuffle(row)
+        idx[t, : len(row)] = row
+        if kind != 1:
+            rng.shuffle(idx[t])
+    idx[3, :] = -1           # no valid index at all
+    idx[8, :] = -1
+    idx[8, K // 2] = 5       # exactly one valid index
+    return idx
+
+
+@pytest.mark.parametrize("K,nh,sink_kind", [(37, 64, "normal"), (640, 64, "normal"),
+                                            (640, 64, "minus_inf"), (640, 128, "large"),
+                                            (1000, 64, "normal")])
+def test_sparse_attn_many_tokens_tensor_core_path(orc, K, nh, sink_kind):
+    """Enough tokens for one work item per SM (hd 512, 64-head groups, K <=
+    1024) take the persistent tcgen05 kernel; every token against the oracle.
+    A third of the compressed rows are scaled x3 so that later chunks beat the
+    running maximum by far (the rescale of O in tensor memory)."""
+    hd = 512
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    m = sms + 13
+    n_a, n_c = 300, 2100
+    g = torch.Generator().manual_seed(K + nh)
+    q = torch.randn(m, nh, hd, generator=g).to(torch.bfloat16)
+    rows_a = torch.randn(n_a, hd, generator=g).to(torch.bfloat16)
+    rb = torch.randn(n_c, hd, generator=g)
+    rb[::3] *= 3.0
+    rows_b = rb.to(torch.bfloat16)
+    sink = torch.randn(nh, generator=g)
+    if sink_kind == "minus_inf":
+        sink[:] = -float("inf")
+    elif sink_kind == "large":
+        sink *= 30
+    idx = _tc_index_rows(m, n_a, n_c, K, np.random.default_rng(K * 3 + nh))
+    lse = torch.empty(m, nh, device="cuda")
+    o = ds41.sparse_attn_sink_fwd(q.cuda(), rows_a.cuda(), rows_b.cuda(),
+                                  torch.from_numpy(idx).cuda(), sink.cuda(), hd ** -0.5, lse=lse)
+    oo, olse, bad = orc.sparse_attn(bf16_bits(q), bf16_bits(rows_a), bf16_bits(rows_b), idx,
+                                    sink.numpy(), np.float32(hd ** -0.5))
+    assert bad == 0
+    assert ds41.device_status() == 0
+    ok, err, worst = attn_close(o.float().cpu().numpy(), oo)
+    assert ok, (err, worst)
+    fin = np.isfinite(olse)
+    assert np.array_equal(np.isfinite(lse.cpu().numpy()), fin)
+    assert np.allclose(lse.cpu().numpy()[fin], olse[fin], atol=1e-3, rtol=1e-4)
+
+
 def test_sparse_attn_bad_index_sets_status(orc):
     nh, hd = 4, 64
     q = torch.randn(1, nh, hd).to(torch.bfloat16).cuda()
