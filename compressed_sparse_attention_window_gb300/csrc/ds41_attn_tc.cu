@@ -21,22 +21,27 @@
 //   S  = Q R^T       M = 64 heads, N = 64 rows, K = 512   (S in tensor memory)
 //   O^T += R^T P^T   M = 128 of hd (4 tiles), N = 64 heads, K = 64 rows
 //
-// With heads as the rows of S, one thread owns one head's scores, so the
-// running max and the denominator need no reductions across threads.  The
-// reference max of a head moves only when a chunk exceeds it by 2^4 (and on the
-// first chunk), so O is rescaled in tensor memory only on those rare chunks.
-// The bound trades accuracy for rescales: the largest weight of a head is then
-// up to 2^4 instead of exactly 1 and takes a bf16 rounding too; with 2^8 the
-// worst error on peaked softmaxes doubled, with 2^4 it stays within 1.3x of an
-// exact running maximum while N(0,1) scores almost never move the reference.
+// A tcgen05.mma instruction costs some 50 cycles of issue however small, so
+// the chunk is as wide as shared memory allows for two row buffers (64 rows),
+// the MMA sequences are fully unrolled on precomputed descriptors, and the
+// four PV tiles are independent accumulators issued in turn.  With heads as
+// the rows of S, the four threads of a quad own one head's scores, so the
+// running max and the denominator need two shuffles.  The reference max of a
+// head moves only when a chunk exceeds it by 2^4 (and on the first chunk), so
+// O is rescaled in tensor memory only on those chunks; the bound trades
+// accuracy for rescales (the largest weight of a head is then up to 2^4
+// instead of exactly 1 and takes a bf16 rounding too: with 2^8 the worst error
+// on peaked softmaxes doubled, with 2^4 it stays within 1.3x of an exact
+// running maximum).
 //
-// Warp roles (256 threads): warp 0 issues TMA copies, warp 1 owns tensor
+// Warp roles (384 threads): warp 0 issues TMA copies, warp 1 owns tensor
 // memory and (one lane) issues the MMAs, warp 2 builds the per-item plans one
-// item ahead, warps 4..7 run the softmax and the epilogue (warp 4+q reads
-// lane quarter q of tensor memory).  Shared memory: Q (64 KiB), two row chunks
-// (2 x 64 KiB), two P tiles (2 x 8 KiB), two plans.  Tensor memory: two S
-// buffers (64 columns each) and O^T (4 x 64 columns).  Every wait is bounded;
-// a timeout raises DS41_E_TIMEOUT and the CTA drains its copies and exits.
+// item ahead, warps 4..7 compute the probabilities, warps 8..11 rescale O when
+// a reference moves and write the normalised output of each item (warp 4+q
+// and 8+q use lane quarter q of tensor memory).  The softmax warps never wait
+// for a PV product or for the output stores.  Every hand-off is an mbarrier
+// with a bounded wait; a timeout raises DS41_E_TIMEOUT, and each role then
+// drains what it started and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -50,19 +55,22 @@ namespace tc {
 constexpr int HD = 512;
 constexpr int NH = 64;            // heads per work item
 constexpr int RC = 64;            // rows per chunk
-constexpr int THREADS = 256;
+constexpr int NRB = 2;            // row buffers (and S buffers)
+constexpr int THREADS = 384;
 constexpr int MAXK = 1024;        // longest index row this kernel takes
 constexpr int DCAP = 2048;        // longest row range loaded as consecutive rows
-constexpr int MAXCH = 64;         // chunks per item (dense <= DCAP/64 per source, lists <= MAXK/64)
+constexpr int MAXCH = 2 * DCAP / RC;  // chunks per item: two consecutive-row sources at most
+constexpr int OOB_ROW = 1 << 29;  // a row coordinate beyond every tensor (reads as zero)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 4.0f;
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t KB_BYTES = RC * 64 * 2;            // one 64-column block of 64 rows: 8 KiB
-constexpr uint32_t Q_OFF = 0;                         // 8 blocks of [64 heads][64 dims]
-constexpr uint32_t R_OFF = 65536;                     // 2 buffers x 8 blocks of [64 rows][64 dims]
-constexpr uint32_t R_BYTES = 65536;
-constexpr uint32_t P_OFF = R_OFF + 2 * R_BYTES;       // 2 buffers of [64 heads][64 rows] bf16
+constexpr uint32_t Q_KB = 64 * 64 * 2;                // Q block [64 heads][64 dims]: 8 KiB
+constexpr uint32_t R_KB = RC * 64 * 2;                // row block [64 rows][64 dims]: 8 KiB
+constexpr uint32_t Q_OFF = 0;                         // 8 Q blocks
+constexpr uint32_t R_OFF = 8 * Q_KB;                  // NRB buffers x 8 row blocks
+constexpr uint32_t R_BYTES = 8 * R_KB;
+constexpr uint32_t P_OFF = R_OFF + NRB * R_BYTES;     // 2 buffers of [64 heads][64 rows] bf16
 constexpr uint32_t P_BYTES = 8192;
 constexpr uint32_t PLAN_OFF = P_OFF + 2 * P_BYTES;    // 2 plans
 constexpr uint32_t PLAN_DESC = 0;                     // MAXCH x uint4
@@ -72,25 +80,33 @@ constexpr uint32_t PLAN_BYTES = PLAN_N + 64;
 constexpr uint32_t BM_OFF = PLAN_OFF + 2 * PLAN_BYTES;  // 2 sources x DCAP bits
 constexpr uint32_t BM_WORDS = DCAP / 32;
 constexpr uint32_t MISC_OFF = BM_OFF + 2 * BM_WORDS * 4;
-constexpr uint32_t MISC_BYTES = 1024;
+constexpr uint32_t MISC_BYTES = 3072;
 constexpr uint32_t SMEM_BYTES = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(PLAN_OFF % 16 == 0 && PLAN_BYTES % 16 == 0, "plan alignment");
 
 // barriers
 enum {
-    B_QFULL, B_QEMPTY, B_RFULL, B_RFULL1, B_SFULL, B_SFULL1, B_SEMPTY, B_SEMPTY1, B_PFULL,
-    B_PFULL1, B_DONE, B_DONE1, B_ODONE, B_OFREE, B_PLANFULL, B_PLANFULL1, B_PLANEMPTY,
-    B_PLANEMPTY1, B_FINAL, NBAR
+    B_QFULL, B_QEMPTY,
+    B_RFULL,                               // NRB: row chunk landed
+    B_DONE = B_RFULL + NRB,                // NRB: PV of the chunk complete (row and P buffers free)
+    B_SFULL = B_DONE + NRB,                // NRB: S of the chunk in tensor memory
+    B_SEMPTY = B_SFULL + NRB,              // NRB: S read by the softmax warps
+    B_CORR = B_SEMPTY + NRB,               // NRB: rescale factors of the chunk written
+    B_PFULL = B_CORR + NRB,                // 2: P written and O rescaled
+    B_ODONE = B_PFULL + 2, B_OFREE,
+    B_INVL, B_INVLFREE = B_INVL + 2,       // 2 each: per-item normalisers
+    B_PLANFULL = B_INVLFREE + 2, B_PLANEMPTY = B_PLANFULL + 2,
+    B_FINAL = B_PLANEMPTY + 2, NBAR
 };
 // misc area layout
 constexpr uint32_t M_BAR = 0;                   // NBAR x 8
-constexpr uint32_t M_TMEM = 256;                // tensor memory base address
-constexpr uint32_t M_ABORT = 260;               // set when any wait gave up
-constexpr uint32_t M_VOTE = 272;                // 2 x 4 ints
-constexpr uint32_t M_CORR = 320;                // 64 floats
-constexpr uint32_t M_INVL = 576;                // 64 floats
-static_assert(NBAR * 8 <= 256 && M_INVL + 256 <= MISC_BYTES, "misc layout");
+constexpr uint32_t M_TMEM = 512;                // tensor memory base address
+constexpr uint32_t M_ABORT = 516;               // set when any wait gave up
+constexpr uint32_t M_FLAG = 528;                // NRB x 4 ints: a warp's heads moved their reference
+constexpr uint32_t M_CORR = 1024;               // NRB x 64 floats
+constexpr uint32_t M_INVL = 2048;               // 2 x 64 floats
+static_assert(NBAR * 8 <= 512 && M_INVL + 512 <= MISC_BYTES, "misc layout");
 
 // tensor memory columns
 constexpr uint32_t TM_S = 0;     // S buffer b at column 64 b
@@ -177,6 +193,23 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[31])
         : "r"(taddr));
 }
+// 16 lanes x 64 columns, spread over the warp like an m16n8 accumulator:
+// register 4 j + e holds (lane base + l/4, column 8 j + 2 (l%4) + e) and
+// register 4 j + 2 + e holds (lane base + l/4 + 8, the same column), l the
+// thread's lane id.
+__device__ __forceinline__ void tc_ld16x256(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {"
+        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {"
@@ -195,9 +228,6 @@ __device__ __forceinline__ void tc_wait_ld() {
 __device__ __forceinline__ void tc_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
-__device__ __forceinline__ void named_sync_softmax() {
-    asm volatile("bar.sync 1, 128;\n" ::: "memory");
-}
 
 // Shared-memory matrix descriptor: 128-byte swizzle, start / leading /
 // stride byte offsets (each encoded >> 4), descriptor version 1.
@@ -211,8 +241,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t IDESC_S = idesc_bf16(64, 64, 0, 0);
-constexpr uint32_t IDESC_PV = idesc_bf16(128, 64, 1, 0);
 
 // A bounded wait that also gives up once another role has given up.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_f,
@@ -233,6 +261,9 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     return false;
 }
 
+constexpr uint32_t IDESC_S = idesc_bf16(64, RC, 0, 0);
+constexpr uint32_t IDESC_PV = idesc_bf16(128, 64, 1, 0);
+
 // Work item k of this CTA -> (token, head group): items are taken from the
 // end (longest index rows first when later tokens see more rows).
 __device__ __forceinline__ void item_of(int j, int m, int hg, int& t, int& g) {
@@ -242,12 +273,6 @@ __device__ __forceinline__ void item_of(int j, int m, int hg, int& t, int& g) {
     g = (int)(r % hg);
 }
 
-// ---------------------------------------------------------------------------
-// Plan warp: index row of one item -> chunk descriptors
-//   desc.x: bit 0 source (0 rows_a, 1 rows_b), bit 1 listed rows
-//   desc.y: first row of a consecutive chunk, or offset into the row list
-//   desc.z/w: mask of the chunk's 64 rows (row r selected iff bit r)
-// ---------------------------------------------------------------------------
 __device__ __forceinline__ int warp_sum(int v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -264,26 +289,43 @@ __device__ __forceinline__ int warp_max(int v) {
     return v;
 }
 
+// ---------------------------------------------------------------------------
+// Plan warp: index row of one item -> chunk descriptors
+//   desc.x: row (consecutive chunk) or list offset (listed chunk) in bits
+//           0..29, source in bit 30 (0 rows_a, 1 rows_b), listed in bit 31
+//   desc.y / desc.z: mask of the chunk's rows 0..31 / 32..63 (row r selected
+//           iff its bit is set)
+// ---------------------------------------------------------------------------
 __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, int lane) {
+    constexpr int KPL = MAXK / 32;  // index entries per lane
     uint4* desc = reinterpret_cast<uint4*>(plan + PLAN_DESC);
     int* list = reinterpret_cast<int*>(plan + PLAN_LIST);
     const int32_t* irow = p.idx + (int64_t)t * p.K;
     const int64_t n_rows = p.n_a + p.n_c;
     const int na = (int)p.n_a;
 
+    // the whole index row in registers (entry 32 k + lane), all loads in flight
+    // at once; invalid entries become -1
+    int vals[KPL];
+#pragma unroll
+    for (int k = 0; k < KPL; k++) {
+        const int j = 32 * k + lane;
+        vals[k] = j < p.K ? __ldg(irow + j) : -1;
+    }
     int cnt[2] = {0, 0}, mn[2] = {INT_MAX, INT_MAX}, mx[2] = {-1, -1};
-    for (int j = lane; j < p.K; j += 32) {
-        const int v = irow[j];
-        if (v == -1) continue;
+#pragma unroll
+    for (int k = 0; k < KPL; k++) {
+        const int v = vals[k];
         if (v < -1 || (int64_t)v >= n_rows) {
             raise_status(p.status, DS41_E_INDEX);
-            continue;
+            vals[k] = -1;
+        } else if (v >= 0) {
+            const int s = v >= na;
+            const int y = s ? v - na : v;
+            cnt[s]++;
+            mn[s] = min(mn[s], y);
+            mx[s] = max(mx[s], y);
         }
-        const int s = v >= na;
-        const int y = s ? v - na : v;
-        cnt[s]++;
-        mn[s] = min(mn[s], y);
-        mx[s] = max(mx[s], y);
     }
     bool dense[2];
     int range[2];
@@ -293,18 +335,19 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
         mn[s] = warp_min(mn[s]);
         mx[s] = warp_max(mx[s]);
         range[s] = cnt[s] ? mx[s] - mn[s] + 1 : 0;
-        dense[s] = cnt[s] > 0 && range[s] <= DCAP && range[s] <= 2 * cnt[s] + RC;
+        dense[s] = cnt[s] > 0 && range[s] <= DCAP && range[s] <= 2 * cnt[s] + 2 * RC;
         if (dense[s]) {
-            const int nw = ((range[s] + RC - 1) / RC) * 2;
+            const int nw = 2 * ((range[s] + RC - 1) / RC);
             for (int w = lane; w < nw; w += 32) bm[s * BM_WORDS + w] = 0u;
         }
     }
     __syncwarp();
     if (dense[0] || dense[1]) {
         bool dup[2] = {false, false};
-        for (int j = lane; j < p.K; j += 32) {
-            const int v = irow[j];
-            if (v < 0 || (int64_t)v >= n_rows) continue;
+#pragma unroll
+        for (int k = 0; k < KPL; k++) {
+            const int v = vals[k];
+            if (v < 0) continue;
             const int s = v >= na;
             if (!dense[s]) continue;
             const int bit = (s ? v - na : v) - mn[s];
@@ -323,10 +366,10 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
     for (int s = 0; s < 2; s++) {
         if (dense[s] || cnt[s] == 0) continue;
         off[s] = pos;
-        for (int base = 0; base < p.K; base += 32) {
-            const int j = base + lane;
-            const int v = j < p.K ? irow[j] : -1;
-            const bool take = v >= 0 && (int64_t)v < n_rows && ((v >= na) == (s == 1));
+#pragma unroll
+        for (int k = 0; k < KPL; k++) {
+            const int v = vals[k];
+            const bool take = v >= 0 && ((v >= na) == (s == 1));
             const uint32_t bal = __ballot_sync(0xffffffffu, take);
             if (take) list[pos + __popc(bal & lt)] = s ? v - na : v;
             pos += __popc(bal);
@@ -336,20 +379,18 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
 #pragma unroll
     for (int s = 0; s < 2; s++) {
         if (cnt[s] == 0) continue;
+        const uint32_t sbit = (uint32_t)s << 30;
         if (dense[s]) {
             const int nck = (range[s] + RC - 1) / RC;
             for (int base = 0; base < nck; base += 32) {
                 const int i = base + lane;
-                uint32_t lo = 0, hi = 0;
-                if (i < nck) {
-                    lo = bm[s * BM_WORDS + 2 * i];
-                    hi = bm[s * BM_WORDS + 2 * i + 1];
-                }
+                const uint32_t lo = i < nck ? bm[s * BM_WORDS + 2 * i] : 0u;
+                const uint32_t hi = i < nck ? bm[s * BM_WORDS + 2 * i + 1] : 0u;
                 const bool keep = (lo | hi) != 0u;
                 const uint32_t bal = __ballot_sync(0xffffffffu, keep);
                 if (keep)
                     desc[nch + __popc(bal & lt)] =
-                        make_uint4((uint32_t)s, (uint32_t)(mn[s] + RC * i), lo, hi);
+                        make_uint4((uint32_t)(mn[s] + RC * i) | sbit, lo, hi, 0u);
                 nch += __popc(bal);
             }
         } else {
@@ -358,13 +399,13 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
                 const int n = min(RC, cnt[s] - RC * i);
                 const uint32_t lo = n >= 32 ? 0xffffffffu : ((1u << n) - 1u);
                 const uint32_t hi = n >= 64 ? 0xffffffffu : (n > 32 ? ((1u << (n - 32)) - 1u) : 0u);
-                desc[nch + i] = make_uint4((uint32_t)s | 2u, (uint32_t)(off[s] + RC * i), lo, hi);
+                desc[nch + i] = make_uint4((uint32_t)(off[s] + RC * i) | sbit | 0x80000000u, lo, hi, 0u);
             }
             nch += nck;
         }
     }
     if (nch == 0) {  // nothing valid: one fully masked chunk of out-of-range (zero) rows
-        if (lane == 0) desc[0] = make_uint4(0u, 1u << 30, 0u, 0u);
+        if (lane == 0) desc[0] = make_uint4((uint32_t)OOB_ROW, 0u, 0u, 0u);
         nch = 1;
     }
     if (lane == 0) *reinterpret_cast<int*>(plan + PLAN_N) = nch;
@@ -387,7 +428,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + MISC_OFF + M_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + MISC_OFF + M_TMEM);
     volatile int* abort_f = reinterpret_cast<volatile int*>(sm + MISC_OFF + M_ABORT);
-    int* vote = reinterpret_cast<int*>(sm + MISC_OFF + M_VOTE);
+    int* flags = reinterpret_cast<int*>(sm + MISC_OFF + M_FLAG);
     float* corr_s = reinterpret_cast<float*>(sm + MISC_OFF + M_CORR);
     float* invl_s = reinterpret_cast<float*>(sm + MISC_OFF + M_INVL);
     uint32_t* bm = reinterpret_cast<uint32_t*>(sm + BM_OFF);
@@ -401,14 +442,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bars[B_QFULL], 1);
         mbar_init(&bars[B_QEMPTY], 1);
-        for (int b = 0; b < 2; b++) {
+        for (int b = 0; b < NRB; b++) {
             mbar_init(&bars[B_RFULL + b], 1);
+            mbar_init(&bars[B_DONE + b], 1);
             mbar_init(&bars[B_SFULL + b], 1);
             mbar_init(&bars[B_SEMPTY + b], 4);
-            mbar_init(&bars[B_PFULL + b], 4);
-            mbar_init(&bars[B_DONE + b], 1);
+            mbar_init(&bars[B_CORR + b], 4);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&bars[B_PFULL + b], 8);
+            mbar_init(&bars[B_INVL + b], 4);
+            mbar_init(&bars[B_INVLFREE + b], 4);
             mbar_init(&bars[B_PLANFULL + b], 1);
-            mbar_init(&bars[B_PLANEMPTY + b], 2);
+            mbar_init(&bars[B_PLANEMPTY + b], 6);  // producer, 4 softmax warps, correction
         }
         mbar_init(&bars[B_ODONE], 1);
         mbar_init(&bars[B_OFREE], 4);
@@ -435,53 +481,53 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------------
         if (lane == 0) {
             uint32_t g = 0;
-            uint32_t q_armed = 0, r_armed[2] = {0, 0};
+            uint32_t q_armed = 0, r_armed[NRB] = {0, 0};
             for (int j = 0; j < ntok; j++) {
                 int t, hgi;
                 item_of(j, p.m, hg, t, hgi);
                 const int slot = j & 1;
                 if (!wait_bar(&bars[B_PLANFULL + slot], (j >> 1) & 1, abort_f, p.status)) break;
                 if (j >= 1 && !wait_bar(&bars[B_QEMPTY], (j - 1) & 1, abort_f, p.status)) break;
-                mbar_arrive_expect_tx(&bars[B_QFULL], 8 * KB_BYTES);
+                mbar_arrive_expect_tx(&bars[B_QFULL], 8 * Q_KB);
                 q_armed++;
                 const int qrow = t * p.nh + hgi * NH;
                 for (int kb = 0; kb < 8; kb++)
-                    tma_load_2d(sbase + Q_OFF + kb * KB_BYTES, &map_q, kb * 64, qrow,
-                                &bars[B_QFULL]);
+                    tma_load_2d(sbase + Q_OFF + kb * Q_KB, &map_q, kb * 64, qrow, &bars[B_QFULL]);
                 const uint8_t* plan = sm + PLAN_OFF + slot * PLAN_BYTES;
                 const uint4* desc = reinterpret_cast<const uint4*>(plan + PLAN_DESC);
                 const int* list = reinterpret_cast<const int*>(plan + PLAN_LIST);
                 const int nch = *reinterpret_cast<const int*>(plan + PLAN_N);
                 bool ok = true;
                 for (int i = 0; i < nch; i++, g++) {
-                    const int b = g & 1;
-                    if (g >= 2 && !wait_bar(&bars[B_DONE + b], ((g - 2) >> 1) & 1, abort_f,
-                                            p.status)) {
+                    const int b = g % NRB;
+                    if (g >= NRB && !wait_bar(&bars[B_DONE + b], ((g - NRB) / NRB) & 1, abort_f,
+                                              p.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars[B_RFULL + b], 8 * KB_BYTES);
+                    mbar_arrive_expect_tx(&bars[B_RFULL + b], 8 * R_KB);
                     r_armed[b]++;
                     const uint4 d = desc[i];
+                    const int pos = (int)(d.x & 0x3FFFFFFFu);
+                    const bool src_b = (d.x >> 30) & 1u;
                     const uint32_t rb = sbase + R_OFF + b * R_BYTES;
-                    if (!(d.x & 2u)) {
-                        const CUtensorMap* mp = (d.x & 1u) ? &map_bd : &map_ad;
+                    if (!(d.x & 0x80000000u)) {
+                        const CUtensorMap* mp = src_b ? &map_bd : &map_ad;
                         for (int kb = 0; kb < 8; kb++)
-                            tma_load_2d(rb + kb * KB_BYTES, mp, kb * 64, (int)d.y,
-                                        &bars[B_RFULL + b]);
+                            tma_load_2d(rb + kb * R_KB, mp, kb * 64, pos, &bars[B_RFULL + b]);
                     } else {
-                        const CUtensorMap* mp = (d.x & 1u) ? &map_bg : &map_ag;
-                        const int cnt = __popc(d.z) + __popc(d.w);
-                        const int* lr = list + d.y;
+                        const CUtensorMap* mp = src_b ? &map_bg : &map_ag;
+                        const int cnt = __popc(d.y) + __popc(d.z);
+                        const int* lr = list + pos;
                         for (int gq = 0; gq < RC / 4; gq++) {
                             int y[4];
 #pragma unroll
                             for (int k = 0; k < 4; k++) {
                                 const int r = 4 * gq + k;
-                                y[k] = r < cnt ? lr[r] : (1 << 30);  // beyond the list: zero fill
+                                y[k] = r < cnt ? lr[r] : OOB_ROW;  // beyond the list: zero fill
                             }
                             for (int kb = 0; kb < 8; kb++)
-                                tma_gather4(rb + kb * KB_BYTES + gq * 512, mp, kb * 64, y[0], y[1],
+                                tma_gather4(rb + kb * R_KB + gq * 512, mp, kb * 64, y[0], y[1],
                                             y[2], y[3], &bars[B_RFULL + b]);
                         }
                     }
@@ -491,12 +537,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // let every copy this CTA started land before the CTA exits
             if (q_armed) wait_bar(&bars[B_QFULL], (q_armed - 1) & 1, abort_f, p.status);
-            for (int b = 0; b < 2; b++)
+            for (int b = 0; b < NRB; b++)
                 if (r_armed[b]) wait_bar(&bars[B_RFULL + b], (r_armed[b] - 1) & 1, abort_f, p.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
-        // MMA issuer (one lane): S(g) may run one chunk ahead of PV(g-1)
+        // MMA issuer (one lane): S may run up to NRB - 1 chunks ahead of PV
         // ------------------------------------------------------------------
         if (lane == 0) {
             int s_tok = 0, s_i = 0, s_n = -1;
@@ -507,27 +553,30 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t q_s = sbase + Q_OFF;
             while (p_tok < ntok) {
                 bool prog = false;
-                if (s_tok < ntok) {
+                if (s_tok < ntok && s_tok < p_tok + 3) {
                     if (s_n < 0 && mbar_test(&bars[B_PLANFULL + (s_tok & 1)], (s_tok >> 1) & 1)) {
                         s_n = *reinterpret_cast<const int*>(sm + PLAN_OFF +
                                                             (s_tok & 1) * PLAN_BYTES + PLAN_N);
                         nring[s_tok & 3] = s_n;
                     }
-                    if (s_n > 0 && sg < pg + 2) {
-                        const int b = sg & 1;
+                    if (s_n > 0 && sg < pg + NRB) {
+                        const int b = sg % NRB;
                         const bool ok =
-                            mbar_test(&bars[B_RFULL + b], (sg >> 1) & 1) &&
-                            (sg < 2 || mbar_test(&bars[B_SEMPTY + b], ((sg - 2) >> 1) & 1)) &&
+                            mbar_test(&bars[B_RFULL + b], (sg / NRB) & 1) &&
+                            (sg < NRB || mbar_test(&bars[B_SEMPTY + b], ((sg - NRB) / NRB) & 1)) &&
                             (s_i > 0 || mbar_test(&bars[B_QFULL], s_tok & 1));
                         if (ok) {
                             tc_fence_after();
-                            const uint32_t r_s = sbase + R_OFF + b * R_BYTES;
-                            const uint32_t d = tmem + TM_S + 64 * b;
-#pragma unroll 4
+                            // S = Q R^T over K = 512: 32 MMAs on descriptors that
+                            // step by a compile-time offset (16-byte units)
+                            const uint64_t qd = sdesc(q_s, 16, 1024);
+                            const uint64_t rd = sdesc(sbase + R_OFF + b * R_BYTES, 16, 1024);
+                            const uint32_t d = tmem + TM_S + RC * b;
+#pragma unroll
                             for (int kk = 0; kk < HD / 16; kk++) {
-                                const uint32_t off = (kk >> 2) * KB_BYTES + (kk & 3) * 32;
-                                tc_mma(d, sdesc(q_s + off, 16, 1024), sdesc(r_s + off, 16, 1024),
-                                       IDESC_S, kk > 0);
+                                tc_mma(d, qd + (((kk >> 2) * Q_KB + (kk & 3) * 32) >> 4),
+                                       rd + (((kk >> 2) * R_KB + (kk & 3) * 32) >> 4), IDESC_S,
+                                       kk > 0 ? 1u : 0u);
                             }
                             tc_commit(&bars[B_SFULL + b]);
                             if (s_i == s_n - 1) tc_commit(&bars[B_QEMPTY]);
@@ -542,23 +591,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 if (pg < sg) {
-                    const int b = pg & 1;
+                    const int b = pg % NRB, pb = pg & 1;
                     const bool ok =
-                        mbar_test(&bars[B_PFULL + b], (pg >> 1) & 1) &&
+                        mbar_test(&bars[B_PFULL + pb], (pg >> 1) & 1) &&
                         (p_i > 0 || p_tok == 0 || mbar_test(&bars[B_OFREE], (p_tok - 1) & 1));
                     if (ok) {
                         tc_fence_after();
-                        const uint32_t r_s = sbase + R_OFF + b * R_BYTES;
-                        const uint32_t p_s = sbase + P_OFF + b * P_BYTES;
+                        // O^T += R^T P^T: the four head-dim tiles are independent
+                        // accumulators, issued in turn for each 16-row step
+                        const uint64_t vd = sdesc(sbase + R_OFF + b * R_BYTES, R_KB, 1024);
+                        const uint64_t pd = sdesc(sbase + P_OFF + pb * P_BYTES, 16, 1024);
+                        const uint32_t acc0 = p_i > 0 ? 1u : 0u;
 #pragma unroll
-                        for (int mt = 0; mt < 4; mt++) {
-                            const uint32_t d = tmem + TM_O + 64 * mt;
+                        for (int kk = 0; kk < RC / 16; kk++)
 #pragma unroll
-                            for (int kk = 0; kk < RC / 16; kk++)
-                                tc_mma(d, sdesc(r_s + 2 * mt * KB_BYTES + kk * 2048, KB_BYTES, 1024),
-                                       sdesc(p_s + kk * 32, 16, 1024), IDESC_PV,
-                                       (p_i > 0 || kk > 0) ? 1u : 0u);
-                        }
+                            for (int mt = 0; mt < 4; mt++)
+                                tc_mma(tmem + TM_O + 64 * mt,
+                                       vd + ((2 * mt * R_KB + kk * 2048) >> 4),
+                                       pd + ((kk * 32) >> 4), IDESC_PV, kk > 0 ? 1u : acc0);
                         tc_commit(&bars[B_DONE + b]);
                         const int pn = nring[p_tok & 3];
                         if (p_i == pn - 1) tc_commit(&bars[B_ODONE]);
@@ -600,166 +650,237 @@ __global__ void __launch_bounds__(THREADS, 1)
             plan_item(p, t, sm + PLAN_OFF + slot * PLAN_BYTES, bm, lane);
             if (lane == 0) mbar_arrive(&bars[B_PLANFULL + slot]);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------------
-        // Softmax + epilogue: warp 4+q reads lane quarter q; with M = 64 the
-        // scores of head 16q + l sit in lane 32q + l (l < 16), one column per
-        // row of the chunk.
+        // Softmax: warp 4+q reads lane quarter q.  With M = 64 the scores of
+        // head 16q + r sit in lane 32q + r (r < 16), one column per row of
+        // the chunk; the 16x256b read gives thread l the heads hA = 16q + l/4
+        // and hB = hA + 8, 16 columns each.
         // ------------------------------------------------------------------
         const int q = warp - 4;
-        const int tid = threadIdx.x - 128;
-        const bool own = lane < 16;
-        const int hl = 16 * q + lane;  // this thread's head (own lanes)
+        const int qi = lane & 3;
+        const int hA = 16 * q + (lane >> 2), hB = hA + 8;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t g = 0;
-        bool bad = false;  // a wait of this thread gave up
         for (int j = 0; j < ntok; j++) {
             int t, hgi;
             item_of(j, p.m, hg, t, hgi);
             const int slot = j & 1;
-            if (!wait_bar(&bars[B_PLANFULL + slot], (j >> 1) & 1, abort_f, p.status)) bad = true;
+            if (!wait_bar(&bars[B_PLANFULL + slot], (j >> 1) & 1, abort_f, p.status)) break;
             const uint8_t* plan = sm + PLAN_OFF + slot * PLAN_BYTES;
             const uint4* desc = reinterpret_cast<const uint4*>(plan + PLAN_DESC);
-            const int nch = bad ? 1 : *reinterpret_cast<const int*>(plan + PLAN_N);
-            float m_ref = -INFINITY, l = 0.0f;
-            bool stop = false;
+            const int nch = *reinterpret_cast<const int*>(plan + PLAN_N);
+            // per head: reference max (log2 units) and this thread's part of the
+            // denominator (the quad's four parts add up to it)
+            float mA = -INFINITY, mB = -INFINITY, lA = 0.0f, lB = 0.0f;
+            bool bad = false;
             for (int i = 0; i < nch; i++, g++) {
-                const int b = g & 1;
-                const uint4 d = bad ? make_uint4(0, 0, 0, 0) : desc[i];
-                if (!bad && !wait_bar(&bars[B_SFULL + b], (g >> 1) & 1, abort_f, p.status))
+                const int b = g % NRB;
+                const uint4 dsc = desc[i];
+                __syncwarp();
+                if (i == nch - 1 && lane == 0)
+                    mbar_arrive(&bars[B_PLANEMPTY + slot]);  // this warp's last read of the plan
+                if (!wait_bar(&bars[B_SFULL + b], (g / NRB) & 1, abort_f, p.status)) {
                     bad = true;
+                    break;
+                }
                 tc_fence_after();
-                uint32_t s0[32], s1[32];
-                tc_ld32(tmem + lane_off + TM_S + 64 * b, s0);
-                tc_ld32(tmem + lane_off + TM_S + 64 * b + 32, s1);
+                uint32_t sr[32];
+                tc_ld16x256(tmem + lane_off + TM_S + RC * b, sr);
                 tc_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_SEMPTY + b]);
-                // scaled scores (log2 units) and the chunk max over selected rows
-                float mx = -INFINITY;
+                // scaled scores (log2 units), -inf where the row is not selected
+                const uint32_t mlo = dsc.y >> (2 * qi), mhi = dsc.z >> (2 * qi);
+                float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < 32; k++) {
-                    const float x0 = __uint_as_float(s0[k]) * p.scale_log2;
-                    const float x1 = __uint_as_float(s1[k]) * p.scale_log2;
-                    s0[k] = __float_as_uint(((d.z >> k) & 1u) ? x0 : -INFINITY);
-                    s1[k] = __float_as_uint(((d.w >> k) & 1u) ? x1 : -INFINITY);
-                    mx = fmaxf(mx, fmaxf(__uint_as_float(s0[k]), __uint_as_float(s1[k])));
+                for (int jr = 0; jr < 8; jr++) {
+#pragma unroll
+                    for (int e = 0; e < 2; e++) {
+                        const bool sel = ((jr < 4 ? mlo : mhi) >> (8 * (jr & 3) + e)) & 1u;
+                        const float xa = sel ? __uint_as_float(sr[4 * jr + e]) * p.scale_log2 : -INFINITY;
+                        const float xb =
+                            sel ? __uint_as_float(sr[4 * jr + 2 + e]) * p.scale_log2 : -INFINITY;
+                        sr[4 * jr + e] = __float_as_uint(xa);
+                        sr[4 * jr + 2 + e] = __float_as_uint(xb);
+                        mxA = fmaxf(mxA, xa);
+                        mxB = fmaxf(mxB, xb);
+                    }
                 }
-                bool need = false;
-                if (i == 0) m_ref = mx;
-                else need = own && mx > m_ref + RESCALE_LOG2;
-                // one vote per chunk: a rescale anywhere, or a wait that gave up
-                const uint32_t v = (__any_sync(0xffffffffu, need) ? 1u : 0u) |
-                                   (__any_sync(0xffffffffu, bad) ? 2u : 0u);
-                if (lane == 0) vote[b * 4 + q] = (int)v;
-                named_sync_softmax();
-                const int all = vote[b * 4 + 0] | vote[b * 4 + 1] | vote[b * 4 + 2] | vote[b * 4 + 3];
-                if (all & 2) {
-                    stop = true;
+                mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+                mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+                mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+                mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+                float cA = 1.0f, cB = 1.0f;
+                if (i == 0) {
+                    mA = mxA;
+                    mB = mxB;
+                } else {
+                    if (mxA > mA + RESCALE_LOG2) {
+                        cA = exp2f(mA - mxA);
+                        mA = mxA;
+                        lA *= cA;
+                    }
+                    if (mxB > mB + RESCALE_LOG2) {
+                        cB = exp2f(mB - mxB);
+                        mB = mxB;
+                        lB *= cB;
+                    }
+                }
+                // hand the rescale factors of this chunk to the correction warps
+                const bool moved = __any_sync(0xffffffffu, cA != 1.0f || cB != 1.0f);
+                if (qi == 0) {
+                    corr_s[b * 64 + hA] = cA;
+                    corr_s[b * 64 + hB] = cB;
+                }
+                if (lane == 0) flags[b * 4 + q] = moved ? 1 : 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_CORR + b]);
+                // probabilities, the denominator, P (bf16) for the PV MMA
+                const float muA = (mA == -INFINITY) ? 0.0f : mA;
+                const float muB = (mB == -INFINITY) ? 0.0f : mB;
+                uint32_t pkA[8], pkB[8];
+#pragma unroll
+                for (int jr = 0; jr < 8; jr++) {
+                    const float a0 = exp2f(__uint_as_float(sr[4 * jr]) - muA);
+                    const float a1 = exp2f(__uint_as_float(sr[4 * jr + 1]) - muA);
+                    const float b0 = exp2f(__uint_as_float(sr[4 * jr + 2]) - muB);
+                    const float b1 = exp2f(__uint_as_float(sr[4 * jr + 3]) - muB);
+                    lA += a0 + a1;
+                    lB += b0 + b1;
+                    pkA[jr] = pack_bf16x2(a0, a1);
+                    pkB[jr] = pack_bf16x2(b0, b1);
+                }
+                const int pb = g & 1;
+                if (g >= 2 && !wait_bar(&bars[B_DONE + (g - 2) % NRB], ((g - 2) / NRB) & 1, abort_f,
+                                        p.status)) {
+                    bad = true;
                     break;
                 }
-                if (i == nch - 1 && tid == 0) mbar_arrive(&bars[B_PLANEMPTY + slot]);
-                if (all & 1) {
-                    // move the reference of the heads that need it; rescale O^T
-                    float corr = 1.0f;
-                    if (need) {
-                        corr = exp2f(m_ref - mx);
-                        m_ref = mx;
-                        l *= corr;
+                {
+                    // row h of P: 8 chunks of 16 bytes (8 rows each), swizzled
+                    // by h % 8; this thread writes 4 bytes of each
+                    uint8_t* pbuf = sm + P_OFF + pb * P_BYTES;
+                    uint8_t* ra = pbuf + (hA >> 3) * 1024 + (hA & 7) * 128 + 4 * qi;
+                    uint8_t* rbp = pbuf + (hB >> 3) * 1024 + (hB & 7) * 128 + 4 * qi;
+#pragma unroll
+                    for (int jr = 0; jr < 8; jr++) {
+                        *reinterpret_cast<uint32_t*>(ra + ((jr ^ (hA & 7)) << 4)) = pkA[jr];
+                        *reinterpret_cast<uint32_t*>(rbp + ((jr ^ (hB & 7)) << 4)) = pkB[jr];
                     }
-                    if (own) corr_s[hl] = corr;
-                    if (!wait_bar(&bars[B_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_f,
-                                  p.status))
-                        bad = true;
-                    tc_fence_after();
-                    named_sync_softmax();
-                    if (!bad) {
-#pragma unroll 1
-                        for (int mt = 0; mt < 4; mt++) {
-#pragma unroll 1
-                            for (int hh = 0; hh < 2; hh++) {
-                                uint32_t ov[32];
-                                const uint32_t ta = tmem + lane_off + TM_O + 64 * mt + 32 * hh;
-                                tc_ld32(ta, ov);
-                                tc_wait_ld();
-#pragma unroll
-                                for (int k = 0; k < 32; k++)
-                                    ov[k] = __float_as_uint(__uint_as_float(ov[k]) *
-                                                            corr_s[32 * hh + k]);
-                                tc_st32(ta, ov);
-                            }
-                        }
-                        tc_wait_st();
-                    }
-                }
-                // probabilities, the denominator, P (bf16) for the PV MMA
-                const float mu = (m_ref == -INFINITY) ? 0.0f : m_ref;
-                float lsum = 0.0f;
-                uint32_t pk[32];
-#pragma unroll
-                for (int k = 0; k < 16; k++) {
-                    const float a0 = exp2f(__uint_as_float(s0[2 * k]) - mu);
-                    const float a1 = exp2f(__uint_as_float(s0[2 * k + 1]) - mu);
-                    const float c0 = exp2f(__uint_as_float(s1[2 * k]) - mu);
-                    const float c1 = exp2f(__uint_as_float(s1[2 * k + 1]) - mu);
-                    lsum += (a0 + a1) + (c0 + c1);
-                    pk[k] = pack_bf16x2(a0, a1);
-                    pk[16 + k] = pack_bf16x2(c0, c1);
-                }
-                l += lsum;
-                if (g >= 2 && !bad &&
-                    !wait_bar(&bars[B_DONE + b], ((g - 2) >> 1) & 1, abort_f, p.status))
-                    bad = true;
-                if (own) {
-                    // row hl of P: 128 bytes = 8 chunks of 16, swizzled by hl % 8
-                    uint8_t* prow = sm + P_OFF + b * P_BYTES + (hl >> 3) * 1024 + (hl & 7) * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; c++)
-                        *reinterpret_cast<uint4*>(prow + ((c ^ (hl & 7)) << 4)) =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 }
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_PFULL + b]);
+                if (lane == 0) mbar_arrive(&bars[B_PFULL + pb]);
             }
-            if (stop) break;
-            // ---- epilogue of this item ----
-            const int h = hgi * NH + hl;
-            if (own) {
+            if (bad) break;
+            // ---- normalisers of this item for the correction warps ----
+            lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+            lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+            lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+            lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+            if (j >= 2 && !wait_bar(&bars[B_INVLFREE + slot], ((j - 2) >> 1) & 1, abort_f, p.status))
+                break;
+            if (qi < 2) {
+                const int hl = qi == 0 ? hA : hB;
+                const float mr = qi == 0 ? mA : mB;
+                const float l = qi == 0 ? lA : lB;
+                const int h = hgi * NH + hl;
                 const float sk = p.sink[h] * LOG2E;
-                const float M = fmaxf(m_ref, sk);
+                const float M = fmaxf(mr, sk);
                 const float Mr = (M == -INFINITY) ? 0.0f : M;
-                const float a = exp2f(m_ref - Mr);
+                const float a = exp2f(mr - Mr);
                 const float L = l * a + exp2f(sk - Mr);
-                invl_s[hl] = (L > 0.0f) ? a / L : 0.0f;
+                invl_s[slot * 64 + hl] = (L > 0.0f) ? a / L : 0.0f;
                 if (p.lse) p.lse[(int64_t)t * p.nh + h] = (Mr + log2f(L)) / LOG2E;
             }
-            if (!bad && !wait_bar(&bars[B_ODONE], j & 1, abort_f, p.status)) bad = true;
-            tc_fence_after();
-            named_sync_softmax();
-            if (!bad) {
-                uint16_t* obase = p.o + ((int64_t)t * p.nh + hgi * NH) * HD;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_INVL + slot]);
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------------
+        // Correction + epilogue: warp 8+q owns lanes 32q.. of O^T (head dims
+        // 128 mt + 32 q + lane of tile mt, one column per head).
+        // ------------------------------------------------------------------
+        const int q = warp - 8;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        uint32_t g = 0;
+        for (int j = 0; j < ntok; j++) {
+            int t, hgi;
+            item_of(j, p.m, hg, t, hgi);
+            const int slot = j & 1;
+            if (!wait_bar(&bars[B_PLANFULL + slot], (j >> 1) & 1, abort_f, p.status)) break;
+            const int nch =
+                *reinterpret_cast<const int*>(sm + PLAN_OFF + slot * PLAN_BYTES + PLAN_N);
+            __syncwarp();
+            if (warp == 8 && lane == 0) mbar_arrive(&bars[B_PLANEMPTY + slot]);
+            bool bad = false;
+            for (int i = 0; i < nch; i++, g++) {
+                const int b = g % NRB;
+                if (!wait_bar(&bars[B_CORR + b], (g / NRB) & 1, abort_f, p.status)) {
+                    bad = true;
+                    break;
+                }
+                const int moved = flags[b * 4 + 0] | flags[b * 4 + 1] | flags[b * 4 + 2] |
+                                  flags[b * 4 + 3];
+                if (moved) {
+                    // O^T holds the chunks before this one once PV(g-1) is done
+                    if (!wait_bar(&bars[B_DONE + (g - 1) % NRB], ((g - 1) / NRB) & 1, abort_f,
+                                  p.status)) {
+                        bad = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float* cf = corr_s + b * 64;
 #pragma unroll 1
-                for (int mt = 0; mt < 4; mt++) {
-                    const int dd = 128 * mt + 32 * q + lane;
+                    for (int mt = 0; mt < 4; mt++) {
 #pragma unroll 1
-                    for (int hh = 0; hh < 2; hh++) {
-                        uint32_t ov[32];
-                        tc_ld32(tmem + lane_off + TM_O + 64 * mt + 32 * hh, ov);
-                        tc_wait_ld();
+                        for (int hh = 0; hh < 2; hh++) {
+                            uint32_t ov[32];
+                            const uint32_t ta = tmem + lane_off + TM_O + 64 * mt + 32 * hh;
+                            tc_ld32(ta, ov);
+                            tc_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; k++) {
-                            const int c = 32 * hh + k;
-                            obase[(int64_t)c * HD + dd] = f2bf(__uint_as_float(ov[k]) * invl_s[c]);
+                            for (int k = 0; k < 32; k++)
+                                ov[k] = __float_as_uint(__uint_as_float(ov[k]) * cf[32 * hh + k]);
+                            tc_st32(ta, ov);
                         }
+                    }
+                    tc_wait_st();
+                    tc_fence_before();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_PFULL + (g & 1)]);
+            }
+            if (bad) break;
+            // ---- epilogue of this item ----
+            if (!wait_bar(&bars[B_INVL + slot], (j >> 1) & 1, abort_f, p.status)) break;
+            if (!wait_bar(&bars[B_ODONE], j & 1, abort_f, p.status)) break;
+            tc_fence_after();
+            const float* inv = invl_s + slot * 64;
+            uint16_t* obase = p.o + ((int64_t)t * p.nh + hgi * NH) * HD;
+#pragma unroll 1
+            for (int mt = 0; mt < 4; mt++) {
+                const int dd = 128 * mt + 32 * q + lane;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t ov[32];
+                    tc_ld32(tmem + lane_off + TM_O + 64 * mt + 32 * hh, ov);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; k++) {
+                        const int c = 32 * hh + k;
+                        obase[(int64_t)c * HD + dd] = f2bf(__uint_as_float(ov[k]) * inv[c]);
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_OFREE]);
+            if (lane == 0) {
+                mbar_arrive(&bars[B_INVLFREE + slot]);
+                mbar_arrive(&bars[B_OFREE]);
+            }
         }
     }
 
@@ -820,6 +941,9 @@ int attn_tc_launch(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const
                    uint16_t* o, float* lse, int64_t m, int64_t nh, unsigned int* status,
                    int sms, cudaStream_t st) {
     using namespace tc;
+    if (n_a >= OOB_ROW || n_c >= OOB_ROW)
+        return fail(DS41_E_RANGE, "ds41_sparse_attn_sink_fwd: %lld + %lld rows exceed the row range",
+                    (long long)n_a, (long long)n_c);
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int rc = get_encode(&enc);
     if (rc) return rc;
