@@ -42,12 +42,8 @@
 // for a PV product or for the output stores.  Every hand-off is an mbarrier
 // with a bounded wait; a timeout raises DS41_E_TIMEOUT, and each role then
 // drains what it started and exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "ds41_internal.cuh"
+#include "ds41_tc.cuh"
 
 namespace ds41 {
 namespace tc {
@@ -125,141 +121,6 @@ struct Params {
     float* lse;
     unsigned int* status;
 };
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0,
-                                            int y1, int y2, int y3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-        "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t acc) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-// 32 consecutive columns of this warp's 32 lanes: r[i] = column col + i of
-// lane (lane quarter base + lane id).
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
-        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-}
-// 16 lanes x 64 columns, spread over the warp like an m16n8 accumulator:
-// register 4 j + e holds (lane base + l/4, column 8 j + 2 (l%4) + e) and
-// register 4 j + 2 + e holds (lane base + l/4 + 8, the same column), l the
-// thread's lane id.
-__device__ __forceinline__ void tc_ld16x256(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {"
-        "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {"
-        "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tc_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: 128-byte swizzle, start / leading /
-// stride byte offsets (each encoded >> 4), descriptor version 1.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Instruction descriptor of kind::f16: bf16 A and B, f32 accumulator, the
-// majorness of A and B (0 = K-major, 1 = M/N-major), N and M.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// A bounded wait that also gives up once another role has given up.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_f,
-                                         unsigned int* status) {
-    for (uint32_t i = 0; i < kWaitPolls; i++) {
-        uint32_t done;
-        asm volatile(
-            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            "selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((i & 63u) == 63u && *abort_f) return false;
-    }
-    *abort_f = 1;
-    raise_status(status, DS41_E_TIMEOUT);
-    return false;
-}
 
 constexpr uint32_t IDESC_S = idesc_bf16(64, RC, 0, 0);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 64, 1, 0);
@@ -896,39 +757,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and the launch
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-static std::mutex g_encode_mu;
-
-static int get_encode(PFN_cuTensorMapEncodeTiled_v12000* out) {
-    std::lock_guard<std::mutex> lk(g_encode_mu);
-    if (!g_encode) {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &qr);
-        if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn)
-            return fail(DS41_E_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    *out = g_encode;
-    return DS41_OK;
-}
-
-// 2-D bf16 map over [rows][512] with a box of 64 columns x box_rows rows and
-// the 128-byte swizzle; elements outside the tensor read as zero.
-static int make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* ptr,
-                    int64_t rows, int box_rows) {
-    cuuint64_t dims[2] = {(cuuint64_t)HD, (cuuint64_t)(rows > 0 ? rows : 1)};
-    cuuint64_t strides[1] = {(cuuint64_t)HD * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(DS41_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return DS41_OK;
-}
-
 }  // namespace tc
 
 bool attn_tc_supported(int64_t m, int64_t nh, int64_t hd, int64_t K, int sms) {
@@ -948,11 +776,11 @@ int attn_tc_launch(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const
     int rc = get_encode(&enc);
     if (rc) return rc;
     CUtensorMap mq, mad, mag, mbd, mbg;
-    if ((rc = make_map(enc, &mq, q, m * nh, 64))) return rc;
-    if ((rc = make_map(enc, &mad, rows_a, n_a, RC))) return rc;
-    if ((rc = make_map(enc, &mag, rows_a, n_a, 1))) return rc;
-    if ((rc = make_map(enc, &mbd, rows_b, n_c, RC))) return rc;
-    if ((rc = make_map(enc, &mbg, rows_b, n_c, 1))) return rc;
+    if ((rc = make_map_bf16(enc, &mq, q, m * nh, HD, 64, 64))) return rc;
+    if ((rc = make_map_bf16(enc, &mad, rows_a, n_a, HD, 64, RC))) return rc;
+    if ((rc = make_map_bf16(enc, &mag, rows_a, n_a, HD, 64, 1))) return rc;
+    if ((rc = make_map_bf16(enc, &mbd, rows_b, n_c, HD, 64, RC))) return rc;
+    if ((rc = make_map_bf16(enc, &mbg, rows_b, n_c, HD, 64, 1))) return rc;
     Params p;
     p.n_a = n_a;
     p.n_c = n_c;

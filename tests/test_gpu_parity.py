@@ -189,6 +189,30 @@ def test_indexer_scores_and_topk(orc, wl):
         assert np.all(np.diff(v) > 0) and np.all(r[len(v):] == -1)
 
 
+@pytest.mark.parametrize("start_pos,ratio", [(0, 8), (1000, 4), (37, 3)])
+def test_indexer_many_tokens_tensor_core_path(orc, start_pos, ratio):
+    """Enough tokens for a group of 4 per SM (64 heads x 128) take the tcgen05
+    scores kernel: every score of every token bit-exact against the oracle,
+    including a ragged last group, groups whose tokens see no row yet (their
+    scores are all -inf) and a ragged last row tile; then the top-k sets."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = DECODE.replace(name="indexer_tc", m=4 * sms + 3, start_pos=start_pos, ratio=ratio,
+                        topk=64)
+    assert wl.Hi == 64 and wl.Di == 128 and wl.n_c > 0
+    inp = make_inputs(wl, seed=start_pos + ratio)
+    idx, scores = _gpu_indexer(wl, inp)
+    sc, bad = orc.indexer_scores(bf16_bits(inp["q_idx"]), bf16_bits(inp["k_idx"])[: wl.n_c],
+                                 inp["w"].numpy(), wl.ratio, wl.start_pos)
+    assert bad == 0
+    gsc = bf16_bits(scores)
+    assert np.array_equal(gsc, sc), np.argwhere(gsc != sc)[:5]
+    win_idx = orc.window_topk_idxs(wl.win, wl.m, wl.start_pos)
+    toks = sample_tokens(wl)
+    oidx = orc.topk_merge(sc[toks], win_idx[toks], wl.n_c, wl.win, wl.ratio, wl.start_pos,
+                          wl.topk, wl.n_a, tokens=toks)
+    assert_idx_sets_equal(idx.cpu().numpy()[toks], oidx, wl.win)
+
+
 @pytest.mark.parametrize("sink_kind", ["normal", "minus_inf", "large"])
 def test_sparse_attn_given_indices(orc, sink_kind):
     wl = TINY_PREFILL.replace(m=40, start_pos=0, topk=12, nh=20, hd=128)
