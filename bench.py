@@ -210,23 +210,28 @@ def slot_bytes(slot) -> int:
 
 
 def launches_per_step(wl) -> int:
-    """Kernels one ds41_csa_forward launches for this workload."""
+    """Kernels one ds41_csa_forward launches for this workload (mirrors the
+    library's plan: fused few-token step, or the four calls)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     hpad = (wl.Hi + 7) // 8 * 8
-    groups = (wl.m + max(1, 128 // hpad) - 1) // max(1, 128 // hpad)
-    if wl.n_c > 0 and groups <= 4 and wl.m * ((wl.nh + 15) // 16) * 4 <= sms:
+    tt = max(1, 128 // hpad)
+    groups = (wl.m + tt - 1) // tt
+    few_attn = wl.m * ((wl.nh + 15) // 16) * 4 <= sms
+    if wl.n_c > 0 and groups <= 4 and few_attn:
         return 3  # fused front (scores + ring + latent), top-k, cluster attention
     n = 1  # ring write
     if wl.G > 0:
         n += 1
     if wl.n_c > 0:
-        hpad = (wl.Hi + 7) // 8 * 8
-        tt = max(1, 128 // hpad)
-        groups = (wl.m + tt - 1) // tt
-        n += 2 + (1 if groups > 4 else 0)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    if wl.m * ((wl.nh + 15) // 16) * 4 <= sms:
+        n += 2  # scores, top-k
+        if groups > 4:
+            n += 1  # keys quantised once
+            if wl.Hi == 64 and wl.Di == 128 and (wl.m + 3) // 4 >= sms:
+                n += 1  # queries quantised for the tensor-core scores
+    if few_attn:
         return n + 1  # few-token cluster kernel
+    if wl.hd == 512 and wl.nh % 64 == 0 and wl.K <= 1024 and wl.m * (wl.nh // 64) >= sms:
+        return n + 1  # persistent tensor-core attention
     heads_groups = (wl.nh + 63) // 64
     chunks = (wl.K + 31) // 32
     ctas = wl.m * heads_groups
@@ -235,8 +240,64 @@ def launches_per_step(wl) -> int:
         splits = min(chunks, (sms + ctas - 1) // ctas)
         cps = (chunks + splits - 1) // splits
         splits = (chunks + cps - 1) // cps
-    n += 1 + (1 if splits > 1 else 0)
-    return n
+    return n + 1 + (1 if splits > 1 else 0)
+
+
+OPS = ["window_ring_write", "compress_latent_write", "indexer_topk", "sparse_attn_sink_fwd"]
+
+
+def call_op(name, wl, inp, out, fc):
+    """One call of one entry point on a layer state (outputs preallocated)."""
+    if name == "window_ring_write":
+        ds41.window_ring_write(inp["kv"], inp["ring"], out["win_idx"], wl.start_pos,
+                               rows_a=out.get("rows_a"))
+    elif name == "compress_latent_write":
+        ds41.compress_latent_write(inp["latent"], fc, inp["cache"], wl.rd, wl.ratio,
+                                   wl.start_pos, wl.m)
+    elif name == "indexer_topk":
+        n_a = ds41.rows_a_len(wl.m, wl.win, wl.start_pos)
+        ds41.indexer_topk(inp["q_idx"], inp["k_idx"][: wl.n_c], inp["w"], out["win_idx"],
+                          wl.ratio, wl.start_pos, wl.topk, n_a, idx=out["idx"],
+                          ws=out.get("ws_idx"))
+    else:
+        if wl.start_pos == 0:
+            rows_a = inp["kv"]
+        elif wl.m == 1:
+            rows_a = inp["ring"]
+        else:
+            rows_a = out["rows_a"]
+        rows_b = inp["cache"][: wl.n_c] if wl.n_c > 0 else None
+        idx = out["idx"] if wl.n_c > 0 else out["win_idx"]
+        ds41.sparse_attn_sink_fwd(inp["q"], rows_a, rows_b, idx, inp["sink"], wl.scale,
+                                  o=out["o"], ws=out.get("ws_attn"))
+
+
+def time_ops(wl, slots, fc, stream, reps=5):
+    """Milliseconds per call of each entry point, from CUDA graphs of one call
+    per layer state replayed ``reps`` times (no host launch gaps)."""
+    res = {}
+    for name in OPS:
+        if name == "compress_latent_write" and wl.G == 0:
+            continue
+        if name == "indexer_topk" and wl.n_c == 0:
+            continue
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for inp, out in slots:
+                call_op(name, wl, inp, out, fc)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        res[name] = e0.elapsed_time(e1) / (reps * len(slots))
+        del g
+    torch.cuda.synchronize()
+    return res
 
 
 def run_ours(args, world, rank, local):
@@ -293,43 +354,13 @@ def run_ours(args, world, rank, local):
     t_max_ms = max_over_ranks(t_ms, world)
     value = wl.m * K * world / (t_max_ms / 1e3)
 
-    # ---- per-op timing (events around each op; the GPU is kept behind the CPU
-    # by a sleep kernel so no launch gap enters the measured intervals)
-    ops = ["window_ring_write", "compress_latent_write", "indexer_topk", "sparse_attn_sink_fwd"]
-    op_ms = {k: 0.0 for k in ops}
-    evs = []
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(int(2e9 * (0.05 + 5e-4 * K)))
-        for i in range(K):
-            inp, out = slots[(W + i) % n_slots]
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-            ev[0].record(stream)
-            win_idx = out["win_idx"]
-            rows_a = ds41.window_ring_write(inp["kv"], inp["ring"], win_idx, wl.start_pos,
-                                            rows_a=out.get("rows_a"))
-            ev[1].record(stream)
-            if wl.G > 0:
-                ds41.compress_latent_write(inp["latent"], fc, inp["cache"], wl.rd, wl.ratio,
-                                           wl.start_pos, wl.m)
-            ev[2].record(stream)
-            if wl.n_c > 0:
-                idx = ds41.indexer_topk(inp["q_idx"], inp["k_idx"][: wl.n_c], inp["w"], win_idx,
-                                        wl.ratio, wl.start_pos, wl.topk, rows_a.shape[0],
-                                        idx=out["idx"], ws=out.get("ws_idx"))
-                rows_b = inp["cache"][: wl.n_c]
-            else:
-                idx, rows_b = win_idx, None
-            ev[3].record(stream)
-            ds41.sparse_attn_sink_fwd(inp["q"], rows_a, rows_b, idx, inp["sink"], wl.scale,
-                                      o=out["o"], ws=out.get("ws_attn"))
-            ev[4].record(stream)
-            evs.append(ev)
-    stream.synchronize()
-    for ev in evs:
-        for j, k in enumerate(ops):
-            op_ms[k] += ev[j].elapsed_time(ev[j + 1]) / K
+    # ---- per-op timing: each op alone, captured as one CUDA graph of
+    # back-to-back calls over the rotating layer states, replayed and timed
+    # with events on the launching stream
+    op_ms = time_ops(wl, slots, fc, stream)
     alg = algorithmic(wl)
     hbm, bf16, bf16_sus, peak_src = load_peaks()
+    ops = list(op_ms)
     dom = max(ops, key=lambda k: op_ms[k])
     d_ms = op_ms[dom]
     if wl.m >= 256 and dom == "sparse_attn_sink_fwd":
