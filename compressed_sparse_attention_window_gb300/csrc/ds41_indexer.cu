@@ -14,6 +14,8 @@
 // scales stay within a moderate range, so the tensor-core sum equals the
 // ordered sum bit for bit; the head sum is an explicit fma chain in head
 // order, identical on every architecture.
+#include <cooperative_groups.h>
+
 #include "ds41_internal.cuh"
 #include "ds41_step1.cuh"
 
@@ -222,49 +224,6 @@ __device__ __forceinline__ uint32_t order_key(uint16_t b) {
     return (b & 0x8000u) ? (uint32_t)(~b & 0xffffu) : (uint32_t)(b | 0x8000u);
 }
 
-// Block-wide exclusive prefix sums of two per-thread counts (blockDim a
-// multiple of 32, <= 1024).  wsum needs 2 * 32 ints.
-__device__ __forceinline__ void block_scan2(int a, int b, int* a_before, int* b_before,
-                                            int* wsum) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int ia = a, ib = b;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int oa = __shfl_up_sync(0xffffffffu, ia, off);
-        const int ob = __shfl_up_sync(0xffffffffu, ib, off);
-        if (lane >= off) {
-            ia += oa;
-            ib += ob;
-        }
-    }
-    if (lane == 31) {
-        wsum[warp] = ia;
-        wsum[32 + warp] = ib;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const int va = lane < nw ? wsum[lane] : 0;
-        const int vb = lane < nw ? wsum[32 + lane] : 0;
-        int xa = va, xb = vb;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int oa = __shfl_up_sync(0xffffffffu, xa, off);
-            const int ob = __shfl_up_sync(0xffffffffu, xb, off);
-            if (lane >= off) {
-                xa += oa;
-                xb += ob;
-            }
-        }
-        if (lane < nw) {
-            wsum[lane] = xa - va;
-            wsum[32 + lane] = xb - vb;
-        }
-    }
-    __syncthreads();
-    *a_before = wsum[warp] + ia - a;
-    *b_before = wsum[32 + warp] + ib - b;
-}
-
 // Warp 0: the bucket b (of 256) holding the kk-th largest key, counting
 // `above` keys already known to be larger; *bucket = b, *cum = above + keys
 // in buckets above b.  Lane l owns buckets 8l .. 8l+7.
@@ -346,10 +305,17 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(
         __syncthreads();
         key.s = skeys;
     }
-    // pass 1: high byte
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    // pass 1: high byte.  Close scores share a bin, so the lanes of a warp
+    // that hold the same bin add their count with one atomic.
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int64_t s = threadIdx.x; s < vis; s += blockDim.x) atomicAdd(&hist[key(s) >> 8], 1);
+    for (int64_t base = threadIdx.x - lane; base < vis; base += blockDim.x) {
+        const int64_t s = base + lane;
+        const uint32_t bin = s < vis ? key(s) >> 8 : 0x10000u;
+        const uint32_t mm = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256u && lane == __ffs(mm) - 1) atomicAdd(&hist[bin], __popc(mm));
+    }
     __syncthreads();
     if (threadIdx.x < 32) find_bucket(hist, kk, 0, &sel[0], &sel[1]);
     __syncthreads();
@@ -359,39 +325,234 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(
     // pass 2: low byte inside bucket hb
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int64_t s = threadIdx.x; s < vis; s += blockDim.x) {
-        const uint32_t k = key(s);
-        if ((k >> 8) == hb) atomicAdd(&hist[k & 0xffu], 1);
+    for (int64_t base = threadIdx.x - lane; base < vis; base += blockDim.x) {
+        const int64_t s = base + lane;
+        uint32_t bin = 0x10000u;
+        if (s < vis) {
+            const uint32_t k = key(s);
+            if ((k >> 8) == hb) bin = k & 0xffu;
+        }
+        const uint32_t mm = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256u && lane == __ffs(mm) - 1) atomicAdd(&hist[bin], __popc(mm));
     }
     __syncthreads();
     if (threadIdx.x < 32) find_bucket(hist, kk, above1, &sel[2], &sel[3]);
     __syncthreads();
     const uint32_t T = (hb << 8) | (uint32_t)sel[2];
     const int need_eq = kk - sel[3];
-    // pass 3: each thread takes a contiguous segment of the visible keys and
-    // counts the keys above T and equal to T; one block scan turns the counts
-    // into output offsets (the equal keys taken are the lowest-numbered
-    // need_eq of them), and every segment is written in ascending row order.
-    const int64_t seg = (vis + blockDim.x - 1) / blockDim.x;
-    const int64_t s_lo = min(vis, (int64_t)threadIdx.x * seg);
-    const int64_t s_hi = min(vis, s_lo + seg);
+    // pass 3: each warp takes a contiguous block of the visible keys, its
+    // lanes interleaved (conflict-free shared-memory reads); ballots count the
+    // keys above T and equal to T, a scan over the warps turns the counts into
+    // output offsets (the equal keys taken are the lowest-numbered need_eq of
+    // them), and every block is written in ascending row order.
+    const int64_t wseg = ((vis + nwarps - 1) / nwarps + 31) & ~int64_t(31);
+    const int64_t w_lo = min(vis, (int64_t)warp * wseg);
+    const int64_t w_hi = min(vis, w_lo + wseg);
+    const uint32_t lt = (1u << lane) - 1u;
     int n_gt = 0, n_eq = 0;
-    for (int64_t s = s_lo; s < s_hi; s++) {
-        const uint32_t k = key(s);
-        n_gt += k > T;
-        n_eq += k == T;
+    for (int64_t b0 = w_lo; b0 < w_hi; b0 += 32) {
+        const int64_t s = b0 + lane;
+        const uint32_t k = s < w_hi ? key(s) : 0u;
+        n_gt += __popc(__ballot_sync(0xffffffffu, s < w_hi && k > T));
+        n_eq += __popc(__ballot_sync(0xffffffffu, s < w_hi && k == T));
     }
-    int gt_before, eq_before;
-    block_scan2(n_gt, n_eq, &gt_before, &eq_before, wsum);
-    int pos = gt_before + min(eq_before, need_eq);
-    int eq_rank = eq_before;
-    for (int64_t s = s_lo; s < s_hi; s++) {
-        const uint32_t k = key(s);
-        bool take = k > T;
-        if (k == T) take = eq_rank++ < need_eq;
-        if (take && pos < kk) out[win + pos++] = (int32_t)(offset + s);
+    if (lane == 0) {
+        wsum[warp] = n_gt;
+        wsum[32 + warp] = n_eq;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int a = lane < nwarps ? wsum[lane] : 0;
+        const int e = lane < nwarps ? wsum[32 + lane] : 0;
+        int xa = a, xe = e;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int oa = __shfl_up_sync(0xffffffffu, xa, off);
+            const int oe = __shfl_up_sync(0xffffffffu, xe, off);
+            if (lane >= off) {
+                xa += oa;
+                xe += oe;
+            }
+        }
+        __syncwarp();
+        if (lane < nwarps) {
+            wsum[lane] = xa - a;
+            wsum[32 + lane] = xe - e;
+        }
+    }
+    __syncthreads();
+    int eq_rank = wsum[32 + warp];
+    int pos = wsum[warp] + min(eq_rank, need_eq);
+    for (int64_t b0 = w_lo; b0 < w_hi; b0 += 32) {
+        const int64_t s = b0 + lane;
+        const uint32_t k = s < w_hi ? key(s) : 0u;
+        const bool eq = s < w_hi && k == T;
+        const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
+        const bool take = (s < w_hi && k > T) || (eq && eq_rank + __popc(eqb & lt) < need_eq);
+        const uint32_t tb = __ballot_sync(0xffffffffu, take);
+        const int at = pos + __popc(tb & lt);
+        if (take && at < kk) out[win + at] = (int32_t)(offset + s);
+        pos += __popc(tb);
+        eq_rank += __popc(eqb);
     }
     for (int j = kk + threadIdx.x; j < ctopk; j += blockDim.x) out[win + j] = -1;
+}
+
+// ---------------------------------------------------------------------------
+// Top-k of few long rows: a cluster of TK_CL CTAs per query, CTA r holding
+// slice r of the visible scores.  The same two histogram passes and the
+// ordered pass as above, with the histograms summed over the cluster through
+// distributed shared memory (every CTA derives the same threshold) and a
+// cluster-wide prefix of the per-CTA counts, so the picks still come out in
+// ascending row order.
+// ---------------------------------------------------------------------------
+constexpr int TK_CL = 8;
+constexpr int TK_THREADS = 512;
+constexpr int TK_SLICE_CAP = 8192;  // keys of a slice staged in shared memory
+
+__global__ void __launch_bounds__(TK_THREADS) topk_cluster_kernel(
+    const uint16_t* __restrict__ scores, const int32_t* __restrict__ win_idx,
+    int32_t* __restrict__ idx, int64_t n_c, int win, int ctopk, int64_t ratio, int64_t start_pos,
+    int64_t offset) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    __shared__ __align__(16) uint16_t skeys[TK_SLICE_CAP];
+    __shared__ int hist1[256], hist2[256], ghist[256];
+    __shared__ int wsum[64];
+    __shared__ int sel[4];
+    __shared__ int tot[2];
+    pdl_wait();  // the scores (and window indices) come from the previous kernel
+    pdl_trigger();
+    const int r = (int)cl.block_rank();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int t = blockIdx.x / TK_CL;
+    const int K = win + ctopk;
+    int32_t* out = idx + (int64_t)t * K;
+    const uint16_t* sc = scores + (int64_t)t * n_c;
+    if (r == 0)
+        for (int j = threadIdx.x; j < win; j += blockDim.x) out[j] = win_idx[(int64_t)t * win + j];
+    const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
+    const int kk = (int)(vis < ctopk ? vis : ctopk);
+    if (vis <= ctopk) {  // the same branch in every CTA of the cluster
+        if (r == 0)
+            for (int j = threadIdx.x; j < ctopk; j += blockDim.x)
+                out[win + j] = (j < vis) ? (int32_t)(offset + j) : -1;
+        return;
+    }
+    const int64_t seg = ((vis + TK_CL - 1) / TK_CL + 7) & ~int64_t(7);
+    const int64_t lo = min(vis, (int64_t)r * seg);
+    const int n = (int)(min(vis, lo + seg) - lo);
+    const bool vec = ((reinterpret_cast<uintptr_t>(sc + lo) & 15u) == 0);
+    const int n8 = vec ? n / 8 : 0;
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(sc + lo) + i);
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+        for (int e = 0; e < 8; e++) skeys[i * 8 + e] = (uint16_t)order_key(h[e]);
+    }
+    for (int i = n8 * 8 + threadIdx.x; i < n; i += blockDim.x) skeys[i] = (uint16_t)order_key(sc[lo + i]);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist1[i] = hist2[i] = 0;
+    __syncthreads();
+    // pass 1: high byte of this slice
+    for (int base = threadIdx.x - lane; base < n; base += blockDim.x) {
+        const int i = base + lane;
+        const uint32_t bin = i < n ? (uint32_t)skeys[i] >> 8 : 0x10000u;
+        const uint32_t mm = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256u && lane == __ffs(mm) - 1) atomicAdd(&hist1[bin], __popc(mm));
+    }
+    cl.sync();  // every slice's histogram is complete
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        int v = 0;
+        for (int q = 0; q < TK_CL; q++) v += cl.map_shared_rank(hist1, q)[i];
+        ghist[i] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) find_bucket(ghist, kk, 0, &sel[0], &sel[1]);
+    __syncthreads();
+    const uint32_t hb = (uint32_t)sel[0];
+    const int above1 = sel[1];
+    // pass 2: low byte inside bucket hb
+    for (int base = threadIdx.x - lane; base < n; base += blockDim.x) {
+        const int i = base + lane;
+        uint32_t bin = 0x10000u;
+        if (i < n && ((uint32_t)skeys[i] >> 8) == hb) bin = skeys[i] & 0xffu;
+        const uint32_t mm = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256u && lane == __ffs(mm) - 1) atomicAdd(&hist2[bin], __popc(mm));
+    }
+    cl.sync();
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        int v = 0;
+        for (int q = 0; q < TK_CL; q++) v += cl.map_shared_rank(hist2, q)[i];
+        ghist[i] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) find_bucket(ghist, kk, above1, &sel[2], &sel[3]);
+    __syncthreads();
+    const uint32_t T = (hb << 8) | (uint32_t)sel[2];
+    const int need_eq = kk - sel[3];
+    // pass 3: per-warp blocks of the slice, counted with ballots
+    const int wseg = ((n + nwarps - 1) / nwarps + 31) & ~31;
+    const int w_lo = min(n, warp * wseg), w_hi = min(n, w_lo + wseg);
+    const uint32_t lt = (1u << lane) - 1u;
+    int n_gt = 0, n_eq = 0;
+    for (int b0 = w_lo; b0 < w_hi; b0 += 32) {
+        const int i = b0 + lane;
+        const uint32_t k = i < w_hi ? skeys[i] : 0u;
+        n_gt += __popc(__ballot_sync(0xffffffffu, i < w_hi && k > T));
+        n_eq += __popc(__ballot_sync(0xffffffffu, i < w_hi && k == T));
+    }
+    if (lane == 0) {
+        wsum[warp] = n_gt;
+        wsum[32 + warp] = n_eq;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int a = lane < nwarps ? wsum[lane] : 0;
+        const int e = lane < nwarps ? wsum[32 + lane] : 0;
+        int xa = a, xe = e;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int oa = __shfl_up_sync(0xffffffffu, xa, off);
+            const int oe = __shfl_up_sync(0xffffffffu, xe, off);
+            if (lane >= off) {
+                xa += oa;
+                xe += oe;
+            }
+        }
+        __syncwarp();
+        if (lane < nwarps) {
+            wsum[lane] = xa - a;
+            wsum[32 + lane] = xe - e;
+        }
+        if (lane == 31) {
+            tot[0] = xa;
+            tot[1] = xe;
+        }
+    }
+    cl.sync();  // every slice's totals are published
+    int gt_before = 0, eq_before = 0;
+    for (int q = 0; q < r; q++) {
+        const int* rt = cl.map_shared_rank(tot, q);
+        gt_before += rt[0];
+        eq_before += rt[1];
+    }
+    int eq_rank = eq_before + wsum[32 + warp];
+    int pos = gt_before + wsum[warp] + min(eq_rank, need_eq);
+    for (int b0 = w_lo; b0 < w_hi; b0 += 32) {
+        const int i = b0 + lane;
+        const uint32_t k = i < w_hi ? skeys[i] : 0u;
+        const bool eq = i < w_hi && k == T;
+        const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
+        const bool take = (i < w_hi && k > T) || (eq && eq_rank + __popc(eqb & lt) < need_eq);
+        const uint32_t tb = __ballot_sync(0xffffffffu, take);
+        const int at = pos + __popc(tb & lt);
+        if (take && at < kk) out[win + at] = (int32_t)(offset + lo + i);
+        pos += __popc(tb);
+        eq_rank += __popc(eqb);
+    }
+    if (r == 0)
+        for (int j = kk + threadIdx.x; j < ctopk; j += blockDim.x) out[win + j] = -1;
+    cl.sync();  // the totals stay readable until every CTA has read them
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -527,16 +688,7 @@ extern "C" int ds41_indexer_topk(const ds41_bf16* q_idx, const ds41_bf16* k_idx,
         default: rc = launch_scores<256>(p, q_idx, ksrc, w, sc, m, Hi, n_c, ratio, start_pos, fill, st); break;
     }
     if (rc) return rc;
-    int threads = n_c >= 8192 ? 1024 : (n_c >= 1024 ? 512 : 256);
-    const int keys_cap = (int)(n_c < 49152 ? n_c : 49152);  // up to 96 KiB of staged keys
-    const size_t ksm = ((size_t)keys_cap * 2 + 15) & ~size_t(15);
-    if (ksm > 48 * 1024)
-        cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ksm);
-    topk_merge_kernel<<<(unsigned)m, threads, ksm, st>>>(sc, win_idx, idx, n_c, (int)win,
-                                                          (int)ctopk, ratio, start_pos, offset,
-                                                          keys_cap);
-    return launch_check("ds41_indexer_topk: top-k kernel");
+    return launch_topk(sc, win_idx, idx, m, n_c, win, ctopk, ratio, start_pos, offset, false, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -569,26 +721,50 @@ int launch_front(const uint16_t* q_idx, const uint16_t* k_idx, const float* w, u
 int launch_topk(const uint16_t* scores, const int32_t* win_idx, int32_t* idx, int64_t m,
                 int64_t n_c, int64_t win, int64_t ctopk, int64_t ratio, int64_t start_pos,
                 int64_t offset, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        na++;
+    }
+    int rc;
+    // Few queries with long rows: a cluster per query splits each row over
+    // TK_CL SMs.  Otherwise one CTA per query.
+    if (m * TK_CL <= 2 * (int64_t)device_sm_count() && n_c >= 1024 &&
+        n_c <= (int64_t)TK_CL * TK_SLICE_CAP) {
+        cfg.gridDim = dim3((unsigned)(m * TK_CL));
+        cfg.blockDim = dim3(TK_THREADS);
+        cfg.dynamicSmemBytes = 0;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = TK_CL;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        na++;
+        cfg.attrs = attr;
+        cfg.numAttrs = na;
+        rc = cuda_check(cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, win_idx, idx, n_c,
+                                           (int)win, (int)ctopk, ratio, start_pos, offset),
+                        "top-k cluster kernel");
+        if (rc) return rc;
+        return launch_check("top-k cluster kernel");
+    }
     const int threads = n_c >= 8192 ? 1024 : (n_c >= 1024 ? 512 : 256);
-    const int keys_cap = (int)(n_c < 49152 ? n_c : 49152);
+    const int keys_cap = (int)(n_c < 49152 ? n_c : 49152);  // up to 96 KiB of staged keys
     const size_t ksm = ((size_t)keys_cap * 2 + 15) & ~size_t(15);
     if (ksm > 48 * 1024)
         cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ksm);
-    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)m);
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = ksm;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    int rc = cuda_check(cudaLaunchKernelEx(&cfg, topk_merge_kernel, scores, win_idx, idx, n_c,
-                                           (int)win, (int)ctopk, ratio, start_pos, offset,
-                                           keys_cap),
-                        "top-k kernel");
+    cfg.numAttrs = na;
+    rc = cuda_check(cudaLaunchKernelEx(&cfg, topk_merge_kernel, scores, win_idx, idx, n_c,
+                                       (int)win, (int)ctopk, ratio, start_pos, offset, keys_cap),
+                    "top-k kernel");
     if (rc) return rc;
     return launch_check("top-k kernel");
 }
