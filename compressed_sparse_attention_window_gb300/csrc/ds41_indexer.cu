@@ -106,6 +106,24 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
         const uint16_t* src = q_idx + ((int64_t)(t0 + (live ? tt : 0)) * Hi + (live ? h : 0)) * DI;
         cp_async16(smem_u32(qs + n * DI + swz<CPR>(n, c) * 8), src + c * 8, live);
     }
+    const int64_t vis_last = visible_rows(t0 + tcount - 1, start_pos, ratio, n_c);
+    const int64_t tiles_vis = (vis_last + IDX_ROWS - 1) / IDX_ROWS;
+    // When the scores are a caller-visible output, rows no query of this
+    // group can see yet are written as -inf too.
+    const int64_t tiles = fill_hidden ? (n_c + IDX_ROWS - 1) / IDX_ROWS : tiles_vis;
+    // The first key tile is fetched together with q, so the two loads overlap.
+    auto fetch_k = [&](int64_t tile) {
+        const int64_t r0 = tile * IDX_ROWS;
+        for (int id = tid; id < IDX_ROWS * CPR; id += IDX_THREADS) {
+            const int r = id / CPR, c = id % CPR;
+            const int64_t row = r0 + r;
+            const bool live = row < n_c;
+            cp_async16(smem_u32(ks + r * DI + swz<CPR>(r, c) * 8),
+                       k_src + (live ? row : 0) * DI + c * 8, live);
+        }
+    };
+    const bool prefetched = (int64_t)blockIdx.y < tiles_vis;
+    if (prefetched) fetch_k(blockIdx.y);
     cp_async_commit();
     for (int n = tid; n < IDX_N; n += IDX_THREADS) {
         const int tt = n / hpad, h = n % hpad;
@@ -113,18 +131,18 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     }
     cp_async_wait<0>();
     __syncthreads();
+    // only the live rows (tokens of the group x Hi heads), rounded up to whole
+    // passes of the block: q8_chunk shuffles over the full warp, and the
+    // padding rows past the live ones are zero (they stay zero)
+    const int live_rows = (tcount - 1) * hpad + Hi;
+    const int q_iters = min(IDX_N * CPR,
+                            (live_rows * CPR + IDX_THREADS - 1) / IDX_THREADS * IDX_THREADS);
 #pragma unroll 1
-    for (int id = tid; id < IDX_N * CPR; id += IDX_THREADS) {
+    for (int id = tid; id < q_iters; id += IDX_THREADS) {
         const int n = id / CPR, c = id % CPR;
         uint4* p = reinterpret_cast<uint4*>(qs + n * DI + swz<CPR>(n, c) * 8);
         *p = q8_chunk(*p, true);
     }
-
-    const int64_t vis_last = visible_rows(t0 + tcount - 1, start_pos, ratio, n_c);
-    const int64_t tiles_vis = (vis_last + IDX_ROWS - 1) / IDX_ROWS;
-    // When the scores are a caller-visible output, rows no query of this
-    // group can see yet are written as -inf too.
-    const int64_t tiles = fill_hidden ? (n_c + IDX_ROWS - 1) / IDX_ROWS : tiles_vis;
 
     for (int64_t tile = blockIdx.y; tile < tiles; tile += ymain) {
         const int64_t r0 = tile * IDX_ROWS;
@@ -136,16 +154,12 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             continue;
         }
         __syncthreads();  // previous tile's readers are done with ks / cs
-        for (int id = tid; id < IDX_ROWS * CPR; id += IDX_THREADS) {
-            const int r = id / CPR, c = id % CPR;
-            const int64_t row = r0 + r;
-            const bool live = row < n_c;
-            cp_async16(smem_u32(ks + r * DI + swz<CPR>(r, c) * 8),
-                       k_src + (live ? row : 0) * DI + c * 8, live);
+        if (!(prefetched && tile == (int64_t)blockIdx.y)) {
+            fetch_k(tile);
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncthreads();
         }
-        cp_async_commit();
-        cp_async_wait<0>();
-        __syncthreads();
         if (KQ_INLINE) {
             // raw keys -> fp4 round trip, in place (rows past n_c are zero)
 #pragma unroll 1
