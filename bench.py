@@ -216,9 +216,16 @@ def launches_per_step(wl) -> int:
     hpad = (wl.Hi + 7) // 8 * 8
     tt = max(1, 128 // hpad)
     groups = (wl.m + tt - 1) // tt
-    few_attn = wl.m * ((wl.nh + 15) // 16) * 4 <= sms
+    dec_groups = wl.m * ((wl.nh + 15) // 16)
+    few_attn = dec_groups * 4 <= sms
     if wl.n_c > 0 and groups <= 4 and few_attn:
-        return 3  # fused front (scores + ring + latent), top-k, cluster attention
+        cl = 16
+        while cl > 1 and (dec_groups * cl > 2 * sms or (wl.K + cl - 1) // cl < 8):
+            cl //= 2
+        kseg = ((wl.n_c + cl - 1) // cl + 7) // 8 * 8
+        if cl >= 4 and (wl.K + cl - 1) // cl <= 2048 and kseg <= 4096:
+            return 2  # fused front (scores + ring + latent), attention selecting its rows
+        return 3  # fused front, top-k, cluster attention
     n = 1  # ring write
     if wl.G > 0:
         n += 1

@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "ds41_internal.cuh"
+#include "ds41_topk.cuh"
 
 namespace ds41 {
 
@@ -316,6 +317,188 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
 }
 
 // ---------------------------------------------------------------------------
+constexpr int TKD_CAP = 4096;  // score keys of one CTA's slice in the fused decode step
+
+// Fill sidx[0 .. j1 - j0) with slice [j0, j1) of the merged index row
+// [window indices | the min(ctopk, visible) best compressed rows in ascending
+// order | -1].  The CL CTAs of the cluster each take one slice of the visible
+// scores, sum their two 8-bit histograms over the cluster (every CTA derives
+// the same threshold; the lowest-numbered ties are taken), and store each
+// pick straight into the index slice of the CTA that owns its position.
+template <int NTH>
+__device__ void dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, int j1, int* sidx,
+                         uint8_t* area, int* hpush, bool write_idx, unsigned int* status) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const int CL = (int)cl.num_blocks(), r = (int)cl.block_rank();
+    uint16_t* skeys = reinterpret_cast<uint16_t*>(area);
+    int* hist = reinterpret_cast<int*>(area + 8192);  // this slice's histogram
+    int* ghist = hist + 256;                          // the cluster's
+    int* wsum = ghist + 256;
+    int* sel = wsum + 64;
+    int* tpush = sel + 8;                             // [16][2] totals of the slices
+    int* hpush1 = hpush;                              // [16][256] histograms of the slices
+    int* hpush2 = hpush + 16 * 256;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = NTH / 32;
+    const int win = tk.win;
+    int64_t vis = (tk.start_pos + t + 1) / tk.ratio;
+    if (vis > tk.n_c) vis = tk.n_c;
+    const int kk = (int)(vis < tk.ctopk ? vis : tk.ctopk);
+    int32_t* orow = tk.idx_out + t * (int64_t)K;
+    // window entries, the picks when every visible row is kept, and padding
+    for (int j = j0 + tid; j < j1; j += NTH) {
+        int v;
+        if (j < win) {
+            v = tk.win_idx[t * win + j];
+        } else if (j - win >= kk) {
+            v = -1;
+        } else if (vis <= tk.ctopk) {
+            v = (int)(tk.offset + (j - win));
+        } else {
+            continue;  // a pick: stored by the CTA that holds its score
+        }
+        sidx[j - j0] = v;
+        if (write_idx) orow[j] = v;
+    }
+    if (vis <= tk.ctopk) return;  // the same branch in every CTA of the cluster
+
+    const int64_t kseg = ((vis + CL - 1) / CL + 7) & ~int64_t(7);
+    const int64_t klo = min(vis, (int64_t)r * kseg);
+    const int n = (int)(min(vis, klo + kseg) - klo);
+    if (n > TKD_CAP) raise_status(status, DS41_E_RANGE);  // excluded by the host plan
+    const int nk = min(n, TKD_CAP);
+    const uint16_t* sc = tk.scores + t * tk.n_c + klo;
+    const bool vec = ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0);
+    const int n8 = vec ? nk / 8 : 0;
+    for (int i = tid; i < n8; i += NTH) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(sc) + i);
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+        for (int e = 0; e < 8; e++) skeys[i * 8 + e] = (uint16_t)order_key(h[e]);
+    }
+    for (int i = n8 * 8 + tid; i < nk; i += NTH) skeys[i] = (uint16_t)order_key(sc[i]);
+    for (int i = tid; i < 256; i += NTH) hist[i] = 0;
+    __syncthreads();
+    for (int base = tid - lane; base < nk; base += NTH) {
+        const int i = base + lane;
+        const uint32_t bin = i < nk ? (uint32_t)skeys[i] >> 8 : 0x10000u;
+        const uint32_t mm = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256u && lane == __ffs(mm) - 1) atomicAdd(&hist[bin], __popc(mm));
+    }
+    __syncthreads();
+    // push this slice's histogram into every CTA; after the barrier the sums are local
+    for (int i = tid; i < 256; i += NTH) {
+        const int v = hist[i];
+        for (int q = 0; q < CL; q++) cl.map_shared_rank(hpush1, q)[r * 256 + i] = v;
+        hist[i] = 0;
+    }
+    cl.sync();
+    for (int i = tid; i < 256; i += NTH) {
+        int v = 0;
+        for (int q = 0; q < CL; q++) v += hpush1[q * 256 + i];
+        ghist[i] = v;
+    }
+    __syncthreads();
+    if (tid < 32) find_bucket(ghist, kk, 0, &sel[0], &sel[1]);
+    __syncthreads();
+    const uint32_t hb = (uint32_t)sel[0];
+    const int above1 = sel[1];
+    for (int base = tid - lane; base < nk; base += NTH) {
+        const int i = base + lane;
+        uint32_t bin = 0x10000u;
+        if (i < nk && ((uint32_t)skeys[i] >> 8) == hb) bin = skeys[i] & 0xffu;
+        const uint32_t mm = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256u && lane == __ffs(mm) - 1) atomicAdd(&hist[bin], __popc(mm));
+    }
+    __syncthreads();
+    for (int i = tid; i < 256; i += NTH) {
+        const int v = hist[i];
+        for (int q = 0; q < CL; q++) cl.map_shared_rank(hpush2, q)[r * 256 + i] = v;
+    }
+    cl.sync();
+    for (int i = tid; i < 256; i += NTH) {
+        int v = 0;
+        for (int q = 0; q < CL; q++) v += hpush2[q * 256 + i];
+        ghist[i] = v;
+    }
+    __syncthreads();
+    if (tid < 32) find_bucket(ghist, kk, above1, &sel[2], &sel[3]);
+    __syncthreads();
+    const uint32_t T = (hb << 8) | (uint32_t)sel[2];
+    const int need_eq = kk - sel[3];
+    // per-warp blocks of the slice, counted with ballots
+    const int wseg = ((nk + NW - 1) / NW + 31) & ~31;
+    const int w_lo = min(nk, warp * wseg), w_hi = min(nk, w_lo + wseg);
+    const uint32_t lt = (1u << lane) - 1u;
+    int n_gt = 0, n_eq = 0;
+    for (int b0 = w_lo; b0 < w_hi; b0 += 32) {
+        const int i = b0 + lane;
+        const uint32_t k = i < w_hi ? skeys[i] : 0u;
+        n_gt += __popc(__ballot_sync(0xffffffffu, i < w_hi && k > T));
+        n_eq += __popc(__ballot_sync(0xffffffffu, i < w_hi && k == T));
+    }
+    if (lane == 0) {
+        wsum[warp] = n_gt;
+        wsum[32 + warp] = n_eq;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int a = lane < NW ? wsum[lane] : 0;
+        const int e = lane < NW ? wsum[32 + lane] : 0;
+        int xa = a, xe = e;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int oa = __shfl_up_sync(0xffffffffu, xa, off);
+            const int oe = __shfl_up_sync(0xffffffffu, xe, off);
+            if (lane >= off) {
+                xa += oa;
+                xe += oe;
+            }
+        }
+        __syncwarp();
+        if (lane < NW) {
+            wsum[lane] = xa - a;
+            wsum[32 + lane] = xe - e;
+        }
+        if (lane == 31) {
+            // push this slice's totals into the CTAs of the later slices
+            for (int q = r + 1; q < CL; q++) {
+                int* dst = cl.map_shared_rank(tpush, q);
+                dst[2 * r] = xa;
+                dst[2 * r + 1] = xe;
+            }
+        }
+    }
+    cl.sync();  // every slice's totals are published
+    int gt_before = 0, eq_before = 0;
+    for (int q = 0; q < r; q++) {
+        gt_before += tpush[2 * q];
+        eq_before += tpush[2 * q + 1];
+    }
+    int eq_rank = eq_before + wsum[32 + warp];
+    int pos = gt_before + wsum[warp] + min(eq_rank, need_eq);
+    for (int b0 = w_lo; b0 < w_hi; b0 += 32) {
+        const int i = b0 + lane;
+        const uint32_t k = i < w_hi ? skeys[i] : 0u;
+        const bool eq = i < w_hi && k == T;
+        const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
+        const bool take = (i < w_hi && k > T) || (eq && eq_rank + __popc(eqb & lt) < need_eq);
+        const uint32_t tb = __ballot_sync(0xffffffffu, take);
+        const int at = pos + __popc(tb & lt);
+        if (take && at < kk) {
+            const int j = win + at;  // position in the merged row
+            const int owner = j / per;
+            const int v = (int)(tk.offset + klo + i);
+            cl.map_shared_rank(sidx, owner)[j - owner * per] = v;
+            if (write_idx) orow[j] = v;
+        }
+        pos += __popc(tb);
+        eq_rank += __popc(eqb);
+    }
+    cl.sync();  // every index slice is complete
+}
+
 // Few-token (decode) path.  A cluster of CL CTAs shares one (token, group of
 // 16 heads); CTA r of the cluster takes slice r of the index row.  Four warps
 // split the head dim: for S each warp reduces over its quarter of hd and the
@@ -341,15 +524,27 @@ struct DecSmem {
     // groups, so ldmatrix reads them without conflicts, and every row can be
     // the destination of one contiguous bulk copy.
     static constexpr int RS = HD + 8;
-    static constexpr int OSTR = HD + 8;  // padded row stride of the staged O (f32)
     static constexpr size_t q_bytes = (size_t)DEC_HEADS * RS * 2;
     static constexpr size_t kv_bytes = (size_t)DEC_NC * RS * 2;  // one buffer
     static constexpr size_t sp_bytes = (size_t)dec_warps<HD>() * DEC_HEADS * DEC_SPS * 4;
-    static constexpr size_t o_bytes = (size_t)DEC_HEADS * OSTR * 4;  // reuses the kv buffers
     static constexpr size_t bar_off = q_bytes + 2 * kv_bytes + sp_bytes;
-    static constexpr size_t total = bar_off + 4 * 8 + 2 * DEC_NC * 4 + 2 * DEC_HEADS * 4 +
-                                    (size_t)DEC_STAGE * 4;
-    static_assert(o_bytes <= 2 * kv_bytes, "O staging must fit in the kv buffers");
+    static constexpr size_t base_end = bar_off + 4 * 8 + 2 * DEC_NC * 4 + 2 * DEC_HEADS * 4 +
+                                       (size_t)DEC_STAGE * 4;
+    // Cluster exchange, written by the other CTAs (push) so that every read
+    // after the barrier is local: the unnormalised O slices [16 ranks][16
+    // heads][HD / CL] (first, in the fused step, the two histograms of the
+    // row selection, [16 ranks][256] each), and (m, l) [16 ranks][2][16].
+    static constexpr size_t xch_off = (base_end + 15) & ~size_t(15);
+    static constexpr size_t xch_bytes =
+        (size_t)DEC_HEADS * HD * 4 > 32768 ? (size_t)DEC_HEADS * HD * 4 : 32768;
+    static constexpr size_t spush_off = xch_off + xch_bytes;
+    static constexpr size_t total = spush_off + 16 * 2 * DEC_HEADS * 4;
+    // the decode step that selects its own rows: score keys of this CTA's
+    // slice, its histogram, the cluster sum, warp counts, selection, and the
+    // per-slice totals pushed by the other CTAs [16][2]
+    static constexpr size_t tk_off = total;
+    static constexpr size_t tk_bytes = 2 * 4096 + 256 * 4 + 256 * 4 + 64 * 4 + 32 + 16 * 2 * 4;
+    static constexpr size_t fused_total = tk_off + tk_bytes;
     static_assert(q_bytes % 16 == 0 && kv_bytes % 16 == 0 && sp_bytes % 16 == 0, "alignment");
 };
 
@@ -360,16 +555,17 @@ struct DecSmem {
 // The warps split the head dim: for S each warp reduces over its slice and the
 // partials are summed in a fixed order by every warp, so all warps hold
 // bit-identical scores and softmax statistics; for P*V each warp owns a slice
-// of the output columns.  At the end the CTAs exchange (m, l) and their
-// unnormalised O through distributed shared memory; CTA r reduces the r-th
-// slice of the columns over the cluster, adds the sink and writes o.  No
-// scratch memory and no second launch.
-template <int HD>
+// of the output columns.  At the end each CTA pushes its (m, l) and the
+// slices of its unnormalised O into the CTAs that reduce them (distributed
+// shared memory); CTA r reduces the r-th slice of the columns over the
+// cluster, adds the sink and writes o.  No scratch memory and no second
+// launch.  In the fused step the cluster first selects the rows itself.
+template <int HD, bool FUSED>
 __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ rows_a, int64_t n_a,
     const uint16_t* __restrict__ rows_b, int64_t n_c, const int32_t* __restrict__ idx, int K,
     const float* __restrict__ sink, float scale_log2, uint16_t* __restrict__ o,
-    float* __restrict__ lse, int nh, unsigned int* status) {
+    float* __restrict__ lse, int nh, unsigned int* status, DecTopk tk) {
     namespace cg = cooperative_groups;
     using SM = DecSmem<HD>;
     constexpr int NW = dec_warps<HD>();
@@ -377,7 +573,6 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     constexpr int RS = SM::RS;
     constexpr int QW = HD / NW;      // head-dim columns per warp
     constexpr int NT = QW / 8;       // output n-tiles per warp
-    constexpr int OSTR = SM::OSTR;
     constexpr uint32_t ROWB = HD * 2;  // bytes of one row
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* qs = reinterpret_cast<uint16_t*>(smem);
@@ -387,7 +582,6 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     int* vflag = reinterpret_cast<int*>(smem + SM::bar_off + 4 * 8);
     float* stat = reinterpret_cast<float*>(vflag + 2 * DEC_NC);  // [2][16]: m then l
     int* sidx = reinterpret_cast<int*>(stat + 2 * DEC_HEADS);      // [DEC_STAGE]
-    float* ostage = reinterpret_cast<float*>(kvs);                // [16][OSTR] after the loop
 
     cg::cluster_group cluster = cg::this_cluster();
     const int CL = (int)cluster.num_blocks();
@@ -428,7 +622,13 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     // before this one.
     pdl_wait();
     const int nst = max(0, min(j1 - j0, DEC_STAGE));
-    for (int j = tid; j < nst; j += NTH) sidx[j] = irow[j0 + j];
+    if constexpr (FUSED) {
+        // select this query's rows here (the scores come from the kernel before)
+        dec_topk<NTH>(tk, t, K, per, j0, j1, sidx, smem + SM::tk_off,
+                      reinterpret_cast<int*>(smem + SM::xch_off), blockIdx.y == 0, status);
+    } else {
+        for (int j = tid; j < nst; j += NTH) sidx[j] = irow[j0 + j];
+    }
     __syncthreads();
     // warp 0: one bulk copy per valid row of the chunk; invalid rows are zeroed
     // (their scores are masked, and 0 * row must stay finite in P*V)
@@ -584,18 +784,29 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         lrow[i] += __shfl_xor_sync(0xffffffffu, lrow[i], 1);
         lrow[i] += __shfl_xor_sync(0xffffffffu, lrow[i], 2);
     }
-    // stage (m, l) and the unnormalised O of this CTA
+    // Push this CTA's (m, l) into every CTA of the cluster and each slice of
+    // its unnormalised O, as bf16 pairs (half the exchanged bytes; the same
+    // relative rounding as the bf16 output), into the CTA that reduces those
+    // columns; after one barrier every read is local.
+    const int cols = HD / CL;
+    float* spush = reinterpret_cast<float*>(smem + SM::spush_off);    // [16 ranks][2][16]
+    uint32_t* opush = reinterpret_cast<uint32_t*>(smem + SM::xch_off);  // [CL ranks][16][cols/2]
     if (warp == 0 && (lane & 3) == 0) {
-        stat[ra] = mrow[0];
-        stat[rb] = mrow[1];
-        stat[DEC_HEADS + ra] = lrow[0];
-        stat[DEC_HEADS + rb] = lrow[1];
+        for (int q = 0; q < CL; q++) {
+            float* dst = cluster.map_shared_rank(spush, q) + rank * 2 * DEC_HEADS;
+            dst[ra] = mrow[0];
+            dst[rb] = mrow[1];
+            dst[DEC_HEADS + ra] = lrow[0];
+            dst[DEC_HEADS + rb] = lrow[1];
+        }
     }
 #pragma unroll
     for (int j = 0; j < NT; j++) {
         const int col = warp * QW + j * 8 + 2 * (lane & 3);
-        *reinterpret_cast<float2*>(ostage + ra * OSTR + col) = make_float2(oacc[j][0], oacc[j][1]);
-        *reinterpret_cast<float2*>(ostage + rb * OSTR + col) = make_float2(oacc[j][2], oacc[j][3]);
+        const int qo = col / cols, cc = (col - qo * cols) >> 1;
+        uint32_t* dst = cluster.map_shared_rank(opush, qo) + rank * DEC_HEADS * (cols / 2);
+        dst[ra * (cols / 2) + cc] = pack_bf16x2(oacc[j][0], oacc[j][1]);
+        dst[rb * (cols / 2) + cc] = pack_bf16x2(oacc[j][2], oacc[j][3]);
     }
     cluster.sync();
 
@@ -607,9 +818,8 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         const int h = h0 + hh;
         float mr = -INFINITY, lr = 0.0f;
         if (r < CL) {
-            const float* st = cluster.map_shared_rank(stat, r);
-            mr = st[hh];
-            lr = st[DEC_HEADS + hh];
+            mr = spush[r * 2 * DEC_HEADS + hh];
+            lr = spush[r * 2 * DEC_HEADS + DEC_HEADS + hh];
         }
         const float sk = (h < nh) ? sink[h] * LOG2E : -INFINITY;
         float M = fmaxf(mr, sk);
@@ -626,35 +836,32 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         if (lse && rank == 0 && r == 0 && h < nh) lse[t * nh + h] = (Mref + log2f(L)) / LOG2E;
     }
     __syncthreads();
-    // CTA `rank` reduces columns [c0, c0 + cols) of the 16 heads, 4 at a time,
-    // with the loads from all ranks issued before the sums.
-    const int cols = HD / CL;
+    // CTA `rank` reduces columns [c0, c0 + cols) of the 16 heads, 4 at a time.
     const int c0 = rank * cols;
     for (int e = tid; e < DEC_HEADS * (cols / 4); e += NTH) {
-        const int hh = e / (cols / 4), c = c0 + 4 * (e % (cols / 4));
+        const int hh = e / (cols / 4), cl4 = 4 * (e % (cols / 4));
         const int h = h0 + hh;
-        float4 v[16];
-#pragma unroll
-        for (int r = 0; r < 16; r++)
-            if (r < CL)
-                v[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(ostage, r) + hh * OSTR + c);
         float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
         for (int r = 0; r < 16; r++) {
             if (r < CL) {
+                const uint2 u = *reinterpret_cast<const uint2*>(opush + (r * DEC_HEADS + hh) * (cols / 2) + cl4 / 2);
+                const float4 v = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                                             __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
                 const float wgt = wts[r * DEC_HEADS + hh];
-                acc.x += v[r].x * wgt;
-                acc.y += v[r].y * wgt;
-                acc.z += v[r].z * wgt;
-                acc.w += v[r].w * wgt;
+                acc.x += v.x * wgt;
+                acc.y += v.y * wgt;
+                acc.z += v.z * wgt;
+                acc.w += v.w * wgt;
             }
         }
         if (h < nh) {
             const uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-            *reinterpret_cast<uint2*>(o + (t * nh + h) * (int64_t)HD + c) = packed;
+            *reinterpret_cast<uint2*>(o + (t * nh + h) * (int64_t)HD + c0 + cl4) = packed;
         }
     }
-    cluster.sync();  // keep this CTA's shared memory alive until all readers are done
+    // no CTA reads another's shared memory after the barrier above, so each
+    // may exit on its own
 }
 
 struct AttnPlan {
@@ -722,9 +929,11 @@ static int launch_attn_decode(const AttnPlan& p, const uint16_t* q, const uint16
                               int64_t n_a, const uint16_t* rows_b, int64_t n_c,
                               const int32_t* idx, int64_t K, const float* sink, float scale,
                               uint16_t* o, float* lse, int64_t m, int64_t nh,
-                              unsigned int* status, cudaStream_t st, bool pdl) {
-    const size_t smem = DecSmem<HD>::total;
-    auto kern = sparse_attn_decode_kernel<HD>;
+                              unsigned int* status, cudaStream_t st, bool pdl,
+                              const DecTopk* tk = nullptr) {
+    const size_t smem = tk ? DecSmem<HD>::fused_total : DecSmem<HD>::total;
+    auto kern = tk ? sparse_attn_decode_kernel<HD, true> : sparse_attn_decode_kernel<HD, false>;
+    const DecTopk tkv = tk ? *tk : DecTopk{};
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (p.cluster > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
@@ -742,7 +951,7 @@ static int launch_attn_decode(const AttnPlan& p, const uint16_t* q, const uint16
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
     int rc = cuda_check(cudaLaunchKernelEx(&cfg, kern, q, rows_a, n_a, rows_b, n_c, idx, (int)K,
-                                           sink, scale * LOG2E, o, lse, (int)nh, status),
+                                           sink, scale * LOG2E, o, lse, (int)nh, status, tkv),
                         "ds41_sparse_attn_sink_fwd: decode kernel");
     if (rc) return rc;
     return launch_check("ds41_sparse_attn_sink_fwd: decode kernel");
@@ -753,10 +962,10 @@ static int launch_attn(const AttnPlan& p, const uint16_t* q, const uint16_t* row
                        const uint16_t* rows_b, int64_t n_c, const int32_t* idx, int64_t K,
                        const float* sink, float scale, uint16_t* o, float* lse, int64_t m,
                        int64_t nh, uint8_t* ws, unsigned int* status, cudaStream_t st,
-                       bool pdl = false) {
+                       bool pdl = false, const DecTopk* tk = nullptr) {
     if (p.cluster > 0)
         return launch_attn_decode<HD>(p, q, rows_a, n_a, rows_b, n_c, idx, K, sink, scale, o, lse,
-                                      m, nh, status, st, pdl);
+                                      m, nh, status, st, pdl, tk);
     if constexpr (HD == 512) {
         if (p.tc > 0)
             return attn_tc_launch(q, rows_a, n_a, rows_b, n_c, idx, K, sink, scale, o, lse, m, nh,
@@ -844,7 +1053,7 @@ size_t attn_ws_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K) {
 int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint16_t* rows_b,
              int64_t n_c, const int32_t* idx, int64_t K, const float* sink, float scale,
              uint16_t* o, float* lse, int64_t m, int64_t nh, int64_t hd, uint8_t* ws,
-             size_t ws_bytes, bool pdl, cudaStream_t st, const char* name) {
+             size_t ws_bytes, bool pdl, cudaStream_t st, const char* name, const DecTopk* tk) {
     unsigned int* status = nullptr;
     int rc = status_word(&status);
     if (rc) return rc;
@@ -855,15 +1064,23 @@ int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint1
     const uint16_t* ra = n_a ? rows_a : rows_b;
     const uint16_t* rb = n_c ? rows_b : rows_a;
     switch (hd) {
-        case 64: return launch_attn<64>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl);
-        case 128: return launch_attn<128>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl);
-        case 256: return launch_attn<256>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl);
-        default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl);
+        case 64: return launch_attn<64>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk);
+        case 128: return launch_attn<128>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk);
+        case 256: return launch_attn<256>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk);
+        default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk);
     }
 }
 
 bool attn_is_cluster_path(int64_t m, int64_t nh, int64_t hd, int64_t K) {
     return plan_attn(m, nh, hd, K, device_sms()).cluster > 0;
+}
+
+bool attn_topk_fusable(int64_t m, int64_t nh, int64_t hd, int64_t K, int64_t n_c) {
+    const AttnPlan p = plan_attn(m, nh, hd, K, device_sms());
+    if (p.cluster < 4) return false;
+    const int64_t per = (K + p.cluster - 1) / p.cluster;
+    const int64_t kseg = ((n_c + p.cluster - 1) / p.cluster + 7) / 8 * 8;
+    return per <= DEC_STAGE && kseg <= TKD_CAP;
 }
 
 }  // namespace ds41

@@ -120,6 +120,12 @@ extern "C" int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf
     uint16_t* scores = static_cast<uint16_t*>(ws);
     int rc = launch_front(q_idx, k_idx, w, scores, m, Hi, Di, n_c, ratio, start_pos, ra, la, st);
     if (rc) return rc;
+    if (attn_topk_fusable(m, nh, hd, K, n_c)) {
+        // the attention clusters select their rows from the scores themselves
+        const DecTopk tk{scores, win_idx, idx, n_c, ratio, start_pos, n_a, (int)win, (int)ctopk};
+        return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
+                        nullptr, 0, true, st, name, &tk);
+    }
     rc = launch_topk(scores, win_idx, idx, m, n_c, win, ctopk, ratio, start_pos, n_a, true, st);
     if (rc) return rc;
     return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,

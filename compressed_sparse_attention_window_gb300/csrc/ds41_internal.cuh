@@ -20,12 +20,27 @@ int launch_topk(const uint16_t* scores, const int32_t* win_idx, int32_t* idx, in
                 int64_t n_c, int64_t win, int64_t ctopk, int64_t ratio, int64_t start_pos,
                 int64_t offset, bool pdl, cudaStream_t st);
 
+// The per-query top-k of the few-token step done by the decode attention
+// clusters themselves (no separate launch, no reload of the index row): the
+// arguments of the merge, as in the top-k kernels of the indexer.
+struct DecTopk {
+    const uint16_t* scores;   // [m][n_c] bf16 indexer scores
+    const int32_t* win_idx;   // [m][win] window indices
+    int32_t* idx_out;         // [m][K] merged index rows (written by head group 0)
+    int64_t n_c, ratio, start_pos, offset;
+    int win, ctopk;
+};
+
 // sparse attention with an explicit plan choice; pdl launches the few-token
-// kernel with programmatic stream serialization
+// kernel with programmatic stream serialization; tk (few-token cluster path
+// only) makes the attention select its rows from the scores first
 int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint16_t* rows_b,
              int64_t n_c, const int32_t* idx, int64_t K, const float* sink, float scale,
              uint16_t* o, float* lse, int64_t m, int64_t nh, int64_t hd, uint8_t* ws,
-             size_t ws_bytes, bool pdl, cudaStream_t st, const char* name);
+             size_t ws_bytes, bool pdl, cudaStream_t st, const char* name,
+             const DecTopk* tk = nullptr);
+// whether the few-token attention can select its own rows for these sizes
+bool attn_topk_fusable(int64_t m, int64_t nh, int64_t hd, int64_t K, int64_t n_c);
 size_t attn_ws_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K);
 bool attn_is_cluster_path(int64_t m, int64_t nh, int64_t hd, int64_t K);
 
