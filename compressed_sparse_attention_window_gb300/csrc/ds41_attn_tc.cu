@@ -11,20 +11,23 @@
 //   s_v = scale * <q[t,h], row_v>
 //
 // Design.  A persistent CTA per SM walks its work items (token, 64 heads).
-// Per item a plan warp turns the index row into chunks of 64 rows: for each
+// Per item a plan warp turns the index row into chunks of 128 rows: for each
 // source (rows_a, rows_b) whose selected rows lie in a compact range the
 // chunks are consecutive rows of that range, loaded by tiled TMA copies, with
-// a 64-bit mask of the selected rows; otherwise the selected rows are listed
+// a 128-bit mask of the selected rows; otherwise the selected rows are listed
 // and fetched by TMA gather4 copies.  Duplicate indices force the list form
 // (each copy then counts once per occurrence, as the definition does).
 //
-//   S  = Q R^T       M = 64 heads, N = 64 rows, K = 512   (S in tensor memory)
-//   O^T += R^T P^T   M = 128 of hd (4 tiles), N = 64 heads, K = 64 rows
+//   S  = Q R^T       M = 64 heads, N = 128 rows, K = 512  (S in tensor memory)
+//   O^T += R^T P^T   M = 128 of hd (4 tiles), N = 64 heads, K = 128 rows
 //
-// A tcgen05.mma instruction costs some 50 cycles of issue however small, so
-// the chunk is as wide as shared memory allows for two row buffers (64 rows),
-// the MMA sequences are fully unrolled on precomputed descriptors, and the
-// four PV tiles are independent accumulators issued in turn.  With heads as
+// A tcgen05.mma instruction costs some 50-70 cycles of issue however small,
+// so the chunk is as wide as the one row buffer shared memory holds next to Q
+// (128 rows, 128 KiB) and the MMA sequences are fully unrolled on
+// precomputed descriptors.  The row buffer is managed in four pairs of
+// 64-column blocks with a barrier each: PV tile t reads pair t only and
+// releases it when done, so the next chunk's loads and the parts of its S
+// follow the PV tile by tile instead of waiting for the whole chunk.  With heads as
 // the rows of S, the four threads of a quad own one head's scores, so the
 // running max and the denominator need two shuffles.  The reference max of a
 // head moves only when a chunk exceeds it by 2^4 (and on the first chunk), so
@@ -50,8 +53,8 @@ namespace tc {
 
 constexpr int HD = 512;
 constexpr int NH = 64;            // heads per work item
-constexpr int RC = 64;            // rows per chunk
-constexpr int NRB = 2;            // row buffers (and S buffers)
+constexpr int RC = 128;           // rows per chunk
+constexpr int NKP = 4;            // pairs of 64-column blocks of the row buffer
 constexpr int THREADS = 384;
 constexpr int MAXK = 1024;        // longest index row this kernel takes
 constexpr int DCAP = 2048;        // longest row range loaded as consecutive rows
@@ -62,15 +65,15 @@ constexpr float RESCALE_LOG2 = 4.0f;
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t Q_KB = 64 * 64 * 2;                // Q block [64 heads][64 dims]: 8 KiB
-constexpr uint32_t R_KB = RC * 64 * 2;                // row block [64 rows][64 dims]: 8 KiB
+constexpr uint32_t R_KB = RC * 64 * 2;                // row block [128 rows][64 dims]: 16 KiB
 constexpr uint32_t Q_OFF = 0;                         // 8 Q blocks
-constexpr uint32_t R_OFF = 8 * Q_KB;                  // NRB buffers x 8 row blocks
+constexpr uint32_t R_OFF = 8 * Q_KB;                  // 8 row blocks (4 pairs)
 constexpr uint32_t R_BYTES = 8 * R_KB;
-constexpr uint32_t P_OFF = R_OFF + NRB * R_BYTES;     // 2 buffers of [64 heads][64 rows] bf16
-constexpr uint32_t P_BYTES = 8192;
-constexpr uint32_t PLAN_OFF = P_OFF + 2 * P_BYTES;    // 2 plans
-constexpr uint32_t PLAN_DESC = 0;                     // MAXCH x uint4
-constexpr uint32_t PLAN_LIST = MAXCH * 16;            // MAXK x int32
+constexpr uint32_t P_OFF = R_OFF + R_BYTES;           // P: 2 blocks of [64 heads][64 rows] bf16
+constexpr uint32_t P_BLK = 8192;
+constexpr uint32_t PLAN_OFF = P_OFF + 2 * P_BLK;      // 2 plans
+constexpr uint32_t PLAN_DESC = 0;                     // MAXCH x 2 uint4
+constexpr uint32_t PLAN_LIST = MAXCH * 32;            // MAXK x int32
 constexpr uint32_t PLAN_N = PLAN_LIST + MAXK * 4;     // chunk count
 constexpr uint32_t PLAN_BYTES = PLAN_N + 64;
 constexpr uint32_t BM_OFF = PLAN_OFF + 2 * PLAN_BYTES;  // 2 sources x DCAP bits
@@ -84,13 +87,13 @@ static_assert(PLAN_OFF % 16 == 0 && PLAN_BYTES % 16 == 0, "plan alignment");
 // barriers
 enum {
     B_QFULL, B_QEMPTY,
-    B_RFULL,                               // NRB: row chunk landed
-    B_DONE = B_RFULL + NRB,                // NRB: PV of the chunk complete (row and P buffers free)
-    B_SFULL = B_DONE + NRB,                // NRB: S of the chunk in tensor memory
-    B_SEMPTY = B_SFULL + NRB,              // NRB: S read by the softmax warps
-    B_CORR = B_SEMPTY + NRB,               // NRB: rescale factors of the chunk written
-    B_PFULL = B_CORR + NRB,                // 2: P written and O rescaled
-    B_ODONE = B_PFULL + 2, B_OFREE,
+    B_RFULL,                               // NKP: block pair of the chunk landed
+    B_REMPTY = B_RFULL + NKP,              // NKP: PV tile done with the block pair
+    B_DONE = B_REMPTY + NKP,               // PV of the chunk complete (P free, O up to date)
+    B_SFULL, B_SEMPTY,                     // S of the chunk in tensor memory / read
+    B_CORR,                                // rescale factors of the chunk written
+    B_PFULL,                               // P written and O rescaled
+    B_ODONE, B_OFREE,
     B_INVL, B_INVLFREE = B_INVL + 2,       // 2 each: per-item normalisers
     B_PLANFULL = B_INVLFREE + 2, B_PLANEMPTY = B_PLANFULL + 2,
     B_FINAL = B_PLANEMPTY + 2, NBAR
@@ -99,13 +102,13 @@ enum {
 constexpr uint32_t M_BAR = 0;                   // NBAR x 8
 constexpr uint32_t M_TMEM = 512;                // tensor memory base address
 constexpr uint32_t M_ABORT = 516;               // set when any wait gave up
-constexpr uint32_t M_FLAG = 528;                // NRB x 4 ints: a warp's heads moved their reference
-constexpr uint32_t M_CORR = 1024;               // NRB x 64 floats
+constexpr uint32_t M_FLAG = 528;                // 4 ints: a warp's heads moved their reference
+constexpr uint32_t M_CORR = 1024;               // 64 floats
 constexpr uint32_t M_INVL = 2048;               // 2 x 64 floats
 static_assert(NBAR * 8 <= 512 && M_INVL + 512 <= MISC_BYTES, "misc layout");
 
 // tensor memory columns
-constexpr uint32_t TM_S = 0;     // S buffer b at column 64 b
+constexpr uint32_t TM_S = 0;     // S at columns 0 .. 127
 constexpr uint32_t TM_O = 128;   // O^T tile mt at column 128 + 64 mt
 constexpr uint32_t TM_COLS = 512;
 
@@ -152,10 +155,10 @@ __device__ __forceinline__ int warp_max(int v) {
 
 // ---------------------------------------------------------------------------
 // Plan warp: index row of one item -> chunk descriptors
-//   desc.x: row (consecutive chunk) or list offset (listed chunk) in bits
-//           0..29, source in bit 30 (0 rows_a, 1 rows_b), listed in bit 31
-//   desc.y / desc.z: mask of the chunk's rows 0..31 / 32..63 (row r selected
-//           iff its bit is set)
+//   desc[2i].x: row (consecutive chunk) or list offset (listed chunk) in bits
+//               0..29, source in bit 30 (0 rows_a, 1 rows_b), listed in bit 31
+//   desc[2i].y/z/w, desc[2i+1].x: mask of the chunk's rows 0..31, 32..63,
+//               64..95, 96..127 (row r selected iff its bit is set)
 // ---------------------------------------------------------------------------
 __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, int lane) {
     constexpr int KPL = MAXK / 32;  // index entries per lane
@@ -196,9 +199,9 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
         mn[s] = warp_min(mn[s]);
         mx[s] = warp_max(mx[s]);
         range[s] = cnt[s] ? mx[s] - mn[s] + 1 : 0;
-        dense[s] = cnt[s] > 0 && range[s] <= DCAP && range[s] <= 2 * cnt[s] + 2 * RC;
+        dense[s] = cnt[s] > 0 && range[s] <= DCAP && range[s] <= 2 * cnt[s] + RC;
         if (dense[s]) {
-            const int nw = 2 * ((range[s] + RC - 1) / RC);
+            const int nw = 4 * ((range[s] + RC - 1) / RC);
             for (int w = lane; w < nw; w += 32) bm[s * BM_WORDS + w] = 0u;
         }
     }
@@ -245,28 +248,39 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
             const int nck = (range[s] + RC - 1) / RC;
             for (int base = 0; base < nck; base += 32) {
                 const int i = base + lane;
-                const uint32_t lo = i < nck ? bm[s * BM_WORDS + 2 * i] : 0u;
-                const uint32_t hi = i < nck ? bm[s * BM_WORDS + 2 * i + 1] : 0u;
-                const bool keep = (lo | hi) != 0u;
+                uint4 mk = make_uint4(0u, 0u, 0u, 0u);
+                if (i < nck) mk = *reinterpret_cast<const uint4*>(bm + s * BM_WORDS + 4 * i);
+                const bool keep = (mk.x | mk.y | mk.z | mk.w) != 0u;
                 const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-                if (keep)
-                    desc[nch + __popc(bal & lt)] =
-                        make_uint4((uint32_t)(mn[s] + RC * i) | sbit, lo, hi, 0u);
+                if (keep) {
+                    const int at = nch + __popc(bal & lt);
+                    desc[2 * at] = make_uint4((uint32_t)(mn[s] + RC * i) | sbit, mk.x, mk.y, mk.z);
+                    desc[2 * at + 1] = make_uint4(mk.w, 0u, 0u, 0u);
+                }
                 nch += __popc(bal);
             }
         } else {
             const int nck = (cnt[s] + RC - 1) / RC;
             for (int i = lane; i < nck; i += 32) {
                 const int n = min(RC, cnt[s] - RC * i);
-                const uint32_t lo = n >= 32 ? 0xffffffffu : ((1u << n) - 1u);
-                const uint32_t hi = n >= 64 ? 0xffffffffu : (n > 32 ? ((1u << (n - 32)) - 1u) : 0u);
-                desc[nch + i] = make_uint4((uint32_t)(off[s] + RC * i) | sbit | 0x80000000u, lo, hi, 0u);
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int nb = n - 32 * k;
+                    w[k] = nb >= 32 ? 0xffffffffu : (nb > 0 ? ((1u << nb) - 1u) : 0u);
+                }
+                desc[2 * (nch + i)] =
+                    make_uint4((uint32_t)(off[s] + RC * i) | sbit | 0x80000000u, w[0], w[1], w[2]);
+                desc[2 * (nch + i) + 1] = make_uint4(w[3], 0u, 0u, 0u);
             }
             nch += nck;
         }
     }
     if (nch == 0) {  // nothing valid: one fully masked chunk of out-of-range (zero) rows
-        if (lane == 0) desc[0] = make_uint4((uint32_t)OOB_ROW, 0u, 0u, 0u);
+        if (lane == 0) {
+            desc[0] = make_uint4((uint32_t)OOB_ROW, 0u, 0u, 0u);
+            desc[1] = make_uint4(0u, 0u, 0u, 0u);
+        }
         nch = 1;
     }
     if (lane == 0) *reinterpret_cast<int*>(plan + PLAN_N) = nch;
@@ -303,15 +317,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bars[B_QFULL], 1);
         mbar_init(&bars[B_QEMPTY], 1);
-        for (int b = 0; b < NRB; b++) {
-            mbar_init(&bars[B_RFULL + b], 1);
-            mbar_init(&bars[B_DONE + b], 1);
-            mbar_init(&bars[B_SFULL + b], 1);
-            mbar_init(&bars[B_SEMPTY + b], 4);
-            mbar_init(&bars[B_CORR + b], 4);
+        for (int k = 0; k < NKP; k++) {
+            mbar_init(&bars[B_RFULL + k], 1);
+            mbar_init(&bars[B_REMPTY + k], 1);
         }
+        mbar_init(&bars[B_DONE], 1);
+        mbar_init(&bars[B_SFULL], 1);
+        mbar_init(&bars[B_SEMPTY], 4);
+        mbar_init(&bars[B_CORR], 4);
+        mbar_init(&bars[B_PFULL], 8);
         for (int b = 0; b < 2; b++) {
-            mbar_init(&bars[B_PFULL + b], 8);
             mbar_init(&bars[B_INVL + b], 4);
             mbar_init(&bars[B_INVLFREE + b], 4);
             mbar_init(&bars[B_PLANFULL + b], 1);
@@ -338,11 +353,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------------
-        // TMA producer (one lane)
+        // TMA producer (one lane): per chunk, block pair k is loaded as soon
+        // as the previous chunk's PV tile k has released it
         // ------------------------------------------------------------------
         if (lane == 0) {
             uint32_t g = 0;
-            uint32_t q_armed = 0, r_armed[NRB] = {0, 0};
+            uint32_t q_armed = 0, r_armed[NKP] = {0, 0, 0, 0};
             for (int j = 0; j < ntok; j++) {
                 int t, hgi;
                 item_of(j, p.m, hg, t, hgi);
@@ -359,37 +375,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int* list = reinterpret_cast<const int*>(plan + PLAN_LIST);
                 const int nch = *reinterpret_cast<const int*>(plan + PLAN_N);
                 bool ok = true;
-                for (int i = 0; i < nch; i++, g++) {
-                    const int b = g % NRB;
-                    if (g >= NRB && !wait_bar(&bars[B_DONE + b], ((g - NRB) / NRB) & 1, abort_f,
-                                              p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&bars[B_RFULL + b], 8 * R_KB);
-                    r_armed[b]++;
-                    const uint4 d = desc[i];
+                for (int i = 0; i < nch && ok; i++, g++) {
+                    const uint4 d = desc[2 * i];
+                    const uint4 d1 = desc[2 * i + 1];
                     const int pos = (int)(d.x & 0x3FFFFFFFu);
                     const bool src_b = (d.x >> 30) & 1u;
-                    const uint32_t rb = sbase + R_OFF + b * R_BYTES;
-                    if (!(d.x & 0x80000000u)) {
-                        const CUtensorMap* mp = src_b ? &map_bd : &map_ad;
-                        for (int kb = 0; kb < 8; kb++)
-                            tma_load_2d(rb + kb * R_KB, mp, kb * 64, pos, &bars[B_RFULL + b]);
-                    } else {
-                        const CUtensorMap* mp = src_b ? &map_bg : &map_ag;
-                        const int cnt = __popc(d.y) + __popc(d.z);
-                        const int* lr = list + pos;
-                        for (int gq = 0; gq < RC / 4; gq++) {
-                            int y[4];
+                    const bool listed = (d.x & 0x80000000u) != 0u;
+                    const int cnt = __popc(d.y) + __popc(d.z) + __popc(d.w) + __popc(d1.x);
+                    const int* lr = list + pos;
+                    for (int kp = 0; kp < NKP; kp++) {
+                        if (g >= 1 && !wait_bar(&bars[B_REMPTY + kp], (g - 1) & 1, abort_f, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars[B_RFULL + kp], 2 * R_KB);
+                        r_armed[kp]++;
+                        const uint32_t rb = sbase + R_OFF + 2 * kp * R_KB;
+                        if (!listed) {
+                            const CUtensorMap* mp = src_b ? &map_bd : &map_ad;
+                            for (int kb = 0; kb < 2; kb++)
+                                tma_load_2d(rb + kb * R_KB, mp, (2 * kp + kb) * 64, pos,
+                                            &bars[B_RFULL + kp]);
+                        } else {
+                            const CUtensorMap* mp = src_b ? &map_bg : &map_ag;
+                            for (int gq = 0; gq < RC / 4; gq++) {
+                                int y[4];
 #pragma unroll
-                            for (int k = 0; k < 4; k++) {
-                                const int r = 4 * gq + k;
-                                y[k] = r < cnt ? lr[r] : OOB_ROW;  // beyond the list: zero fill
+                                for (int k = 0; k < 4; k++) {
+                                    const int r = 4 * gq + k;
+                                    y[k] = r < cnt ? lr[r] : OOB_ROW;  // beyond the list: zero fill
+                                }
+                                for (int kb = 0; kb < 2; kb++)
+                                    tma_gather4(rb + kb * R_KB + gq * 512, mp, (2 * kp + kb) * 64,
+                                                y[0], y[1], y[2], y[3], &bars[B_RFULL + kp]);
                             }
-                            for (int kb = 0; kb < 8; kb++)
-                                tma_gather4(rb + kb * R_KB + gq * 512, mp, kb * 64, y[0], y[1],
-                                            y[2], y[3], &bars[B_RFULL + b]);
                         }
                     }
                 }
@@ -398,87 +417,97 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // let every copy this CTA started land before the CTA exits
             if (q_armed) wait_bar(&bars[B_QFULL], (q_armed - 1) & 1, abort_f, p.status);
-            for (int b = 0; b < NRB; b++)
-                if (r_armed[b]) wait_bar(&bars[B_RFULL + b], (r_armed[b] - 1) & 1, abort_f, p.status);
+            for (int kp = 0; kp < NKP; kp++)
+                if (r_armed[kp]) wait_bar(&bars[B_RFULL + kp], (r_armed[kp] - 1) & 1, abort_f, p.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
-        // MMA issuer (one lane): S may run up to NRB - 1 chunks ahead of PV
+        // MMA issuer (one lane).  PV tiles first: tile k of PV(g) releases
+        // block pair k, whose load for chunk g + 1 then feeds part k of
+        // S(g + 1), so S of the next chunk follows the PV tile by tile.
         // ------------------------------------------------------------------
         if (lane == 0) {
-            int s_tok = 0, s_i = 0, s_n = -1;
-            int p_tok = 0, p_i = 0;
+            int s_tok = 0, s_i = 0, s_n = -1, s_kp = 0;
+            int p_tok = 0, p_i = 0, p_mt = 0;
             uint32_t sg = 0, pg = 0;
             int nring[4] = {0, 0, 0, 0};
             uint32_t idle = 0;
             const uint32_t q_s = sbase + Q_OFF;
+            const uint32_t r_s = sbase + R_OFF;
+            const uint32_t p_s = sbase + P_OFF;
             while (p_tok < ntok) {
                 bool prog = false;
-                if (s_tok < ntok && s_tok < p_tok + 3) {
+                if (pg < sg) {
+                    const bool ok =
+                        p_mt > 0 ||
+                        (mbar_test(&bars[B_PFULL], pg & 1) &&
+                         (p_i > 0 || p_tok == 0 || mbar_test(&bars[B_OFREE], (p_tok - 1) & 1)));
+                    if (ok) {
+                        if (p_mt == 0) tc_fence_after();
+                        // O^T tile p_mt += R^T P^T over the 128 rows of the chunk
+                        // (P in two K blocks of 64 rows)
+                        const uint64_t vd = sdesc(r_s + 2 * p_mt * R_KB, R_KB, 1024);
+                        const uint64_t pd = sdesc(p_s, 16, 1024);
+                        const uint32_t acc0 = p_i > 0 ? 1u : 0u;
+                        const uint32_t d = tmem + TM_O + 64 * p_mt;
+#pragma unroll
+                        for (int kk = 0; kk < RC / 16; kk++)
+                            tc_mma(d, vd + ((kk * 2048) >> 4),
+                                   pd + (((kk >> 2) * P_BLK + (kk & 3) * 32) >> 4), IDESC_PV,
+                                   kk > 0 ? 1u : acc0);
+                        tc_commit(&bars[B_REMPTY + p_mt]);
+                        if (++p_mt == 4) {
+                            p_mt = 0;
+                            tc_commit(&bars[B_DONE]);
+                            const int pn = nring[p_tok & 3];
+                            if (p_i == pn - 1) tc_commit(&bars[B_ODONE]);
+                            pg++;
+                            if (++p_i == pn) {
+                                p_tok++;
+                                p_i = 0;
+                            }
+                        }
+                        prog = true;
+                    }
+                }
+                if (s_tok < ntok && s_tok < p_tok + 3 && sg <= pg + 1) {
                     if (s_n < 0 && mbar_test(&bars[B_PLANFULL + (s_tok & 1)], (s_tok >> 1) & 1)) {
                         s_n = *reinterpret_cast<const int*>(sm + PLAN_OFF +
                                                             (s_tok & 1) * PLAN_BYTES + PLAN_N);
                         nring[s_tok & 3] = s_n;
                     }
-                    if (s_n > 0 && sg < pg + NRB) {
-                        const int b = sg % NRB;
+                    if (s_n > 0) {
                         const bool ok =
-                            mbar_test(&bars[B_RFULL + b], (sg / NRB) & 1) &&
-                            (sg < NRB || mbar_test(&bars[B_SEMPTY + b], ((sg - NRB) / NRB) & 1)) &&
-                            (s_i > 0 || mbar_test(&bars[B_QFULL], s_tok & 1));
+                            mbar_test(&bars[B_RFULL + s_kp], sg & 1) &&
+                            (s_kp > 0 ||
+                             ((sg < 1 || mbar_test(&bars[B_SEMPTY], (sg - 1) & 1)) &&
+                              (s_i > 0 || mbar_test(&bars[B_QFULL], s_tok & 1))));
                         if (ok) {
                             tc_fence_after();
-                            // S = Q R^T over K = 512: 32 MMAs on descriptors that
-                            // step by a compile-time offset (16-byte units)
-                            const uint64_t qd = sdesc(q_s, 16, 1024);
-                            const uint64_t rd = sdesc(sbase + R_OFF + b * R_BYTES, 16, 1024);
-                            const uint32_t d = tmem + TM_S + RC * b;
+                            // part s_kp of S = Q R^T: the 64-column blocks 2 s_kp and
+                            // 2 s_kp + 1, 8 MMAs on descriptors stepped by offsets in
+                            // 16-byte units
+                            const uint32_t kb0 = 2 * s_kp;
+                            const uint64_t qd = sdesc(q_s + kb0 * Q_KB, 16, 1024);
+                            const uint64_t rd = sdesc(r_s + kb0 * R_KB, 16, 1024);
 #pragma unroll
-                            for (int kk = 0; kk < HD / 16; kk++) {
-                                tc_mma(d, qd + (((kk >> 2) * Q_KB + (kk & 3) * 32) >> 4),
+                            for (int kk = 0; kk < 8; kk++)
+                                tc_mma(tmem + TM_S, qd + (((kk >> 2) * Q_KB + (kk & 3) * 32) >> 4),
                                        rd + (((kk >> 2) * R_KB + (kk & 3) * 32) >> 4), IDESC_S,
-                                       kk > 0 ? 1u : 0u);
-                            }
-                            tc_commit(&bars[B_SFULL + b]);
-                            if (s_i == s_n - 1) tc_commit(&bars[B_QEMPTY]);
-                            sg++;
-                            if (++s_i == s_n) {
-                                s_tok++;
-                                s_i = 0;
-                                s_n = -1;
+                                       (s_kp > 0 || kk > 0) ? 1u : 0u);
+                            if (++s_kp == NKP) {
+                                s_kp = 0;
+                                tc_commit(&bars[B_SFULL]);
+                                if (s_i == s_n - 1) tc_commit(&bars[B_QEMPTY]);
+                                sg++;
+                                if (++s_i == s_n) {
+                                    s_tok++;
+                                    s_i = 0;
+                                    s_n = -1;
+                                }
                             }
                             prog = true;
                         }
-                    }
-                }
-                if (pg < sg) {
-                    const int b = pg % NRB, pb = pg & 1;
-                    const bool ok =
-                        mbar_test(&bars[B_PFULL + pb], (pg >> 1) & 1) &&
-                        (p_i > 0 || p_tok == 0 || mbar_test(&bars[B_OFREE], (p_tok - 1) & 1));
-                    if (ok) {
-                        tc_fence_after();
-                        // O^T += R^T P^T: the four head-dim tiles are independent
-                        // accumulators, issued in turn for each 16-row step
-                        const uint64_t vd = sdesc(sbase + R_OFF + b * R_BYTES, R_KB, 1024);
-                        const uint64_t pd = sdesc(sbase + P_OFF + pb * P_BYTES, 16, 1024);
-                        const uint32_t acc0 = p_i > 0 ? 1u : 0u;
-#pragma unroll
-                        for (int kk = 0; kk < RC / 16; kk++)
-#pragma unroll
-                            for (int mt = 0; mt < 4; mt++)
-                                tc_mma(tmem + TM_O + 64 * mt,
-                                       vd + ((2 * mt * R_KB + kk * 2048) >> 4),
-                                       pd + ((kk * 32) >> 4), IDESC_PV, kk > 0 ? 1u : acc0);
-                        tc_commit(&bars[B_DONE + b]);
-                        const int pn = nring[p_tok & 3];
-                        if (p_i == pn - 1) tc_commit(&bars[B_ODONE]);
-                        pg++;
-                        if (++p_i == pn) {
-                            p_tok++;
-                            p_i = 0;
-                        }
-                        prog = true;
                     }
                 }
                 if (prog) {
@@ -515,8 +544,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------------
         // Softmax: warp 4+q reads lane quarter q.  With M = 64 the scores of
         // head 16q + r sit in lane 32q + r (r < 16), one column per row of
-        // the chunk; the 16x256b read gives thread l the heads hA = 16q + l/4
-        // and hB = hA + 8, 16 columns each.
+        // the chunk; the 16x256b reads give thread l the heads hA = 16q + l/4
+        // and hB = hA + 8, 32 columns each.
         // ------------------------------------------------------------------
         const int q = warp - 4;
         const int qi = lane & 3;
@@ -536,30 +565,33 @@ __global__ void __launch_bounds__(THREADS, 1)
             float mA = -INFINITY, mB = -INFINITY, lA = 0.0f, lB = 0.0f;
             bool bad = false;
             for (int i = 0; i < nch; i++, g++) {
-                const int b = g % NRB;
-                const uint4 dsc = desc[i];
+                const uint4 d0 = desc[2 * i];
+                const uint32_t m3 = desc[2 * i + 1].x;
                 __syncwarp();
                 if (i == nch - 1 && lane == 0)
                     mbar_arrive(&bars[B_PLANEMPTY + slot]);  // this warp's last read of the plan
-                if (!wait_bar(&bars[B_SFULL + b], (g / NRB) & 1, abort_f, p.status)) {
+                if (!wait_bar(&bars[B_SFULL], g & 1, abort_f, p.status)) {
                     bad = true;
                     break;
                 }
                 tc_fence_after();
-                uint32_t sr[32];
-                tc_ld16x256(tmem + lane_off + TM_S + RC * b, sr);
+                uint32_t sr[64];
+                tc_ld16x256(tmem + lane_off + TM_S, *reinterpret_cast<uint32_t(*)[32]>(sr));
+                tc_ld16x256(tmem + lane_off + TM_S + 64, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
                 tc_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_SEMPTY + b]);
-                // scaled scores (log2 units), -inf where the row is not selected
-                const uint32_t mlo = dsc.y >> (2 * qi), mhi = dsc.z >> (2 * qi);
+                if (lane == 0) mbar_arrive(&bars[B_SEMPTY]);
+                // scaled scores (log2 units), -inf where the row is not selected:
+                // register 4 jr + e (+2) holds column 8 jr + 2 qi + e, jr = 0..15
+                const uint32_t mw[4] = {d0.y >> (2 * qi), d0.z >> (2 * qi), d0.w >> (2 * qi),
+                                        m3 >> (2 * qi)};
                 float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
-                for (int jr = 0; jr < 8; jr++) {
+                for (int jr = 0; jr < 16; jr++) {
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
-                        const bool sel = ((jr < 4 ? mlo : mhi) >> (8 * (jr & 3) + e)) & 1u;
+                        const bool sel = (mw[jr >> 2] >> (8 * (jr & 3) + e)) & 1u;
                         const float xa = sel ? __uint_as_float(sr[4 * jr + e]) * p.scale_log2 : -INFINITY;
                         const float xb =
                             sel ? __uint_as_float(sr[4 * jr + 2 + e]) * p.scale_log2 : -INFINITY;
@@ -592,18 +624,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // hand the rescale factors of this chunk to the correction warps
                 const bool moved = __any_sync(0xffffffffu, cA != 1.0f || cB != 1.0f);
                 if (qi == 0) {
-                    corr_s[b * 64 + hA] = cA;
-                    corr_s[b * 64 + hB] = cB;
+                    corr_s[hA] = cA;
+                    corr_s[hB] = cB;
                 }
-                if (lane == 0) flags[b * 4 + q] = moved ? 1 : 0;
+                if (lane == 0) flags[q] = moved ? 1 : 0;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_CORR + b]);
+                if (lane == 0) mbar_arrive(&bars[B_CORR]);
                 // probabilities, the denominator, P (bf16) for the PV MMA
                 const float muA = (mA == -INFINITY) ? 0.0f : mA;
                 const float muB = (mB == -INFINITY) ? 0.0f : mB;
-                uint32_t pkA[8], pkB[8];
+                uint32_t pkA[16], pkB[16];
 #pragma unroll
-                for (int jr = 0; jr < 8; jr++) {
+                for (int jr = 0; jr < 16; jr++) {
                     const float a0 = exp2f(__uint_as_float(sr[4 * jr]) - muA);
                     const float a1 = exp2f(__uint_as_float(sr[4 * jr + 1]) - muA);
                     const float b0 = exp2f(__uint_as_float(sr[4 * jr + 2]) - muB);
@@ -613,27 +645,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                     pkA[jr] = pack_bf16x2(a0, a1);
                     pkB[jr] = pack_bf16x2(b0, b1);
                 }
-                const int pb = g & 1;
-                if (g >= 2 && !wait_bar(&bars[B_DONE + (g - 2) % NRB], ((g - 2) / NRB) & 1, abort_f,
-                                        p.status)) {
+                // P is free once PV(g - 1) is done
+                if (g >= 1 && !wait_bar(&bars[B_DONE], (g - 1) & 1, abort_f, p.status)) {
                     bad = true;
                     break;
                 }
                 {
-                    // row h of P: 8 chunks of 16 bytes (8 rows each), swizzled
-                    // by h % 8; this thread writes 4 bytes of each
-                    uint8_t* pbuf = sm + P_OFF + pb * P_BYTES;
-                    uint8_t* ra = pbuf + (hA >> 3) * 1024 + (hA & 7) * 128 + 4 * qi;
-                    uint8_t* rbp = pbuf + (hB >> 3) * 1024 + (hB & 7) * 128 + 4 * qi;
+                    // row h of P block k: 8 chunks of 16 bytes (8 rows each),
+                    // swizzled by h % 8; this thread writes 4 bytes of each
 #pragma unroll
-                    for (int jr = 0; jr < 8; jr++) {
-                        *reinterpret_cast<uint32_t*>(ra + ((jr ^ (hA & 7)) << 4)) = pkA[jr];
-                        *reinterpret_cast<uint32_t*>(rbp + ((jr ^ (hB & 7)) << 4)) = pkB[jr];
+                    for (int jr = 0; jr < 16; jr++) {
+                        uint8_t* pb = sm + P_OFF + (jr >> 3) * P_BLK;
+                        const int c = jr & 7;
+                        *reinterpret_cast<uint32_t*>(pb + (hA >> 3) * 1024 + (hA & 7) * 128 +
+                                                     ((c ^ (hA & 7)) << 4) + 4 * qi) = pkA[jr];
+                        *reinterpret_cast<uint32_t*>(pb + (hB >> 3) * 1024 + (hB & 7) * 128 +
+                                                     ((c ^ (hB & 7)) << 4) + 4 * qi) = pkB[jr];
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_PFULL + pb]);
+                if (lane == 0) mbar_arrive(&bars[B_PFULL]);
             }
             if (bad) break;
             // ---- normalisers of this item for the correction warps ----
@@ -678,22 +710,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (warp == 8 && lane == 0) mbar_arrive(&bars[B_PLANEMPTY + slot]);
             bool bad = false;
             for (int i = 0; i < nch; i++, g++) {
-                const int b = g % NRB;
-                if (!wait_bar(&bars[B_CORR + b], (g / NRB) & 1, abort_f, p.status)) {
+                if (!wait_bar(&bars[B_CORR], g & 1, abort_f, p.status)) {
                     bad = true;
                     break;
                 }
-                const int moved = flags[b * 4 + 0] | flags[b * 4 + 1] | flags[b * 4 + 2] |
-                                  flags[b * 4 + 3];
+                const int moved = flags[0] | flags[1] | flags[2] | flags[3];
                 if (moved) {
                     // O^T holds the chunks before this one once PV(g-1) is done
-                    if (!wait_bar(&bars[B_DONE + (g - 1) % NRB], ((g - 1) / NRB) & 1, abort_f,
-                                  p.status)) {
+                    if (!wait_bar(&bars[B_DONE], (g - 1) & 1, abort_f, p.status)) {
                         bad = true;
                         break;
                     }
                     tc_fence_after();
-                    const float* cf = corr_s + b * 64;
 #pragma unroll 1
                     for (int mt = 0; mt < 4; mt++) {
 #pragma unroll 1
@@ -704,7 +732,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             tc_wait_ld();
 #pragma unroll
                             for (int k = 0; k < 32; k++)
-                                ov[k] = __float_as_uint(__uint_as_float(ov[k]) * cf[32 * hh + k]);
+                                ov[k] = __float_as_uint(__uint_as_float(ov[k]) * corr_s[32 * hh + k]);
                             tc_st32(ta, ov);
                         }
                     }
@@ -712,7 +740,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_before();
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_PFULL + (g & 1)]);
+                if (lane == 0) mbar_arrive(&bars[B_PFULL]);
             }
             if (bad) break;
             // ---- epilogue of this item ----
