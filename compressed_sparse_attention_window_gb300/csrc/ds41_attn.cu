@@ -318,15 +318,154 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
 
 // ---------------------------------------------------------------------------
 constexpr int TKD_CAP = 4096;  // score keys of one CTA's slice in the fused decode step
+constexpr int TKD_WHIST = 10752;  // per-warp histograms of the local selection, in its area
+
+// Split halves of a cluster barrier: every CTA arrives once it has started,
+// and waits before its first access to another CTA's shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+}
+
+// The selection of dec_topk when every visible score fits in registers
+// (vis <= TKD_CAP, at most TKD_CAP / NTH per thread): each CTA ranks all of
+// them itself, with the same two 8-bit histogram passes, threshold and tie
+// rule (the lowest-numbered ties) as the cluster version, and keeps the picks
+// whose positions fall in its own slice [j0, j1).  Thread (w, l) holds the run of
+// kpt consecutive scores starting at kpt (32 w + l), so index order is warp,
+// lane, register; the histograms are per warp (no same-address atomics across
+// warps), and positions come from one warp scan.  No cluster traffic.
+template <int NTH>
+__device__ void dec_topk_local(const DecTopk& tk, int64_t t, int vis, int kk, int win, int j0, int j1,
+                               int* sidx, uint8_t* area, int32_t* orow, bool write_idx) {
+    constexpr int NW = NTH / 32;
+    constexpr int KMAX = TKD_CAP / NTH;  // 16 with 8 warps
+    static_assert(NTH * KMAX == TKD_CAP && KMAX % 8 == 0, "keys per thread");
+    int* hist = reinterpret_cast<int*>(area + 8192);
+    int* hist2 = hist + 256;
+    int* wsum = hist2 + 256;
+    int* sel = wsum + 64;
+    int* whist = reinterpret_cast<int*>(area + TKD_WHIST);  // [NW][256]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (kk <= 0) return;
+    const int kpt = (vis + NTH - 1) / NTH;
+    const int i0 = kpt * tid;  // first score of this thread
+    const uint16_t* sc = tk.scores + t * tk.n_c;
+    uint32_t key[KMAX];
+    const bool vec = (kpt & 7) == 0 && ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0);
+#pragma unroll
+    for (int v = 0; v < KMAX / 8; v++) {
+        const int b0 = i0 + 8 * v;
+        if (8 * v >= kpt || b0 >= vis) continue;
+        if (vec && b0 + 8 <= vis) {  // whole groups of eight only: nothing past vis is read
+            uint4 u = __ldg(reinterpret_cast<const uint4*>(sc + b0));
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&u);
+#pragma unroll
+            for (int e = 0; e < 8; e++) key[8 * v + e] = order_key(h[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                if (8 * v + e < kpt && b0 + e < vis) key[8 * v + e] = order_key(sc[b0 + e]);
+        }
+    }
+    // keys past vis (or past kpt) take no part: n_mine counts the live ones
+    const int n_mine = max(0, min(kpt, vis - i0));
+    int* wh = whist + warp * 256;
+#pragma unroll
+    for (int e = 0; e < 8; e++) wh[lane + 32 * e] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < KMAX; e++)
+        if (e < n_mine) atomicAdd(&wh[key[e] >> 8], 1);
+    __syncthreads();
+    for (int b = tid; b < 256; b += NTH) {
+        int v = 0;
+#pragma unroll
+        for (int w = 0; w < NW; w++) {
+            v += whist[w * 256 + b];
+            whist[w * 256 + b] = 0;
+        }
+        hist[b] = v;
+    }
+    __syncthreads();
+    if (tid < 32) find_bucket(hist, kk, 0, &sel[0], &sel[1]);
+    __syncthreads();
+    const uint32_t hb = (uint32_t)sel[0];
+#pragma unroll
+    for (int e = 0; e < KMAX; e++)
+        if (e < n_mine && (key[e] >> 8) == hb) atomicAdd(&wh[key[e] & 0xffu], 1);
+    __syncthreads();
+    for (int b = tid; b < 256; b += NTH) {
+        int v = 0;
+#pragma unroll
+        for (int w = 0; w < NW; w++) v += whist[w * 256 + b];
+        hist2[b] = v;
+    }
+    __syncthreads();
+    if (tid < 32) find_bucket(hist2, kk, sel[1], &sel[2], &sel[3]);
+    __syncthreads();
+    const uint32_t T = (hb << 8) | (uint32_t)sel[2];
+    const int need_eq = kk - sel[3];
+    int n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int e = 0; e < KMAX; e++) {
+        if (e < n_mine) {
+            n_gt += key[e] > T ? 1 : 0;
+            n_eq += key[e] == T ? 1 : 0;
+        }
+    }
+    // exclusive prefixes over the lanes of the warp, then over the warps
+    int x_gt = n_gt, x_eq = n_eq;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, x_gt, off);
+        const int b = __shfl_up_sync(0xffffffffu, x_eq, off);
+        if (lane >= off) {
+            x_gt += a;
+            x_eq += b;
+        }
+    }
+    if (lane == 31) {
+        wsum[warp] = x_gt;
+        wsum[32 + warp] = x_eq;
+    }
+    __syncthreads();
+    int gt = x_gt - n_gt, eq = x_eq - n_eq;
+    for (int w = 0; w < warp; w++) {
+        gt += wsum[w];
+        eq += wsum[32 + w];
+    }
+#pragma unroll
+    for (int e = 0; e < KMAX; e++) {
+        if (e < n_mine) {
+            const bool is_eq = key[e] == T;
+            const bool take = key[e] > T || (is_eq && eq < need_eq);
+            if (take) {
+                const int j = win + gt + min(eq, need_eq);  // position in the merged row
+                if (j >= j0 && j < j1) {
+                    const int v = (int)(tk.offset + i0 + e);
+                    sidx[j - j0] = v;
+                    if (write_idx) orow[j] = v;
+                }
+            }
+            gt += key[e] > T ? 1 : 0;
+            eq += is_eq ? 1 : 0;
+        }
+    }
+}
 
 // Fill sidx[0 .. j1 - j0) with slice [j0, j1) of the merged index row
 // [window indices | the min(ctopk, visible) best compressed rows in ascending
-// order | -1].  The CL CTAs of the cluster each take one slice of the visible
-// scores, sum their two 8-bit histograms over the cluster (every CTA derives
-// the same threshold; the lowest-numbered ties are taken), and store each
-// pick straight into the index slice of the CTA that owns its position.
+// order | -1].  Up to TKD_CAP visible scores every CTA ranks them all itself
+// (dec_topk_local).  Beyond, the CL CTAs of the cluster each take one slice
+// of the visible scores, sum their two 8-bit histograms over the cluster
+// (every CTA derives the same threshold; the lowest-numbered ties are taken),
+// and store each pick straight into the index slice of the CTA that owns its
+// position.  Returns whether it waited on the cluster barrier's first phase.
 template <int NTH>
-__device__ void dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, int j1, int* sidx,
+__device__ bool dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, int j1, int* sidx,
                          uint8_t* area, int* hpush, bool write_idx, unsigned int* status) {
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
@@ -361,7 +500,12 @@ __device__ void dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, i
         sidx[j - j0] = v;
         if (write_idx) orow[j] = v;
     }
-    if (vis <= tk.ctopk) return;  // the same branch in every CTA of the cluster
+    if (vis <= tk.ctopk) return false;  // the same branch in every CTA of the cluster
+    if (vis <= TKD_CAP) {
+        dec_topk_local<NTH>(tk, t, (int)vis, kk, win, j0, j1, sidx, area, orow, write_idx);
+        return false;
+    }
+    cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
 
     const int64_t kseg = ((vis + CL - 1) / CL + 7) & ~int64_t(7);
     const int64_t klo = min(vis, (int64_t)r * kseg);
@@ -497,6 +641,7 @@ __device__ void dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, i
         eq_rank += __popc(eqb);
     }
     cl.sync();  // every index slice is complete
+    return true;
 }
 
 // Few-token (decode) path.  A cluster of CL CTAs shares one (token, group of
@@ -543,7 +688,8 @@ struct DecSmem {
     // slice, its histogram, the cluster sum, warp counts, selection, and the
     // per-slice totals pushed by the other CTAs [16][2]
     static constexpr size_t tk_off = total;
-    static constexpr size_t tk_bytes = 2 * 4096 + 256 * 4 + 256 * 4 + 64 * 4 + 32 + 16 * 2 * 4;
+    static constexpr size_t tk_bytes = TKD_WHIST + (size_t)dec_warps<HD>() * 256 * 4;
+    static_assert(2 * 4096 + 256 * 4 + 256 * 4 + 64 * 4 + 32 + 16 * 2 * 4 <= TKD_WHIST, "selection area");
     static constexpr size_t fused_total = tk_off + tk_bytes;
     static_assert(q_bytes % 16 == 0 && kv_bytes % 16 == 0 && sp_bytes % 16 == 0, "alignment");
 };
@@ -603,6 +749,8 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         mbar_init_fence();
     }
     __syncthreads();
+    cluster_arrive_relaxed();  // this CTA has started (waited on before any remote store)
+    bool cl_waited = false;
     // q rows of this head group (rows past nh are zero); q is an input, so it
     // is read before waiting for the previous kernel.
     if (warp == 0) {
@@ -624,8 +772,8 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     const int nst = max(0, min(j1 - j0, DEC_STAGE));
     if constexpr (FUSED) {
         // select this query's rows here (the scores come from the kernel before)
-        dec_topk<NTH>(tk, t, K, per, j0, j1, sidx, smem + SM::tk_off,
-                      reinterpret_cast<int*>(smem + SM::xch_off), blockIdx.y == 0, status);
+        cl_waited = dec_topk<NTH>(tk, t, K, per, j0, j1, sidx, smem + SM::tk_off,
+                                  reinterpret_cast<int*>(smem + SM::xch_off), blockIdx.y == 0, status);
     } else {
         for (int j = tid; j < nst; j += NTH) sidx[j] = irow[j0 + j];
     }
@@ -787,26 +935,45 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     // Push this CTA's (m, l) into every CTA of the cluster and each slice of
     // its unnormalised O, as bf16 pairs (half the exchanged bytes; the same
     // relative rounding as the bf16 output), into the CTA that reduces those
-    // columns; after one barrier every read is local.
+    // columns; after one barrier every read is local.  Both are staged in this
+    // CTA's shared memory first ((m, l) in stat, the O slices in sp, laid out
+    // as the receivers' blocks) so that every remote store moves 16 bytes.
     const int cols = HD / CL;
     float* spush = reinterpret_cast<float*>(smem + SM::spush_off);    // [16 ranks][2][16]
     uint32_t* opush = reinterpret_cast<uint32_t*>(smem + SM::xch_off);  // [CL ranks][16][cols/2]
+    uint32_t* ostage = reinterpret_cast<uint32_t*>(sp);                 // [CL][16][cols/2]
+    static_assert((size_t)DEC_HEADS * HD * 2 <= SM::sp_bytes && (SM::bar_off + 32 + 2 * DEC_NC * 4) % 16 == 0,
+                  "O staging; (m, l) staging read as 16-byte pieces");
     if (warp == 0 && (lane & 3) == 0) {
-        for (int q = 0; q < CL; q++) {
-            float* dst = cluster.map_shared_rank(spush, q) + rank * 2 * DEC_HEADS;
-            dst[ra] = mrow[0];
-            dst[rb] = mrow[1];
-            dst[DEC_HEADS + ra] = lrow[0];
-            dst[DEC_HEADS + rb] = lrow[1];
-        }
+        stat[ra] = mrow[0];
+        stat[rb] = mrow[1];
+        stat[DEC_HEADS + ra] = lrow[0];
+        stat[DEC_HEADS + rb] = lrow[1];
     }
 #pragma unroll
     for (int j = 0; j < NT; j++) {
         const int col = warp * QW + j * 8 + 2 * (lane & 3);
         const int qo = col / cols, cc = (col - qo * cols) >> 1;
-        uint32_t* dst = cluster.map_shared_rank(opush, qo) + rank * DEC_HEADS * (cols / 2);
+        uint32_t* dst = ostage + qo * DEC_HEADS * (cols / 2);
         dst[ra * (cols / 2) + cc] = pack_bf16x2(oacc[j][0], oacc[j][1]);
         dst[rb * (cols / 2) + cc] = pack_bf16x2(oacc[j][2], oacc[j][3]);
+    }
+    __syncthreads();
+    if (!cl_waited) cluster_wait();
+    {
+        const int per_q = 2 * cols;  // 16-byte pieces of one receiver's block
+        for (int c = tid; c < CL * per_q; c += NTH) {
+            const int qd = c / per_q;
+            uint4* dst = reinterpret_cast<uint4*>(cluster.map_shared_rank(opush, qd)) +
+                         rank * per_q + (c - qd * per_q);
+            *dst = reinterpret_cast<const uint4*>(ostage)[c];
+        }
+        for (int c = tid; c < CL * 8; c += NTH) {
+            const int qd = c >> 3;
+            uint4* dst = reinterpret_cast<uint4*>(cluster.map_shared_rank(spush, qd) + rank * 2 * DEC_HEADS) +
+                         (c & 7);
+            *dst = reinterpret_cast<const uint4*>(stat)[c & 7];
+        }
     }
     cluster.sync();
 

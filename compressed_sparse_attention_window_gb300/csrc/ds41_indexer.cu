@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     // When the scores are a caller-visible output, rows no query of this
     // group can see yet are written as -inf too.
     const int64_t tiles = fill_hidden ? (n_c + IDX_ROWS - 1) / IDX_ROWS : tiles_vis;
-    // The first key tile is fetched together with q, so the two loads overlap.
+    cp_async_commit();  // group of q
+    // The first key tile is fetched together with q, so the two loads overlap,
+    // and q is quantised while the tile is still in flight.
     auto fetch_k = [&](int64_t tile) {
         const int64_t r0 = tile * IDX_ROWS;
         for (int id = tid; id < IDX_ROWS * CPR; id += IDX_THREADS) {
@@ -125,12 +127,12 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     };
     const bool prefetched = (int64_t)blockIdx.y < tiles_vis;
     if (prefetched) fetch_k(blockIdx.y);
-    cp_async_commit();
+    cp_async_commit();  // group of the first key tile (empty when not prefetched)
     for (int n = tid; n < IDX_N; n += IDX_THREADS) {
         const int tt = n / hpad, h = n % hpad;
         wsm[n] = (tt < tcount && h < Hi) ? w[(int64_t)(t0 + tt) * Hi + h] : 0.0f;
     }
-    cp_async_wait<0>();
+    cp_async_wait<1>();  // this thread's q copies have landed
     __syncthreads();
     // only the live rows (tokens of the group x Hi heads), rounded up to whole
     // passes of the block: q8_chunk shuffles over the full warp, and the
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
         uint4* p = reinterpret_cast<uint4*>(qs + n * DI + swz<CPR>(n, c) * 8);
         *p = q8_chunk(*p, true);
     }
+    cp_async_wait<0>();  // the first key tile (its readers sync below)
 
     for (int64_t tile = blockIdx.y; tile < tiles; tile += ymain) {
         const int64_t r0 = tile * IDX_ROWS;

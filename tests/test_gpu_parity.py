@@ -394,7 +394,11 @@ def test_forward_no_compressed_rows_yet(orc):
 CSA_CASES = ["tiny_prefill", "decode", "long_decode", "chunked_prefill", "prefill"]
 CSA_EXTRA = [TINY_PREFILL.replace(m=1, start_pos=43), TINY_PREFILL.replace(m=3, start_pos=37),
              TINY_PREFILL.replace(m=1, start_pos=2), DECODE.replace(start_pos=8190),
-             DECODE.replace(m=2, start_pos=5000), TINY_PREFILL.replace(m=2, start_pos=0)]
+             DECODE.replace(m=2, start_pos=5000), TINY_PREFILL.replace(m=2, start_pos=0),
+             # tied scores: every CTA ranks all 2048 (or 546) visible rows itself ...
+             DECODE.replace(structure="repeat"), CHUNKED.replace(m=1, start_pos=70000),
+             # ... or, past 4096 visible rows, the cluster splits them
+             DECODE.replace(start_pos=16399, structure="repeat")]
 
 
 @pytest.mark.parametrize("wl", [WORKLOADS[n] for n in CSA_CASES] + CSA_EXTRA,
