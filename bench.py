@@ -23,6 +23,7 @@ own GPU; no data-path collective; value = all ranks' tokens / max time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -113,6 +114,45 @@ def algorithmic(wl):
             "flops": 4 * wl.nh * wl.hd * rows},
     }
     return ops
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def csrc_digest() -> str:
+    """sha256 (first 16 hex digits) over the CUDA sources, by sorted name: the
+    kernels that a set of ncu counters describes."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "compressed_sparse_attention_window_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, op: str):
+    """DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per call of
+    `op` on `workload`, from profiles/dram_traffic.txt, when they were taken on
+    the current kernel sources; None otherwise."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            lines = fh.read().splitlines()
+    except OSError:
+        return None
+    digest, table = None, {}
+    for line in lines:
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        if f[0] == "csrc" and len(f) >= 2:
+            digest = f[1]
+        elif len(f) >= 3:
+            table[(f[0], f[1])] = float(f[2])
+    if digest != csrc_digest():
+        return None
+    return table.get((workload, op))
 
 
 def load_peaks():
@@ -380,7 +420,8 @@ def run_ours(args, world, rank, local):
                 "frac": achieved / hbm}
     roof.update({"kernel": dom, "ms_per_launch": d_ms, "algorithmic_bytes": alg[dom]["bytes"],
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
-                 else "fallback", "traffic": args.traffic})
+                 else "fallback",
+                 "traffic": args.traffic if args.traffic is not None else recorded_traffic(wl.name, dom)})
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(wl, slots, fc, stream, K, W, n_slots)
@@ -454,28 +495,31 @@ def run_only(args, local):
 
 
 def run_e2e(wl, slots, fc, stream, K, W, n_slots):
-    """The same metric through ds41.forward (eager, the call a user makes), with
-    each step's inputs copied from pinned host memory and the output read back."""
-    names = ["q", "kv", "latent", "q_idx", "w"]
-    host = []
-    for s in range(min(n_slots, 8)):
-        inp, _ = slots[s]
-        host.append({k: inp[k].cpu().pin_memory() for k in names})
+    """The same metric through ds41_csa_forward_host, the C-ABI call for
+    host-resident step data, prepared once per layer state (ds41.HostStep):
+    every step copies that step's inputs from page-locked host memory into
+    the device buffers (laid out back to back on both sides, so in one copy),
+    runs the step and copies o back to host memory, on one stream; the layer
+    states stay resident."""
+    names = ds41.STEP_INPUTS
     o_host = torch.empty(slots[0][1]["o"].shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
-    d2h = o_host.numel() * o_host.element_size()
-
-    def step(i):
-        inp, out = slots[i % n_slots]
-        hs = host[i % len(host)]
+    steps = []
+    for s in range(n_slots):
+        inp, out = slots[s]
+        dev_in = ds41.step_input_buffers(wl, inp["q"].device)
+        host_in = ds41.step_input_buffers(wl, "cpu", pinned=True)
         for k in names:
-            inp[k].copy_(hs[k], non_blocking=True)
-        ds41.csa_forward(inp, wl, fc, out)
-        o_host.copy_(out["o"], non_blocking=True)
+            host_in[k].copy_(inp[k].cpu())
+        e_inp = dict(inp)
+        e_inp.update(dev_in)
+        steps.append(ds41.HostStep(host_in, e_inp, wl, fc, out, h_o=o_host))
+    h2d = sum(t.numel() * t.element_size() for t in steps[0]._keep[0].values())
+    d2h = o_host.numel() * o_host.element_size()
+    sid = stream.cuda_stream
 
     with torch.cuda.stream(stream):
         for i in range(W):
-            step(i)
+            steps[i % n_slots](sid)
     stream.synchronize()
     t0 = time.perf_counter()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -483,14 +527,15 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots):
     with torch.cuda.stream(stream):
         e0.record(stream)
         for i in range(K):
-            step(W + i)
+            steps[(W + i) % n_slots](sid)
         e1.record(stream)
     stream.synchronize()
     wall = time.perf_counter() - t0
     ms = max(e0.elapsed_time(e1), wall * 1e3)
     return {"value": wl.m * K / (ms / 1e3), "unit": "query-tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "how": "ds41.csa_forward eager per step; pinned H2D of q/kv/latent/q_idx/w, D2H of o"}
+            "how": "ds41_csa_forward_host per step (prepared call): one pinned H2D of "
+                   "q/kv/latent/q_idx/w, the step, D2H of o, one stream"}
 
 
 # ---------------------------------------------------------------------------
@@ -568,7 +613,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of CPU oracle work for the cpu_baseline field")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per launch of the dominant kernel, if known")
+                    help="ncu dram bytes per call of the dominant op (default: "
+                         "profiles/dram_traffic.txt when taken on the current sources)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     help="profiling mode: time eager calls of one op (or 'step') and exit")

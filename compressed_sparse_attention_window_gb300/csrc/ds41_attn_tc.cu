@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int s_tok = 0, s_i = 0, s_n = -1, s_kp = 0;
             int p_tok = 0, p_i = 0, p_mt = 0;
             uint32_t sg = 0, pg = 0;
-            int nring[4] = {0, 0, 0, 0};
+            uint32_t nring = 0;  // chunk counts of the last four items, 8 bits each
             uint32_t idle = 0;
             const uint32_t q_s = sbase + Q_OFF;
             const uint32_t r_s = sbase + R_OFF;
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (++p_mt == 4) {
                             p_mt = 0;
                             tc_commit(&bars[B_DONE]);
-                            const int pn = nring[p_tok & 3];
+                            const int pn = (int)((nring >> (8 * (p_tok & 3))) & 0xffu);
                             if (p_i == pn - 1) tc_commit(&bars[B_ODONE]);
                             pg++;
                             if (++p_i == pn) {
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (s_n < 0 && mbar_test(&bars[B_PLANFULL + (s_tok & 1)], (s_tok >> 1) & 1)) {
                         s_n = *reinterpret_cast<const int*>(sm + PLAN_OFF +
                                                             (s_tok & 1) * PLAN_BYTES + PLAN_N);
-                        nring[s_tok & 3] = s_n;
+                        nring = (nring & ~(0xffu << (8 * (s_tok & 3)))) | ((uint32_t)s_n << (8 * (s_tok & 3)));
                     }
                     if (s_n > 0) {
                         const bool ok =

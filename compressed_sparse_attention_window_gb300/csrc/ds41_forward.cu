@@ -131,3 +131,86 @@ extern "C" int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf
     return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
                     nullptr, 0, true, st, name);
 }
+
+// The step with its per-step inputs and its output in host memory: one copy
+// per input into the caller's device buffers, the step, and one copy of o
+// back, all on the caller's stream.
+extern "C" int ds41_csa_forward_host(
+    const ds41_bf16* h_q, const ds41_bf16* h_kv, const ds41_bf16* h_latent, const ds41_bf16* h_q_idx,
+    const float* h_w, ds41_bf16* h_o, ds41_bf16* q, ds41_bf16* kv, ds41_bf16* ring, ds41_bf16* rows_a,
+    ds41_bf16* latent, const float* freqs_cis, int64_t max_pos, ds41_bf16* cache, int64_t cache_rows,
+    ds41_bf16* q_idx, const ds41_bf16* k_idx, float* w, const float* sink, float scale,
+    int32_t* win_idx, int32_t* idx, ds41_bf16* o, float* lse, int64_t m, int64_t start_pos,
+    int64_t nh, int64_t hd, int64_t rd, int64_t win, int64_t ratio, int64_t topk, int64_t Hi,
+    int64_t Di, void* ws, size_t ws_bytes, ds41_stream_t stream) {
+    const char* name = "ds41_csa_forward_host";
+    DS41_REQUIRE(m >= 1 && m < (int64_t(1) << 31) && start_pos >= 0 && ratio >= 1 && nh >= 1 &&
+                     hd >= 1 && Hi >= 1 && Di >= 1,
+                 DS41_E_ARG, "%s: m=%lld start_pos=%lld ratio=%lld", name, (long long)m,
+                 (long long)start_pos, (long long)ratio);
+    const int64_t G = (start_pos + m) / ratio - start_pos / ratio;
+    DS41_REQUIRE(h_q && h_kv && h_q_idx && h_w && h_o && q && kv && q_idx && w && o &&
+                     (G == 0 || (h_latent && latent)),
+                 DS41_E_ARG, "%s: null pointer", name);
+    cudaStream_t st = (cudaStream_t)stream;
+    struct Copy {
+        void* dst;
+        const void* src;
+        size_t bytes;
+    };
+    const Copy in[5] = {{q, h_q, (size_t)(m * nh * hd) * 2},
+                        {kv, h_kv, (size_t)(m * hd) * 2},
+                        {latent, h_latent, (size_t)(G * hd) * 2},
+                        {q_idx, h_q_idx, (size_t)(m * Hi * Di) * 2},
+                        {w, h_w, (size_t)(m * Hi) * 4}};
+    for (const Copy& c : in) {
+        if (c.bytes == 0) continue;
+        const int rc = cuda_check(cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st),
+                                  "ds41_csa_forward_host: input copy");
+        if (rc) return rc;
+    }
+    const int rc = ds41_csa_forward(q, kv, ring, rows_a, latent, freqs_cis, max_pos, cache, cache_rows,
+                                    q_idx, k_idx, w, sink, scale, win_idx, idx, o, lse, m, start_pos,
+                                    nh, hd, rd, win, ratio, topk, Hi, Di, ws, ws_bytes, stream);
+    if (rc) return rc;
+    return cuda_check(cudaMemcpyAsync(h_o, o, (size_t)(m * nh * hd) * 2, cudaMemcpyDeviceToHost, st),
+                      "ds41_csa_forward_host: output copy");
+}
+
+extern "C" size_t ds41_step_inputs_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_t hd,
+                                         int64_t ratio, int64_t Hi, int64_t Di) {
+    if (m < 1 || start_pos < 0 || ratio < 1) return 0;
+    const int64_t G = (start_pos + m) / ratio - start_pos / ratio;
+    return (size_t)(m * nh * hd + m * hd + G * hd + m * Hi * Di) * 2 + (size_t)(m * Hi) * 4;
+}
+
+// The same with the step's inputs in one block on each side: one copy in.
+extern "C" int ds41_csa_forward_host_packed(
+    const void* h_in, void* d_in, ds41_bf16* h_o, ds41_bf16* ring, ds41_bf16* rows_a,
+    const float* freqs_cis, int64_t max_pos, ds41_bf16* cache, int64_t cache_rows,
+    const ds41_bf16* k_idx, const float* sink, float scale, int32_t* win_idx, int32_t* idx,
+    ds41_bf16* o, float* lse, int64_t m, int64_t start_pos, int64_t nh, int64_t hd, int64_t rd,
+    int64_t win, int64_t ratio, int64_t topk, int64_t Hi, int64_t Di, void* ws, size_t ws_bytes,
+    ds41_stream_t stream) {
+    const char* name = "ds41_csa_forward_host_packed";
+    const size_t bytes = ds41_step_inputs_bytes(m, start_pos, nh, hd, ratio, Hi, Di);
+    DS41_REQUIRE(bytes > 0 && h_in && d_in && h_o && o, DS41_E_ARG, "%s: m=%lld, null pointer",
+                 name, (long long)m);
+    const int64_t G = (start_pos + m) / ratio - start_pos / ratio;
+    char* d = static_cast<char*>(d_in);
+    ds41_bf16* q = reinterpret_cast<ds41_bf16*>(d);
+    ds41_bf16* kv = q + m * nh * hd;
+    ds41_bf16* latent = kv + m * hd;
+    ds41_bf16* q_idx = latent + G * hd;
+    float* w = reinterpret_cast<float*>(q_idx + m * Hi * Di);
+    cudaStream_t st = (cudaStream_t)stream;
+    int rc = cuda_check(cudaMemcpyAsync(d_in, h_in, bytes, cudaMemcpyHostToDevice, st),
+                        "ds41_csa_forward_host_packed: input copy");
+    if (rc) return rc;
+    rc = ds41_csa_forward(q, kv, ring, rows_a, G > 0 ? latent : nullptr, freqs_cis, max_pos, cache,
+                          cache_rows, q_idx, k_idx, w, sink, scale, win_idx, idx, o, lse, m,
+                          start_pos, nh, hd, rd, win, ratio, topk, Hi, Di, ws, ws_bytes, stream);
+    if (rc) return rc;
+    return cuda_check(cudaMemcpyAsync(h_o, o, (size_t)(m * nh * hd) * 2, cudaMemcpyDeviceToHost, st),
+                      "ds41_csa_forward_host_packed: output copy");
+}

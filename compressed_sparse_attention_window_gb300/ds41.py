@@ -8,6 +8,7 @@ missing or a call fails, an exception is raised.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 from typing import Dict, Optional
 
@@ -46,6 +47,11 @@ SIGNATURES = {
     "ds41_csa_workspace_bytes": (_SZ, [_I64] * 9),
     "ds41_csa_forward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _P, _P, _F,
                                         _P, _P, _P, _P] + [_I64] * 10 + [_P, _SZ, _P]),
+    "ds41_csa_forward_host": (ctypes.c_int, [_P] * 6 + [_P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P,
+                                             _P, _P, _F, _P, _P, _P, _P] + [_I64] * 10 + [_P, _SZ, _P]),
+    "ds41_step_inputs_bytes": (_SZ, [_I64] * 7),
+    "ds41_csa_forward_host_packed": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _F,
+                                                    _P, _P, _P, _P] + [_I64] * 10 + [_P, _SZ, _P]),
     "ds41_sparse_attn_noalloc_capacity": (_SZ, []),
     "ds41_sparse_attn_sink_fwd_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F,
                                                          _P, _P, _I64, _I64, _I64, _P]),
@@ -287,6 +293,144 @@ def csa_forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
     if wl.n_c == 0:
         out["idx"] = out["win_idx"]
     return out
+
+
+STEP_INPUTS = ("q", "kv", "latent", "q_idx", "w")
+
+
+def step_input_buffers(wl, device="cpu", pinned: bool = False) -> Dict[str, torch.Tensor]:
+    """Views q [m, nh, hd], kv [m, hd], latent [G, hd] (bf16), q_idx [m, Hi, Di]
+    (bf16) and w [m, Hi] (f32) laid out back to back, in that order, in one
+    block of ``device`` memory (page-locked when ``pinned``).  Host and device
+    buffers built this way let ds41_csa_forward_host move a step's inputs in
+    one copy."""
+    shapes = [("q", (wl.m, wl.nh, wl.hd), _BF), ("kv", (wl.m, wl.hd), _BF),
+              ("latent", (max(wl.G, 0), wl.hd), _BF), ("q_idx", (wl.m, wl.Hi, wl.Di), _BF),
+              ("w", (wl.m, wl.Hi), torch.float32)]
+    sizes = [math.prod(sh) * (2 if dt == _BF else 4) for _, sh, dt in shapes]
+    block = torch.empty(sum(sizes), dtype=torch.uint8, device=device)
+    if pinned:
+        block = block.pin_memory()
+    views, off = {}, 0
+    for (k, sh, dt), n in zip(shapes, sizes):
+        views[k] = block[off:off + n].view(dt).view(sh)
+        off += n
+    return views
+
+
+def _packed(bufs: Dict[str, torch.Tensor], wl) -> bool:
+    """Whether the step inputs in ``bufs`` lie back to back, in STEP_INPUTS
+    order, in one allocation (as step_input_buffers lays them out)."""
+    prev = None
+    for k in STEP_INPUTS:
+        t = bufs[k]
+        if t.numel() == 0:  # latent when the call completes no group: 0 bytes
+            continue
+        if not t.is_contiguous():
+            return False
+        if prev is not None:
+            if (t.untyped_storage().data_ptr() != prev.untyped_storage().data_ptr()
+                    or t.data_ptr() != prev.data_ptr() + prev.numel() * prev.element_size()):
+                return False
+        prev = t
+    n = load().ds41_step_inputs_bytes(wl.m, wl.start_pos, wl.nh, wl.hd, wl.ratio, wl.Hi, wl.Di)
+    q = bufs["q"]
+    return prev.data_ptr() + prev.numel() * prev.element_size() - q.data_ptr() == n
+
+
+class HostStep:
+    """ds41_csa_forward_host prepared once for fixed buffers, as a serving loop
+    runs a layer's step again and again: the step inputs q, kv, latent, q_idx,
+    w come from the host tensors ``host`` (page-locked for asynchronous copies)
+    into the device tensors of the same names in ``inp``, o goes back into the
+    host tensor ``h_o`` (allocated page-locked when None).  The arguments are
+    checked and marshalled here; each call only enqueues the copies and the
+    step on the stream and returns ``h_o``, which holds the result once the
+    stream has reached the copy.  When both sides hold the inputs as one block
+    (step_input_buffers), the call is ds41_csa_forward_host_packed: one copy
+    in instead of five."""
+
+    def __init__(self, host: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], wl,
+                 freqs_cis: torch.Tensor, out: Optional[Dict[str, torch.Tensor]] = None,
+                 h_o: Optional[torch.Tensor] = None):
+        out = {} if out is None else out
+        dev = inp["q"].device
+        m, win = wl.m, wl.win
+        for k in STEP_INPUTS:
+            if k == "latent" and wl.G <= 0:
+                continue
+            t, d = host[k], inp[k]
+            if t.is_cuda or t.dtype != d.dtype or not t.is_contiguous() or t.shape != d.shape:
+                raise ValueError(f"HostStep: host[{k!r}] must be a contiguous CPU tensor shaped "
+                                 f"and typed like the device one")
+        if h_o is None:
+            h_o = torch.empty(tuple(inp["q"].shape), dtype=_BF).pin_memory()
+        if h_o.is_cuda or h_o.dtype != _BF or tuple(h_o.shape) != tuple(inp["q"].shape):
+            raise ValueError("HostStep: h_o must be a CPU bf16 tensor shaped like q")
+        if "win_idx" not in out:
+            out["win_idx"] = torch.empty(m, win, dtype=torch.int32, device=dev)
+        if "idx" not in out:
+            out["idx"] = torch.empty(m, wl.K, dtype=torch.int32, device=dev)
+        if "o" not in out:
+            out["o"] = torch.empty_like(inp["q"])
+        chunk = wl.start_pos > 0 and m > 1
+        if chunk and "rows_a" not in out:
+            out["rows_a"] = torch.empty(win + m, wl.hd, dtype=torch.bfloat16, device=dev)
+        need = csa_workspace_bytes(wl)
+        ws = out.get("ws_csa")
+        if need and (ws is None or ws.numel() < need):
+            ws = out["ws_csa"] = torch.empty(need, dtype=torch.uint8, device=dev)
+        g = wl.G > 0
+        self.packed = _packed(host, wl) and _packed(inp, wl) and inp["q"].data_ptr() % 16 == 0
+        if self.packed:
+            # one block each side: ds41_csa_forward_host_packed, one copy in
+            self._args = (
+                host["q"].data_ptr(), inp["q"].data_ptr(), h_o.data_ptr(),
+                _ptr(inp["ring"], _BF, "ring"), _ptr(out.get("rows_a") if chunk else None),
+                _ptr(freqs_cis, torch.float32, "freqs_cis"), freqs_cis.shape[0],
+                _ptr(inp["cache"], _BF, "cache"), inp["cache"].shape[0],
+                _ptr(inp["k_idx"], _BF, "k_idx"), _ptr(inp["sink"], torch.float32, "sink"),
+                float(wl.scale), _ptr(out["win_idx"], torch.int32, "win_idx"),
+                _ptr(out["idx"], torch.int32, "idx"), _ptr(out["o"], _BF, "o"),
+                _ptr(out.get("lse"), torch.float32, "lse"), m, wl.start_pos, wl.nh, wl.hd, wl.rd,
+                win, wl.ratio, wl.topk, wl.Hi, wl.Di, _ptr(ws) if need else None, need)
+            self._name = "ds41_csa_forward_host_packed"
+        else:
+            self._name = "ds41_csa_forward_host"
+            self._args = (
+                host["q"].data_ptr(), host["kv"].data_ptr(), host["latent"].data_ptr() if g else None,
+                host["q_idx"].data_ptr(), host["w"].data_ptr(), h_o.data_ptr(),
+                _ptr(inp["q"], _BF, "q"), _ptr(inp["kv"], _BF, "kv"),
+                _ptr(inp["ring"], _BF, "ring"), _ptr(out.get("rows_a") if chunk else None),
+                _ptr(inp["latent"], _BF, "latent") if g else None,
+                _ptr(freqs_cis, torch.float32, "freqs_cis"), freqs_cis.shape[0],
+                _ptr(inp["cache"], _BF, "cache"), inp["cache"].shape[0],
+                _ptr(inp["q_idx"], _BF, "q_idx"), _ptr(inp["k_idx"], _BF, "k_idx"),
+                _ptr(inp["w"], torch.float32, "w"), _ptr(inp["sink"], torch.float32, "sink"),
+                float(wl.scale), _ptr(out["win_idx"], torch.int32, "win_idx"),
+                _ptr(out["idx"], torch.int32, "idx"), _ptr(out["o"], _BF, "o"),
+                _ptr(out.get("lse"), torch.float32, "lse"), m, wl.start_pos, wl.nh, wl.hd, wl.rd, win,
+                wl.ratio, wl.topk, wl.Hi, wl.Di, _ptr(ws) if need else None, need)
+        self._keep = (host, inp, out, freqs_cis)  # the buffers stay alive with the call
+        self._fn = getattr(load(), self._name)
+        self.h_o = h_o
+        if wl.n_c == 0:
+            out["idx"] = out["win_idx"]
+
+    def __call__(self, stream: Optional[int] = None) -> torch.Tensor:
+        rc = self._fn(*self._args, _stream() if stream is None else stream)
+        if rc != 0:
+            raise DS41Error(self._name, rc,
+                            load().ds41_last_error().decode(errors="replace"))
+        return self.h_o
+
+
+def csa_forward_host(host: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], wl,
+                     freqs_cis: torch.Tensor, out: Optional[Dict[str, torch.Tensor]] = None,
+                     h_o: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One ds41_csa_forward_host call (see :class:`HostStep`) on the current
+    stream; returns the host tensor of o."""
+    return HostStep(host, inp, wl, freqs_cis, out, h_o)()
 
 
 def forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,

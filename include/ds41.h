@@ -223,7 +223,7 @@ size_t ds41_csa_workspace_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_
  * needed only for a chunk of m > 1 tokens past position 0; latent /
  * freqs_cis only when the call completes a group; lse is nullable.  idx is
  * [m, win + min(topk, n_c)] with n_c = (start_pos + m)/ratio (unused when
- * n_c == 0).  Few-token calls run in three launches chained on the device
+ * n_c == 0).  Few-token calls run in two or three launches chained on the device
  * (programmatic dependent launch), larger ones as the four calls. */
 int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring, ds41_bf16* rows_a,
                      const ds41_bf16* latent, const float* freqs_cis, int64_t max_pos,
@@ -233,6 +233,54 @@ int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring, d
                      int64_t start_pos, int64_t nh, int64_t hd, int64_t rd, int64_t win,
                      int64_t ratio, int64_t topk, int64_t Hi, int64_t Di, void* ws,
                      size_t ws_bytes, ds41_stream_t stream);
+
+/* ds41_csa_forward for a caller whose per-step inputs and output live in
+ * host memory (no counterpart in the paper, which computes on the host): the
+ * inputs h_q [m, nh, hd], h_kv [m, hd], h_latent [G, hd] (read only when the
+ * call completes G > 0 groups, G = (start_pos + m)/ratio - start_pos/ratio;
+ * may be NULL otherwise), h_q_idx [m, Hi, Di] and h_w [m, Hi] are copied into
+ * the device buffers q, kv, latent, q_idx and w (caller-owned, same shapes),
+ * ds41_csa_forward runs on them, and o is copied into h_o [m, nh, hd]; the
+ * other arguments are ds41_csa_forward's.  Everything is enqueued on `stream`
+ * in that order; the call returns without waiting, and h_o holds the result
+ * once the stream has reached that point (cudaStreamSynchronize).  The copies
+ * are asynchronous only for page-locked host memory (cudaHostAlloc /
+ * cudaHostRegister); pageable buffers work but the copies then block the
+ * calling thread.  The host buffers must stay valid and unmodified until the
+ * stream has passed the copies.  Errors: ds41_csa_forward's, DS41_E_ARG for a
+ * NULL pointer, DS41_E_CUDA when a copy cannot be enqueued (the copies
+ * enqueued before stay enqueued). */
+int ds41_csa_forward_host(const ds41_bf16* h_q, const ds41_bf16* h_kv, const ds41_bf16* h_latent,
+                          const ds41_bf16* h_q_idx, const float* h_w, ds41_bf16* h_o,
+                          ds41_bf16* q, ds41_bf16* kv, ds41_bf16* ring, ds41_bf16* rows_a,
+                          ds41_bf16* latent, const float* freqs_cis, int64_t max_pos,
+                          ds41_bf16* cache, int64_t cache_rows, ds41_bf16* q_idx,
+                          const ds41_bf16* k_idx, float* w, const float* sink, float scale,
+                          int32_t* win_idx, int32_t* idx, ds41_bf16* o, float* lse, int64_t m,
+                          int64_t start_pos, int64_t nh, int64_t hd, int64_t rd, int64_t win,
+                          int64_t ratio, int64_t topk, int64_t Hi, int64_t Di, void* ws,
+                          size_t ws_bytes, ds41_stream_t stream);
+
+/* Bytes of one step's inputs packed back to back as [q | kv | latent | q_idx |
+ * w] (the layout ds41_csa_forward_host_packed takes): 2 (m nh hd + m hd +
+ * G hd + m Hi Di) + 4 m Hi, G as above; 0 for m < 1, start_pos < 0 or
+ * ratio < 1. */
+size_t ds41_step_inputs_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_t hd,
+                              int64_t ratio, int64_t Hi, int64_t Di);
+
+/* ds41_csa_forward_host with the step's inputs in one block on each side:
+ * h_in (host) and d_in (device, 16-byte aligned) each hold q, kv, latent,
+ * q_idx and w back to back in that order, ds41_step_inputs_bytes bytes, so
+ * they go over in one copy; the kernels read the inputs from d_in.  Same
+ * results, stream behaviour and errors as ds41_csa_forward_host. */
+int ds41_csa_forward_host_packed(const void* h_in, void* d_in, ds41_bf16* h_o, ds41_bf16* ring,
+                                 ds41_bf16* rows_a, const float* freqs_cis, int64_t max_pos,
+                                 ds41_bf16* cache, int64_t cache_rows, const ds41_bf16* k_idx,
+                                 const float* sink, float scale, int32_t* win_idx, int32_t* idx,
+                                 ds41_bf16* o, float* lse, int64_t m, int64_t start_pos,
+                                 int64_t nh, int64_t hd, int64_t rd, int64_t win, int64_t ratio,
+                                 int64_t topk, int64_t Hi, int64_t Di, void* ws, size_t ws_bytes,
+                                 ds41_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Step 3 without caller-provided scratch                                     */

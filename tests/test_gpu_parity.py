@@ -423,3 +423,47 @@ def test_csa_forward_matches_oracle_and_the_four_calls(orc, wl):
     assert_idx_sets_equal(out1["idx"].cpu().numpy()[toks], ref["idx"], wl.win)
     ok, err, worst = attn_close(out1["o"].float().cpu().numpy()[toks], ref["o"])
     assert ok, (wl.name, err, worst)
+
+
+@pytest.mark.parametrize("wl", [WORKLOADS["decode"], WORKLOADS["tiny_prefill"],
+                                TINY_PREFILL.replace(m=3, start_pos=37), CHUNKED.replace(m=2, start_pos=70000)],
+                         ids=lambda w: f"{w.name}-{w.m}-{w.start_pos}")
+@pytest.mark.parametrize("packed", [False, True])
+def test_csa_forward_host_buffers(wl, packed):
+    """ds41_csa_forward_host (inputs and output in page-locked host memory,
+    copied on the stream; separate buffers, or one block on each side that the
+    call moves in one copy) gives bit-for-bit the results of ds41_csa_forward
+    on device tensors, and leaves the same layer state; a prepared call runs
+    again with the same result."""
+    inp = make_inputs(wl)
+    fc = ds41.yarn_freqs_cis(wl.rd, max(wl.max_pos, 1))
+    dev_ref = to_dev(inp)
+    ref = ds41.csa_forward(dev_ref, wl, fc)
+    dev = to_dev(inp)
+    step = ds41.STEP_INPUTS
+    if packed:
+        dev.update(ds41.step_input_buffers(wl, "cuda"))
+        host = ds41.step_input_buffers(wl, "cpu", pinned=True)
+        for k in step:
+            host[k].copy_(inp[k])
+    else:
+        host = {k: inp[k].contiguous().pin_memory() for k in step}
+    for k in step:  # the device buffers start as garbage: the call must fill them
+        dev[k].fill_(7)
+    out = {}
+    h_o = ds41.csa_forward_host(host, dev, wl, fc, out)
+    torch.cuda.synchronize()
+    assert torch.equal(h_o, ref["o"].cpu())
+    assert torch.equal(out["idx"], ref["idx"])
+    assert torch.equal(dev["ring"], dev_ref["ring"]) and torch.equal(dev["cache"], dev_ref["cache"])
+    # a prepared call, run twice from the same starting layer state
+    start = to_dev(inp)
+    again = ds41.HostStep(host, dev, wl, fc, out, h_o=h_o)
+    assert again.packed == packed  # one block each side: the packed entry point
+    for _ in range(2):
+        h_o.zero_()
+        dev["ring"].copy_(start["ring"])
+        dev["cache"].copy_(start["cache"])
+        again()
+        torch.cuda.synchronize()
+        assert torch.equal(h_o, ref["o"].cpu())
