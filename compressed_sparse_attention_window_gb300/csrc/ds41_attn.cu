@@ -655,7 +655,7 @@ __device__ bool dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, i
 // No scratch memory and no second launch.
 // ---------------------------------------------------------------------------
 constexpr int DEC_HEADS = 16;
-constexpr int DEC_NC = 32;
+constexpr int DEC_NC = 48;  // gathered rows per chunk: a 16-CTA slice of 640 rows (40) in one chunk
 constexpr int DEC_SPS = DEC_NC + 8;  // padded row stride of the partial scores (no bank conflicts)
 constexpr int DEC_STAGE = 2048;      // indices of a CTA's slice staged in shared memory
 // warps per CTA: 8 when the head dim gives every warp at least two n-tiles
@@ -778,28 +778,48 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         for (int j = tid; j < nst; j += NTH) sidx[j] = irow[j0 + j];
     }
     __syncthreads();
-    // warp 0: one bulk copy per valid row of the chunk; invalid rows are zeroed
-    // (their scores are masked, and 0 * row must stay finite in P*V)
+    // warp 0: one bulk copy per valid row of the chunk (row r by lane r % 32);
+    // invalid rows are zeroed (their scores are masked, and 0 * row must stay
+    // finite in P*V)
+    constexpr int RPL = (DEC_NC + 31) / 32;  // rows per lane
     auto load_chunk = [&](int chunk, int buf) {
-        const int j = j0 + chunk * DEC_NC + lane;
-        int64_t v = -1;
-        if (j < j1) v = (j - j0 < nst) ? sidx[j - j0] : irow[j];
-        const bool ok = v >= 0 && v < n_rows;
-        if (j < j1 && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
-        const unsigned bal = __ballot_sync(0xffffffffu, ok);
+        int64_t vr[RPL];
+        bool okr[RPL];
+        uint32_t nok = 0;
+#pragma unroll
+        for (int i = 0; i < RPL; i++) {
+            const int r = lane + 32 * i;
+            const int j = j0 + chunk * DEC_NC + r;
+            const bool in = r < DEC_NC && j < j1;
+            int64_t v = -1;
+            if (in) v = (j - j0 < nst) ? sidx[j - j0] : irow[j];
+            const bool ok = v >= 0 && v < n_rows;
+            if (in && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
+            nok += __popc(__ballot_sync(0xffffffffu, ok));
+            vr[i] = v;
+            okr[i] = ok;
+        }
         // order this buffer's earlier generic-proxy writes before the copies
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        if (lane == 0) mbar_arrive_expect_tx(&bars[1 + buf], (uint32_t)__popc(bal) * ROWB);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[1 + buf], nok * ROWB);
         __syncwarp();
-        uint16_t* dst = kvs + buf * (DEC_NC * RS) + lane * RS;
-        if (ok) {
-            const uint16_t* src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
-            bulk_g2s(dst, src, ROWB, &bars[1 + buf]);
-        } else {
-            for (int c = 0; c < HD / 8; c++) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < RPL; i++) {
+            const int r = lane + 32 * i;
+            if (r >= DEC_NC) continue;
+            uint16_t* dst = kvs + buf * (DEC_NC * RS) + r * RS;
+            if (okr[i]) {
+                const int64_t v = vr[i];
+                const uint16_t* src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
+                bulk_g2s(dst, src, ROWB, &bars[1 + buf]);
+            } else {
+                for (int c = 0; c < HD / 8; c++) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+            }
+            vflag[buf * DEC_NC + r] = okr[i] ? 1 : 0;
         }
-        vflag[buf * DEC_NC + lane] = ok ? 1 : 0;
     };
+    constexpr int NCT = DEC_NC / 8;   // n-tiles of 8 rows per chunk
+    constexpr int NKS = DEC_NC / 16;  // k-steps of 16 rows per chunk in P*V
 
     float oacc[NT][4];
 #pragma unroll
@@ -817,9 +837,9 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         if (!mbar_wait(&bars[1 + buf], (chunk >> 1) & 1, kWaitPolls)) failed = true;
         __syncthreads();  // zero-filled rows and flags of warp 0 are visible
         const uint16_t* kv = kvs + buf * (DEC_NC * RS);
-        float sacc[4][4];
+        float sacc[NCT][4];
 #pragma unroll
-        for (int j = 0; j < 4; j++) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
+        for (int j = 0; j < NCT; j++) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
 #pragma unroll 1
         for (int kk = 0; kk < QW / 16; kk++) {
             uint32_t a0, a1, a2, a3;
@@ -829,7 +849,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
                 ldsm_x4(smem_u32(qs + r * RS + c * 8), a0, a1, a2, a3);
             }
 #pragma unroll
-            for (int jj = 0; jj < 2; jj++) {
+            for (int jj = 0; jj < NKS; jj++) {
                 uint32_t b0, b1, b2, b3;
                 const int r = jj * 16 + (lane & 7) + (lane >> 4) * 8;
                 const int c = warp * (QW / 8) + kk * 2 + ((lane >> 3) & 1);
@@ -841,15 +861,15 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         // partial scores of the NW slices of hd, summed in a fixed order by all
         float* mine = sp + warp * (DEC_HEADS * DEC_SPS);
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
+        for (int j = 0; j < NCT; j++) {
             const int col = j * 8 + 2 * (lane & 3);
             *reinterpret_cast<float2*>(mine + ra * DEC_SPS + col) = make_float2(sacc[j][0], sacc[j][1]);
             *reinterpret_cast<float2*>(mine + rb * DEC_SPS + col) = make_float2(sacc[j][2], sacc[j][3]);
         }
         __syncthreads();
-        float sv[4][4];
+        float sv[NCT][4];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
+        for (int j = 0; j < NCT; j++) {
             const int col = j * 8 + 2 * (lane & 3);
             float2 xa = *reinterpret_cast<const float2*>(sp + ra * DEC_SPS + col);
             float2 xb = *reinterpret_cast<const float2*>(sp + rb * DEC_SPS + col);
@@ -868,7 +888,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         }
         float mx[2] = {mrow[0], mrow[1]};
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
+        for (int j = 0; j < NCT; j++) {
             mx[0] = fmaxf(mx[0], fmaxf(sv[j][0], sv[j][1]));
             mx[1] = fmaxf(mx[1], fmaxf(sv[j][2], sv[j][3]));
         }
@@ -885,9 +905,9 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
             mrow[i] = mx[i];
             lrow[i] *= corr[i];
         }
-        uint32_t pa[2][4];
+        uint32_t pa[NKS][4];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
+        for (int j = 0; j < NCT; j++) {
             const float p0 = exp2f(sv[j][0] - muse[0]), p1 = exp2f(sv[j][1] - muse[0]);
             const float p2 = exp2f(sv[j][2] - muse[1]), p3 = exp2f(sv[j][3] - muse[1]);
             lrow[0] += p0 + p1;
@@ -903,7 +923,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
             oacc[j][3] *= corr[1];
         }
 #pragma unroll
-        for (int ks = 0; ks < 2; ks++) {
+        for (int ks = 0; ks < NKS; ks++) {
 #pragma unroll
             for (int jj = 0; jj < NT / 2; jj++) {
                 uint32_t b0, b1, b2, b3;
