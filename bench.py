@@ -430,9 +430,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": t_max_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: m={wl.m} start_pos={wl.start_pos} heads={wl.nh}x{wl.hd}"
-                               f" rope={wl.rd} window={wl.win} ratio={wl.ratio} compressed_rows="
-                               f"{wl.n_c} topk={wl.topk} indexer={wl.Hi}x{wl.Di}",
+        "config": {"workload": workload_desc(wl),
                    "global_batch": wl.m * world, "parallelism": f"replicas{world}",
                    "l2": f"inputs larger than L2: {n_slots} rotating layer states x "
                          f"{per / 2**20:.2f} MiB = {n_slots * per / 2**20:.0f} MiB "
@@ -586,6 +584,13 @@ def oracle_rate(wl, steps=None, budget_s=None):
                       f"and latent writes run whole every time"}
 
 
+def workload_desc(wl) -> str:
+    """The workload's name and sizes, the same string in both arms' config."""
+    return (f"{wl.name}: m={wl.m} start_pos={wl.start_pos} heads={wl.nh}x{wl.hd} rope={wl.rd} "
+            f"window={wl.win} ratio={wl.ratio} compressed_rows={wl.n_c} topk={wl.topk} "
+            f"indexer={wl.Hi}x{wl.Di}")
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return None
@@ -597,7 +602,8 @@ def run_reference(args, world, rank):
             "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": 1e3 * cb["seconds"] / max(1, K), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "global_batch": min(wl.m, 8), "parallelism": "cpu"},
+            "config": {"workload": workload_desc(wl), "global_batch": wl.m,
+                       "parallelism": "cpu oracle, bounded sample (see cpu_baseline.sample)"},
             "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
             "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
