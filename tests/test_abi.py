@@ -90,3 +90,33 @@ def test_workspace_sizes_are_host_only(lib):
     # the indexer needs scratch for its scores unless the caller takes them
     assert lib.ds41_indexer_workspace_bytes(4096, 64, 128, 1024, 0) >= 4096 * 1024 * 2
     assert lib.ds41_indexer_workspace_bytes(1, 64, 128, 2048, 1) == 0
+
+
+def test_host_buffer_entry_points_check_arguments(lib):
+    """ds41_csa_forward_host[_packed] reject bad sizes and missing buffers on
+    the host, before any copy is enqueued."""
+    # sizes of the decode workload: m=1, start_pos=8191, 64x512 heads, ratio 4,
+    # indexer 64x128: q 64 KiB + kv 1 KiB + one latent row 1 KiB + q_idx 16 KiB + w 256 B
+    assert lib.ds41_step_inputs_bytes(1, 8191, 64, 512, 4, 64, 128) == 65536 + 1024 + 1024 + 16384 + 256
+    # no group completes: no latent bytes
+    assert lib.ds41_step_inputs_bytes(1, 8192, 64, 512, 4, 64, 128) == 65536 + 1024 + 16384 + 256
+    assert lib.ds41_step_inputs_bytes(0, 0, 64, 512, 4, 64, 128) == 0
+    f = ctypes.c_float(0.04)
+    sizes = (8191, 64, 512, 64, 128, 4, 512, 64, 128)  # start_pos nh hd rd win ratio topk Hi Di
+
+    def host_call(h_latent, m):
+        # h_q h_kv h_latent h_q_idx h_w h_o | q kv ring rows_a latent freqs_cis max_pos cache
+        # cache_rows q_idx k_idx w sink scale win_idx idx o lse | m, sizes | ws ws_bytes stream
+        return lib.ds41_csa_forward_host(FAKE, FAKE, h_latent, FAKE, FAKE, FAKE,
+                                         FAKE, FAKE, FAKE, None, FAKE, FAKE, 1 << 20, FAKE, 1 << 20,
+                                         FAKE, FAKE, FAKE, FAKE, f, FAKE, FAKE, FAKE, None,
+                                         m, *sizes, None, 0, None)
+
+    # per-buffer form: a completed group needs h_latent
+    assert host_call(None, 1) == 1 and "null pointer" in _err(lib)
+    assert host_call(FAKE, 0) == 1  # no token
+    # packed form: no host block
+    rc = lib.ds41_csa_forward_host_packed(None, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, FAKE, 1 << 20,
+                                          FAKE, FAKE, f, FAKE, FAKE, FAKE, None,
+                                          1, *sizes, None, 0, None)
+    assert rc == 1 and "null pointer" in _err(lib)
