@@ -97,7 +97,8 @@ def attn_valid_rows(wl) -> int:
 
 
 def algorithmic(wl):
-    """Per-op algorithmic bytes and flops of one step."""
+    """Per-op algorithmic bytes and flops of one step: each input and output
+    once, the valid gathered rows, and the causally visible indexer pairs."""
     bf, m = 2, wl.m
     rows = attn_valid_rows(wl)
     pairs = sum(min(wl.n_c, (wl.start_pos + t + 1) // wl.ratio) for t in range(wl.m))
