@@ -425,7 +425,7 @@ def run_ours(args, world, rank, local):
                  "traffic": args.traffic if args.traffic is not None else recorded_traffic(wl.name, dom)})
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(wl, slots, fc, stream, K, W, n_slots)
+    e2e = run_e2e(wl, slots, fc, stream, K, W, n_slots, world)
 
     res = {
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
@@ -493,7 +493,7 @@ def run_only(args, local):
                       "ms_per_call": e0.elapsed_time(e1) / args.steps, "slots": len(slots)}))
 
 
-def run_e2e(wl, slots, fc, stream, K, W, n_slots):
+def run_e2e(wl, slots, fc, stream, K, W, n_slots, world=1):
     """The same metric through ds41_csa_forward_host, the C-ABI call for
     host-resident step data, prepared once per layer state (ds41.HostStep):
     every step copies that step's inputs from page-locked host memory into
@@ -520,6 +520,7 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots):
         for i in range(W):
             steps[i % n_slots](sid)
     stream.synchronize()
+    barrier(world)
     t0 = time.perf_counter()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -530,8 +531,8 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots):
         e1.record(stream)
     stream.synchronize()
     wall = time.perf_counter() - t0
-    ms = max(e0.elapsed_time(e1), wall * 1e3)
-    return {"value": wl.m * K / (ms / 1e3), "unit": "query-tokens/s",
+    ms = max_over_ranks(max(e0.elapsed_time(e1), wall * 1e3), world)
+    return {"value": wl.m * K * world / (ms / 1e3), "unit": "query-tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "how": "ds41_csa_forward_host per step (prepared call): one pinned H2D of "
                    "q/kv/latent/q_idx/w, the step, D2H of o, one stream"}
@@ -637,13 +638,13 @@ def main():
         res = run_reference(args, world, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
-        return
-    res, wl = run_ours(args, world, rank, local)
-    if rank == 0:
-        if world == 1 and not args.no_cpu_baseline:
-            cb = oracle_rate(wl, budget_s=args.cpu_budget)
-            res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
-        print(json.dumps(res), flush=True)
+    else:
+        res, wl = run_ours(args, world, rank, local)
+        if rank == 0:
+            if world == 1 and not args.no_cpu_baseline:
+                cb = oracle_rate(wl, budget_s=args.cpu_budget)
+                res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+            print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
