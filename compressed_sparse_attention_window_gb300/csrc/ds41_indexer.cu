@@ -66,8 +66,10 @@ __device__ __forceinline__ int64_t visible_rows(int64_t t, int64_t start_pos, in
 // tiles: k tile -> shared (quantised on the fly, or copied when kq holds the
 // pre-quantised keys), 4 warps x 16 rows x 128 columns of bf16 MMA, the
 // accumulator through shared memory, then one thread per (row, token) runs the
-// ordered head chain and writes the bf16 score.
-template <int DI, bool KQ_INLINE>
+// ordered head chain and writes the bf16 score.  NARROW: at most IDX_N / 2
+// live (token, head) columns (one token of 64 heads), so the eight warps split
+// those instead of computing on padding.
+template <int DI, bool KQ_INLINE, bool NARROW>
 __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_src,
     const float* __restrict__ w, uint16_t* __restrict__ scores, int m, int Hi, int hpad, int TT,
@@ -175,8 +177,8 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             __syncthreads();
         }
 
-        // 8 warps: warp w owns rows 16*(w%4).. and columns 64*(w/4)..
-        constexpr int WN = IDX_N / 2;  // columns per warp
+        // 8 warps: warp w owns rows 16*(w%4).. and columns WN*(w/4)..
+        constexpr int WN = NARROW ? IDX_N / 4 : IDX_N / 2;  // columns per warp
         const int wr = (warp & 3) * 16, wc = (warp >> 2) * WN;
         float acc[WN / 8][4];
 #pragma unroll
@@ -584,17 +586,15 @@ static int launch_scores(const IndexerPlan& p, const uint16_t* q, const uint16_t
     const RingArgs ra = side ? *ring : RingArgs{};
     const LatentArgs la = side ? *lat : LatentArgs{};
     dim3 grid((unsigned)p.groups, (unsigned)(ysplit + (side ? 1 : 0)));
-    if (p.prequant) {
-        auto kern = indexer_scores_kernel<DI, false>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<grid, IDX_THREADS, smem, st>>>(q, k, w, scores, (int)m, (int)Hi, p.hpad, p.TT, n_c,
-                                              ratio, start_pos, fill_hidden, (int)ysplit, ra, la);
-    } else {
-        auto kern = indexer_scores_kernel<DI, true>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<grid, IDX_THREADS, smem, st>>>(q, k, w, scores, (int)m, (int)Hi, p.hpad, p.TT, n_c,
-                                              ratio, start_pos, fill_hidden, (int)ysplit, ra, la);
-    }
+    // every group's live columns fit in half the tile: one token of <= 64 heads
+    const bool narrow = (int64_t)p.hpad * (m < p.TT ? m : p.TT) <= IDX_N / 2;
+    auto kern = p.prequant ? (narrow ? indexer_scores_kernel<DI, false, true>
+                                     : indexer_scores_kernel<DI, false, false>)
+                           : (narrow ? indexer_scores_kernel<DI, true, true>
+                                     : indexer_scores_kernel<DI, true, false>);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<grid, IDX_THREADS, smem, st>>>(q, k, w, scores, (int)m, (int)Hi, p.hpad, p.TT, n_c,
+                                          ratio, start_pos, fill_hidden, (int)ysplit, ra, la);
     return launch_check("ds41_indexer_topk: scores kernel");
 }
 
