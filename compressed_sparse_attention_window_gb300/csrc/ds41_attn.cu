@@ -460,22 +460,24 @@ __device__ void dec_topk_local(const DecTopk& tk, int64_t t, int vis, int kk, in
 // [window indices | the min(ctopk, visible) best compressed rows in ascending
 // order | -1].  Up to TKD_CAP visible scores every CTA ranks them all itself
 // (dec_topk_local).  Beyond, the CL CTAs of the cluster each take one slice
-// of the visible scores, sum their two 8-bit histograms over the cluster
-// (every CTA derives the same threshold; the lowest-numbered ties are taken),
-// and store each pick straight into the index slice of the CTA that owns its
-// position.  Returns whether it waited on the cluster barrier's first phase.
+// of the visible scores (in registers, as there), sum their two 8-bit
+// histograms over the cluster (every CTA derives the same threshold; the
+// lowest-numbered ties are taken), take the counts of the earlier slices from
+// their pushed histograms and above-bucket counts, and store each pick
+// straight into the index slice of the CTA that owns its position: three
+// cluster barriers.  Returns whether it waited on the cluster barrier's first
+// phase.
 template <int NTH>
 __device__ bool dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, int j1, int* sidx,
                          uint8_t* area, int* hpush, bool write_idx, unsigned int* status) {
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
     const int CL = (int)cl.num_blocks(), r = (int)cl.block_rank();
-    uint16_t* skeys = reinterpret_cast<uint16_t*>(area);
     int* hist = reinterpret_cast<int*>(area + 8192);  // this slice's histogram
     int* ghist = hist + 256;                          // the cluster's
     int* wsum = ghist + 256;
     int* sel = wsum + 64;
-    int* tpush = sel + 8;                             // [16][2] totals of the slices
+    int* tpush = sel + 8;                             // [16]: each slice's keys above bucket hb
     int* hpush1 = hpush;                              // [16][256] histograms of the slices
     int* hpush2 = hpush + 16 * 256;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -512,133 +514,149 @@ __device__ bool dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, i
     const int n = (int)(min(vis, klo + kseg) - klo);
     if (n > TKD_CAP) raise_status(status, DS41_E_RANGE);  // excluded by the host plan
     const int nk = min(n, TKD_CAP);
+    // this slice's keys in registers: thread tid holds the run of kpt
+    // consecutive scores from kpt * tid, so index order is warp, lane, register
+    constexpr int KMAX = TKD_CAP / NTH;
+    int* whist = reinterpret_cast<int*>(area + TKD_WHIST);  // [NW][256]
+    const int kpt = (nk + NTH - 1) / NTH;
+    const int i0 = kpt * tid;
     const uint16_t* sc = tk.scores + t * tk.n_c + klo;
-    const bool vec = ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0);
-    const int n8 = vec ? nk / 8 : 0;
-    for (int i = tid; i < n8; i += NTH) {
-        uint4 v = __ldg(reinterpret_cast<const uint4*>(sc) + i);
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
+    uint32_t key[KMAX];
+    const bool vec = (kpt & 7) == 0 && ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0);
 #pragma unroll
-        for (int e = 0; e < 8; e++) skeys[i * 8 + e] = (uint16_t)order_key(h[e]);
+    for (int v = 0; v < KMAX / 8; v++) {
+        const int b0 = i0 + 8 * v;
+        if (8 * v >= kpt || b0 >= nk) continue;
+        if (vec && b0 + 8 <= nk) {  // whole groups of eight only: nothing past the slice is read
+            uint4 u = __ldg(reinterpret_cast<const uint4*>(sc + b0));
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&u);
+#pragma unroll
+            for (int e = 0; e < 8; e++) key[8 * v + e] = order_key(h[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                if (8 * v + e < kpt && b0 + e < nk) key[8 * v + e] = order_key(sc[b0 + e]);
+        }
     }
-    for (int i = n8 * 8 + tid; i < nk; i += NTH) skeys[i] = (uint16_t)order_key(sc[i]);
-    for (int i = tid; i < 256; i += NTH) hist[i] = 0;
+    const int n_mine = max(0, min(kpt, nk - i0));
+    int* wh = whist + warp * 256;
+#pragma unroll
+    for (int e = 0; e < 8; e++) wh[lane + 32 * e] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < KMAX; e++)
+        if (e < n_mine) atomicAdd(&wh[key[e] >> 8], 1);
     __syncthreads();
-    for (int base = tid - lane; base < nk; base += NTH) {
-        const int i = base + lane;
-        const uint32_t bin = i < nk ? (uint32_t)skeys[i] >> 8 : 0x10000u;
-        const uint32_t mm = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256u && lane == __ffs(mm) - 1) atomicAdd(&hist[bin], __popc(mm));
-    }
-    __syncthreads();
-    // push this slice's histogram into every CTA; after the barrier the sums are local
-    for (int i = tid; i < 256; i += NTH) {
-        const int v = hist[i];
-        for (int q = 0; q < CL; q++) cl.map_shared_rank(hpush1, q)[r * 256 + i] = v;
-        hist[i] = 0;
+    // this slice's top-byte histogram: kept here, and pushed into every CTA
+    for (int b = tid; b < 256; b += NTH) {
+        int v = 0;
+#pragma unroll
+        for (int w = 0; w < NW; w++) {
+            v += whist[w * 256 + b];
+            whist[w * 256 + b] = 0;
+        }
+        hist[b] = v;
+        for (int q = 0; q < CL; q++) cl.map_shared_rank(hpush1, q)[r * 256 + b] = v;
     }
     cl.sync();
-    for (int i = tid; i < 256; i += NTH) {
+    for (int b = tid; b < 256; b += NTH) {
         int v = 0;
-        for (int q = 0; q < CL; q++) v += hpush1[q * 256 + i];
-        ghist[i] = v;
+        for (int q = 0; q < CL; q++) v += hpush1[q * 256 + b];
+        ghist[b] = v;
     }
     __syncthreads();
     if (tid < 32) find_bucket(ghist, kk, 0, &sel[0], &sel[1]);
     __syncthreads();
     const uint32_t hb = (uint32_t)sel[0];
     const int above1 = sel[1];
-    for (int base = tid - lane; base < nk; base += NTH) {
-        const int i = base + lane;
-        uint32_t bin = 0x10000u;
-        if (i < nk && ((uint32_t)skeys[i] >> 8) == hb) bin = skeys[i] & 0xffu;
-        const uint32_t mm = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256u && lane == __ffs(mm) - 1) atomicAdd(&hist[bin], __popc(mm));
+#pragma unroll
+    for (int e = 0; e < KMAX; e++)
+        if (e < n_mine && (key[e] >> 8) == hb) atomicAdd(&wh[key[e] & 0xffu], 1);
+    if (warp == 0) {
+        // keys of this slice in buckets above hb, for the other slices' prefixes
+        int a = 0;
+        for (int b = (int)hb + 1 + lane; b < 256; b += 32) a += hist[b];
+        a = __reduce_add_sync(0xffffffffu, a);
+        if (lane < CL) cl.map_shared_rank(tpush, lane)[r] = a;
     }
     __syncthreads();
-    for (int i = tid; i < 256; i += NTH) {
-        const int v = hist[i];
-        for (int q = 0; q < CL; q++) cl.map_shared_rank(hpush2, q)[r * 256 + i] = v;
+    // this slice's low-byte histogram of bucket hb, pushed into every CTA; with
+    // the above counts it gives every slice's count of keys above and at the
+    // threshold, so no further exchange is needed before the picks
+    for (int b = tid; b < 256; b += NTH) {
+        int v = 0;
+#pragma unroll
+        for (int w = 0; w < NW; w++) v += whist[w * 256 + b];
+        for (int q = 0; q < CL; q++) cl.map_shared_rank(hpush2, q)[r * 256 + b] = v;
     }
     cl.sync();
-    for (int i = tid; i < 256; i += NTH) {
+    for (int b = tid; b < 256; b += NTH) {
         int v = 0;
-        for (int q = 0; q < CL; q++) v += hpush2[q * 256 + i];
-        ghist[i] = v;
+        for (int q = 0; q < CL; q++) v += hpush2[q * 256 + b];
+        ghist[b] = v;
     }
     __syncthreads();
     if (tid < 32) find_bucket(ghist, kk, above1, &sel[2], &sel[3]);
     __syncthreads();
     const uint32_t T = (hb << 8) | (uint32_t)sel[2];
     const int need_eq = kk - sel[3];
-    // per-warp blocks of the slice, counted with ballots
-    const int wseg = ((nk + NW - 1) / NW + 31) & ~31;
-    const int w_lo = min(nk, warp * wseg), w_hi = min(nk, w_lo + wseg);
-    const uint32_t lt = (1u << lane) - 1u;
-    int n_gt = 0, n_eq = 0;
-    for (int b0 = w_lo; b0 < w_hi; b0 += 32) {
-        const int i = b0 + lane;
-        const uint32_t k = i < w_hi ? skeys[i] : 0u;
-        n_gt += __popc(__ballot_sync(0xffffffffu, i < w_hi && k > T));
-        n_eq += __popc(__ballot_sync(0xffffffffu, i < w_hi && k == T));
+    if (warp == 0) {
+        // keys above and at the threshold in the slices before this one
+        const int tl = sel[2];
+        int g = 0, e = 0;
+        for (int q = 0; q < r; q++) {
+            int a = 0;
+            for (int b = tl + 1 + lane; b < 256; b += 32) a += hpush2[q * 256 + b];
+            g += __reduce_add_sync(0xffffffffu, a) + tpush[q];
+            e += hpush2[q * 256 + tl];
+        }
+        if (lane == 0) {
+            sel[4] = g;
+            sel[5] = e;
+        }
     }
-    if (lane == 0) {
-        wsum[warp] = n_gt;
-        wsum[32 + warp] = n_eq;
+    int n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int e = 0; e < KMAX; e++) {
+        if (e < n_mine) {
+            n_gt += key[e] > T ? 1 : 0;
+            n_eq += key[e] == T ? 1 : 0;
+        }
+    }
+    int x_gt = n_gt, x_eq = n_eq;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, x_gt, off);
+        const int b = __shfl_up_sync(0xffffffffu, x_eq, off);
+        if (lane >= off) {
+            x_gt += a;
+            x_eq += b;
+        }
+    }
+    if (lane == 31) {
+        wsum[warp] = x_gt;
+        wsum[32 + warp] = x_eq;
     }
     __syncthreads();
-    if (warp == 0) {
-        const int a = lane < NW ? wsum[lane] : 0;
-        const int e = lane < NW ? wsum[32 + lane] : 0;
-        int xa = a, xe = e;
+    int gt = sel[4] + x_gt - n_gt, eq = sel[5] + x_eq - n_eq;
+    for (int w = 0; w < warp; w++) {
+        gt += wsum[w];
+        eq += wsum[32 + w];
+    }
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int oa = __shfl_up_sync(0xffffffffu, xa, off);
-            const int oe = __shfl_up_sync(0xffffffffu, xe, off);
-            if (lane >= off) {
-                xa += oa;
-                xe += oe;
+    for (int e = 0; e < KMAX; e++) {
+        if (e < n_mine) {
+            const bool is_eq = key[e] == T;
+            if (key[e] > T || (is_eq && eq < need_eq)) {
+                const int j = win + gt + min(eq, need_eq);  // position in the merged row
+                const int owner = j / per;
+                const int v = (int)(tk.offset + klo + i0 + e);
+                cl.map_shared_rank(sidx, owner)[j - owner * per] = v;
+                if (write_idx) orow[j] = v;
             }
+            gt += key[e] > T ? 1 : 0;
+            eq += is_eq ? 1 : 0;
         }
-        __syncwarp();
-        if (lane < NW) {
-            wsum[lane] = xa - a;
-            wsum[32 + lane] = xe - e;
-        }
-        if (lane == 31) {
-            // push this slice's totals into the CTAs of the later slices
-            for (int q = r + 1; q < CL; q++) {
-                int* dst = cl.map_shared_rank(tpush, q);
-                dst[2 * r] = xa;
-                dst[2 * r + 1] = xe;
-            }
-        }
-    }
-    cl.sync();  // every slice's totals are published
-    int gt_before = 0, eq_before = 0;
-    for (int q = 0; q < r; q++) {
-        gt_before += tpush[2 * q];
-        eq_before += tpush[2 * q + 1];
-    }
-    int eq_rank = eq_before + wsum[32 + warp];
-    int pos = gt_before + wsum[warp] + min(eq_rank, need_eq);
-    for (int b0 = w_lo; b0 < w_hi; b0 += 32) {
-        const int i = b0 + lane;
-        const uint32_t k = i < w_hi ? skeys[i] : 0u;
-        const bool eq = i < w_hi && k == T;
-        const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
-        const bool take = (i < w_hi && k > T) || (eq && eq_rank + __popc(eqb & lt) < need_eq);
-        const uint32_t tb = __ballot_sync(0xffffffffu, take);
-        const int at = pos + __popc(tb & lt);
-        if (take && at < kk) {
-            const int j = win + at;  // position in the merged row
-            const int owner = j / per;
-            const int v = (int)(tk.offset + klo + i);
-            cl.map_shared_rank(sidx, owner)[j - owner * per] = v;
-            if (write_idx) orow[j] = v;
-        }
-        pos += __popc(tb);
-        eq_rank += __popc(eqb);
     }
     cl.sync();  // every index slice is complete
     return true;
