@@ -548,15 +548,18 @@ __device__ bool dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, i
         if (e < n_mine) atomicAdd(&wh[key[e] >> 8], 1);
     __syncthreads();
     // this slice's top-byte histogram: kept here, and pushed into every CTA
-    for (int b = tid; b < 256; b += NTH) {
-        int v = 0;
+    // (four bins a thread, 16-byte remote stores)
+    if (tid < 64) {
+        int4 v = make_int4(0, 0, 0, 0);
 #pragma unroll
         for (int w = 0; w < NW; w++) {
-            v += whist[w * 256 + b];
-            whist[w * 256 + b] = 0;
+            int4* h = reinterpret_cast<int4*>(whist + w * 256 + 4 * tid);
+            const int4 x = *h;
+            v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+            *h = make_int4(0, 0, 0, 0);
         }
-        hist[b] = v;
-        for (int q = 0; q < CL; q++) cl.map_shared_rank(hpush1, q)[r * 256 + b] = v;
+        *reinterpret_cast<int4*>(hist + 4 * tid) = v;
+        for (int q = 0; q < CL; q++) reinterpret_cast<int4*>(cl.map_shared_rank(hpush1 + r * 256, q))[tid] = v;
     }
     cl.sync();
     for (int b = tid; b < 256; b += NTH) {
@@ -583,11 +586,14 @@ __device__ bool dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, i
     // this slice's low-byte histogram of bucket hb, pushed into every CTA; with
     // the above counts it gives every slice's count of keys above and at the
     // threshold, so no further exchange is needed before the picks
-    for (int b = tid; b < 256; b += NTH) {
-        int v = 0;
+    if (tid < 64) {
+        int4 v = make_int4(0, 0, 0, 0);
 #pragma unroll
-        for (int w = 0; w < NW; w++) v += whist[w * 256 + b];
-        for (int q = 0; q < CL; q++) cl.map_shared_rank(hpush2, q)[r * 256 + b] = v;
+        for (int w = 0; w < NW; w++) {
+            const int4 x = *reinterpret_cast<const int4*>(whist + w * 256 + 4 * tid);
+            v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+        }
+        for (int q = 0; q < CL; q++) reinterpret_cast<int4*>(cl.map_shared_rank(hpush2 + r * 256, q))[tid] = v;
     }
     cl.sync();
     for (int b = tid; b < 256; b += NTH) {

@@ -381,15 +381,18 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(
 
 // ---------------------------------------------------------------------------
 // Top-k of few long rows: a cluster of TK_CL CTAs per query, CTA r holding
-// slice r of the visible scores.  The same two histogram passes and the
-// ordered pass as above, with the histograms summed over the cluster through
+// slice r of the visible scores (up to TK_SMALL keys, staged in shared
+// memory; longer slices: topk_cluster_big_kernel).  The same two histogram
+// passes and the ordered pass as above, with the histograms summed over the
+// cluster through
 // distributed shared memory (every CTA derives the same threshold) and a
 // cluster-wide prefix of the per-CTA counts, so the picks still come out in
 // ascending row order.
 // ---------------------------------------------------------------------------
 constexpr int TK_CL = 8;
 constexpr int TK_THREADS = 512;
-constexpr int TK_SLICE_CAP = 8192;  // keys of a slice staged in shared memory
+constexpr int TK_SLICE_CAP = 8192;  // keys of a slice
+constexpr int TK_SMALL = 2048;      // slices up to this size: keys staged in shared memory
 
 __global__ void __launch_bounds__(TK_THREADS) topk_cluster_kernel(
     const uint16_t* __restrict__ scores, const int32_t* __restrict__ win_idx,
@@ -534,6 +537,205 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_kernel(
     if (r == 0)
         for (int j = kk + threadIdx.x; j < ctopk; j += blockDim.x) out[win + j] = -1;
     cl.sync();  // the totals stay readable until every CTA has read them
+}
+
+// ---------------------------------------------------------------------------
+// The same for long slices (more than TK_SMALL keys a CTA): CTA r holds
+// slice r of the visible scores as 16-bit order keys in registers (a run of
+// consecutive keys per thread, so index order is warp, lane, register).  The
+// same two 8-bit histogram passes (per-warp histograms), with every slice's
+// histogram pushed into every CTA of the cluster, so each CTA derives the same
+// threshold from local sums; with the second pass each slice also pushes its
+// count of keys above the threshold's bucket, from which every CTA knows how
+// many picks and ties the earlier slices hold.  The picks, in ascending row
+// order, go straight to global memory: two cluster barriers, and no CTA reads
+// another's shared memory.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
+    const uint16_t* __restrict__ scores, const int32_t* __restrict__ win_idx,
+    int32_t* __restrict__ idx, int64_t n_c, int win, int ctopk, int64_t ratio, int64_t start_pos,
+    int64_t offset) {
+    namespace cg = cooperative_groups;
+    constexpr int NW = TK_THREADS / 32;
+    constexpr int KMAX = TK_SLICE_CAP / TK_THREADS;
+    cg::cluster_group cl = cg::this_cluster();
+    __shared__ __align__(16) int whist[NW][256];      // per-warp histograms
+    __shared__ __align__(16) int hist[256];           // this slice's pass-1 histogram
+    __shared__ __align__(16) int hpush1[TK_CL][256];  // every slice's pass-1 histogram (pushed)
+    __shared__ __align__(16) int hpush2[TK_CL][256];  // every slice's pass-2 histogram (pushed)
+    __shared__ int above[TK_CL];               // every slice's keys above bucket hb (pushed)
+    __shared__ int ghist[256];
+    __shared__ int wsum[64];
+    __shared__ int sel[8];
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");  // this CTA has started
+    pdl_wait();  // the scores (and window indices) come from the previous kernel
+    pdl_trigger();
+    const int r = (int)cl.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t = blockIdx.x / TK_CL;
+    const int K = win + ctopk;
+    int32_t* out = idx + (int64_t)t * K;
+    const uint16_t* sc = scores + (int64_t)t * n_c;
+    if (r == 0)
+        for (int j = tid; j < win; j += TK_THREADS) out[j] = win_idx[(int64_t)t * win + j];
+    const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
+    const int kk = (int)(vis < ctopk ? vis : ctopk);
+    if (vis <= ctopk) {  // the same branch in every CTA of the cluster
+        if (r == 0)
+            for (int j = tid; j < ctopk; j += TK_THREADS)
+                out[win + j] = (j < vis) ? (int32_t)(offset + j) : -1;
+        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+        return;
+    }
+    const int64_t seg = ((vis + TK_CL - 1) / TK_CL + 7) & ~int64_t(7);
+    const int64_t lo = min(vis, (int64_t)r * seg);
+    const int n = (int)(min(vis, lo + seg) - lo);  // <= TK_SLICE_CAP (host plan)
+    const int kpt = (n + TK_THREADS - 1) / TK_THREADS;
+    const int i0 = kpt * tid;
+    const uint16_t* ss = sc + lo;
+    uint32_t key[KMAX];
+    const bool vec = (kpt & 7) == 0 && ((reinterpret_cast<uintptr_t>(ss) & 15u) == 0);
+#pragma unroll
+    for (int v = 0; v < KMAX / 8; v++) {
+        const int b0 = i0 + 8 * v;
+        if (8 * v >= kpt || b0 >= n) continue;
+        if (vec && b0 + 8 <= n) {  // whole groups of eight only: nothing past the slice is read
+            uint4 u = __ldg(reinterpret_cast<const uint4*>(ss + b0));
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&u);
+#pragma unroll
+            for (int e = 0; e < 8; e++) key[8 * v + e] = order_key(h[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                if (8 * v + e < kpt && b0 + e < n) key[8 * v + e] = order_key(ss[b0 + e]);
+        }
+    }
+    const int n_mine = max(0, min(kpt, n - i0));
+    int* wh = whist[warp];
+#pragma unroll
+    for (int e = 0; e < 8; e++) wh[lane + 32 * e] = 0;
+    __syncwarp();
+    // pass 1: high byte of this slice
+#pragma unroll
+    for (int e = 0; e < KMAX; e++)
+        if (e < n_mine) atomicAdd(&wh[key[e] >> 8], 1);
+    __syncthreads();
+    asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");  // every CTA has started
+    // sums of four bins a thread, pushed as 16-byte remote stores
+    if (tid < 64) {
+        int4 v = make_int4(0, 0, 0, 0);
+#pragma unroll
+        for (int w = 0; w < NW; w++) {
+            int4* h = reinterpret_cast<int4*>(&whist[w][4 * tid]);
+            const int4 x = *h;
+            v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+            *h = make_int4(0, 0, 0, 0);
+        }
+        *reinterpret_cast<int4*>(&hist[4 * tid]) = v;
+        for (int q = 0; q < TK_CL; q++)
+            reinterpret_cast<int4*>(cl.map_shared_rank(&hpush1[r][0], q))[tid] = v;
+    }
+    cl.sync();  // every slice's histogram is in every CTA
+    for (int b = tid; b < 256; b += TK_THREADS) {
+        int v = 0;
+#pragma unroll
+        for (int q = 0; q < TK_CL; q++) v += hpush1[q][b];
+        ghist[b] = v;
+    }
+    __syncthreads();
+    if (tid < 32) find_bucket(ghist, kk, 0, &sel[0], &sel[1]);
+    __syncthreads();
+    const uint32_t hb = (uint32_t)sel[0];
+    const int above1 = sel[1];
+    // pass 2: low byte inside bucket hb
+#pragma unroll
+    for (int e = 0; e < KMAX; e++)
+        if (e < n_mine && (key[e] >> 8) == hb) atomicAdd(&wh[key[e] & 0xffu], 1);
+    if (warp == 0) {
+        int a = 0;
+        for (int b = (int)hb + 1 + lane; b < 256; b += 32) a += hist[b];
+        a = __reduce_add_sync(0xffffffffu, a);
+        if (lane < TK_CL) cl.map_shared_rank(above, lane)[r] = a;
+    }
+    __syncthreads();
+    if (tid < 64) {
+        int4 v = make_int4(0, 0, 0, 0);
+#pragma unroll
+        for (int w = 0; w < NW; w++) {
+            const int4 x = *reinterpret_cast<const int4*>(&whist[w][4 * tid]);
+            v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+        }
+        for (int q = 0; q < TK_CL; q++)
+            reinterpret_cast<int4*>(cl.map_shared_rank(&hpush2[r][0], q))[tid] = v;
+    }
+    cl.sync();  // every slice's low-byte histogram and above count are in every CTA
+    for (int b = tid; b < 256; b += TK_THREADS) {
+        int v = 0;
+#pragma unroll
+        for (int q = 0; q < TK_CL; q++) v += hpush2[q][b];
+        ghist[b] = v;
+    }
+    __syncthreads();
+    if (tid < 32) find_bucket(ghist, kk, above1, &sel[2], &sel[3]);
+    __syncthreads();
+    const uint32_t T = (hb << 8) | (uint32_t)sel[2];
+    const int need_eq = kk - sel[3];
+    if (warp == 0) {
+        // keys above and at the threshold in the slices before this one
+        const int tl = sel[2];
+        int g = 0, e = 0;
+        for (int q = 0; q < r; q++) {
+            int a = 0;
+            for (int b = tl + 1 + lane; b < 256; b += 32) a += hpush2[q][b];
+            g += __reduce_add_sync(0xffffffffu, a) + above[q];
+            e += hpush2[q][tl];
+        }
+        if (lane == 0) {
+            sel[4] = g;
+            sel[5] = e;
+        }
+    }
+    int n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int e = 0; e < KMAX; e++) {
+        if (e < n_mine) {
+            n_gt += key[e] > T ? 1 : 0;
+            n_eq += key[e] == T ? 1 : 0;
+        }
+    }
+    int x_gt = n_gt, x_eq = n_eq;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, x_gt, off);
+        const int b = __shfl_up_sync(0xffffffffu, x_eq, off);
+        if (lane >= off) {
+            x_gt += a;
+            x_eq += b;
+        }
+    }
+    if (lane == 31) {
+        wsum[warp] = x_gt;
+        wsum[32 + warp] = x_eq;
+    }
+    __syncthreads();
+    int gt = sel[4] + x_gt - n_gt, eq = sel[5] + x_eq - n_eq;
+    for (int w = 0; w < warp; w++) {
+        gt += wsum[w];
+        eq += wsum[32 + w];
+    }
+#pragma unroll
+    for (int e = 0; e < KMAX; e++) {
+        if (e < n_mine) {
+            const bool is_eq = key[e] == T;
+            if (key[e] > T || (is_eq && eq < need_eq))
+                out[win + gt + min(eq, need_eq)] = (int32_t)(offset + lo + i0 + e);
+            gt += key[e] > T ? 1 : 0;
+            eq += is_eq ? 1 : 0;
+        }
+    }
+    if (r == 0)
+        for (int j = kk + tid; j < ctopk; j += TK_THREADS) out[win + j] = -1;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -724,7 +926,9 @@ int launch_topk(const uint16_t* scores, const int32_t* win_idx, int32_t* idx, in
         na++;
         cfg.attrs = attr;
         cfg.numAttrs = na;
-        rc = cuda_check(cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, win_idx, idx, n_c,
+        const bool big = n_c > (int64_t)TK_CL * TK_SMALL;
+        rc = cuda_check(cudaLaunchKernelEx(&cfg, big ? topk_cluster_big_kernel : topk_cluster_kernel,
+                                           scores, win_idx, idx, n_c,
                                            (int)win, (int)ctopk, ratio, start_pos, offset),
                         "top-k cluster kernel");
         if (rc) return rc;

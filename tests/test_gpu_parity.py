@@ -165,7 +165,9 @@ def _gpu_indexer(wl, inp, with_scores=True):
 
 INDEXER_CASES = [TINY_PREFILL, TINY_PREFILL.replace(topk=64), DECODE, LONG_DECODE, CHUNKED,
                  PREFILL, TINY_PREFILL.replace(m=37, start_pos=5, Hi=5, Di=64),
-                 DECODE.replace(start_pos=8191 + 9, m=1, topk=4000)]
+                 DECODE.replace(start_pos=8191 + 9, m=1, topk=4000),
+                 # tied scores in long slices (the cluster top-k with keys in registers)
+                 LONG_DECODE.replace(structure="repeat")]
 
 
 @pytest.mark.parametrize("wl", INDEXER_CASES, ids=lambda w: f"{w.name}-{w.m}-{w.start_pos}-{w.topk}-{w.Hi}")
