@@ -240,6 +240,116 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
 // larger key and the lowest-numbered rows with key T, writing them in
 // ascending row order.
 // ---------------------------------------------------------------------------
+// Top-k of many short rows (at most TKW_MAX visible scores): one warp per
+// query, eight queries a CTA, no block-wide barrier.  Lane l holds the run of
+// kpl consecutive order keys from kpl * l in registers (index order lane,
+// register); the two 8-bit histogram passes go into the warp's own shared
+// histogram, the warp finds the threshold, and one warp scan places the picks
+// (the lowest-numbered ties first), merged after the window indices.
+// ---------------------------------------------------------------------------
+constexpr int TKW_WARPS = 8;
+constexpr int TKW_KPL = 32;               // keys per lane at most
+constexpr int TKW_MAX = 32 * TKW_KPL;     // 1024 visible scores
+
+__global__ void __launch_bounds__(32 * TKW_WARPS) topk_warp_kernel(
+    const uint16_t* __restrict__ scores, const int32_t* __restrict__ win_idx,
+    int32_t* __restrict__ idx, int64_t m, int64_t n_c, int win, int ctopk, int64_t ratio,
+    int64_t start_pos, int64_t offset) {
+    __shared__ __align__(16) int hist_all[TKW_WARPS][256];
+    __shared__ int sel_all[TKW_WARPS][4];
+    pdl_wait();     // the scores (and window indices) come from the previous kernel
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = (int64_t)blockIdx.x * TKW_WARPS + warp;
+    if (t >= m) return;  // whole warps only: the rest of the CTA syncs nothing with it
+    int* hist = hist_all[warp];
+    int* sel = sel_all[warp];
+    const int K = win + ctopk;
+    int32_t* out = idx + t * K;
+    const uint16_t* sc = scores + t * n_c;
+    for (int j = lane; j < win; j += 32) out[j] = win_idx[t * win + j];
+    const int64_t vis64 = visible_rows(t, start_pos, ratio, n_c);
+    const int vis = (int)vis64;  // <= TKW_MAX (host plan)
+    const int kk = vis < ctopk ? vis : ctopk;
+    if (vis <= ctopk) {
+        for (int j = lane; j < ctopk; j += 32) out[win + j] = (j < vis) ? (int32_t)(offset + j) : -1;
+        return;
+    }
+    const int kpl = (vis + 31) / 32;
+    const int i0 = kpl * lane;
+    const int n_mine = max(0, min(kpl, vis - i0));
+    uint32_t key[TKW_KPL];
+    const bool vec = (kpl & 7) == 0 && ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0);
+#pragma unroll
+    for (int v = 0; v < TKW_KPL / 8; v++) {
+        const int b0 = i0 + 8 * v;
+        if (8 * v >= n_mine) continue;
+        if (vec && 8 * v + 8 <= n_mine) {  // whole groups of eight only
+            uint4 u = __ldg(reinterpret_cast<const uint4*>(sc + b0));
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&u);
+#pragma unroll
+            for (int e = 0; e < 8; e++) key[8 * v + e] = order_key(h[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                if (8 * v + e < n_mine) key[8 * v + e] = order_key(__ldg(sc + b0 + e));
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; e++) hist[lane + 32 * e] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < TKW_KPL; e++)
+        if (e < n_mine) atomicAdd(&hist[key[e] >> 8], 1);
+    __syncwarp();
+    find_bucket(hist, kk, 0, &sel[0], &sel[1]);
+    __syncwarp();
+    const uint32_t hb = (uint32_t)sel[0];
+    const int above1 = sel[1];
+#pragma unroll
+    for (int e = 0; e < 8; e++) hist[lane + 32 * e] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < TKW_KPL; e++)
+        if (e < n_mine && (key[e] >> 8) == hb) atomicAdd(&hist[key[e] & 0xffu], 1);
+    __syncwarp();
+    find_bucket(hist, kk, above1, &sel[2], &sel[3]);
+    __syncwarp();
+    const uint32_t T = (hb << 8) | (uint32_t)sel[2];
+    const int need_eq = kk - sel[3];
+    int n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int e = 0; e < TKW_KPL; e++) {
+        if (e < n_mine) {
+            n_gt += key[e] > T ? 1 : 0;
+            n_eq += key[e] == T ? 1 : 0;
+        }
+    }
+    int x_gt = n_gt, x_eq = n_eq;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, x_gt, off);
+        const int b = __shfl_up_sync(0xffffffffu, x_eq, off);
+        if (lane >= off) {
+            x_gt += a;
+            x_eq += b;
+        }
+    }
+    int gt = x_gt - n_gt, eq = x_eq - n_eq;
+#pragma unroll
+    for (int e = 0; e < TKW_KPL; e++) {
+        if (e < n_mine) {
+            const bool is_eq = key[e] == T;
+            if (key[e] > T || (is_eq && eq < need_eq))
+                out[win + gt + min(eq, need_eq)] = (int32_t)(offset + i0 + e);
+            gt += key[e] > T ? 1 : 0;
+            eq += is_eq ? 1 : 0;
+        }
+    }
+    for (int j = kk + lane; j < ctopk; j += 32) out[win + j] = -1;
+}
+
+// ---------------------------------------------------------------------------
 struct KeySrc {
     const uint16_t* g;
     const uint16_t* s;
@@ -912,6 +1022,20 @@ int launch_topk(const uint16_t* scores, const int32_t* win_idx, int32_t* idx, in
         na++;
     }
     int rc;
+    // Many queries with rows of 513..1024 scores: a warp per query (shorter
+    // rows gain nothing over one CTA per query).
+    if (n_c > TKW_MAX / 2 && n_c <= TKW_MAX && m * 32 > (int64_t)device_sm_count()) {
+        cfg.gridDim = dim3((unsigned)((m + TKW_WARPS - 1) / TKW_WARPS));
+        cfg.blockDim = dim3(32 * TKW_WARPS);
+        cfg.dynamicSmemBytes = 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = na;
+        rc = cuda_check(cudaLaunchKernelEx(&cfg, topk_warp_kernel, scores, win_idx, idx, m, n_c,
+                                           (int)win, (int)ctopk, ratio, start_pos, offset),
+                        "top-k warp kernel");
+        if (rc) return rc;
+        return launch_check("top-k warp kernel");
+    }
     // Few queries with long rows: a cluster per query splits each row over
     // TK_CL SMs.  Otherwise one CTA per query.
     if (m * TK_CL <= 2 * (int64_t)device_sm_count() && n_c >= 1024 &&
