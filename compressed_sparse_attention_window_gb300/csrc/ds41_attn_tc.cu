@@ -14,9 +14,12 @@
 // Per item a plan warp turns the index row into chunks of 128 rows: for each
 // source (rows_a, rows_b) whose selected rows lie in a compact range the
 // chunks are consecutive rows of that range, loaded by tiled TMA copies, with
-// a 128-bit mask of the selected rows; otherwise the selected rows are listed
-// and fetched by TMA gather4 copies.  Duplicate indices force the list form
-// (each copy then counts once per occurrence, as the definition does).
+// a 128-bit mask of the selected rows; otherwise (or when the range would take
+// more chunks than the rows themselves) the selected rows are listed and
+// gathered by the softmax warps as 16-byte cp.async pieces, which they fetch
+// while the tensor core works through PV of the chunk before.  Duplicate
+// indices force the list form (each copy then counts once per occurrence, as
+// the definition does).
 //
 //   S  = Q R^T       M = 64 heads, N = 128 rows, K = 512  (S in tensor memory)
 //   O^T += R^T P^T   M = 128 of hd (4 tiles), N = 64 heads, K = 128 rows
@@ -37,12 +40,13 @@
 // on peaked softmaxes doubled, with 2^4 it stays within 1.3x of an exact
 // running maximum).
 //
-// Warp roles (384 threads): warp 0 issues TMA copies, warp 1 owns tensor
-// memory and (one lane) issues the MMAs, warp 2 builds the per-item plans one
-// item ahead, warps 4..7 compute the probabilities, warps 8..11 rescale O when
-// a reference moves and write the normalised output of each item (warp 4+q
-// and 8+q use lane quarter q of tensor memory).  The softmax warps never wait
-// for a PV product or for the output stores.  Every hand-off is an mbarrier
+// Warp roles (384 threads): warp 0 issues the TMA copies (Q, consecutive-row
+// chunks), warp 1 owns tensor memory and (one lane) issues the MMAs, warp 2
+// builds the per-item plans one item ahead, warps 4..7 compute the
+// probabilities and gather the listed chunks' rows (warp 4+q block pair q),
+// warps 8..11 rescale the columns of O whose head's reference moved and write
+// the normalised output of each item (warp 4+q and 8+q use lane quarter q of
+// tensor memory).  The softmax warps never wait for the output stores.  Every hand-off is an mbarrier
 // with a bounded wait; a timeout raises DS41_E_TIMEOUT, and each role then
 // drains what it started and exits.
 #include "ds41_internal.cuh"
@@ -62,6 +66,7 @@ constexpr int MAXCH = 2 * DCAP / RC;  // chunks per item: two consecutive-row so
 constexpr int OOB_ROW = 1 << 29;  // a row coordinate beyond every tensor (reads as zero)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 4.0f;
+constexpr int CORR_FEW = 8;        // moved heads rescaled column by column
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t Q_KB = 64 * 64 * 2;                // Q block [64 heads][64 dims]: 8 KiB
@@ -73,8 +78,10 @@ constexpr uint32_t P_OFF = R_OFF + R_BYTES;           // P: 2 blocks of [64 head
 constexpr uint32_t P_BLK = 8192;
 constexpr uint32_t PLAN_OFF = P_OFF + 2 * P_BLK;      // 2 plans
 constexpr uint32_t PLAN_DESC = 0;                     // MAXCH x 2 uint4
-constexpr uint32_t PLAN_LIST = MAXCH * 32;            // MAXK x int32
-constexpr uint32_t PLAN_N = PLAN_LIST + MAXK * 4;     // chunk count
+constexpr uint32_t PLAN_LIST = MAXCH * 32;            // int32 row list
+constexpr uint32_t PLAN_N = PLAN_LIST + (MAXK + RC + 4) * 4;  // chunk count (the list
+                                                      // has room for a 4-aligned start and a
+                                                      // full chunk read past its end)
 constexpr uint32_t PLAN_BYTES = PLAN_N + 64;
 constexpr uint32_t BM_OFF = PLAN_OFF + 2 * PLAN_BYTES;  // 2 sources x DCAP bits
 constexpr uint32_t BM_WORDS = DCAP / 32;
@@ -113,6 +120,8 @@ constexpr uint32_t TM_O = 128;   // O^T tile mt at column 128 + 64 mt
 constexpr uint32_t TM_COLS = 512;
 
 struct Params {
+    const uint16_t* rows_a;  // [n_a][HD]
+    const uint16_t* rows_b;  // [n_c][HD]
     int64_t n_a, n_c;
     const int32_t* idx;
     int K;
@@ -137,6 +146,31 @@ __device__ __forceinline__ void item_of(int j, int m, int hg, int& t, int& g) {
     g = (int)(r % hg);
 }
 
+constexpr uint32_t NEG_INF_BITS = 0xff800000u;
+
+// 2^x by the special function unit, denormal results flushed to zero: a
+// head's denominator is at least 1 (its reference maximum is the maximum of
+// some chunk, whose weight is 1), so a weight below 2^-126 changes nothing.
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// two floats to bf16 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// four 8x8 b16 fragments to shared memory, lane l giving the address of row
+// l % 8 of fragment l / 8
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 __device__ __forceinline__ int warp_sum(int v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -151,6 +185,49 @@ __device__ __forceinline__ int warp_max(int v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
+}
+
+// ---------------------------------------------------------------------------
+// Block pair kp of a listed chunk (descriptor d, d1 of the plan), fetched by
+// one warp as 16-byte cp.async pieces into the row blocks' 128-byte swizzled
+// layout (the layout the tiled copies produce); rows past the list are zero.
+// Lane l copies piece l % 16 of rows 64 (l / 16) .. 64 (l / 16) + 63, so each
+// instruction reads two 256-byte row segments.  Returns once the pieces have
+// landed and a proxy fence has made them visible to the tensor core.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ void gather_pair(const Params& p, const uint8_t* plan, uint4 d, uint4 d1, int kp,
+                            uint32_t sbase, int lane) {
+    const int* list = reinterpret_cast<const int*>(plan + PLAN_LIST) + (d.x & 0x3FFFFFFFu);
+    const int cnt = __popc(d.y) + __popc(d.z) + __popc(d.w) + __popc(d1.x);
+    const uint16_t* src = ((d.x >> 30) & 1u) ? p.rows_b : p.rows_a;
+    const int c = lane & 15;                  // 16-byte piece of the pair's 256 bytes
+    const int blk = 2 * kp + (c >> 3);        // 64-column block
+    const int cc = c & 7;                     // 16-byte column within the block
+    const uint16_t* col = src + blk * 64 + cc * 8;
+    const uint32_t dst0 = sbase + R_OFF + blk * R_KB;
+    const int r0 = 64 * (lane >> 4);
+#pragma unroll 4
+    for (int m4 = 0; m4 < 64; m4 += 4) {
+        const int r = r0 + m4;
+        const int4 rows = *reinterpret_cast<const int4*>(list + r);  // list has RC slack entries
+        const int rr[4] = {rows.x, rows.y, rows.z, rows.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int rk = r + k;
+            const uint32_t dst = dst0 + rk * 128 + ((cc ^ (rk & 7)) << 4);
+            if (rk < cnt)
+                cp_async16(dst, col + (int64_t)rr[k] * HD);
+            else
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(dst), "r"(0u)
+                             : "memory");
+        }
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -199,7 +276,9 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
         mn[s] = warp_min(mn[s]);
         mx[s] = warp_max(mx[s]);
         range[s] = cnt[s] ? mx[s] - mn[s] + 1 : 0;
-        dense[s] = cnt[s] > 0 && range[s] <= DCAP && range[s] <= 2 * cnt[s] + RC;
+        // consecutive rows where they take no more chunks than the list
+        dense[s] = cnt[s] > 0 && range[s] <= DCAP &&
+                   (range[s] + RC - 1) / RC <= (cnt[s] + RC - 1) / RC;
         if (dense[s]) {
             const int nw = 4 * ((range[s] + RC - 1) / RC);
             for (int w = lane; w < nw; w += 32) bm[s * BM_WORDS + w] = 0u;
@@ -229,6 +308,7 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
 #pragma unroll
     for (int s = 0; s < 2; s++) {
         if (dense[s] || cnt[s] == 0) continue;
+        pos = (pos + 3) & ~3;  // a listed chunk's rows start 16-byte aligned
         off[s] = pos;
 #pragma unroll
         for (int k = 0; k < KPL; k++) {
@@ -293,9 +373,8 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
 __global__ void __launch_bounds__(THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_ad,
-                   const __grid_constant__ CUtensorMap map_ag,
                    const __grid_constant__ CUtensorMap map_bd,
-                   const __grid_constant__ CUtensorMap map_bg, const Params p) {
+                   const Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -358,7 +437,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------------
         if (lane == 0) {
             uint32_t g = 0;
-            uint32_t q_armed = 0, r_armed[NKP] = {0, 0, 0, 0};
+            uint32_t q_armed = 0;
             for (int j = 0; j < ntok; j++) {
                 int t, hgi;
                 item_of(j, p.m, hg, t, hgi);
@@ -372,53 +451,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_load_2d(sbase + Q_OFF + kb * Q_KB, &map_q, kb * 64, qrow, &bars[B_QFULL]);
                 const uint8_t* plan = sm + PLAN_OFF + slot * PLAN_BYTES;
                 const uint4* desc = reinterpret_cast<const uint4*>(plan + PLAN_DESC);
-                const int* list = reinterpret_cast<const int*>(plan + PLAN_LIST);
                 const int nch = *reinterpret_cast<const int*>(plan + PLAN_N);
                 bool ok = true;
                 for (int i = 0; i < nch && ok; i++, g++) {
                     const uint4 d = desc[2 * i];
-                    const uint4 d1 = desc[2 * i + 1];
+                    // a listed chunk's rows are gathered by the softmax warps
+                    if (d.x & 0x80000000u) continue;
                     const int pos = (int)(d.x & 0x3FFFFFFFu);
                     const bool src_b = (d.x >> 30) & 1u;
-                    const bool listed = (d.x & 0x80000000u) != 0u;
-                    const int cnt = __popc(d.y) + __popc(d.z) + __popc(d.w) + __popc(d1.x);
-                    const int* lr = list + pos;
+                    const CUtensorMap* mp = src_b ? &map_bd : &map_ad;
                     for (int kp = 0; kp < NKP; kp++) {
                         if (g >= 1 && !wait_bar(&bars[B_REMPTY + kp], (g - 1) & 1, abort_f, p.status)) {
                             ok = false;
                             break;
                         }
                         mbar_arrive_expect_tx(&bars[B_RFULL + kp], 2 * R_KB);
-                        r_armed[kp]++;
                         const uint32_t rb = sbase + R_OFF + 2 * kp * R_KB;
-                        if (!listed) {
-                            const CUtensorMap* mp = src_b ? &map_bd : &map_ad;
-                            for (int kb = 0; kb < 2; kb++)
-                                tma_load_2d(rb + kb * R_KB, mp, (2 * kp + kb) * 64, pos,
-                                            &bars[B_RFULL + kp]);
-                        } else {
-                            const CUtensorMap* mp = src_b ? &map_bg : &map_ag;
-                            for (int gq = 0; gq < RC / 4; gq++) {
-                                int y[4];
-#pragma unroll
-                                for (int k = 0; k < 4; k++) {
-                                    const int r = 4 * gq + k;
-                                    y[k] = r < cnt ? lr[r] : OOB_ROW;  // beyond the list: zero fill
-                                }
-                                for (int kb = 0; kb < 2; kb++)
-                                    tma_gather4(rb + kb * R_KB + gq * 512, mp, (2 * kp + kb) * 64,
-                                                y[0], y[1], y[2], y[3], &bars[B_RFULL + kp]);
-                            }
-                        }
+                        for (int kb = 0; kb < 2; kb++)
+                            tma_load_2d(rb + kb * R_KB, mp, (2 * kp + kb) * 64, pos,
+                                        &bars[B_RFULL + kp]);
                     }
                 }
                 if (!ok) break;
                 mbar_arrive(&bars[B_PLANEMPTY + slot]);
             }
-            // let every copy this CTA started land before the CTA exits
+            // let every copy this CTA started land before the CTA exits: the
+            // last chunk's block pairs land after every earlier chunk's (a pair
+            // is loaded only once the PV of the chunk before has read it)
             if (q_armed) wait_bar(&bars[B_QFULL], (q_armed - 1) & 1, abort_f, p.status);
-            for (int kp = 0; kp < NKP; kp++)
-                if (r_armed[kp]) wait_bar(&bars[B_RFULL + kp], (r_armed[kp] - 1) & 1, abort_f, p.status);
+            if (g >= 1)
+                for (int kp = 0; kp < NKP; kp++)
+                    wait_bar(&bars[B_RFULL + kp], (g - 1) & 1, abort_f, p.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
@@ -550,9 +613,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp - 4;
         const int qi = lane & 3;
         const int hA = 16 * q + (lane >> 2), hB = hA + 8;
+        // |scale| in log2 units, at least 1e-30 so that a zero scale keeps
+        // -inf (an unselected row) at -inf: its logits become s * 1e-30,
+        // which is 0 in float arithmetic for every finite bf16 score product
+        const bool neg = p.scale_log2 < 0.0f;
+        const float sc = fmaxf(fabsf(p.scale_log2), 1e-30f);
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t g = 0;
-        for (int j = 0; j < ntok; j++) {
+        // Softmax warp q also gathers block pair q of every listed chunk (the
+        // tensor-memory lane quarter and the pair share the index): the first
+        // chunk here, every later one once PV of the chunk before it has
+        // released the pair, which is when this warp has nothing else to do.
+        bool start_ok = true;
+        if (ntok > 0) {
+            start_ok = wait_bar(&bars[B_PLANFULL], 0, abort_f, p.status);
+            const uint4* d0s = reinterpret_cast<const uint4*>(sm + PLAN_OFF + PLAN_DESC);
+            if (start_ok && (d0s[0].x & 0x80000000u)) {
+                gather_pair(p, sm + PLAN_OFF, d0s[0], d0s[1], q, sbase, lane);
+                if (lane == 0) mbar_arrive(&bars[B_RFULL + q]);
+            }
+        }
+        for (int j = 0; j < ntok && start_ok; j++) {
             int t, hgi;
             item_of(j, p.m, hg, t, hgi);
             const int slot = j & 1;
@@ -582,68 +663,92 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_SEMPTY]);
-                // scaled scores (log2 units), -inf where the row is not selected:
-                // register 4 jr + e (+2) holds column 8 jr + 2 qi + e, jr = 0..15
-                const uint32_t mw[4] = {d0.y >> (2 * qi), d0.z >> (2 * qi), d0.w >> (2 * qi),
-                                        m3 >> (2 * qi)};
+                // raw scores, -inf where the row is not selected (a chunk with
+                // every row selected skips the masking): register 4 jr + e (+2)
+                // holds column 8 jr + 2 qi + e, jr = 0..15.  With a negative
+                // scale the scores change sign so that sc = |scale log2 e|.
+                if (neg) {
+#pragma unroll
+                    for (int k = 0; k < 64; k++) sr[k] ^= 0x80000000u;
+                }
+                if ((d0.y & d0.z & d0.w & m3) != 0xffffffffu) {
+                    const uint32_t mw[4] = {d0.y >> (2 * qi), d0.z >> (2 * qi),
+                                            d0.w >> (2 * qi), m3 >> (2 * qi)};
+#pragma unroll
+                    for (int jr = 0; jr < 16; jr++) {
+#pragma unroll
+                        for (int e = 0; e < 2; e++) {
+                            const bool sel = (mw[jr >> 2] >> (8 * (jr & 3) + e)) & 1u;
+                            if (!sel) {
+                                sr[4 * jr + e] = NEG_INF_BITS;
+                                sr[4 * jr + 2 + e] = NEG_INF_BITS;
+                            }
+                        }
+                    }
+                }
                 float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
                 for (int jr = 0; jr < 16; jr++) {
-#pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        const bool sel = (mw[jr >> 2] >> (8 * (jr & 3) + e)) & 1u;
-                        const float xa = sel ? __uint_as_float(sr[4 * jr + e]) * p.scale_log2 : -INFINITY;
-                        const float xb =
-                            sel ? __uint_as_float(sr[4 * jr + 2 + e]) * p.scale_log2 : -INFINITY;
-                        sr[4 * jr + e] = __float_as_uint(xa);
-                        sr[4 * jr + 2 + e] = __float_as_uint(xb);
-                        mxA = fmaxf(mxA, xa);
-                        mxB = fmaxf(mxB, xb);
-                    }
+                    mxA = fmaxf(mxA, fmaxf(__uint_as_float(sr[4 * jr]), __uint_as_float(sr[4 * jr + 1])));
+                    mxB = fmaxf(mxB, fmaxf(__uint_as_float(sr[4 * jr + 2]), __uint_as_float(sr[4 * jr + 3])));
                 }
                 mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
                 mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
                 mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
                 mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+                // chunk maxima in log2 units (sc > 0, so -inf stays -inf)
+                mxA *= sc;
+                mxB *= sc;
                 float cA = 1.0f, cB = 1.0f;
                 if (i == 0) {
                     mA = mxA;
                     mB = mxB;
                 } else {
                     if (mxA > mA + RESCALE_LOG2) {
-                        cA = exp2f(mA - mxA);
+                        cA = ex2_ftz(mA - mxA);
                         mA = mxA;
                         lA *= cA;
                     }
                     if (mxB > mB + RESCALE_LOG2) {
-                        cB = exp2f(mB - mxB);
+                        cB = ex2_ftz(mB - mxB);
                         mB = mxB;
                         lB *= cB;
                     }
                 }
-                // hand the rescale factors of this chunk to the correction warps
-                const bool moved = __any_sync(0xffffffffu, cA != 1.0f || cB != 1.0f);
+                // hand the rescale factors of this chunk to the correction warps,
+                // with the mask of this warp's heads that moved (bit r: head
+                // 16 q + r; the four lanes of a quad agree, so lane 4 r speaks
+                // for heads hA and hB of quad r)
+                const uint32_t mvA = __ballot_sync(0xffffffffu, cA != 1.0f);
+                const uint32_t mvB = __ballot_sync(0xffffffffu, cB != 1.0f);
                 if (qi == 0) {
                     corr_s[hA] = cA;
                     corr_s[hB] = cB;
                 }
-                if (lane == 0) flags[q] = moved ? 1 : 0;
+                if (lane == 0) {
+                    uint32_t m16 = 0;
+#pragma unroll
+                    for (int r = 0; r < 8; r++)
+                        m16 |= (((mvA >> (4 * r)) & 1u) << r) | (((mvB >> (4 * r)) & 1u) << (8 + r));
+                    flags[q] = (int)m16;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_CORR]);
-                // probabilities, the denominator, P (bf16) for the PV MMA
-                const float muA = (mA == -INFINITY) ? 0.0f : mA;
-                const float muB = (mB == -INFINITY) ? 0.0f : mB;
+                // probabilities 2^(sc s - m), the denominator, P (bf16) for the
+                // PV MMA; an unselected row (-inf) gives 0
+                const float nmA = (mA == -INFINITY) ? 0.0f : -mA;
+                const float nmB = (mB == -INFINITY) ? 0.0f : -mB;
                 uint32_t pkA[16], pkB[16];
 #pragma unroll
                 for (int jr = 0; jr < 16; jr++) {
-                    const float a0 = exp2f(__uint_as_float(sr[4 * jr]) - muA);
-                    const float a1 = exp2f(__uint_as_float(sr[4 * jr + 1]) - muA);
-                    const float b0 = exp2f(__uint_as_float(sr[4 * jr + 2]) - muB);
-                    const float b1 = exp2f(__uint_as_float(sr[4 * jr + 3]) - muB);
+                    const float a0 = ex2_ftz(fmaf(__uint_as_float(sr[4 * jr]), sc, nmA));
+                    const float a1 = ex2_ftz(fmaf(__uint_as_float(sr[4 * jr + 1]), sc, nmA));
+                    const float b0 = ex2_ftz(fmaf(__uint_as_float(sr[4 * jr + 2]), sc, nmB));
+                    const float b1 = ex2_ftz(fmaf(__uint_as_float(sr[4 * jr + 3]), sc, nmB));
                     lA += a0 + a1;
                     lB += b0 + b1;
-                    pkA[jr] = pack_bf16x2(a0, a1);
-                    pkB[jr] = pack_bf16x2(b0, b1);
+                    pkA[jr] = pack_bf16x2_rn(a0, a1);
+                    pkB[jr] = pack_bf16x2_rn(b0, b1);
                 }
                 // P is free once PV(g - 1) is done
                 if (g >= 1 && !wait_bar(&bars[B_DONE], (g - 1) & 1, abort_f, p.status)) {
@@ -652,20 +757,50 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 {
                     // row h of P block k: 8 chunks of 16 bytes (8 rows each),
-                    // swizzled by h % 8; this thread writes 4 bytes of each
+                    // swizzled by h % 8.  The registers of column block jr are
+                    // the 8x8 fragments (heads 16 q .. 16 q + 7 | + 8 .. + 15,
+                    // columns 8 jr ..): four fragments per stmatrix, lane l
+                    // giving the address of row l % 8 of fragment l / 8.
+                    const int fr = lane >> 3;                 // fragment of this lane's address
+                    const int h = 16 * q + 8 * (fr & 1) + (lane & 7);
+                    const uint32_t rowa = sbase + P_OFF + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll
-                    for (int jr = 0; jr < 16; jr++) {
-                        uint8_t* pb = sm + P_OFF + (jr >> 3) * P_BLK;
-                        const int c = jr & 7;
-                        *reinterpret_cast<uint32_t*>(pb + (hA >> 3) * 1024 + (hA & 7) * 128 +
-                                                     ((c ^ (hA & 7)) << 4) + 4 * qi) = pkA[jr];
-                        *reinterpret_cast<uint32_t*>(pb + (hB >> 3) * 1024 + (hB & 7) * 128 +
-                                                     ((c ^ (hB & 7)) << 4) + 4 * qi) = pkB[jr];
+                    for (int jp = 0; jp < 8; jp++) {
+                        const int jr = 2 * jp + (fr >> 1);
+                        const uint32_t addr = rowa + (jr >> 3) * P_BLK + (((jr & 7) ^ (h & 7)) << 4);
+                        stmatrix_x4(addr, pkA[2 * jp], pkB[2 * jp], pkA[2 * jp + 1], pkB[2 * jp + 1]);
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_PFULL]);
+                // the next chunk (of this item or the next), if its rows are listed
+                const uint8_t* nplan = plan;
+                int ni = i + 1;
+                if (ni == nch) {
+                    ni = -1;
+                    if (j + 1 < ntok) {
+                        const int ns = (j + 1) & 1;
+                        if (!wait_bar(&bars[B_PLANFULL + ns], ((j + 1) >> 1) & 1, abort_f, p.status)) {
+                            bad = true;
+                            break;
+                        }
+                        nplan = sm + PLAN_OFF + ns * PLAN_BYTES;
+                        ni = 0;
+                    }
+                }
+                if (ni >= 0) {
+                    const uint4* nd = reinterpret_cast<const uint4*>(nplan + PLAN_DESC);
+                    const uint4 dn = nd[2 * ni];
+                    if (dn.x & 0x80000000u) {
+                        if (!wait_bar(&bars[B_REMPTY + q], g & 1, abort_f, p.status)) {
+                            bad = true;
+                            break;
+                        }
+                        gather_pair(p, nplan, dn, nd[2 * ni + 1], q, sbase, lane);
+                        if (lane == 0) mbar_arrive(&bars[B_RFULL + q]);
+                    }
+                }
             }
             if (bad) break;
             // ---- normalisers of this item for the correction warps ----
@@ -714,26 +849,70 @@ __global__ void __launch_bounds__(THREADS, 1)
                     bad = true;
                     break;
                 }
-                const int moved = flags[0] | flags[1] | flags[2] | flags[3];
-                if (moved) {
+                // heads whose reference moved (head h is column h of every O^T
+                // tile): a few are rescaled column by column, more in groups of
+                // 16 columns (the heads of one softmax warp)
+                const uint32_t f0 = (uint32_t)flags[0], f1 = (uint32_t)flags[1];
+                const uint32_t f2 = (uint32_t)flags[2], f3 = (uint32_t)flags[3];
+                const uint64_t mv = (uint64_t)(f0 | (f1 << 16)) | ((uint64_t)(f2 | (f3 << 16)) << 32);
+                const int nmv = __popcll(mv);
+                if (nmv) {
                     // O^T holds the chunks before this one once PV(g-1) is done
                     if (!wait_bar(&bars[B_DONE], (g - 1) & 1, abort_f, p.status)) {
                         bad = true;
                         break;
                     }
                     tc_fence_after();
+                    const uint32_t ta = tmem + lane_off + TM_O;
+                    if (nmv <= CORR_FEW) {
+                        uint32_t hv[CORR_FEW][4];
+                        int hs[CORR_FEW];
+                        uint64_t rest = mv;
+#pragma unroll
+                        for (int k = 0; k < CORR_FEW; k++) {
+                            hs[k] = __ffsll((long long)rest) - 1;  // -1 once none are left
+                            rest &= rest - 1;
+                            if (k < nmv) {
+#pragma unroll
+                                for (int mt = 0; mt < 4; mt++) tc_ld1(ta + 64 * mt + hs[k], hv[k][mt]);
+                            }
+                        }
+                        tc_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < CORR_FEW; k++) {
+                            if (k < nmv) {
+                                const float c = corr_s[hs[k]];
+#pragma unroll
+                                for (int mt = 0; mt < 4; mt++) {
+                                    hv[k][mt] = __float_as_uint(__uint_as_float(hv[k][mt]) * c);
+                                    tc_st1(ta + 64 * mt + hs[k], hv[k][mt]);
+                                }
+                            }
+                        }
+                    } else {
 #pragma unroll 1
-                    for (int mt = 0; mt < 4; mt++) {
-#pragma unroll 1
-                        for (int hh = 0; hh < 2; hh++) {
-                            uint32_t ov[32];
-                            const uint32_t ta = tmem + lane_off + TM_O + 64 * mt + 32 * hh;
-                            tc_ld32(ta, ov);
+                        for (int w = 0; w < 4; w++) {
+                            if (!((mv >> (16 * w)) & 0xffffu)) continue;
+                            float c[16];
+#pragma unroll
+                            for (int k = 0; k < 16; k += 4) {
+                                const float4 v = *reinterpret_cast<const float4*>(corr_s + 16 * w + k);
+                                c[k] = v.x;
+                                c[k + 1] = v.y;
+                                c[k + 2] = v.z;
+                                c[k + 3] = v.w;
+                            }
+                            uint32_t ov[4][16];
+#pragma unroll
+                            for (int mt = 0; mt < 4; mt++) tc_ld16(ta + 64 * mt + 16 * w, ov[mt]);
                             tc_wait_ld();
 #pragma unroll
-                            for (int k = 0; k < 32; k++)
-                                ov[k] = __float_as_uint(__uint_as_float(ov[k]) * corr_s[32 * hh + k]);
-                            tc_st32(ta, ov);
+                            for (int mt = 0; mt < 4; mt++) {
+#pragma unroll
+                                for (int k = 0; k < 16; k++)
+                                    ov[mt][k] = __float_as_uint(__uint_as_float(ov[mt][k]) * c[k]);
+                                tc_st16(ta + 64 * mt + 16 * w, ov[mt]);
+                            }
                         }
                     }
                     tc_wait_st();
@@ -803,12 +982,10 @@ int attn_tc_launch(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int rc = get_encode(&enc);
     if (rc) return rc;
-    CUtensorMap mq, mad, mag, mbd, mbg;
+    CUtensorMap mq, mad, mbd;
     if ((rc = make_map_bf16(enc, &mq, q, m * nh, HD, 64, 64))) return rc;
     if ((rc = make_map_bf16(enc, &mad, rows_a, n_a, HD, 64, RC))) return rc;
-    if ((rc = make_map_bf16(enc, &mag, rows_a, n_a, HD, 64, 1))) return rc;
     if ((rc = make_map_bf16(enc, &mbd, rows_b, n_c, HD, 64, RC))) return rc;
-    if ((rc = make_map_bf16(enc, &mbg, rows_b, n_c, HD, 64, 1))) return rc;
     Params p;
     p.n_a = n_a;
     p.n_c = n_c;
@@ -817,6 +994,8 @@ int attn_tc_launch(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const
     p.nh = (int)nh;
     p.m = (int)m;
     p.scale_log2 = scale * LOG2E;
+    p.rows_a = rows_a;
+    p.rows_b = rows_b;
     p.sink = sink;
     p.o = o;
     p.lse = lse;
@@ -828,7 +1007,7 @@ int attn_tc_launch(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const
                                          (int)SMEM_BYTES),
                     "ds41_sparse_attn_sink_fwd: tensor-core kernel attributes");
     if (rc) return rc;
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(mq, mad, mag, mbd, mbg, p);
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(mq, mad, mbd, p);
     return launch_check("ds41_sparse_attn_sink_fwd: tensor-core kernel");
 }
 

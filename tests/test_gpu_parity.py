@@ -268,18 +268,25 @@ def test_sparse_attn_few_token_paths(orc, K, m, nh):
 def _tc_index_rows(m, n_a, n_c, K, rng):
     """Index rows that exercise every chunk form of the many-token kernel:
     compact ranges of both sources (consecutive-row chunks with masks),
-    scattered rows (listed rows), repeated rows, rows with no or one valid
-    index, and padding with -1."""
+    scattered rows and sparse ranges (listed rows), repeated rows, rows with
+    no or one valid index, and padding with -1."""
     idx = np.full((m, K), -1, np.int32)
     for t in range(m):
-        kind = t % 5
-        if kind == 0:   # a window-like run of rows_a + half of a range of rows_b
+        kind = t % 6
+        if kind == 0:   # a window-like run of rows_a + most of a range of rows_b,
+            #             the range rounded up to whole 128-row chunks (kept as
+            #             consecutive-row chunks with holes in their masks)
             w = min(K // 3, n_a)
             a0 = rng.integers(0, n_a - w + 1)
             nb = min(K - w, n_c // 2)
-            b0 = rng.integers(0, n_c - 2 * nb + 1)
-            picks = b0 + rng.permutation(2 * nb)[:nb]
+            span = min(-(-nb // 128) * 128, n_c)
+            b0 = rng.integers(0, n_c - span + 1)
+            picks = b0 + rng.permutation(span)[:nb]
             row = np.concatenate([np.arange(a0, a0 + w), n_a + picks])
+        elif kind == 5:  # half of a range of rows_b: listed rows (fewer chunks)
+            nb = min(K, n_c // 2)
+            b0 = rng.integers(0, n_c - 2 * nb + 1)
+            row = n_a + b0 + rng.permutation(2 * nb)[:nb]
         elif kind == 1:  # scattered over everything
             row = rng.permutation(n_a + n_c)[:K]
         elif kind == 2:  # a compact range with repeated rows
@@ -303,14 +310,17 @@ def _tc_index_rows(m, n_a, n_c, K, rng):
     return idx
 
 
-@pytest.mark.parametrize("K,nh,sink_kind", [(37, 64, "normal"), (640, 64, "normal"),
-                                            (640, 64, "minus_inf"), (640, 128, "large"),
-                                            (1000, 64, "normal")])
-def test_sparse_attn_many_tokens_tensor_core_path(orc, K, nh, sink_kind):
+@pytest.mark.parametrize("K,nh,sink_kind,sm", [(37, 64, "normal", 1.0), (640, 64, "normal", 1.0),
+                                               (640, 64, "minus_inf", 1.0), (640, 128, "large", 1.0),
+                                               (1000, 64, "normal", 1.0), (640, 64, "normal", -1.0),
+                                               (300, 64, "normal", 0.0)])
+def test_sparse_attn_many_tokens_tensor_core_path(orc, K, nh, sink_kind, sm):
     """Enough tokens for one work item per SM (hd 512, 64-head groups, K <=
     1024) take the persistent tcgen05 kernel; every token against the oracle.
     A third of the compressed rows are scaled x3 so that later chunks beat the
-    running maximum by far (the rescale of O in tensor memory)."""
+    running maximum by far (the rescale of O in tensor memory).  The scale is
+    head_dim^-0.5 times sm: a negative scale flips which rows weigh most, and
+    a zero scale weighs every selected row alike."""
     hd = 512
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     m = sms + 13
@@ -328,10 +338,11 @@ def test_sparse_attn_many_tokens_tensor_core_path(orc, K, nh, sink_kind):
         sink *= 30
     idx = _tc_index_rows(m, n_a, n_c, K, np.random.default_rng(K * 3 + nh))
     lse = torch.empty(m, nh, device="cuda")
+    scale = float(np.float32(hd ** -0.5 * sm))
     o = ds41.sparse_attn_sink_fwd(q.cuda(), rows_a.cuda(), rows_b.cuda(),
-                                  torch.from_numpy(idx).cuda(), sink.cuda(), hd ** -0.5, lse=lse)
+                                  torch.from_numpy(idx).cuda(), sink.cuda(), scale, lse=lse)
     oo, olse, bad = orc.sparse_attn(bf16_bits(q), bf16_bits(rows_a), bf16_bits(rows_b), idx,
-                                    sink.numpy(), np.float32(hd ** -0.5))
+                                    sink.numpy(), np.float32(scale))
     assert bad == 0
     assert ds41.device_status() == 0
     ok, err, worst = attn_close(o.float().cpu().numpy(), oo)
