@@ -87,6 +87,8 @@ def _sig(lib):
     s("ds41o_topk_merge", None, _P, _P, _P, _I64, _P, _I64, _I64, _I64, _I64, _I64, _I64)
     s("ds41o_sparse_attn", _I64, _P, _P, _I64, _P, _I64, _P, _I64, _P, _F, _P, _P, _I64, _I64,
       _P, _I64)
+    s("ds41o_attn_out_proj", None, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+      _I64, _P, _I64)
     for n in ("ds41o_to_e2m1_rne_array", "ds41o_f32_to_bf16_array", "ds41o_f32_to_e4m3_array",
               "ds41o_e4m3_to_f32_array", "ds41o_pow2_ceil_array"):
         s(n, None, _P, _P, _I64)
@@ -320,6 +322,29 @@ def sparse_attn(q: np.ndarray, rows_a: np.ndarray, rows_b: Optional[np.ndarray],
                                   _ptr(_c(sink, np.float32)), float(scale), _ptr(o), _ptr(lse),
                                   nh, hd, _ptr(tk), tk.size)
     return o, lse, int(bad)
+
+
+def attn_out_proj(o: np.ndarray, fc: np.ndarray, wo_a: np.ndarray, wo_b: np.ndarray, rd: int,
+                  groups: int, start_pos: int, tokens: Optional[Sequence[int]] = None):
+    """Reading of the output side of ``attention_any`` (compress.rs): inverse
+    RoPE of o at each token's position, the grouped wo_a projection rounded to
+    bf16, then ``linear_bf16`` with wo_b.  o [m,nh,hd] bf16 bits, wo_a
+    [groups*o_rank, nh*hd/groups] and wo_b [dim, groups*o_rank] bf16 bits.
+    Returns (og bf16 bits [nt, groups*o_rank], out f64 [nt, dim])."""
+    oo = _c(o, np.uint16)
+    m, nh, hd = oo.shape
+    wa = _c(wo_a, np.uint16)
+    wb = _c(wo_b, np.uint16)
+    gr, gw = wa.shape
+    dim = wb.shape[0]
+    assert nh * hd == groups * gw and gr % groups == 0 and wb.shape[1] == gr
+    tk = _c(range(m) if tokens is None else tokens, np.int64)
+    og = np.empty((tk.size, gr), np.uint16)
+    out = np.empty((tk.size, dim), np.float64)
+    lib().ds41o_attn_out_proj(_ptr(oo), _ptr(_c(fc, np.float32)), _ptr(wa), _ptr(wb), _ptr(og),
+                              _ptr(out), nh, hd, rd, groups, gr // groups, dim, start_pos, _ptr(tk),
+                              tk.size)
+    return og, out
 
 
 def num_threads() -> int:

@@ -541,6 +541,55 @@ int64_t ds41o_sparse_attn(const uint16_t* q, const uint16_t* rows_a, int64_t n_a
     return bad;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Output side of the layer.  [compress] attention_any, after sparse_attn:    */
+/* o is rotated back (apply_rotary with inverse = true at each head's token   */
+/* position), split into `groups` groups of gw = nh*hd/groups values, and     */
+/* each group is projected by its own o_rank rows of wo_a, every result       */
+/* rounded to bf16 (to_bf16_rne); the groups*o_rank values then go through    */
+/* linear_bf16 with wo_b, [dim, groups*o_rank].  linear_bf16's body is not    */
+/* printed: reading, out = og . wo_b^T with no rounding of the result.        */
+/* Here the dot products are accumulated in f64; og is rounded to f32 and     */
+/* then to bf16 (the pages round an f32 sum).  o is the attention output as   */
+/* given ([n_tokens][nh*hd] bf16 bits, token tokens[i] at position            */
+/* start_pos + tokens[i]); og is [n_tokens][groups*o_rank] bf16 bits and out  */
+/* [n_tokens][dim].                                                           */
+/* ------------------------------------------------------------------------- */
+void ds41o_attn_out_proj(const uint16_t* o, const float* fc, const uint16_t* wo_a,
+                         const uint16_t* wo_b, uint16_t* og, double* out, int64_t nh, int64_t hd,
+                         int64_t rd, int64_t groups, int64_t o_rank, int64_t dim,
+                         int64_t start_pos, const int64_t* tokens, int64_t n_tokens) {
+    const int64_t gw = nh * hd / groups, gr = groups * o_rank;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t ti = 0; ti < n_tokens; ti++) {
+        const int64_t t = tokens[ti];
+        float* x = (float*)malloc(sizeof(float) * (size_t)(nh * hd));
+        int64_t* hp = (int64_t*)malloc(sizeof(int64_t) * (size_t)nh);
+        for (int64_t i = 0; i < nh * hd; i++) x[i] = ds41o_bf16_to_f32(o[t * nh * hd + i]);
+        for (int64_t h = 0; h < nh; h++) hp[h] = start_pos + t;
+        ds41o_apply_rotary(x, nh, hd, rd, hp, fc, 1);
+        uint16_t* gv = og + ti * gr;
+        for (int64_t g = 0; g < groups; g++) {
+            const float* xg = x + g * gw;
+            for (int64_t r = 0; r < o_rank; r++) {
+                const uint16_t* wr = wo_a + (g * o_rank + r) * gw;
+                double acc = 0.0;
+                for (int64_t i = 0; i < gw; i++) acc += (double)xg[i] * (double)ds41o_bf16_to_f32(wr[i]);
+                gv[g * o_rank + r] = ds41o_f32_to_bf16_rne((float)acc);
+            }
+        }
+        for (int64_t j = 0; j < dim; j++) {
+            const uint16_t* wr = wo_b + j * gr;
+            double acc = 0.0;
+            for (int64_t k = 0; k < gr; k++)
+                acc += (double)ds41o_bf16_to_f32(gv[k]) * (double)ds41o_bf16_to_f32(wr[k]);
+            out[ti * dim + j] = acc;
+        }
+        free(x);
+        free(hp);
+    }
+}
+
 /* Number of threads OpenMP will use (1 without OpenMP). */
 int ds41o_num_threads(void) {
 #ifdef _OPENMP

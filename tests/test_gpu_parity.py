@@ -438,6 +438,33 @@ def test_csa_forward_matches_oracle_and_the_four_calls(orc, wl):
     assert ok, (wl.name, err, worst)
 
 
+@pytest.mark.parametrize("name", ["decode", "long_decode", "tiny_prefill", "chunked_prefill", "prefill"])
+def test_csa_forward_graph_replay_matches_eager(name):
+    """The whole step captured as one CUDA graph (the form the benchmark
+    replays, launches chained by programmatic dependent launch) gives bit for
+    bit the outputs and the layer state of the same step run eagerly."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    fc = ds41.yarn_freqs_cis(wl.rd, max(wl.max_pos, 1))
+    dev_e = to_dev(inp)
+    out_e = ds41.csa_forward(dev_e, wl, fc)
+    out_g = {}
+    ds41.csa_forward(to_dev(inp), wl, fc, out_g)  # allocates the outputs outside the capture
+    dev_g = to_dev(inp)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ds41.csa_forward(dev_g, wl, fc, out_g)
+    for k in ("o", "idx"):
+        out_g[k].fill_(0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert ds41.device_status() == 0
+    assert torch.equal(dev_g["ring"], dev_e["ring"]) and torch.equal(dev_g["cache"], dev_e["cache"])
+    assert torch.equal(out_g["idx"], out_e["idx"])
+    assert torch.equal(out_g["o"], out_e["o"])
+
+
 @pytest.mark.parametrize("wl", [WORKLOADS["decode"], WORKLOADS["tiny_prefill"],
                                 TINY_PREFILL.replace(m=3, start_pos=37), CHUNKED.replace(m=2, start_pos=70000)],
                          ids=lambda w: f"{w.name}-{w.m}-{w.start_pos}")
