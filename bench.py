@@ -39,7 +39,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from compressed_sparse_attention_window_gb300 import ds41  # noqa: E402
-from compressed_sparse_attention_window_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+from compressed_sparse_attention_window_gb300.workloads import (OUT_PROJ, WORKLOADS, make_inputs,  # noqa: E402
+                                                                 make_out_proj_weights)
 
 METRIC = "query-tokens/s of compressed sparse attn fwd (decode, prefill); % HBM/TC roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -348,6 +349,55 @@ def time_ops(wl, slots, fc, stream, reps=5):
     return res
 
 
+def time_out_proj(wl, slots, fc, stream, hbm, bf16, reps=5):
+    """The output side of the layer (inverse RoPE, grouped wo_a, wo_b; not part
+    of the step) on the step's attention output: milliseconds per call from a
+    CUDA graph of back-to-back calls, and its roofline.  The weights (176 MiB
+    at the sizes below) exceed L2, so every call streams them from HBM."""
+    P = OUT_PROJ
+    dev = slots[0][1]["o"].device
+    w = make_out_proj_weights(wl.nh, wl.hd, P["groups"], P["o_rank"], P["dim"], device="cpu")
+    wa, wb = w["wo_a"].to(dev), w["wo_b"].to(dev)
+    o = slots[0][1]["o"]
+    og = torch.empty(wl.m, wa.shape[0], dtype=torch.bfloat16, device=dev)
+    out = torch.empty(wl.m, P["dim"], dtype=torch.float32, device=dev)
+
+    def call():
+        ds41.attn_out_proj(o, fc, wa, wb, wl.rd, P["groups"], wl.start_pos, og=og, out=out)
+
+    with torch.cuda.stream(stream):
+        call()  # warm-up outside the capture (library handle, kernel attributes)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(4):
+                call()
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * 4)
+    del g
+    gr, gw = wa.shape
+    flops = 2.0 * wl.m * (wl.nh * wl.hd * P["o_rank"] + gr * P["dim"])
+    nbytes = 2.0 * (wa.numel() + wb.numel()) + wl.m * (2.0 * gr * 2 + 4.0 * P["dim"]
+                                                        + 2.0 * wl.nh * wl.hd)
+    if wl.m >= 64:
+        ach = flops / (ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
+                "frac": ach / bf16}
+    else:
+        ach = nbytes / (ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
+    roof.update({"ms_per_call": ms, "flops": flops, "algorithmic_bytes": nbytes,
+                 "config": f"groups {P['groups']}, o_rank {P['o_rank']}, dim {P['dim']}, "
+                           f"synthetic bf16 weights; inverse RoPE kernel + cuBLAS GEMMs"})
+    return roof
+
+
 def run_ours(args, world, rank, local):
     wl = WORKLOADS[args.workload]
     dev = torch.device("cuda", local)
@@ -424,6 +474,9 @@ def run_ours(args, world, rank, local):
                  else "fallback",
                  "traffic": args.traffic if args.traffic is not None else recorded_traffic(wl.name, dom)})
 
+    # ---- the next row of the layer (not in the step): the output side
+    out_proj = time_out_proj(wl, slots, fc, stream, hbm, bf16) if wl.hd == 512 else None
+
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(wl, slots, fc, stream, K, W, n_slots, world)
 
@@ -439,6 +492,7 @@ def run_ours(args, world, rank, local):
                    "timing": "CUDA-graph replay per step, CUDA events on the launching stream"},
         "roofline": roof,
         "per_op_ms": op_ms,
+        "next_rows": {"attn_out_proj": out_proj} if out_proj else {},
         "e2e": e2e,
         "gpu_launches": launches_per_step(wl) * K,
         "clocks": ck,

@@ -10,7 +10,7 @@ from __future__ import annotations
 import ctypes
 import math
 import os
-from typing import Dict, Optional
+from typing import Dict, Optional, Tuple
 
 import torch
 
@@ -42,6 +42,8 @@ SIGNATURES = {
     "ds41_indexer_topk": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                          _I64, _I64, _I64, _P, _SZ, _P]),
     "ds41_sparse_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
+    "ds41_attn_out_proj": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                          _I64, _I64, _I64, _I64, _P]),
     "ds41_sparse_attn_sink_fwd": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F, _P, _P,
                                                  _I64, _I64, _I64, _P, _SZ, _P]),
     "ds41_csa_workspace_bytes": (_SZ, [_I64] * 9),
@@ -252,6 +254,27 @@ def sparse_attn_sink_fwd_noalloc(q: torch.Tensor, rows_a: torch.Tensor,
           _ptr(sink, torch.float32, "sink"), float(scale), _ptr(o, _BF, "o"),
           _ptr(lse, torch.float32, "lse"), m, nh, hd, _stream())
     return o
+
+
+def attn_out_proj(o: torch.Tensor, freqs_cis: torch.Tensor, wo_a: torch.Tensor,
+                  wo_b: torch.Tensor, rd: int, groups: int, start_pos: int,
+                  og: Optional[torch.Tensor] = None,
+                  out: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """ds41_attn_out_proj: o [m, nh, hd] bf16 is rotated back IN PLACE; returns
+    (og [m, groups*o_rank] bf16, out [m, dim] f32)."""
+    m, nh, hd = o.shape
+    gr = wo_a.shape[0]
+    dim = wo_b.shape[0]
+    if og is None:
+        og = torch.empty(m, gr, dtype=torch.bfloat16, device=o.device)
+    if out is None:
+        out = torch.empty(m, dim, dtype=torch.float32, device=o.device)
+    _call("ds41_attn_out_proj", _ptr(o, _BF, "o"),
+          _ptr(freqs_cis, torch.float32, "freqs_cis") if rd else None,
+          freqs_cis.shape[0] if rd else start_pos + m, _ptr(wo_a, _BF, "wo_a"),
+          _ptr(wo_b, _BF, "wo_b"), _ptr(og, _BF, "og"), _ptr(out, torch.float32, "out"), m,
+          start_pos, nh, hd, rd, groups, gr // groups, dim, _stream())
+    return og, out
 
 
 def csa_workspace_bytes(wl) -> int:

@@ -162,6 +162,24 @@ def make_inputs(wl: Workload, device: str = "cpu", seed: Optional[int] = None,
     return out
 
 
+# The output side of the layer (inverse RoPE, grouped wo_a, wo_b).  The pages
+# give neither the model width nor the projection's rank or group count; these
+# sizes are our choice: 8 groups of 4096 values (8 heads of 512), o_rank 1024,
+# model width 7168.
+OUT_PROJ = {"groups": 8, "o_rank": 1024, "dim": 7168}
+
+
+def make_out_proj_weights(nh: int, hd: int, groups: int, o_rank: int, dim: int, seed: int = 7,
+                          device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """Synthetic projection weights: wo_a [groups*o_rank, nh*hd/groups] and
+    wo_b [dim, groups*o_rank], bf16 N(0, 1) / sqrt(fan-in)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    gw = nh * hd // groups
+    wa = torch.randn(groups * o_rank, gw, generator=g, device=device) / math.sqrt(gw)
+    wb = torch.randn(dim, groups * o_rank, generator=g, device=device) / math.sqrt(groups * o_rank)
+    return {"wo_a": _bf16(wa), "wo_b": _bf16(wb)}
+
+
 def bf16_bits(x: torch.Tensor):
     """A bf16 tensor's bit patterns as a numpy uint16 array (CPU copy)."""
     return x.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")

@@ -317,6 +317,37 @@ int ds41_sparse_attn_sink_fwd_noalloc(const ds41_bf16* q, const ds41_bf16* rows_
                                       float* lse, int64_t m, int64_t nh, int64_t hd,
                                       ds41_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* The output side of the layer                                               */
+/* ------------------------------------------------------------------------ */
+/* compress.rs, attention_any after sparse_attn: o is rotated back
+ * (apply_rotary with inverse = true, each head at its token's position),
+ * split into `groups` groups of gw = nh*hd/groups values, and each group is
+ * projected by its own o_rank rows of wo_a, every result rounded to bf16
+ * (to_bf16_rne); then linear_bf16 with wo_b (body not on the pages: read as
+ * og . wo_b^T with an unrounded f32 result).  This library computes
+ *   o[t, h, hd-rd+2i .. +1] <- the pair rotated by -angle of table column i
+ *       at position start_pos + t, each product rounded, then the sum, and
+ *       the result rounded to bf16 (IN PLACE: o is overwritten)
+ *   og[t, g*o_rank + r] = bf16(sum_i o[t, g*gw + i] * wo_a[g*o_rank + r, i])
+ *   out[t, j] = sum_k og[t, k] * wo_b[j, k]                           (f32)
+ * with f32 accumulation in an unspecified order (cuBLAS), so og can differ
+ * from a differently ordered sum by one bf16 step.
+ *   o        [m, nh, hd] bf16, in/out (the attention output; rotated back)
+ *   freqs_cis [max_pos, rd/2, 2] f32 (cos, sin), as ds41_yarn_freqs_cis
+ *   wo_a     [groups*o_rank, gw] bf16;  wo_b [dim, groups*o_rank] bf16
+ *   og       [m, groups*o_rank] bf16 output;  out [m, dim] f32 output
+ *   All caller-owned device memory, 16-byte aligned.  hd % 8 == 0, rd even
+ *   and <= hd (rd = 0: no rotation, freqs_cis may be NULL), gw % 8 == 0,
+ *   groups*o_rank % 8 == 0, dim % 4 == 0, start_pos + m <= max_pos.
+ * Errors: DS41_E_ARG / DS41_E_RANGE before anything is enqueued; DS41_E_CUDA
+ * when the rotation's launch or a cuBLAS call fails (the rotation may then
+ * have run).  Thread-safe: the library's cuBLAS handle is used under a lock. */
+int ds41_attn_out_proj(ds41_bf16* o, const float* freqs_cis, int64_t max_pos,
+                       const ds41_bf16* wo_a, const ds41_bf16* wo_b, ds41_bf16* og, float* out,
+                       int64_t m, int64_t start_pos, int64_t nh, int64_t hd, int64_t rd,
+                       int64_t groups, int64_t o_rank, int64_t dim, ds41_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

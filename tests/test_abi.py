@@ -120,3 +120,20 @@ def test_host_buffer_entry_points_check_arguments(lib):
                                           FAKE, FAKE, f, FAKE, FAKE, FAKE, None,
                                           1, *sizes, None, 0, None)
     assert rc == 1 and "null pointer" in _err(lib)
+
+
+def test_attn_out_proj_checks_arguments(lib):
+    """ds41_attn_out_proj rejects bad sizes and pointers on the host, before
+    anything is enqueued (no GPU needed)."""
+    def call(o=FAKE, fc=FAKE, max_pos=100, m=2, start_pos=0, nh=4, hd=64, rd=16, groups=2,
+             o_rank=32, dim=48, og=FAKE):
+        return lib.ds41_attn_out_proj(o, fc, max_pos, FAKE, FAKE, og, FAKE, m, start_pos, nh, hd,
+                                      rd, groups, o_rank, dim, None)
+    assert call(m=0) == 2                      # no token
+    assert call(start_pos=99) == 2             # positions past freqs_cis
+    assert call(o=None) == 1 and "non-null" in _err(lib)
+    assert call(og=None) == 1
+    assert call(rd=15) == 1                    # odd rotary width
+    assert call(groups=3) == 1                 # 256 values do not split into 3 groups
+    assert call(dim=50) == 1                   # dim % 4
+    assert call(fc=None) == 1                  # a rotation needs the table

@@ -11,8 +11,9 @@ import torch
 from compressed_sparse_attention_window_gb300 import ds41
 from compressed_sparse_attention_window_gb300.workloads import (CHUNKED, DECODE, LONG_DECODE,
                                                                  PREFILL, TINY_PREFILL, WORKLOADS,
-                                                                 bf16_bits, from_bits,
-                                                                 make_inputs)
+                                                                 OUT_PROJ, bf16_bits, from_bits,
+                                                                 make_inputs,
+                                                                 make_out_proj_weights)
 from helpers import (assert_idx_sets_equal, attn_close, oracle_forward, sample_tokens, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -507,3 +508,74 @@ def test_csa_forward_host_buffers(wl, packed):
         again()
         torch.cuda.synchronize()
         assert torch.equal(h_o, ref["o"].cpu())
+
+
+# --------------------------------------------------------------------------
+# The output side of the layer: inverse RoPE, grouped wo_a, wo_b
+# --------------------------------------------------------------------------
+def _out_proj_check(orc, o_bits, fc, wa, wb, og, out, rd, groups, start_pos, toks):
+    """og against the oracle's f64-summed og.  Here the rotated dims of o are
+    rounded to bf16 (the tensor-core operand; the oracle keeps them f32, as
+    the pages do), which moves each product by at most 2^-9 of its size (a
+    rotated value is at most the norm of its pair, so allow 2^-8), and og's
+    own bf16 rounding can then land one step apart (2^-7 relative):
+      |og - og_ref| <= 2^-8 * sum_i |o_i| |w_i| + 2^-7 |og_ref|.
+    out within 1e-2 of its rms plus 1e-2 relative (bf16 operands)."""
+    rog, rout = orc.attn_out_proj(o_bits, fc, bf16_bits(wa), bf16_bits(wb), rd=rd, groups=groups,
+                                  start_pos=start_pos, tokens=toks)
+    gog = og.float().cpu().numpy()[toks].astype(np.float64)
+    fog = (rog.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    m, nh, hd = o_bits.shape
+    ao = np.abs((o_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    ao = ao.reshape(m, groups, -1)[toks]
+    aw = np.abs(wa.float().numpy().astype(np.float64))
+    o_rank = aw.shape[0] // groups
+    S = np.concatenate([ao[:, g] @ aw[g * o_rank:(g + 1) * o_rank].T for g in range(groups)], 1)
+    assert np.all(np.abs(gog - fog) <= 2.0 ** -8 * S + 2.0 ** -7 * np.abs(fog))
+    gout = out.cpu().numpy()[toks].astype(np.float64)
+    rms = np.sqrt(np.mean(rout ** 2))
+    err = np.abs(gout - rout)
+    assert np.all(err <= 1e-2 * rms + 1e-2 * np.abs(rout)), (err.max(), rms)
+
+
+@pytest.mark.parametrize("m,nh,hd,rd,groups,o_rank,dim,start_pos",
+                         [(3, 4, 64, 16, 2, 32, 48, 5), (37, 8, 128, 32, 4, 64, 200, 0),
+                          (1, 64, 512, 64, 8, 1024, 7168, 8191)])
+def test_attn_out_proj_matches_oracle(orc, m, nh, hd, rd, groups, o_rank, dim, start_pos):
+    """ds41_attn_out_proj against the oracle, every token, from a small case
+    to one decode token at the full sizes."""
+    g = torch.Generator().manual_seed(m + nh + dim)
+    o = torch.randn(m, nh, hd, generator=g).to(torch.bfloat16)
+    wts = make_out_proj_weights(nh, hd, groups, o_rank, dim, seed=m)
+    fc = ds41.yarn_freqs_cis(rd, start_pos + m) if rd else torch.zeros(1, 1, 2).cuda()
+    o_bits = bf16_bits(o)
+    od = o.cuda()
+    og, out = ds41.attn_out_proj(od, fc, wts["wo_a"].cuda(), wts["wo_b"].cuda(), rd, groups,
+                                 start_pos)
+    torch.cuda.synchronize()
+    _out_proj_check(orc, o_bits, fc.cpu().numpy(), wts["wo_a"], wts["wo_b"], og, out, rd, groups,
+                    start_pos, list(range(m)))
+    # only the rotary dims of o changed
+    od_f = bf16_bits(od.cpu()).reshape(m, nh, hd)
+    assert np.array_equal(od_f[:, :, : hd - rd], o_bits.reshape(m, nh, hd)[:, :, : hd - rd])
+
+
+@pytest.mark.parametrize("name", ["prefill", "chunked_prefill"])
+def test_attn_out_proj_full_size_sampled(orc, name):
+    """The attention output of a many-token workload through the output side
+    at the full sizes, checked on sampled tokens."""
+    wl = WORKLOADS[name]
+    P = OUT_PROJ
+    inp = make_inputs(wl)
+    dev = to_dev(inp)
+    fc = ds41.yarn_freqs_cis(wl.rd, wl.max_pos)
+    o = ds41.csa_forward(dev, wl, fc)["o"]
+    o_bits = bf16_bits(o)
+    wts = make_out_proj_weights(wl.nh, wl.hd, P["groups"], P["o_rank"], P["dim"])
+    og, out = ds41.attn_out_proj(o, fc, wts["wo_a"].cuda(), wts["wo_b"].cuda(), wl.rd, P["groups"],
+                                 wl.start_pos)
+    torch.cuda.synchronize()
+    assert ds41.device_status() == 0
+    toks = sample_tokens(wl)[:8]
+    _out_proj_check(orc, o_bits, fc.cpu().numpy(), wts["wo_a"], wts["wo_b"], og, out, wl.rd,
+                    P["groups"], wl.start_pos, toks)
