@@ -398,6 +398,35 @@ def time_out_proj(wl, slots, fc, stream, hbm, bf16, reps=5):
     return roof
 
 
+def time_reuse(wl, slots, stream, reps=5):
+    """The step of a layer that reuses the source layer's compressed rows and
+    picks (ring write, index merge, attention; not part of the measured step):
+    milliseconds per call from a CUDA graph of one call per layer state, each
+    on that state's cache and the picks its own step left in idx."""
+    ctopk = wl.K - wl.win
+    cidx = [out["idx"][:, wl.win:].contiguous() if ctopk else None for _, out in slots]
+    outs = [{} for _ in slots]
+    with torch.cuda.stream(stream):
+        for (inp, _), c, o in zip(slots, cidx, outs):
+            ds41.csa_forward_reuse(inp, wl, inp["cache"], c, o)  # allocates outside the capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for (inp, _), c, o in zip(slots, cidx, outs):
+                ds41.csa_forward_reuse(inp, wl, inp["cache"], c, o)
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * len(slots))
+    del g
+    return {"ms_per_step": ms, "query_tokens_per_s": wl.m / (ms / 1e3),
+            "steps": "ring write, index merge (when the layer has compressed picks), attention"}
+
+
 def run_ours(args, world, rank, local):
     wl = WORKLOADS[args.workload]
     dev = torch.device("cuda", local)
@@ -474,11 +503,13 @@ def run_ours(args, world, rank, local):
                  else "fallback",
                  "traffic": args.traffic if args.traffic is not None else recorded_traffic(wl.name, dom)})
 
-    # ---- the next row of the layer (not in the step): the output side
-    out_proj = time_out_proj(wl, slots, fc, stream, hbm, bf16) if wl.hd == 512 else None
-
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(wl, slots, fc, stream, K, W, n_slots, world)
+
+    # ---- the next rows of the layer (not in the step): the output side, and
+    # the step of a layer that reuses a source layer's rows and picks
+    out_proj = time_out_proj(wl, slots, fc, stream, hbm, bf16) if wl.hd == 512 else None
+    reuse = time_reuse(wl, slots, stream)
 
     res = {
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
@@ -492,7 +523,8 @@ def run_ours(args, world, rank, local):
                    "timing": "CUDA-graph replay per step, CUDA events on the launching stream"},
         "roofline": roof,
         "per_op_ms": op_ms,
-        "next_rows": {"attn_out_proj": out_proj} if out_proj else {},
+        "next_rows": dict({"attn_out_proj": out_proj} if out_proj else {},
+                          csa_forward_reuse=reuse),
         "e2e": e2e,
         "gpu_launches": launches_per_step(wl) * K,
         "clocks": ck,

@@ -214,3 +214,60 @@ extern "C" int ds41_csa_forward_host_packed(
     return cuda_check(cudaMemcpyAsync(h_o, o, (size_t)(m * nh * hd) * 2, cudaMemcpyDeviceToHost, st),
                       "ds41_csa_forward_host_packed: output copy");
 }
+
+// ---------------------------------------------------------------------------
+// A layer that reuses the last source layer's compressed rows and picks
+// ---------------------------------------------------------------------------
+// idx row t = the window indices of t, then the shared picks of t.
+__global__ void merge_shared_kernel(const int32_t* win_idx, const int32_t* cidx, int32_t* idx,
+                                    int64_t m, int win, int ctopk) {
+    const int K = win + ctopk;
+    const int64_t total = m * K;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
+         k += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = k / K;
+        const int j = (int)(k % K);
+        idx[k] = j < win ? win_idx[t * win + j] : cidx[t * ctopk + (j - win)];
+    }
+}
+
+extern "C" int ds41_csa_forward_reuse(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring,
+                                      ds41_bf16* rows_a, const ds41_bf16* cache,
+                                      const int32_t* cidx, int64_t ctopk, const float* sink,
+                                      float scale, int32_t* win_idx, int32_t* idx, ds41_bf16* o,
+                                      float* lse, int64_t m, int64_t start_pos, int64_t nh,
+                                      int64_t hd, int64_t win, int64_t ratio, void* ws,
+                                      size_t ws_bytes, ds41_stream_t stream) {
+    const char* name = "ds41_csa_forward_reuse";
+    DS41_REQUIRE(m >= 1 && m < (int64_t(1) << 31), DS41_E_RANGE, "%s: m=%lld", name,
+                 (long long)m);
+    DS41_REQUIRE(start_pos >= 0 && start_pos + m < (int64_t(1) << 31), DS41_E_RANGE,
+                 "%s: start_pos=%lld", name, (long long)start_pos);
+    DS41_REQUIRE(ratio >= 1 && win >= 1 && win <= (int64_t(1) << 20), DS41_E_ARG,
+                 "%s: ratio=%lld win=%lld", name, (long long)ratio, (long long)win);
+    const int64_t n_c = (start_pos + m) / ratio;
+    DS41_REQUIRE(ctopk >= 0 && ctopk <= n_c && ctopk <= (int64_t(1) << 20), DS41_E_ARG,
+                 "%s: ctopk=%lld with %lld compressed rows", name, (long long)ctopk,
+                 (long long)n_c);
+    DS41_REQUIRE(ctopk == 0 || (cidx && idx && cache), DS41_E_ARG,
+                 "%s: cidx, idx and cache are required when ctopk > 0", name);
+    const int64_t n_a = ds41_rows_a_len(m, win, start_pos);
+    int rc = ds41_window_ring_write(kv, ring, rows_a, win_idx, nullptr, m, hd, win, start_pos,
+                                    stream);
+    if (rc) return rc;
+    const int32_t* att_idx = win_idx;
+    if (ctopk > 0) {
+        const int64_t total = m * (win + ctopk);
+        const int threads = 256;
+        const int64_t blocks = (total + threads - 1) / threads;
+        merge_shared_kernel<<<(unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0,
+                              (cudaStream_t)stream>>>(win_idx, cidx, idx, m, (int)win,
+                                                      (int)ctopk);
+        if ((rc = launch_check(name))) return rc;
+        att_idx = idx;
+    }
+    const ds41_bf16* rows_a_used = start_pos == 0 ? kv : (m == 1 ? ring : rows_a);
+    return ds41_sparse_attn_sink_fwd(q, rows_a_used, n_a, ctopk ? cache : nullptr,
+                                     ctopk ? n_c : 0, att_idx, win + ctopk, sink, scale, o, lse,
+                                     m, nh, hd, ws, ws_bytes, stream);
+}

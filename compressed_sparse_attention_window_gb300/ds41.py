@@ -42,6 +42,9 @@ SIGNATURES = {
     "ds41_indexer_topk": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                          _I64, _I64, _I64, _P, _SZ, _P]),
     "ds41_sparse_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
+    "ds41_csa_forward_reuse": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _F, _P, _P, _P,
+                                              _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, ctypes.c_size_t,
+                                              _P]),
     "ds41_attn_out_proj": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                           _I64, _I64, _I64, _I64, _P]),
     "ds41_sparse_attn_sink_fwd": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F, _P, _P,
@@ -254,6 +257,40 @@ def sparse_attn_sink_fwd_noalloc(q: torch.Tensor, rows_a: torch.Tensor,
           _ptr(sink, torch.float32, "sink"), float(scale), _ptr(o, _BF, "o"),
           _ptr(lse, torch.float32, "lse"), m, nh, hd, _stream())
     return o
+
+
+def csa_forward_reuse(inp: Dict[str, torch.Tensor], wl, cache: torch.Tensor,
+                      cidx: Optional[torch.Tensor],
+                      out: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
+    """ds41_csa_forward_reuse: the step of a layer that reuses the source
+    layer's compressed rows ``cache`` and picks ``cidx`` [m, ctopk] (offset
+    applied); q, kv, ring, sink come from ``inp``.  Returns win_idx, idx, o."""
+    out = {} if out is None else out
+    dev = inp["q"].device
+    m, win = wl.m, wl.win
+    ctopk = 0 if cidx is None else cidx.shape[1]
+    if "win_idx" not in out:
+        out["win_idx"] = torch.empty(m, win, dtype=torch.int32, device=dev)
+    if "idx" not in out:
+        out["idx"] = torch.empty(m, win + ctopk, dtype=torch.int32, device=dev)
+    if "o" not in out:
+        out["o"] = torch.empty_like(inp["q"])
+    chunk = wl.start_pos > 0 and m > 1
+    if chunk and "rows_a" not in out:
+        out["rows_a"] = torch.empty(win + m, wl.hd, dtype=torch.bfloat16, device=dev)
+    need = sparse_attn_workspace_bytes(m, wl.nh, wl.hd, win + ctopk)
+    ws = out.get("ws_reuse")
+    if need and (ws is None or ws.numel() < need):
+        ws = out["ws_reuse"] = torch.empty(need, dtype=torch.uint8, device=dev)
+    _call("ds41_csa_forward_reuse", _ptr(inp["q"], _BF, "q"), _ptr(inp["kv"], _BF, "kv"),
+          _ptr(inp["ring"], _BF, "ring"), _ptr(out.get("rows_a") if chunk else None),
+          _ptr(cache, _BF, "cache") if ctopk else None,
+          _ptr(cidx, torch.int32, "cidx") if ctopk else None, ctopk,
+          _ptr(inp["sink"], torch.float32, "sink"), float(wl.scale),
+          _ptr(out["win_idx"], torch.int32, "win_idx"), _ptr(out["idx"], torch.int32, "idx"),
+          _ptr(out["o"], _BF, "o"), _ptr(out.get("lse"), torch.float32, "lse"), m, wl.start_pos,
+          wl.nh, wl.hd, win, wl.ratio, _ptr(ws) if need else None, need, _stream())
+    return out
 
 
 def attn_out_proj(o: torch.Tensor, freqs_cis: torch.Tensor, wo_a: torch.Tensor,

@@ -234,6 +234,30 @@ int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring, d
                      int64_t ratio, int64_t topk, int64_t Hi, int64_t Di, void* ws,
                      size_t ws_bytes, ds41_stream_t stream);
 
+/* forward.rs, AttnV41::forward, for a layer that is neither a kv source
+ * nor an index source: it writes its own window ring and window indices,
+ * takes the compressed rows (rows_b) and the compressed picks of the last
+ * source layer (the shared slots compress_kv and topk_idxs), merges its
+ * window indices with those picks, and attends.  No latent write, no indexer.
+ *   q [m, nh, hd], kv [m, hd], ring [win, hd], rows_a as ds41_csa_forward
+ *   cache [>= n_c, hd] bf16: the source layer's compressed rows, n_c =
+ *       (start_pos + m)/ratio of them visible
+ *   cidx [m, ctopk] int32: the source layer's picks, already offset by
+ *       ds41_rows_a_len (as ds41_indexer_topk writes them after the window
+ *       part of its idx rows); ctopk = min(topk, n_c), NULL when 0
+ *   win_idx [m, win] and idx [m, win + ctopk] int32 outputs (idx row t = the
+ *       window indices of t, then cidx row t; idx is unused when ctopk == 0)
+ *   o, lse, sink, scale as ds41_sparse_attn_sink_fwd.
+ * Scratch: ds41_sparse_attn_workspace_bytes(m, nh, hd, win + ctopk).  Errors
+ * as the three calls it makes (ring write, index merge, attention); an index
+ * in cidx past n_a + n_c raises DS41_E_INDEX on the device and is skipped. */
+int ds41_csa_forward_reuse(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring,
+                           ds41_bf16* rows_a, const ds41_bf16* cache, const int32_t* cidx,
+                           int64_t ctopk, const float* sink, float scale, int32_t* win_idx,
+                           int32_t* idx, ds41_bf16* o, float* lse, int64_t m, int64_t start_pos,
+                           int64_t nh, int64_t hd, int64_t win, int64_t ratio, void* ws,
+                           size_t ws_bytes, ds41_stream_t stream);
+
 /* ds41_csa_forward for a caller whose per-step inputs and output live in
  * host memory (no counterpart in the paper, which computes on the host): the
  * inputs h_q [m, nh, hd], h_kv [m, hd], h_latent [G, hd] (read only when the

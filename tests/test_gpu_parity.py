@@ -579,3 +579,57 @@ def test_attn_out_proj_full_size_sampled(orc, name):
     toks = sample_tokens(wl)[:8]
     _out_proj_check(orc, o_bits, fc.cpu().numpy(), wts["wo_a"], wts["wo_b"], og, out, wl.rd,
                     P["groups"], wl.start_pos, toks)
+
+
+# --------------------------------------------------------------------------
+# A layer that reuses the source layer's compressed rows and picks
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["decode", "long_decode", "tiny_prefill", "chunked_prefill",
+                                  "prefill"])
+def test_csa_forward_reuse(orc, name):
+    """ds41_csa_forward_reuse for a second layer (its own q, kv, ring, sink)
+    on the first layer's compressed rows and picks: bit for bit the ring
+    write, the merge and the attention called separately, and the oracle's
+    attention over the oracle's own window indices and picks of the first
+    layer."""
+    wl = WORKLOADS[name]
+    fc = ds41.yarn_freqs_cis(wl.rd, max(wl.max_pos, 1))
+    src = make_inputs(wl)
+    dev_s = to_dev(src)
+    out_s = ds41.csa_forward(dev_s, wl, fc)
+    ctopk = wl.K - wl.win
+    cidx = out_s["idx"][:, wl.win:].contiguous() if ctopk else None
+    cache = dev_s["cache"]
+    lay = make_inputs(wl, seed=4242)
+    dev_r = to_dev(lay)
+    out_r = ds41.csa_forward_reuse(dev_r, wl, cache, cidx)
+    # the same through the separate entry points
+    dev_c = to_dev(lay)
+    chunk = wl.start_pos > 0 and wl.m > 1
+    rows_a = torch.empty(wl.win + wl.m, wl.hd, dtype=torch.bfloat16, device="cuda") if chunk else None
+    win_idx = torch.empty(wl.m, wl.win, dtype=torch.int32, device="cuda")
+    ds41.window_ring_write(dev_c["kv"], dev_c["ring"], win_idx, wl.start_pos, rows_a=rows_a)
+    ra = dev_c["kv"] if wl.start_pos == 0 else (dev_c["ring"] if wl.m == 1 else rows_a)
+    idx = torch.cat([win_idx, cidx], 1) if ctopk else win_idx
+    o_c = ds41.sparse_attn_sink_fwd(dev_c["q"], ra, cache[: wl.n_c] if ctopk else None, idx,
+                                    dev_c["sink"], wl.scale)
+    torch.cuda.synchronize()
+    assert ds41.device_status() == 0
+    assert torch.equal(dev_r["ring"], dev_c["ring"])
+    assert torch.equal(out_r["win_idx"], win_idx)
+    if ctopk:
+        assert torch.equal(out_r["idx"], idx)
+    assert torch.equal(out_r["o"], o_c)
+    # the oracle: this layer's rows_a and window indices, the first layer's picks
+    toks = sample_tokens(wl) if wl.m > 128 else list(range(wl.m))
+    ref_s = oracle_forward(orc, wl, src, tokens=toks, fc=fc.cpu().numpy())
+    _, rows_a_o = orc.window_ring_write(bf16_bits(lay["kv"]), bf16_bits(lay["ring"]), wl.win,
+                                        wl.start_pos)
+    win_o = orc.window_topk_idxs(wl.win, wl.m, wl.start_pos)[toks]
+    idx_o = np.concatenate([win_o, ref_s["idx"][:, wl.win:]], 1) if ctopk else win_o
+    o_ref, _, bad = orc.sparse_attn(bf16_bits(lay["q"]), rows_a_o,
+                                    ref_s["cache"][: wl.n_c] if ctopk else None, idx_o,
+                                    lay["sink"].numpy(), wl.scale, tokens=toks)
+    assert bad == 0
+    ok, err, worst = attn_close(out_r["o"].float().cpu().numpy()[toks], o_ref)
+    assert ok, (name, err, worst)
