@@ -251,6 +251,17 @@ extern "C" int ds41_csa_forward_reuse(const ds41_bf16* q, const ds41_bf16* kv, d
                  (long long)n_c);
     DS41_REQUIRE(ctopk == 0 || (cidx && idx && cache), DS41_E_ARG,
                  "%s: cidx, idx and cache are required when ctopk > 0", name);
+    // the attention's own checks, made before the ring write is enqueued
+    DS41_REQUIRE(nh >= 1 && nh <= 65535 && (hd == 64 || hd == 128 || hd == 256 || hd == 512),
+                 DS41_E_ARG, "%s: nh=%lld hd=%lld (hd must be 64, 128, 256 or 512)", name,
+                 (long long)nh, (long long)hd);
+    DS41_REQUIRE(q && sink && o && aligned16(q) && aligned16(o) && (ctopk == 0 || aligned16(cache)),
+                 DS41_E_ARG, "%s: q, sink and o must be non-null; q, o, cache 16-byte aligned",
+                 name);
+    const size_t need = ds41_sparse_attn_workspace_bytes(m, nh, hd, win + ctopk);
+    DS41_REQUIRE(need == 0 || (ws && ws_bytes >= need), DS41_E_WORKSPACE,
+                 "%s: workspace of %zu bytes needed, %zu given", name, need, ws ? ws_bytes : 0);
+    DS41_REQUIRE(need == 0 || aligned16(ws), DS41_E_ARG, "%s: ws must be 16-byte aligned", name);
     const int64_t n_a = ds41_rows_a_len(m, win, start_pos);
     int rc = ds41_window_ring_write(kv, ring, rows_a, win_idx, nullptr, m, hd, win, start_pos,
                                     stream);

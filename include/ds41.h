@@ -248,9 +248,10 @@ int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring, d
  *   win_idx [m, win] and idx [m, win + ctopk] int32 outputs (idx row t = the
  *       window indices of t, then cidx row t; idx is unused when ctopk == 0)
  *   o, lse, sink, scale as ds41_sparse_attn_sink_fwd.
- * Scratch: ds41_sparse_attn_workspace_bytes(m, nh, hd, win + ctopk).  Errors
- * as the three calls it makes (ring write, index merge, attention); an index
- * in cidx past n_a + n_c raises DS41_E_INDEX on the device and is skipped. */
+ * Scratch: ds41_sparse_attn_workspace_bytes(m, nh, hd, win + ctopk).  Errors:
+ * those of ds41_window_ring_write and ds41_sparse_attn_sink_fwd, all checked
+ * before anything is enqueued; an index in cidx past n_a + n_c raises
+ * DS41_E_INDEX on the device and is skipped. */
 int ds41_csa_forward_reuse(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring,
                            ds41_bf16* rows_a, const ds41_bf16* cache, const int32_t* cidx,
                            int64_t ctopk, const float* sink, float scale, int32_t* win_idx,

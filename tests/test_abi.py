@@ -137,3 +137,23 @@ def test_attn_out_proj_checks_arguments(lib):
     assert call(groups=3) == 1                 # 256 values do not split into 3 groups
     assert call(dim=50) == 1                   # dim % 4
     assert call(fc=None) == 1                  # a rotation needs the table
+
+
+def test_csa_forward_reuse_checks_arguments(lib):
+    """ds41_csa_forward_reuse checks the ring write's and the attention's
+    arguments before it enqueues anything (no GPU needed; the workspace size
+    depends on the device and is not checked here)."""
+    f = ctypes.c_float(0.04)
+
+    def call(q=FAKE, cidx=FAKE, ctopk=512, hd=512, m=1, start_pos=8191, ratio=4, ws=FAKE,
+             ws_bytes=1 << 30):
+        # q kv ring rows_a cache cidx ctopk sink scale win_idx idx o lse | m start_pos nh hd win
+        # ratio | ws ws_bytes stream
+        return lib.ds41_csa_forward_reuse(q, FAKE, FAKE, None, FAKE, cidx, ctopk, FAKE, f, FAKE,
+                                          FAKE, FAKE, None, m, start_pos, 64, hd, 128, ratio, ws,
+                                          ws_bytes, None)
+    assert call(m=0) == 2
+    assert call(ctopk=4096) == 1               # more picks than compressed rows
+    assert call(cidx=None) == 1                # picks required when ctopk > 0
+    assert call(hd=96) == 1                    # the attention's head width
+    assert call(q=None) == 1
