@@ -11,10 +11,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Tensor pointers are DEVICE pointers owned by the caller (for example
- *   torch allocations).  Nothing here allocates device memory.  Entry points
- *   that need scratch memory take (ws, ws_bytes); the matching
- *   *_workspace_bytes function says how much.  Host pointers are marked
- *   "host".
+ *   torch allocations).  The entry points allocate no device memory, with
+ *   one exception: the first ds41_attn_out_proj call creates the library's
+ *   cuBLAS handle, which holds cuBLAS's own workspace.  Entry points that
+ *   need scratch memory take (ws, ws_bytes); the matching *_workspace_bytes
+ *   function says how much.  Host pointers are marked "host".
  * - bf16 tensors are passed as uint16_t bit patterns (ds41_bf16).
  * - Layouts are row-major and contiguous; every device pointer must be 16-byte
  *   aligned.
