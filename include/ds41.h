@@ -261,7 +261,7 @@ int ds41_csa_forward_reuse(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* r
                            size_t ws_bytes, ds41_stream_t stream);
 
 /* ds41_csa_forward for a caller whose per-step inputs and output live in
- * host memory (no counterpart in the paper, which computes on the host): the
+ * host memory (no counterpart on the pages, whose reference computes on the host): the
  * inputs h_q [m, nh, hd], h_kv [m, hd], h_latent [G, hd] (read only when the
  * call completes G > 0 groups, G = (start_pos + m)/ratio - start_pos/ratio;
  * may be NULL otherwise), h_q_idx [m, Hi, Di] and h_w [m, Hi] are copied into
@@ -311,7 +311,7 @@ int ds41_csa_forward_host_packed(const void* h_in, void* d_in, ds41_bf16* h_o, d
 /* ------------------------------------------------------------------------ */
 /* Step 3 without caller-provided scratch                                     */
 /* ------------------------------------------------------------------------ */
-/* No counterpart in the paper: this entry point exists for callers that
+/* No counterpart on the pages: this entry point exists for callers that
  * cannot allocate device memory.  Examples are serving runtimes that reserve
  * all device memory when they start and forbid any allocation afterwards
  * (cudaMalloc can synchronise the device and fragment a carefully packed
