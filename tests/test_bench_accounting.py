@@ -1,0 +1,54 @@
+"""The algorithmic work bench.py divides by (the roofline numerators), pinned
+to closed forms worked out by hand, and the guard that reports recorded DRAM
+traffic only for the kernel sources it was measured on."""
+import bench
+from compressed_sparse_attention_window_gb300.workloads import WORKLOADS
+
+
+def test_prefill_valid_rows_closed_form():
+    """Prefill (m = 4096 at 0, window 128, ratio 4, top-k 512): token t sees
+    min(t + 1, 128) window rows and min(512, (t + 1) // 4) compressed rows.
+    Window: 1 + .. + 128 + (4096 - 128) * 128 = 8256 + 507904 = 516160.
+    Compressed: n = t + 1 below 2048 gives each q = 0 .. 511 four times,
+    4 * (511 * 512 / 2) = 523264; n = 2048 .. 4096 gives 2049 * 512 = 1049088.
+    Total 2088512 rows; attention flops 4 * 64 * 512 * rows = 273.7 G."""
+    wl = WORKLOADS["prefill"]
+    assert bench.attn_valid_rows(wl) == 516160 + 523264 + 1049088 == 2088512
+    alg = bench.algorithmic(wl)
+    assert alg["sparse_attn_sink_fwd"]["flops"] == 4 * 64 * 512 * 2088512
+    assert round(alg["sparse_attn_sink_fwd"]["flops"] / 1e9, 1) == 273.7
+
+
+def test_chunked_and_decode_valid_rows():
+    """Chunked prefill (m = 1024 at 65536, ratio 128): every token has a full
+    window of 128 and at least 65537 // 128 = 512 visible rows, so the top-512
+    keeps 512: 1024 * 640 = 655360 rows (85.9 GFLOP).  Decode at 8191 sees 128
+    window rows and 8192 // 4 = 2048 compressed rows, keeps 512: 640 rows."""
+    ch = WORKLOADS["chunked_prefill"]
+    assert bench.attn_valid_rows(ch) == 1024 * 640
+    assert round(bench.algorithmic(ch)["sparse_attn_sink_fwd"]["flops"] / 1e9, 1) == 85.9
+    assert bench.attn_valid_rows(WORKLOADS["decode"]) == 640
+    assert bench.attn_valid_rows(WORKLOADS["long_decode"]) == 128 + 2048
+
+
+def test_indexer_pairs_closed_form():
+    """Prefill indexer flops: 2 * 64 * 128 per causally visible (query, row)
+    pair; token t sees min(1024, n // 4) rows, n = t + 1.  n = 1 .. 2047 gives
+    q = 0 .. 511 four times (523264), n = 2048 .. 4095 gives q = 512 .. 1023
+    four times (4 * (512 + 1023) * 512 / 2 = 1571840), and n = 4096 gives
+    1024: 2096128 pairs."""
+    alg = bench.algorithmic(WORKLOADS["prefill"])
+    assert alg["indexer_topk"]["flops"] == 2 * 64 * 128 * 2096128
+
+
+def test_recorded_traffic_only_for_matching_sources(tmp_path, monkeypatch):
+    """The committed table carries the digest of the current CUDA sources and
+    gives numbers; the same table under another digest gives none."""
+    assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") is not None
+    assert bench.recorded_traffic("prefill", "no_such_op") is None
+    other = tmp_path / "dram_traffic.txt"
+    with open(bench.TRAFFIC_FILE) as f:
+        text = f.read()
+    other.write_text(text.replace("csrc " + bench.csrc_digest(), "csrc 0000000000000000"))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(other))
+    assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") is None
