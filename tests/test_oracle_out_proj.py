@@ -5,7 +5,9 @@ wo_a projection rounded to bf16, then linear_bf16 with wo_b.
 Each pin checks the oracle against something other than its own formula: a
 worked example done by hand, the forward rotation it must undo, a single
 group that must reproduce the grouped form with block-diagonal weights, exact
-scaling by powers of two, and bf16 ties whose rounding the definition fixes.
+scaling by powers of two, bf16 ties whose rounding the definition fixes, and
+numpy's matrix product with torch's bf16 rounding on sizes where no two
+dimensions are equal.
 """
 import numpy as np
 import torch
@@ -131,3 +133,27 @@ def test_out_proj_og_rounds_ties_to_even(orc):
     og, out = orc.attn_out_proj(o, fc, wa, wb, rd=0, groups=1, start_pos=0)
     assert np.array_equal(_f(og), [[1.0, 1 + 2 ** -6]])
     assert np.array_equal(out, [[1.0]])
+
+
+def test_out_proj_products_against_library_matmul(orc):
+    """Both products against numpy's matrix product (f64) on the oracle's own
+    rotated o (the rotation is pinned above), with torch's bf16 rounding for
+    og: sizes chosen so that no dimension equals another (a transposed wo_a or
+    wo_b, or a wrong group stride, cannot line up)."""
+    rng = np.random.default_rng(5)
+    m, nh, hd, rd, groups, o_rank, dim = 3, 6, 16, 8, 3, 5, 7
+    start_pos = 2
+    gw = nh * hd // groups
+    fc = _table(rd, start_pos + m)
+    o = _bits(rng.standard_normal((m, nh, hd)))
+    wa = _bits(rng.standard_normal((groups * o_rank, gw)))
+    wb = _bits(rng.standard_normal((dim, groups * o_rank)))
+    og, out = orc.attn_out_proj(o, fc, wa, wb, rd=rd, groups=groups, start_pos=start_pos)
+    pos = np.repeat(np.arange(start_pos, start_pos + m), nh)
+    x = orc.apply_rotary(_f(o).astype(np.float32).reshape(m * nh, hd), rd, pos, fc, inverse=True)
+    x = x.astype(np.float64).reshape(m, groups, gw)
+    waf = _f(wa).reshape(groups, o_rank, gw)
+    acc = np.einsum("mgi,gri->mgr", x, waf).reshape(m, groups * o_rank)
+    want_og = _bits(acc.astype(np.float32))
+    assert np.array_equal(og, want_og)
+    assert np.allclose(out, _f(og) @ _f(wb).T, rtol=1e-12, atol=1e-12)
