@@ -541,7 +541,19 @@ def run_only(args, local):
     fc = ds41.yarn_freqs_cis(wl.rd, wl.max_pos, device=dev)
     slots = build_slots(wl, args.slots, dev)
     for inp, out in slots:
-        ds41.forward(inp, wl, fc, out)  # fills win_idx / idx for the later ops
+        ds41.forward(inp, wl, fc, out)  # fills win_idx / idx / o for the later ops
+    P = OUT_PROJ
+    wts = {}
+    if args.only == "attn_out_proj":
+        w = make_out_proj_weights(wl.nh, wl.hd, P["groups"], P["o_rank"], P["dim"])
+        wts = {k: v.to(dev) for k, v in w.items()}
+        for inp, out in slots:
+            out["og"] = torch.empty(wl.m, wts["wo_a"].shape[0], dtype=torch.bfloat16, device=dev)
+            out["proj"] = torch.empty(wl.m, P["dim"], dtype=torch.float32, device=dev)
+    elif args.only == "csa_forward_reuse":
+        for inp, out in slots:
+            out["cidx"] = out["idx"][:, wl.win:].contiguous() if wl.K > wl.win else None
+            out["reuse"] = {}
     torch.cuda.synchronize()
 
     def op(i):
@@ -562,6 +574,11 @@ def run_only(args, local):
             rows_a = {0: inp["kv"]}.get(wl.start_pos, inp["ring"] if wl.m == 1 else out.get("rows_a"))
             ds41.sparse_attn_sink_fwd(inp["q"], rows_a, inp["cache"][: wl.n_c], out["idx"],
                                       inp["sink"], wl.scale, o=out["o"], ws=out.get("ws_attn"))
+        elif args.only == "attn_out_proj":
+            ds41.attn_out_proj(out["o"], fc, wts["wo_a"], wts["wo_b"], wl.rd, P["groups"],
+                               wl.start_pos, og=out["og"], out=out["proj"])
+        elif args.only == "csa_forward_reuse":
+            ds41.csa_forward_reuse(inp, wl, inp["cache"], out["cidx"], out["reuse"])
         else:
             raise SystemExit(f"unknown op {args.only}")
 
