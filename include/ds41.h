@@ -368,7 +368,9 @@ int ds41_sparse_attn_sink_fwd_noalloc(const ds41_bf16* q, const ds41_bf16* rows_
  *   groups*o_rank % 8 == 0, dim % 4 == 0, start_pos + m <= max_pos.
  * Errors: DS41_E_ARG / DS41_E_RANGE before anything is enqueued; DS41_E_CUDA
  * when the rotation's launch or a cuBLAS call fails (the rotation may then
- * have run).  Thread-safe: the library's cuBLAS handle is used under a lock. */
+ * have run).  Thread-safe: the library's one cuBLAS handle is used under a
+ * lock.  The handle belongs to the device current at the first call, so a
+ * process calls this entry point on one device (one process per GPU). */
 int ds41_attn_out_proj(ds41_bf16* o, const float* freqs_cis, int64_t max_pos,
                        const ds41_bf16* wo_a, const ds41_bf16* wo_b, ds41_bf16* og, float* out,
                        int64_t m, int64_t start_pos, int64_t nh, int64_t hd, int64_t rd,
