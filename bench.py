@@ -3,20 +3,25 @@
 
 One step = the whole hot path for one batch of synthetic input: window ring
 write + window indices, compressed latent write, fp4 indexer scores + top-k +
-merge, sparse attention with the sink.  The default workload is single-token
+merge, sparse attention with the sink.  The headline workload is single-token
 decode (m=1 at start_pos 8191, 64 heads x 512, window 128, ratio 4 -> 2048
 compressed rows, top-k 512, indexer 64 x 128); ``--workload`` picks another.
+The same run measures the other four workloads (tiny prefill, prefill, long
+decode, chunked prefill) the same way and reports them under ``configs``
+(``--headline-only`` skips them).
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier +
 synchronize on both sides, CUDA events on the launching stream, each step a
-CUDA-graph replay of the four C-ABI calls.  Steps rotate over independent
-layer states whose total size exceeds twice the L2 cache, so every step reads
-its window ring, latent cache and indexer keys from HBM.  The JSON line adds
-the roofline of the dominant kernel (timed again with events around it), the
-end-to-end rate through the public API with host buffers, the SM clocks seen
-during the timed region, and the CPU oracle timed on a bounded sample.
+CUDA-graph replay of the whole step.  Steps rotate over independent layer
+states whose total size exceeds twice the L2 cache, so every step reads its
+window ring, latent cache and indexer keys from HBM.  Each workload's entry
+adds the roofline of its dominant op (timed again with events around it),
+the end-to-end rate through the public API with host buffers, the number of
+kernel launches in the timed region (the kernel nodes of the captured step),
+the SM clocks seen during the timed region, and the CPU oracle timed per
+stage, single-threaded and on all host cores, on a bounded sample.
 
-``--impl reference`` times the CPU oracle itself on the same workload.
+``--impl reference`` times the CPU oracle itself on the headline workload.
 Multi-GPU (torchrun): every rank runs independent replicas of the step on its
 own GPU; no data-path collective; value = all ranks' tokens / max time.
 """
@@ -224,19 +229,20 @@ class Clocks:
 # ---------------------------------------------------------------------------
 def build_slots(wl, n_slots, device, seed0=1000):
     """Independent layer states (inputs + outputs + workspaces) for rotation."""
+    sz = ds41.step_sizes(wl)
     slots = []
     for s in range(n_slots):
         inp = make_inputs(wl, device=device, seed=seed0 + s)
         out = {"win_idx": torch.empty(wl.m, wl.win, dtype=torch.int32, device=device)}
         if wl.start_pos > 0 and wl.m > 1:
             out["rows_a"] = torch.empty(wl.win + wl.m, wl.hd, dtype=torch.bfloat16, device=device)
-        if wl.n_c > 0:
-            out["idx"] = torch.empty(wl.m, wl.K, dtype=torch.int32, device=device)
-            nb = ds41.indexer_workspace_bytes(wl.m, wl.Hi, wl.Di, wl.n_c, False)
+        if sz.n_c > 0:
+            out["idx"] = torch.empty(wl.m, sz.K, dtype=torch.int32, device=device)
+            nb = ds41.indexer_workspace_bytes(wl.m, wl.Hi, wl.Di, sz.n_c, False)
             if nb:
                 out["ws_idx"] = torch.empty(nb, dtype=torch.uint8, device=device)
         out["o"] = torch.empty(wl.m, wl.nh, wl.hd, dtype=torch.bfloat16, device=device)
-        nb = ds41.sparse_attn_workspace_bytes(wl.m, wl.nh, wl.hd, wl.K)
+        nb = ds41.sparse_attn_workspace_bytes(wl.m, wl.nh, wl.hd, sz.K)
         if nb:
             out["ws_attn"] = torch.empty(nb, dtype=torch.uint8, device=device)
         nb = ds41.csa_workspace_bytes(wl)
@@ -252,37 +258,39 @@ def slot_bytes(slot) -> int:
 
 
 def launches_per_step(wl) -> int:
-    """Kernels one ds41_csa_forward launches for this workload (mirrors the
-    library's plan: fused few-token step, or the four calls)."""
+    """Kernels one ds41_csa_forward launches for this workload, mirroring the
+    library's plan (fused few-token step, or the four calls).  Used only when
+    the captured graph cannot be inspected (see kernel_nodes)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sz = ds41.step_sizes(wl)
     hpad = (wl.Hi + 7) // 8 * 8
     tt = max(1, 128 // hpad)
     groups = (wl.m + tt - 1) // tt
     dec_groups = wl.m * ((wl.nh + 15) // 16)
     few_attn = dec_groups * 4 <= sms
-    if wl.n_c > 0 and groups <= 4 and few_attn:
+    if sz.n_c > 0 and groups <= 4 and few_attn:
         cl = 16
-        while cl > 1 and (dec_groups * cl > 2 * sms or (wl.K + cl - 1) // cl < 8):
+        while cl > 1 and (dec_groups * cl > 2 * sms or (sz.K + cl - 1) // cl < 8):
             cl //= 2
-        kseg = ((wl.n_c + cl - 1) // cl + 7) // 8 * 8
-        if cl >= 4 and (wl.K + cl - 1) // cl <= 2048 and kseg <= 4096:
-            return 2  # fused front (scores + ring + latent), attention selecting its rows
-        return 3  # fused front, top-k, cluster attention
-    n = 1  # ring write
-    if wl.G > 0:
+        kseg = ((sz.n_c + cl - 1) // cl + 7) // 8 * 8
+        if cl >= 4 and (sz.K + cl - 1) // cl <= 2048 and kseg <= 4096:
+            return 2
+        return 3
+    n = 1
+    if sz.G > 0:
         n += 1
-    if wl.n_c > 0:
-        n += 2  # scores, top-k
+    if sz.n_c > 0:
+        n += 2
         if groups > 4:
-            n += 1  # keys quantised once
+            n += 1
             if wl.Hi == 64 and wl.Di == 128 and (wl.m + 3) // 4 >= sms:
-                n += 1  # queries quantised for the tensor-core scores
+                n += 1
     if few_attn:
-        return n + 1  # few-token cluster kernel
-    if wl.hd == 512 and wl.nh % 64 == 0 and wl.K <= 1024 and wl.m * (wl.nh // 64) >= sms:
-        return n + 1  # persistent tensor-core attention
+        return n + 1
+    if wl.hd == 512 and wl.nh % 64 == 0 and sz.K <= 1024 and wl.m * (wl.nh // 64) >= sms:
+        return n + 1
     heads_groups = (wl.nh + 63) // 64
-    chunks = (wl.K + 31) // 32
+    chunks = (sz.K + 31) // 32
     ctas = wl.m * heads_groups
     splits = 1
     if ctas < sms:
@@ -292,11 +300,42 @@ def launches_per_step(wl) -> int:
     return n + 1 + (1 if splits > 1 else 0)
 
 
+def kernel_nodes(wl, slot, fc, stream):
+    """Kernel launches of one step, counted as the kernel nodes of the step
+    captured in a CUDA graph (driver API cuGraphGetNodes / cuGraphNodeGetType
+    on the captured graph).  Returns (count, how)."""
+    import ctypes
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+        with torch.cuda.graph(g, stream=stream):
+            ds41.csa_forward(slot[0], wl, fc, slot[1])
+        raw = g.raw_cuda_graph()
+        cu = ctypes.CDLL("libcuda.so.1")
+        n = ctypes.c_size_t(0)
+        if cu.cuGraphGetNodes(ctypes.c_void_p(raw), None, ctypes.byref(n)) != 0:
+            raise RuntimeError("cuGraphGetNodes")
+        nodes = (ctypes.c_void_p * max(1, n.value))()
+        if cu.cuGraphGetNodes(ctypes.c_void_p(raw), nodes, ctypes.byref(n)) != 0:
+            raise RuntimeError("cuGraphGetNodes")
+        kinds = []
+        for i in range(n.value):
+            t = ctypes.c_int(-1)
+            if cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) != 0:
+                raise RuntimeError("cuGraphNodeGetType")
+            kinds.append(t.value)
+        del g
+        torch.cuda.synchronize()
+        return sum(1 for k in kinds if k == 0), "kernel nodes of the captured step (CU_GRAPH_NODE_TYPE_KERNEL)"
+    except Exception as e:  # older torch without keep_graph / raw_cuda_graph
+        return launches_per_step(wl), f"the library's launch plan mirrored on the host ({type(e).__name__})"
+
+
 OPS = ["window_ring_write", "compress_latent_write", "indexer_topk", "sparse_attn_sink_fwd"]
 
 
 def call_op(name, wl, inp, out, fc):
     """One call of one entry point on a layer state (outputs preallocated)."""
+    sz = ds41.step_sizes(wl)
     if name == "window_ring_write":
         ds41.window_ring_write(inp["kv"], inp["ring"], out["win_idx"], wl.start_pos,
                                rows_a=out.get("rows_a"))
@@ -304,9 +343,8 @@ def call_op(name, wl, inp, out, fc):
         ds41.compress_latent_write(inp["latent"], fc, inp["cache"], wl.rd, wl.ratio,
                                    wl.start_pos, wl.m)
     elif name == "indexer_topk":
-        n_a = ds41.rows_a_len(wl.m, wl.win, wl.start_pos)
-        ds41.indexer_topk(inp["q_idx"], inp["k_idx"][: wl.n_c], inp["w"], out["win_idx"],
-                          wl.ratio, wl.start_pos, wl.topk, n_a, idx=out["idx"],
+        ds41.indexer_topk(inp["q_idx"], inp["k_idx"][: sz.n_c], inp["w"], out["win_idx"],
+                          wl.ratio, wl.start_pos, wl.topk, sz.n_a, idx=out["idx"],
                           ws=out.get("ws_idx"))
     else:
         if wl.start_pos == 0:
@@ -315,8 +353,8 @@ def call_op(name, wl, inp, out, fc):
             rows_a = inp["ring"]
         else:
             rows_a = out["rows_a"]
-        rows_b = inp["cache"][: wl.n_c] if wl.n_c > 0 else None
-        idx = out["idx"] if wl.n_c > 0 else out["win_idx"]
+        rows_b = inp["cache"][: sz.n_c] if sz.n_c > 0 else None
+        idx = out["idx"] if sz.n_c > 0 else out["win_idx"]
         ds41.sparse_attn_sink_fwd(inp["q"], rows_a, rows_b, idx, inp["sink"], wl.scale,
                                   o=out["o"], ws=out.get("ws_attn"))
 
@@ -324,11 +362,12 @@ def call_op(name, wl, inp, out, fc):
 def time_ops(wl, slots, fc, stream, reps=5):
     """Milliseconds per call of each entry point, from CUDA graphs of one call
     per layer state replayed ``reps`` times (no host launch gaps)."""
+    sz = ds41.step_sizes(wl)
     res = {}
     for name in OPS:
-        if name == "compress_latent_write" and wl.G == 0:
+        if name == "compress_latent_write" and sz.G == 0:
             continue
-        if name == "indexer_topk" and wl.n_c == 0:
+        if name == "indexer_topk" and sz.n_c == 0:
             continue
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -394,7 +433,7 @@ def time_out_proj(wl, slots, fc, stream, hbm, bf16, reps=5):
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
     roof.update({"ms_per_call": ms, "flops": flops, "algorithmic_bytes": nbytes,
                  "config": f"groups {P['groups']}, o_rank {P['o_rank']}, dim {P['dim']}, "
-                           f"synthetic bf16 weights; inverse RoPE kernel + cuBLAS GEMMs"})
+                           "synthetic bf16 weights; inverse RoPE kernel + cuBLAS GEMMs"})
     return roof
 
 
@@ -403,7 +442,7 @@ def time_reuse(wl, slots, stream, reps=5):
     picks (ring write, index merge, attention; not part of the measured step):
     milliseconds per call from a CUDA graph of one call per layer state, each
     on that state's cache and the picks its own step left in idx."""
-    ctopk = wl.K - wl.win
+    ctopk = ds41.step_sizes(wl).ctopk
     cidx = [out["idx"][:, wl.win:].contiguous() if ctopk else None for _, out in slots]
     outs = [{} for _ in slots]
     with torch.cuda.stream(stream):
@@ -427,10 +466,38 @@ def time_reuse(wl, slots, stream, reps=5):
             "steps": "ring write, index merge (when the layer has compressed picks), attention"}
 
 
-def run_ours(args, world, rank, local):
-    wl = WORKLOADS[args.workload]
-    dev = torch.device("cuda", local)
-    ds41.load()
+def dominant_roofline(wl, op_ms, args):
+    """The roofline of the op that takes longest per call: algorithmic flops on
+    the bf16 tensor peak for many-token attention, algorithmic bytes on HBM
+    otherwise."""
+    alg = algorithmic(wl)
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    dom = max(op_ms, key=lambda k: op_ms[k])
+    d_ms = op_ms[dom]
+    if wl.m >= 256 and dom == "sparse_attn_sink_fwd":
+        achieved = alg[dom]["flops"] / (d_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                "frac": achieved / bf16}
+    else:
+        achieved = alg[dom]["bytes"] / (d_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm}
+    traffic = args.traffic if (args.traffic is not None and wl.name == args.workload) \
+        else recorded_traffic(wl.name, dom)
+    roof.update({"kernel": dom, "ms_per_launch": d_ms, "algorithmic_bytes": alg[dom]["bytes"],
+                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
+                 else "fallback",
+                 "traffic": traffic})
+    if "flops" in alg[dom]:
+        roof["algorithmic_flops"] = alg[dom]["flops"]
+    return roof
+
+
+def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
+    """The measurement of one workload: K timed CUDA-graph steps (max over
+    ranks), the dominant op's roofline, per-op times, e2e through the host
+    buffer API, the kernel launches in the timed region, clocks, and (with
+    ``extras``) the next rows of the layer."""
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
     fc = ds41.yarn_freqs_cis(wl.rd, wl.max_pos, device=dev)
@@ -441,12 +508,12 @@ def run_ours(args, world, rank, local):
     slots = one + (build_slots(wl, n_slots - 1, dev, seed0=2000) if n_slots > 1 else [])
     torch.cuda.synchronize()
 
-    stream = torch.cuda.Stream(device=dev)
     # eager warm-up of every slot (sets kernel attributes, status word)
     with torch.cuda.stream(stream):
         for inp, out in slots:
             ds41.csa_forward(inp, wl, fc, out)
     stream.synchronize()
+    launches, launches_how = kernel_nodes(wl, slots[0], fc, stream)
 
     graphs = []
     for inp, out in slots:
@@ -456,13 +523,12 @@ def run_ours(args, world, rank, local):
         graphs.append(g)
     torch.cuda.synchronize()
 
-    K, W = args.steps, args.warmup
     with torch.cuda.stream(stream):
         for i in range(W):
             graphs[i % n_slots].replay()
     stream.synchronize()
 
-    clocks = Clocks(local)
+    clocks = Clocks(dev.index if dev.index is not None else 0)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -479,57 +545,70 @@ def run_ours(args, world, rank, local):
     ck = clocks.stop()
     t_ms = e0.elapsed_time(e1)
     t_max_ms = max_over_ranks(t_ms, world)
-    value = wl.m * K * world / (t_max_ms / 1e3)
+    del graphs
 
-    # ---- per-op timing: each op alone, captured as one CUDA graph of
-    # back-to-back calls over the rotating layer states, replayed and timed
-    # with events on the launching stream
     op_ms = time_ops(wl, slots, fc, stream)
-    alg = algorithmic(wl)
-    hbm, bf16, bf16_sus, peak_src = load_peaks()
-    ops = list(op_ms)
-    dom = max(ops, key=lambda k: op_ms[k])
-    d_ms = op_ms[dom]
-    if wl.m >= 256 and dom == "sparse_attn_sink_fwd":
-        achieved = alg[dom]["flops"] / (d_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                "frac": achieved / bf16}
-    else:
-        achieved = alg[dom]["bytes"] / (d_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm}
-    roof.update({"kernel": dom, "ms_per_launch": d_ms, "algorithmic_bytes": alg[dom]["bytes"],
-                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
-                 else "fallback",
-                 "traffic": args.traffic if args.traffic is not None else recorded_traffic(wl.name, dom)})
+    roof = dominant_roofline(wl, op_ms, args)
+    # e2e: at most 20 steps for the big prefills (hundreds of MB of copies each)
+    k_e2e = K if wl.m < 256 else min(K, 20)
+    e2e = run_e2e(wl, slots, fc, stream, k_e2e, W, n_slots, world)
+    res = {"value": wl.m * K * world / (t_max_ms / 1e3), "unit": "query-tokens/s",
+           "steps": K, "warmup": W, "ms_per_step": t_max_ms / K,
+           "workload": workload_desc(wl),
+           "l2": f"inputs larger than L2: {n_slots} rotating layer states x "
+                 f"{per / 2**20:.2f} MiB = {n_slots * per / 2**20:.0f} MiB "
+                 f"(L2 {l2 / 2**20:.0f} MiB)",
+           "roofline": roof, "per_op_ms": op_ms, "e2e": e2e,
+           "gpu_launches": launches * K, "gpu_launches_per_step": launches,
+           "gpu_launches_how": launches_how, "clocks": ck}
+    if extras:
+        hbm, bf16, _, _ = load_peaks()
+        out_proj = time_out_proj(wl, slots, fc, stream, hbm, bf16) if wl.hd == 512 else None
+        reuse = time_reuse(wl, slots, stream)
+        res["next_rows"] = dict({"attn_out_proj": out_proj} if out_proj else {},
+                                csa_forward_reuse=reuse)
+    del slots, one
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
-    # ---- end to end through the public API with host buffers
-    e2e = run_e2e(wl, slots, fc, stream, K, W, n_slots, world)
 
-    # ---- the next rows of the layer (not in the step): the output side, and
-    # the step of a layer that reuses a source layer's rows and picks
-    out_proj = time_out_proj(wl, slots, fc, stream, hbm, bf16) if wl.hd == 512 else None
-    reuse = time_reuse(wl, slots, stream)
-
+def run_ours(args, world, rank, local):
+    wl = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    ds41.load()
+    stream = torch.cuda.Stream(device=dev)
+    K, W = args.steps, args.warmup
+    head = measure_workload(wl, K, W, world, dev, stream, args)
+    configs = {}
+    if not args.headline_only:
+        for name in CONFIG_ORDER:
+            if name == wl.name:
+                continue
+            configs[name] = measure_workload(WORKLOADS[name], K, W, world, dev, stream, args,
+                                             extras=False)
     res = {
-        "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
-        "steps": K, "warmup": W, "ms_per_step": t_max_ms / K, "higher_is_better": True,
+        "metric": METRIC, "value": head["value"], "unit": "query-tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(wl),
+        "config": {"workload": head["workload"],
                    "global_batch": wl.m * world, "parallelism": f"replicas{world}",
-                   "l2": f"inputs larger than L2: {n_slots} rotating layer states x "
-                         f"{per / 2**20:.2f} MiB = {n_slots * per / 2**20:.0f} MiB "
-                         f"(L2 {l2 / 2**20:.0f} MiB)",
+                   "l2": head["l2"],
                    "timing": "CUDA-graph replay per step, CUDA events on the launching stream"},
-        "roofline": roof,
-        "per_op_ms": op_ms,
-        "next_rows": dict({"attn_out_proj": out_proj} if out_proj else {},
-                          csa_forward_reuse=reuse),
-        "e2e": e2e,
-        "gpu_launches": launches_per_step(wl) * K,
-        "clocks": ck,
+        "roofline": head["roofline"],
+        "per_op_ms": head["per_op_ms"],
+        "next_rows": head["next_rows"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "gpu_launches_how": head["gpu_launches_how"],
+        "clocks": head["clocks"],
     }
+    if configs:
+        res["configs"] = configs
     return res, wl
+
+
+CONFIG_ORDER = ["tiny_prefill", "decode", "prefill", "long_decode", "chunked_prefill"]
 
 
 def run_only(args, local):
@@ -540,6 +619,7 @@ def run_only(args, local):
     ds41.load()
     fc = ds41.yarn_freqs_cis(wl.rd, wl.max_pos, device=dev)
     slots = build_slots(wl, args.slots, dev)
+    sz = ds41.step_sizes(wl)
     for inp, out in slots:
         ds41.forward(inp, wl, fc, out)  # fills win_idx / idx / o for the later ops
     P = OUT_PROJ
@@ -552,7 +632,7 @@ def run_only(args, local):
             out["proj"] = torch.empty(wl.m, P["dim"], dtype=torch.float32, device=dev)
     elif args.only == "csa_forward_reuse":
         for inp, out in slots:
-            out["cidx"] = out["idx"][:, wl.win:].contiguous() if wl.K > wl.win else None
+            out["cidx"] = out["idx"][:, wl.win:].contiguous() if sz.ctopk else None
             out["reuse"] = {}
     torch.cuda.synchronize()
 
@@ -560,20 +640,8 @@ def run_only(args, local):
         inp, out = slots[i % len(slots)]
         if args.only == "step":
             ds41.csa_forward(inp, wl, fc, out)
-        elif args.only == "window_ring_write":
-            ds41.window_ring_write(inp["kv"], inp["ring"], out["win_idx"], wl.start_pos,
-                                   rows_a=out.get("rows_a"))
-        elif args.only == "compress_latent_write":
-            ds41.compress_latent_write(inp["latent"], fc, inp["cache"], wl.rd, wl.ratio,
-                                       wl.start_pos, wl.m)
-        elif args.only == "indexer_topk":
-            ds41.indexer_topk(inp["q_idx"], inp["k_idx"][: wl.n_c], inp["w"], out["win_idx"],
-                              wl.ratio, wl.start_pos, wl.topk, wl.n_a, idx=out["idx"],
-                              ws=out.get("ws_idx"))
-        elif args.only == "sparse_attn_sink_fwd":
-            rows_a = {0: inp["kv"]}.get(wl.start_pos, inp["ring"] if wl.m == 1 else out.get("rows_a"))
-            ds41.sparse_attn_sink_fwd(inp["q"], rows_a, inp["cache"][: wl.n_c], out["idx"],
-                                      inp["sink"], wl.scale, o=out["o"], ws=out.get("ws_attn"))
+        elif args.only in OPS:
+            call_op(args.only, wl, inp, out, fc)
         elif args.only == "attn_out_proj":
             ds41.attn_out_proj(out["o"], fc, wts["wo_a"], wts["wo_b"], wl.rd, P["groups"],
                                wl.start_pos, og=out["og"], out=out["proj"])
@@ -636,7 +704,7 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots, world=1):
     wall = time.perf_counter() - t0
     ms = max_over_ranks(max(e0.elapsed_time(e1), wall * 1e3), world)
     return {"value": wl.m * K * world / (ms / 1e3), "unit": "query-tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "how": "ds41_csa_forward_host per step (prepared call): one pinned H2D of "
                    "q/kv/latent/q_idx/w, the step, D2H of o, one stream"}
 
@@ -644,49 +712,97 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots, world=1):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
-def oracle_rate(wl, steps=None, budget_s=None):
-    """Time the oracle's whole forward on a bounded sample of the workload:
-    ``steps`` forwards (or as many as fit in ``budget_s``), each over at most
-    8 query tokens (ring and latent writes run whole every time)."""
-    import numpy as np
+STAGES = ["window_ring_write", "compress_latent_write", "indexer_topk", "sparse_attn_sink_fwd"]
 
-    import oracle
+
+def _oracle_inputs(wl):
     from compressed_sparse_attention_window_gb300.workloads import bf16_bits
     inp = make_inputs(wl)
     b = {k: bf16_bits(inp[k]) for k in ("q", "kv", "latent", "q_idx", "ring", "cache", "k_idx")}
-    sink, w = inp["sink"].numpy(), inp["w"].numpy()
+    return b, inp["sink"].numpy(), inp["w"].numpy()
+
+
+def oracle_stage_rates(wl, budget_s, threads, toks_per=8, min_forwards=1, seed=0):
+    """The oracle's forward (``oracle.forward``) timed stage by stage on a
+    bounded sample of the workload, with ``threads`` OpenMP threads: repeated
+    forwards, each running the ring and latent writes whole and the indexer +
+    top-k and the attention for ``toks_per`` sampled query tokens, until
+    ``budget_s`` seconds (at least ``min_forwards`` forwards).  Per stage,
+    query-tokens/s = tokens the stage processed / its seconds (m per forward
+    for the two writes, the sampled tokens for the other two); the whole step
+    rate adds the stages' seconds per token."""
+    import numpy as np
+
+    import oracle
+    b, sink, w = _oracle_inputs(wl)
     fc = oracle.yarn_freqs_cis(wl.rd, wl.max_pos)
-    toks_per = min(wl.m, 8)
-    rng = np.random.default_rng(0)
-    done_tokens, n = 0, 0
+    prev = oracle.num_threads()
+    oracle.set_num_threads(threads)
+    used = oracle.num_threads()
+    rng = np.random.default_rng(seed)
+    tp = min(wl.m, toks_per)
+    timings, n, sampled = {}, 0, 0
     t0 = time.perf_counter()
-    while True:
-        if steps is not None and n >= steps:
-            break
-        if budget_s is not None and time.perf_counter() - t0 >= budget_s:
-            break
-        toks = sorted(rng.choice(wl.m, toks_per, replace=False).tolist()) if wl.m > 1 else [0]
-        ring, rows_a = oracle.window_ring_write(b["kv"], b["ring"], wl.win, wl.start_pos)
-        win_idx = oracle.window_topk_idxs(wl.win, wl.m, wl.start_pos)
-        cache, _, _ = oracle.compress_latent_write(b["latent"], fc, b["cache"], wl.rd, wl.ratio,
-                                                   wl.start_pos)
-        if wl.n_c > 0:
-            sc, _ = oracle.indexer_scores(b["q_idx"], b["k_idx"][: wl.n_c], w, wl.ratio,
-                                          wl.start_pos, tokens=toks)
-            idx = oracle.topk_merge(sc, win_idx[toks], wl.n_c, wl.win, wl.ratio, wl.start_pos,
-                                    wl.topk, wl.n_a, tokens=toks)
-            rows_b = cache[: wl.n_c]
-        else:
-            idx, rows_b = win_idx[toks], None
-        oracle.sparse_attn(b["q"], rows_a, rows_b, idx, sink, wl.scale, tokens=toks)
-        done_tokens += len(toks)
-        n += 1
+    try:
+        while n < min_forwards or time.perf_counter() - t0 < budget_s:
+            toks = sorted(rng.choice(wl.m, tp, replace=False).tolist()) if wl.m > 1 else [0]
+            oracle.forward(b["kv"], b["ring"], b["latent"], b["cache"], b["q_idx"], b["k_idx"],
+                           w, b["q"], sink, win=wl.win, ratio=wl.ratio, start_pos=wl.start_pos,
+                           topk=wl.topk, rd=wl.rd, tokens=toks, fc=fc, timings=timings)
+            n += 1
+            sampled += len(toks)
+    finally:
+        oracle.set_num_threads(prev)
     el = time.perf_counter() - t0
-    return {"value": done_tokens / el, "unit": "query-tokens/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": el,
-            "sample": f"{n} oracle forwards of {toks_per} query token(s) each "
-                      f"({done_tokens} tokens, {el:.1f} s) on the {wl.name} workload; the ring "
-                      f"and latent writes run whole every time"}
+    per = {}
+    sec_per_token = 0.0
+    for st in STAGES:
+        if st not in timings:
+            continue
+        tokens = n * wl.m if st in ("window_ring_write", "compress_latent_write") else sampled
+        per[st] = {"seconds": timings[st], "tokens": tokens,
+                   "query_tokens_per_s": tokens / timings[st] if timings[st] > 0 else None}
+        sec_per_token += timings[st] / tokens
+    return {"value": 1.0 / sec_per_token, "threads": used, "forwards": n,
+            "sampled_tokens": sampled, "seconds": el, "per_stage": per}
+
+
+def oracle_baseline(wl, budget_s):
+    """cpu_baseline: the oracle as it stands, single-threaded and on all host
+    cores, per stage, about ``budget_s`` seconds in all (a third single)."""
+    import oracle
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    single = oracle_stage_rates(wl, budget_s / 3.0, 1, toks_per=2 if wl.m > 1 else 1)
+    par = oracle_stage_rates(wl, 2.0 * budget_s / 3.0, cores)
+    return {"value": par["value"], "unit": "query-tokens/s", "cores": par["threads"],
+            "kind": "oracle",
+            "sample": (f"{wl.name}: {par['forwards']} oracle forwards on {par['threads']} threads "
+                       f"({par['sampled_tokens']} sampled query tokens through the indexer + "
+                       f"top-k and the attention, the ring and latent writes whole each time, "
+                       f"{par['seconds']:.1f} s), and {single['forwards']} single-threaded "
+                       f"({single['sampled_tokens']} sampled tokens, {single['seconds']:.1f} s); "
+                       f"value = the whole step's rate on all cores, extrapolated from the "
+                       f"per-stage seconds per token"),
+            "host_cores": cores,
+            "per_stage": {st: {"omp": par["per_stage"][st]["query_tokens_per_s"],
+                               "single": single["per_stage"][st]["query_tokens_per_s"]}
+                          for st in par["per_stage"]},
+            "single_thread": {"value": single["value"], "unit": "query-tokens/s"}}
+
+
+def oracle_rate(wl, steps=None, budget_s=None):
+    """The reference arm's measure: ``steps`` oracle forwards on all host
+    cores (see oracle_stage_rates), whole-step query-tokens/s."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    r = oracle_stage_rates(wl, 0.0 if steps else (budget_s or 0.0), cores,
+                           min_forwards=steps or 1)
+    return {"value": r["value"], "unit": "query-tokens/s", "cores": r["threads"], "kind": "oracle",
+            "seconds": r["seconds"],
+            "sample": f"{r['forwards']} oracle forwards of {r['sampled_tokens'] // max(1, r['forwards'])} "
+                      f"sampled query token(s) each on the {wl.name} workload ({r['seconds']:.1f} s), "
+                      f"the ring and latent writes whole each time; value extrapolated from the "
+                      f"per-stage seconds per token",
+            "per_stage": {k: v["query_tokens_per_s"] for k, v in r["per_stage"].items()}}
 
 
 def workload_desc(wl) -> str:
@@ -709,7 +825,8 @@ def run_reference(args, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_desc(wl), "global_batch": wl.m,
                        "parallelism": "cpu oracle, bounded sample (see cpu_baseline.sample)"},
-            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample",
+                                                "per_stage")},
             "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -721,10 +838,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--headline-only", action="store_true",
+                    help="measure only --workload, not the other four under 'configs'")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
-                    help="seconds of CPU oracle work for the cpu_baseline field")
+                    help="seconds of CPU oracle work for the headline's cpu_baseline "
+                         "(a quarter of it for each other workload)")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per call of the dominant op (default: "
+                    help="ncu dram bytes per call of the headline's dominant op (default: "
                          "profiles/dram_traffic.txt when taken on the current sources)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
@@ -745,8 +865,9 @@ def main():
         res, wl = run_ours(args, world, rank, local)
         if rank == 0:
             if world == 1 and not args.no_cpu_baseline:
-                cb = oracle_rate(wl, budget_s=args.cpu_budget)
-                res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+                res["cpu_baseline"] = oracle_baseline(wl, args.cpu_budget)
+                for name, c in res.get("configs", {}).items():
+                    c["cpu_baseline"] = oracle_baseline(WORKLOADS[name], args.cpu_budget / 4.0)
             print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -144,10 +144,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// A bounded wait that also gives up once another role has given up.
+// A bounded wait that also gives up once another role has given up.  After
+// `polls` polls (about a second for the default) it sets the abort flag,
+// raises DS41_E_TIMEOUT in the status word and returns false.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_f,
-                                         unsigned int* status) {
-    for (uint32_t i = 0; i < kWaitPolls; i++) {
+                                         unsigned int* status, uint32_t polls = kWaitPolls) {
+    for (uint32_t i = 0; i < polls; i++) {
         uint32_t done;
         asm volatile(
             "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"

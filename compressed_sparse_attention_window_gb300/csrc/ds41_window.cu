@@ -30,6 +30,25 @@ extern "C" int64_t ds41_rows_a_len(int64_t m, int64_t win, int64_t start_pos) {
     return win + m;
 }
 
+extern "C" int ds41_step_sizes(int64_t m, int64_t start_pos, int64_t win, int64_t ratio,
+                               int64_t topk, int64_t* out) {
+    const char* name = "ds41_step_sizes";
+    DS41_REQUIRE(out, DS41_E_ARG, "%s: out is NULL", name);
+    DS41_REQUIRE(m >= 1 && start_pos >= 0 && start_pos + m < (int64_t(1) << 31), DS41_E_RANGE,
+                 "%s: m=%lld start_pos=%lld", name, (long long)m, (long long)start_pos);
+    DS41_REQUIRE(win >= 1 && ratio >= 1 && topk >= 1, DS41_E_ARG,
+                 "%s: win=%lld ratio=%lld topk=%lld", name, (long long)win, (long long)ratio,
+                 (long long)topk);
+    const int64_t n_c = (start_pos + m) / ratio;  // compress_len
+    const int64_t ctopk = n_c == 0 ? 0 : (topk < n_c ? topk : n_c);
+    out[0] = ds41_rows_a_len(m, win, start_pos);
+    out[1] = n_c;
+    out[2] = n_c - start_pos / ratio;  // groups this call completes
+    out[3] = ctopk;
+    out[4] = win + ctopk;
+    return DS41_OK;
+}
+
 extern "C" int ds41_window_ring_write(const ds41_bf16* kv, ds41_bf16* ring, ds41_bf16* rows_a,
                                       int32_t* win_idx, int64_t* n_a, int64_t m, int64_t hd,
                                       int64_t win, int64_t start_pos, ds41_stream_t stream) {

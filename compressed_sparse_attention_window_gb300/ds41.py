@@ -10,7 +10,7 @@ from __future__ import annotations
 import ctypes
 import math
 import os
-from typing import Dict, Optional, Tuple
+from typing import Dict, NamedTuple, Optional, Tuple
 
 import torch
 
@@ -35,6 +35,7 @@ SIGNATURES = {
     "ds41_fp4_quant_e4m3": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _P]),
     "ds41_yarn_freqs_cis": (ctypes.c_int, [_P, _I64, _I64, _I64, _F, _F, _F, _F, _P]),
     "ds41_rows_a_len": (_I64, [_I64, _I64, _I64]),
+    "ds41_step_sizes": (ctypes.c_int, [_I64, _I64, _I64, _I64, _I64, _P]),
     "ds41_window_ring_write": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "ds41_compress_latent_write": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _I64, _I64, _I64,
                                                   _I64, _I64, _I64, _P]),
@@ -57,6 +58,7 @@ SIGNATURES = {
     "ds41_step_inputs_bytes": (_SZ, [_I64] * 7),
     "ds41_csa_forward_host_packed": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _F,
                                                     _P, _P, _P, _P] + [_I64] * 10 + [_P, _SZ, _P]),
+    "ds41_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, ctypes.c_int, _P, _P]),
     "ds41_sparse_attn_noalloc_capacity": (_SZ, []),
     "ds41_sparse_attn_sink_fwd_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F,
                                                          _P, _P, _I64, _I64, _I64, _P]),
@@ -123,6 +125,16 @@ def device_status(reset: bool = True) -> int:
     return int(v.value)
 
 
+def selftest_wait_timeout(polls: int, arrive: bool, result: torch.Tensor) -> None:
+    """ds41_selftest_wait_timeout: one bounded mbarrier wait of ``polls`` polls
+    that runs out (arrive False) or completes (arrive True); ``result`` is an
+    int32 CUDA tensor of at least 2 elements."""
+    if result.numel() < 2:
+        raise ValueError("result: at least 2 int32 elements")
+    _call("ds41_selftest_wait_timeout", int(polls), 1 if arrive else 0,
+          _ptr(result, torch.int32, "result"), _stream())
+
+
 def fp4_quant(x: torch.Tensor, e4m3: bool, want_codes: bool = False):
     """ds41_fp4_quant_e8m0 (block 32) / ds41_fp4_quant_e4m3 (block 16) on the
     rows of a 2-D bf16 tensor.  Returns y, or (y, codes, scales)."""
@@ -150,6 +162,23 @@ def yarn_freqs_cis(dim: int, seqlen: int, original_seq_len: int = 65536, base: f
 
 def rows_a_len(m: int, win: int, start_pos: int) -> int:
     return int(load().ds41_rows_a_len(m, win, start_pos))
+
+
+class StepSizes(NamedTuple):
+    """Row counts of one call, from ds41_step_sizes."""
+    n_a: int    # rows the window indices point into; offset of the picks
+    n_c: int    # compress_len: compressed rows after the call
+    G: int      # groups (latent rows) the call completes
+    ctopk: int  # compressed picks per query
+    K: int      # merged index row length, win + ctopk
+
+
+def step_sizes(wl) -> StepSizes:
+    """ds41_step_sizes for the call parameters of ``wl`` (m, start_pos, win,
+    ratio, topk)."""
+    a = (ctypes.c_int64 * 5)()
+    _call("ds41_step_sizes", wl.m, wl.start_pos, wl.win, wl.ratio, wl.topk, ctypes.addressof(a))
+    return StepSizes(*[int(v) for v in a])
 
 
 def window_ring_write(kv: torch.Tensor, ring: torch.Tensor, win_idx: torch.Tensor, start_pos: int,
@@ -212,6 +241,35 @@ def indexer_topk(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor,
     return idx
 
 
+def _check_attn(q, rows_a, rows_b, idx, sink, o, lse) -> None:
+    """Shapes and device of the attention's tensors, checked before the C call
+    (the C ABI sees only pointers, so an undersized o or lse would be written
+    past its end on the device)."""
+    if q.dim() != 3:
+        raise ValueError(f"q: expected [m, nh, hd], got {tuple(q.shape)}")
+    m, nh, hd = q.shape
+    dev = q.device
+    if dev.type != "cuda" or dev.index != torch.cuda.current_device():
+        raise ValueError(f"q is on {dev}, the current device is cuda:{torch.cuda.current_device()}: "
+                         "the call runs on the current device's stream")
+    for name, t in (("rows_a", rows_a), ("rows_b", rows_b), ("idx", idx), ("sink", sink),
+                    ("o", o), ("lse", lse)):
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, q on {dev}")
+    if rows_a.dim() != 2 or rows_a.shape[1] != hd:
+        raise ValueError(f"rows_a: expected [n_a, {hd}], got {tuple(rows_a.shape)}")
+    if rows_b is not None and (rows_b.dim() != 2 or rows_b.shape[1] != hd):
+        raise ValueError(f"rows_b: expected [n_c, {hd}], got {tuple(rows_b.shape)}")
+    if idx.dim() != 2 or idx.shape[0] != m:
+        raise ValueError(f"idx: expected [{m}, K], got {tuple(idx.shape)}")
+    if tuple(sink.shape) != (nh,):
+        raise ValueError(f"sink: expected [{nh}], got {tuple(sink.shape)}")
+    if o is not None and tuple(o.shape) != (m, nh, hd):
+        raise ValueError(f"o: expected {(m, nh, hd)}, got {tuple(o.shape)}")
+    if lse is not None and tuple(lse.shape) != (m, nh):
+        raise ValueError(f"lse: expected {(m, nh)}, got {tuple(lse.shape)}")
+
+
 def sparse_attn_workspace_bytes(m, nh, hd, K) -> int:
     return int(load().ds41_sparse_attn_workspace_bytes(m, nh, hd, K))
 
@@ -221,6 +279,7 @@ def sparse_attn_sink_fwd(q: torch.Tensor, rows_a: torch.Tensor, rows_b: Optional
                          o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                          ws: Optional[torch.Tensor] = None) -> torch.Tensor:
     """ds41_sparse_attn_sink_fwd: o [m, nh, hd] bf16 (lse [m, nh] f32 if given)."""
+    _check_attn(q, rows_a, rows_b, idx, sink, o, lse)
     m, nh, hd = q.shape
     K = idx.shape[1]
     n_a = rows_a.shape[0]
@@ -248,7 +307,11 @@ def sparse_attn_sink_fwd_noalloc(q: torch.Tensor, rows_a: torch.Tensor,
                                  lse: Optional[torch.Tensor] = None) -> torch.Tensor:
     """ds41_sparse_attn_sink_fwd_noalloc: the attention for callers that cannot
     allocate device memory; the library's static scratch holds the split
-    partials.  ``o`` (and ``lse``) must be provided by the caller."""
+    partials.  ``o`` (and ``lse``) must be provided by the caller, on the
+    current device like every other tensor."""
+    if o is None:
+        raise ValueError("o: the caller provides the output")
+    _check_attn(q, rows_a, rows_b, idx, sink, o, lse)
     m, nh, hd = q.shape
     K = idx.shape[1]
     n_c = 0 if rows_b is None else rows_b.shape[0]
@@ -326,10 +389,11 @@ def csa_forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
     out = {} if out is None else out
     dev = inp["q"].device
     m, win = wl.m, wl.win
+    sz = step_sizes(wl)
     if "win_idx" not in out:
         out["win_idx"] = torch.empty(m, win, dtype=torch.int32, device=dev)
     if "idx" not in out:
-        out["idx"] = torch.empty(m, wl.K, dtype=torch.int32, device=dev)
+        out["idx"] = torch.empty(m, sz.K, dtype=torch.int32, device=dev)
     if "o" not in out:
         out["o"] = torch.empty_like(inp["q"])
     chunk = wl.start_pos > 0 and m > 1
@@ -341,7 +405,7 @@ def csa_forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
         ws = out["ws_csa"] = torch.empty(need, dtype=torch.uint8, device=dev)
     _call("ds41_csa_forward", _ptr(inp["q"], _BF, "q"), _ptr(inp["kv"], _BF, "kv"),
           _ptr(inp["ring"], _BF, "ring"), _ptr(out.get("rows_a") if chunk else None),
-          _ptr(inp["latent"], _BF, "latent") if wl.G > 0 else None,
+          _ptr(inp["latent"], _BF, "latent") if sz.G > 0 else None,
           _ptr(freqs_cis, torch.float32, "freqs_cis"), freqs_cis.shape[0],
           _ptr(inp["cache"], _BF, "cache"), inp["cache"].shape[0], _ptr(inp["q_idx"], _BF, "q_idx"),
           _ptr(inp["k_idx"], _BF, "k_idx"), _ptr(inp["w"], torch.float32, "w"),
@@ -350,7 +414,7 @@ def csa_forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
           _ptr(out["o"], _BF, "o"), _ptr(out.get("lse"), torch.float32, "lse"), m, wl.start_pos,
           wl.nh, wl.hd, wl.rd, win, wl.ratio, wl.topk, wl.Hi, wl.Di, _ptr(ws) if need else None,
           need, _stream())
-    if wl.n_c == 0:
+    if sz.n_c == 0:
         out["idx"] = out["win_idx"]
     return out
 
@@ -365,7 +429,7 @@ def step_input_buffers(wl, device="cpu", pinned: bool = False) -> Dict[str, torc
     buffers built this way let ds41_csa_forward_host move a step's inputs in
     one copy."""
     shapes = [("q", (wl.m, wl.nh, wl.hd), _BF), ("kv", (wl.m, wl.hd), _BF),
-              ("latent", (max(wl.G, 0), wl.hd), _BF), ("q_idx", (wl.m, wl.Hi, wl.Di), _BF),
+              ("latent", (step_sizes(wl).G, wl.hd), _BF), ("q_idx", (wl.m, wl.Hi, wl.Di), _BF),
               ("w", (wl.m, wl.Hi), torch.float32)]
     sizes = [math.prod(sh) * (2 if dt == _BF else 4) for _, sh, dt in shapes]
     block = torch.empty(sum(sizes), dtype=torch.uint8, device=device)
@@ -416,8 +480,9 @@ class HostStep:
         out = {} if out is None else out
         dev = inp["q"].device
         m, win = wl.m, wl.win
+        sz = step_sizes(wl)
         for k in STEP_INPUTS:
-            if k == "latent" and wl.G <= 0:
+            if k == "latent" and sz.G <= 0:
                 continue
             t, d = host[k], inp[k]
             if t.is_cuda or t.dtype != d.dtype or not t.is_contiguous() or t.shape != d.shape:
@@ -430,7 +495,7 @@ class HostStep:
         if "win_idx" not in out:
             out["win_idx"] = torch.empty(m, win, dtype=torch.int32, device=dev)
         if "idx" not in out:
-            out["idx"] = torch.empty(m, wl.K, dtype=torch.int32, device=dev)
+            out["idx"] = torch.empty(m, sz.K, dtype=torch.int32, device=dev)
         if "o" not in out:
             out["o"] = torch.empty_like(inp["q"])
         chunk = wl.start_pos > 0 and m > 1
@@ -440,7 +505,7 @@ class HostStep:
         ws = out.get("ws_csa")
         if need and (ws is None or ws.numel() < need):
             ws = out["ws_csa"] = torch.empty(need, dtype=torch.uint8, device=dev)
-        g = wl.G > 0
+        g = sz.G > 0
         self.packed = _packed(host, wl) and _packed(inp, wl) and inp["q"].data_ptr() % 16 == 0
         if self.packed:
             # one block each side: ds41_csa_forward_host_packed, one copy in
@@ -474,7 +539,7 @@ class HostStep:
         self._keep = (host, inp, out, freqs_cis)  # the buffers stay alive with the call
         self._fn = getattr(load(), self._name)
         self.h_o = h_o
-        if wl.n_c == 0:
+        if sz.n_c == 0:
             out["idx"] = out["win_idx"]
 
     def __call__(self, stream: Optional[int] = None) -> torch.Tensor:
@@ -510,15 +575,16 @@ def forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
                                rows_a=out.get("rows_a"))
     if wl.start_pos > 0 and m > 1:
         out["rows_a"] = rows_a
-    if wl.G > 0:
+    sz = step_sizes(wl)
+    if sz.G > 0:
         compress_latent_write(inp["latent"], freqs_cis, inp["cache"], wl.rd, wl.ratio,
                               wl.start_pos, m)
     n_a = rows_a.shape[0]
-    if wl.n_c > 0:
-        idx = indexer_topk(inp["q_idx"], inp["k_idx"][: wl.n_c], inp["w"], out["win_idx"],
+    if sz.n_c > 0:
+        idx = indexer_topk(inp["q_idx"], inp["k_idx"][: sz.n_c], inp["w"], out["win_idx"],
                            wl.ratio, wl.start_pos, wl.topk, n_a, idx=out.get("idx"),
                            ws=out.get("ws_idx"))
-        rows_b = inp["cache"][: wl.n_c]
+        rows_b = inp["cache"][: sz.n_c]
     else:
         idx = out["win_idx"]
         rows_b = None

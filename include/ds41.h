@@ -102,6 +102,20 @@ int ds41_yarn_freqs_cis(float* out, int64_t dim, int64_t seqlen, int64_t origina
  * position 0.  Host function, no device work. */
 int64_t ds41_rows_a_len(int64_t m, int64_t win, int64_t start_pos);
 
+/* The row counts of a call of m tokens at start_pos (host function, no device
+ * work), written to the host array out[5]:
+ *   out[0] n_a   = ds41_rows_a_len(m, win, start_pos), the offset of the picks
+ *   out[1] n_c   = (start_pos + m)/ratio, compress_len of forward.rs and
+ *                  compress.rs (compressed rows that exist after the call)
+ *   out[2] G     = n_c - start_pos/ratio, the groups the call completes (the
+ *                  latent rows it writes, from cache row start_pos/ratio on)
+ *   out[3] ctopk = min(topk, n_c) (0 when n_c == 0: no indexer runs)
+ *   out[4] K     = win + ctopk, the length of a merged index row
+ * DS41_E_ARG for a NULL out or win, ratio or topk below 1; DS41_E_RANGE for
+ * m < 1, start_pos < 0 or start_pos + m >= 2^31. */
+int ds41_step_sizes(int64_t m, int64_t start_pos, int64_t win, int64_t ratio, int64_t topk,
+                    int64_t* out /* host [5] */);
+
 /* forward.rs, "the window ring" block, and compress.rs attention_any's ring
  * update: the row of position q goes to ring slot q mod win; when m > win
  * only the newest row of each slot is kept.  Also writes the window indices
@@ -334,7 +348,8 @@ int ds41_csa_forward_host_packed(const void* h_in, void* d_in, ds41_bf16* h_o, d
  * contents; nothing in it has to start at zero, because each split writes its
  * partial before the merge reads it.  Calls whose work overlaps on the GPU
  * (on different streams, or on different host threads) race on the array:
- * order them on one stream. */
+ * order them on one stream.  All tensors must be on the current device, whose
+ * array the call uses. */
 size_t ds41_sparse_attn_noalloc_capacity(void);
 
 int ds41_sparse_attn_sink_fwd_noalloc(const ds41_bf16* q, const ds41_bf16* rows_a, int64_t n_a,
@@ -342,6 +357,24 @@ int ds41_sparse_attn_sink_fwd_noalloc(const ds41_bf16* q, const ds41_bf16* rows_
                                       int64_t K, const float* sink, float scale, ds41_bf16* o,
                                       float* lse, int64_t m, int64_t nh, int64_t hd,
                                       ds41_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Self-test of the bounded device waits                                      */
+/* ------------------------------------------------------------------------ */
+/* No counterpart on the pages.  Every mbarrier wait in the tensor-core and
+ * decode kernels gives up after a bound (about a second): it sets the
+ * kernel's abort flag, raises DS41_E_TIMEOUT in the device status word, and
+ * the kernel drains its copies, frees its tensor memory and returns, so the
+ * context stays usable.  This call runs that path on purpose: one CTA that
+ * holds 32 columns of tensor memory waits `polls` polls (1 .. 2^22) on an
+ * mbarrier of count 1.  With arrive == 0 nobody arrives, the wait runs out
+ * and DS41_E_TIMEOUT is raised; with arrive != 0 the thread arrives first and
+ * the wait completes.
+ *   result [2] int32 device output (16-byte aligned): result[0] = 1 if the
+ *          wait completed, 0 if it gave up; result[1] = the abort flag as
+ *          another warp reads it afterwards.
+ * Errors: DS41_E_ARG (bad pointer or polls), DS41_E_CUDA (launch). */
+int ds41_selftest_wait_timeout(uint32_t polls, int arrive, int32_t* result, ds41_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* The output side of the layer                                               */

@@ -80,6 +80,9 @@ def _sig(lib):
     s("ds41o_window_ring_write", None, _P, _P, _P, _I64, _I64, _I64, _I64)
     s("ds41o_window_topk_idxs", None, _I64, _I64, _I64, _P)
     s("ds41o_new_groups", _I64, _I64, _I64, _I64)
+    s("ds41o_compress_len", _I64, _I64, _I64, _I64)
+    s("ds41o_merged_len", _I64, _I64, _I64, _I64)
+    s("ds41o_attn_scale", _F, _I64)
     s("ds41o_compress_latent_write", None, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64)
     s("ds41o_visible_rows", _I64, _I64, _I64, _I64, _I64)
     s("ds41o_indexer_scores", _I64, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P,
@@ -235,16 +238,42 @@ def window_topk_idxs(win: int, m: int, start_pos: int) -> np.ndarray:
 
 
 def new_groups(m, ratio, start_pos) -> int:
+    """Groups of ``ratio`` positions the call of m tokens at start_pos completes."""
     return int(lib().ds41o_new_groups(m, ratio, start_pos))
 
 
+def compress_len(m, ratio, start_pos) -> int:
+    """forward.rs / compress.rs ``compress_len``: compressed rows after the call."""
+    return int(lib().ds41o_compress_len(m, ratio, start_pos))
+
+
+def merged_len(win, topk, n_c) -> int:
+    """Length of a merged index row: win window indices + min(topk, n_c) picks."""
+    return int(lib().ds41o_merged_len(win, topk, n_c))
+
+
+def step_sizes(m: int, win: int, ratio: int, start_pos: int, topk: int) -> dict:
+    """The row counts of one call as the oracle derives them: n_c
+    (compress_len), G (new groups), n_a (rows_a length, the picks' offset),
+    K (merged row length) and ctopk = K - win."""
+    n_c = compress_len(m, ratio, start_pos)
+    K = merged_len(win, topk, n_c)
+    return {"n_c": n_c, "G": new_groups(m, ratio, start_pos),
+            "n_a": rows_a_len(m, win, start_pos), "K": K, "ctopk": K - win}
+
+
 def compress_latent_write(latent: np.ndarray, fc: np.ndarray, cache: np.ndarray, rd: int,
-                          ratio: int, start_pos: int, with_codes: bool = True):
-    """forward.rs latent branch / compress.rs latent branch.  Returns (cache after,
-    codes [rows, hd/2], scales [rows, hd/16]) where codes/scales are filled only
-    for the rows written."""
+                          ratio: int, start_pos: int, m: int, with_codes: bool = True):
+    """forward.rs latent branch / compress.rs latent branch for a call of m
+    tokens at start_pos: the oracle's own ``new_groups`` decides how many
+    latent rows the call writes, and ``latent`` must hold exactly that many.
+    Returns (cache after, codes [rows, hd/2], scales [rows, hd/16]) where
+    codes/scales are filled only for the rows written."""
     lat = _c(latent, np.uint16)
-    G, hd = lat.shape
+    G = new_groups(m, ratio, start_pos)
+    assert lat.ndim == 2 and lat.shape[0] == max(G, 0), (
+        f"latent holds {lat.shape[0]} rows, the call completes {G} groups")
+    hd = lat.shape[1]
     c2 = _c(cache, np.uint16).copy()
     rows = c2.shape[0]
     codes = np.zeros((rows, hd // 2), np.uint8) if with_codes else None
@@ -345,6 +374,70 @@ def attn_out_proj(o: np.ndarray, fc: np.ndarray, wo_a: np.ndarray, wo_b: np.ndar
                               _ptr(out), nh, hd, rd, groups, gr // groups, dim, start_pos, _ptr(tk),
                               tk.size)
     return og, out
+
+
+def attn_scale(hd: int) -> float:
+    """compress.rs attention_any: ``scale = (hd as f32).powf(-0.5)``."""
+    return float(lib().ds41o_attn_scale(hd))
+
+
+def forward(kv, ring, latent, cache, q_idx, k_idx, w, q, sink, *, win: int, ratio: int,
+            start_pos: int, topk: int, rd: int, tokens: Optional[Sequence[int]] = None,
+            fc: Optional[np.ndarray] = None, timings: Optional[dict] = None) -> dict:
+    """One layer's forward in the order of forward.rs AttnV41::forward and
+    compress.rs attention_any: ring write + window indices, latent write,
+    indexer scores + top-k + merge (only when a compressed row exists),
+    sparse attention with the sink.  bf16 tensors as uint16 bit arrays: kv
+    [m, hd], ring [win, hd], latent [G, hd], cache [>= n_c, hd], q_idx
+    [m, Hi, Di], k_idx [>= n_c, Di], q [m, nh, hd]; w [m, Hi] and sink [nh]
+    f32.  Every row count (n_c, G, n_a, K) comes from this module's own
+    functions.  The indexer, top-k and attention run for ``tokens`` (default:
+    all).  ``timings``, when given, accumulates seconds per stage under
+    "window_ring_write", "compress_latent_write", "indexer_topk" and
+    "sparse_attn_sink_fwd"."""
+    import time
+    m = np.asarray(kv).shape[0]
+    hd = np.asarray(kv).shape[1]
+    sz = step_sizes(m, win, ratio, start_pos, topk)
+    n_c = sz["n_c"]
+    toks = list(range(m)) if tokens is None else list(tokens)
+
+    def tick(name, t0):
+        if timings is not None:
+            timings[name] = timings.get(name, 0.0) + time.perf_counter() - t0
+
+    t0 = time.perf_counter()
+    ring2, rows_a = window_ring_write(kv, ring, win, start_pos)
+    win_idx = window_topk_idxs(win, m, start_pos)
+    tick("window_ring_write", t0)
+    if fc is None:
+        fc = yarn_freqs_cis(rd, start_pos + m)
+    t0 = time.perf_counter()
+    cache2, codes, scales = compress_latent_write(latent, fc, cache, rd, ratio, start_pos, m)
+    tick("compress_latent_write", t0)
+    res = dict(ring=ring2, rows_a=rows_a, win_idx=win_idx, cache=cache2, codes=codes,
+               scales=scales, tokens=toks, fc=fc, sizes=sz)
+    if n_c > 0:
+        t0 = time.perf_counter()
+        sc, bad = indexer_scores(q_idx, _c(k_idx, np.uint16)[:n_c], w, ratio, start_pos,
+                                 tokens=toks)
+        assert bad == 0, f"{bad} indexer dots are not exact in f32 for these inputs"
+        idx = topk_merge(sc, win_idx[toks], n_c, win, ratio, start_pos, topk, sz["n_a"],
+                         tokens=toks)
+        tick("indexer_topk", t0)
+        res["scores"] = sc
+        rows_b = cache2[:n_c]
+    else:
+        idx = win_idx[toks]
+        rows_b = None
+    assert idx.shape[1] == sz["K"]
+    res["idx"] = idx
+    t0 = time.perf_counter()
+    o, lse, bad = sparse_attn(q, rows_a, rows_b, idx, sink, attn_scale(hd), tokens=toks)
+    tick("sparse_attn_sink_fwd", t0)
+    assert bad == 0
+    res["o"], res["lse"] = o, lse
+    return res
 
 
 def num_threads() -> int:

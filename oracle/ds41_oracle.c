@@ -353,8 +353,28 @@ void ds41o_window_topk_idxs(int64_t win, int64_t m, int64_t start_pos, int32_t* 
 /* rotated, rounded to bf16, sent through the e4m3 fp4 round trip (block 16)  */
 /* and stored.                                                                 */
 /* ------------------------------------------------------------------------- */
+/* compress_len ([forward] AttnV41::forward, [compress] attention_any): the  */
+/* compressed rows that exist once positions 0 .. start_pos+m-1 are in, one   */
+/* per complete group of ratio positions.                                     */
+int64_t ds41o_compress_len(int64_t m, int64_t ratio, int64_t start_pos) {
+    return (start_pos + m) / ratio;
+}
+
+/* Groups this call completes: those past the start_pos/ratio rows that were  */
+/* complete before it (the cache row the latent copy starts at).              */
 int64_t ds41o_new_groups(int64_t m, int64_t ratio, int64_t start_pos) {
-    return (start_pos + m) / ratio - start_pos / ratio;
+    return ds41o_compress_len(m, ratio, start_pos) - start_pos / ratio;
+}
+
+/* Length of a merged index row: the win window indices, then                */
+/* ctopk = min(topk, compress_len) compressed picks (0 when no compressed row */
+/* exists yet, when the pages skip the indexer).                             */
+/* scale = head_dim^-0.5 as [compress] attention_any computes it: an f32 pow. */
+float ds41o_attn_scale(int64_t hd) { return powf((float)hd, -0.5f); }
+
+int64_t ds41o_merged_len(int64_t win, int64_t topk, int64_t n_c) {
+    int64_t ctopk = (n_c == 0) ? 0 : (topk < n_c ? topk : n_c);
+    return win + ctopk;
 }
 
 void ds41o_compress_latent_write(const uint16_t* latent, const float* fc, uint16_t* cache,

@@ -30,36 +30,21 @@ def sample_tokens(wl: Workload, n_random: int = 24, seed: int = 0):
 
 
 def oracle_forward(orc, wl: Workload, inp, tokens=None, fc=None):
-    """The oracle's forward for workload ``wl`` on CPU inputs ``inp``, with the
-    indexer, top-k and attention evaluated for ``tokens`` (default: all)."""
-    toks = list(range(wl.m)) if tokens is None else list(tokens)
-    kv, ring = bf16_bits(inp["kv"]), bf16_bits(inp["ring"])
-    ring2, rows_a = orc.window_ring_write(kv, ring, wl.win, wl.start_pos)
-    win_idx = orc.window_topk_idxs(wl.win, wl.m, wl.start_pos)
-    if fc is None:
-        fc = orc.yarn_freqs_cis(wl.rd, wl.max_pos)
-    cache, codes, scales = orc.compress_latent_write(bf16_bits(inp["latent"]), fc,
-                                                     bf16_bits(inp["cache"]), wl.rd, wl.ratio,
-                                                     wl.start_pos)
-    res = dict(ring=ring2, rows_a=rows_a, win_idx=win_idx, cache=cache, codes=codes,
-               scales=scales, tokens=toks, fc=fc)
-    if wl.n_c > 0:
-        sc, bad = orc.indexer_scores(bf16_bits(inp["q_idx"]), bf16_bits(inp["k_idx"])[: wl.n_c],
-                                     inp["w"].numpy(), wl.ratio, wl.start_pos, tokens=toks)
-        assert bad == 0, f"{bad} indexer dots are not exact in f32 for these inputs"
-        idx = orc.topk_merge(sc, win_idx[toks], wl.n_c, wl.win, wl.ratio, wl.start_pos, wl.topk,
-                             wl.n_a, tokens=toks)
-        res["scores"] = sc
-        rows_b = cache[: wl.n_c]
-    else:
-        idx = win_idx[toks]
-        rows_b = None
-    res["idx"] = idx
-    o, lse, bad = orc.sparse_attn(bf16_bits(inp["q"]), rows_a, rows_b, idx,
-                                  inp["sink"].numpy(), wl.scale, tokens=toks)
-    assert bad == 0
-    res["o"], res["lse"] = o, lse
-    return res
+    """The oracle's forward (``oracle.forward``) for workload ``wl`` on CPU
+    inputs ``inp``, with the indexer, top-k and attention evaluated for
+    ``tokens`` (default: all).  The workload supplies only the call's
+    parameters (window, ratio, position, top-k, rope width); every row count
+    the forward uses is the oracle's own."""
+    b = {k: bf16_bits(inp[k]) for k in ("kv", "ring", "latent", "cache", "q_idx", "k_idx", "q")}
+    return orc.forward(b["kv"], b["ring"], b["latent"], b["cache"], b["q_idx"], b["k_idx"],
+                       inp["w"].numpy(), b["q"], inp["sink"].numpy(), win=wl.win, ratio=wl.ratio,
+                       start_pos=wl.start_pos, topk=wl.topk, rd=wl.rd, tokens=tokens, fc=fc)
+
+
+def osizes(orc, wl: Workload) -> dict:
+    """The row counts (n_c, G, n_a, K, ctopk) of workload ``wl``'s call, as
+    the oracle derives them."""
+    return orc.step_sizes(wl.m, wl.win, wl.ratio, wl.start_pos, wl.topk)
 
 
 def to_dev(inp, device="cuda"):
@@ -92,5 +77,5 @@ def bf16_f32(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy()
 
 
-__all__ = ["sample_tokens", "oracle_forward", "to_dev", "assert_idx_sets_equal", "attn_close",
+__all__ = ["sample_tokens", "oracle_forward", "osizes", "to_dev", "assert_idx_sets_equal", "attn_close",
            "make_inputs", "bf16_to_np", "bf16_f32", "ATOL", "RTOL"]

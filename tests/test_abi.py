@@ -45,6 +45,28 @@ def test_rows_a_len(lib):
     assert lib.ds41_rows_a_len(1024, 128, 65536) == 1152
 
 
+def test_step_sizes(lib):
+    """ds41_step_sizes on the five workloads' call parameters, against the row
+    counts worked out by hand: n_a, n_c, G, ctopk, K."""
+    from compressed_sparse_attention_window_gb300.workloads import WORKLOADS
+    want = {"tiny_prefill": (64, 16, 16, 8, 24), "decode": (128, 2048, 1, 512, 640),
+            "prefill": (4096, 1024, 1024, 512, 640), "long_decode": (128, 32768, 1, 2048, 2176),
+            "chunked_prefill": (1152, 520, 8, 512, 640)}
+    for name, w in want.items():
+        assert tuple(ds41.step_sizes(WORKLOADS[name])) == w, name
+    out = (ctypes.c_int64 * 5)()
+    assert lib.ds41_step_sizes(3, 0, 16, 4, 8, ctypes.addressof(out)) == 0
+    assert tuple(out) == (3, 0, 0, 0, 16)  # no compressed row yet: no picks
+    assert lib.ds41_step_sizes(0, 0, 16, 4, 8, ctypes.addressof(out)) == 2
+    assert lib.ds41_step_sizes(3, 0, 16, 0, 8, ctypes.addressof(out)) == 1
+    assert lib.ds41_step_sizes(3, 0, 16, 4, 8, None) == 1
+
+
+def test_selftest_checks_arguments(lib):
+    assert lib.ds41_selftest_wait_timeout(100, 0, None, None) == 1
+    assert lib.ds41_selftest_wait_timeout(0, 0, FAKE, None) == 1
+
+
 def _err(lib):
     return lib.ds41_last_error().decode()
 

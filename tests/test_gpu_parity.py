@@ -14,7 +14,8 @@ from compressed_sparse_attention_window_gb300.workloads import (CHUNKED, DECODE,
                                                                  OUT_PROJ, bf16_bits, from_bits,
                                                                  make_inputs,
                                                                  make_out_proj_weights)
-from helpers import (assert_idx_sets_equal, attn_close, oracle_forward, sample_tokens, to_dev)
+from helpers import (assert_idx_sets_equal, attn_close, oracle_forward, osizes, sample_tokens,
+                     to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -139,15 +140,16 @@ def test_latent_write_bit_exact(orc, wl):
     rows = cache_d.shape[0]
     codes = torch.zeros(rows, wl.hd // 2, dtype=torch.uint8, device="cuda")
     scales = torch.zeros(rows, wl.hd // 16, dtype=torch.uint8, device="cuda")
-    if wl.G > 0:
+    if ds41.step_sizes(wl).G > 0:
         ds41.compress_latent_write(inp["latent"].cuda(), torch.from_numpy(fc).cuda(), cache_d,
                                    wl.rd, wl.ratio, wl.start_pos, wl.m, codes, scales)
     ocache, ocodes, oscales = orc.compress_latent_write(bf16_bits(inp["latent"]), fc,
                                                         bf16_bits(inp["cache"]), wl.rd, wl.ratio,
-                                                        wl.start_pos)
+                                                        wl.start_pos, wl.m)
     assert np.array_equal(bf16_bits(cache_d), ocache)
-    first = wl.start_pos // wl.ratio
-    sl = slice(first, first + wl.G)
+    osz = osizes(orc, wl)
+    first = osz["n_c"] - osz["G"]
+    sl = slice(first, first + osz["G"])
     assert np.array_equal(codes.cpu().numpy()[sl], ocodes[sl])
     assert np.array_equal(scales.cpu().numpy()[sl], oscales[sl])
 
@@ -158,9 +160,10 @@ def _gpu_indexer(wl, inp, with_scores=True):
         np.ascontiguousarray(np.zeros((wl.m, wl.win), np.int32))).cuda()
     from oracle import window_topk_idxs
     win_idx.copy_(torch.from_numpy(window_topk_idxs(wl.win, wl.m, wl.start_pos)))
-    scores = torch.empty(wl.m, wl.n_c, dtype=torch.bfloat16, device="cuda") if with_scores else None
-    idx = ds41.indexer_topk(dev["q_idx"], dev["k_idx"][: wl.n_c], dev["w"], win_idx, wl.ratio,
-                            wl.start_pos, wl.topk, wl.n_a, scores=scores)
+    sz = ds41.step_sizes(wl)
+    scores = torch.empty(wl.m, sz.n_c, dtype=torch.bfloat16, device="cuda") if with_scores else None
+    idx = ds41.indexer_topk(dev["q_idx"], dev["k_idx"][: sz.n_c], dev["w"], win_idx, wl.ratio,
+                            wl.start_pos, wl.topk, sz.n_a, scores=scores)
     return idx, scores
 
 
@@ -176,14 +179,15 @@ def test_indexer_scores_and_topk(orc, wl):
     inp = make_inputs(wl)
     idx, scores = _gpu_indexer(wl, inp)
     toks = sample_tokens(wl) if wl.m > 128 else list(range(wl.m))
-    sc, bad = orc.indexer_scores(bf16_bits(inp["q_idx"]), bf16_bits(inp["k_idx"])[: wl.n_c],
+    osz = osizes(orc, wl)
+    sc, bad = orc.indexer_scores(bf16_bits(inp["q_idx"]), bf16_bits(inp["k_idx"])[: osz["n_c"]],
                                  inp["w"].numpy(), wl.ratio, wl.start_pos, tokens=toks)
     assert bad == 0
     gsc = bf16_bits(scores)[toks]
     assert np.array_equal(gsc, sc), np.argwhere(gsc != sc)[:5]
     win_idx = orc.window_topk_idxs(wl.win, wl.m, wl.start_pos)
-    oidx = orc.topk_merge(sc, win_idx[toks], wl.n_c, wl.win, wl.ratio, wl.start_pos, wl.topk,
-                          wl.n_a, tokens=toks)
+    oidx = orc.topk_merge(sc, win_idx[toks], osz["n_c"], wl.win, wl.ratio, wl.start_pos, wl.topk,
+                          osz["n_a"], tokens=toks)
     assert_idx_sets_equal(idx.cpu().numpy()[toks], oidx, wl.win)
     # the picks of a row come in ascending row order, -1 padding last
     g = idx.cpu().numpy()[:, wl.win:]
@@ -201,18 +205,19 @@ def test_indexer_many_tokens_tensor_core_path(orc, start_pos, ratio):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     wl = DECODE.replace(name="indexer_tc", m=4 * sms + 3, start_pos=start_pos, ratio=ratio,
                         topk=64)
-    assert wl.Hi == 64 and wl.Di == 128 and wl.n_c > 0
+    osz = osizes(orc, wl)
+    assert wl.Hi == 64 and wl.Di == 128 and osz["n_c"] > 0
     inp = make_inputs(wl, seed=start_pos + ratio)
     idx, scores = _gpu_indexer(wl, inp)
-    sc, bad = orc.indexer_scores(bf16_bits(inp["q_idx"]), bf16_bits(inp["k_idx"])[: wl.n_c],
+    sc, bad = orc.indexer_scores(bf16_bits(inp["q_idx"]), bf16_bits(inp["k_idx"])[: osz["n_c"]],
                                  inp["w"].numpy(), wl.ratio, wl.start_pos)
     assert bad == 0
     gsc = bf16_bits(scores)
     assert np.array_equal(gsc, sc), np.argwhere(gsc != sc)[:5]
     win_idx = orc.window_topk_idxs(wl.win, wl.m, wl.start_pos)
     toks = sample_tokens(wl)
-    oidx = orc.topk_merge(sc[toks], win_idx[toks], wl.n_c, wl.win, wl.ratio, wl.start_pos,
-                          wl.topk, wl.n_a, tokens=toks)
+    oidx = orc.topk_merge(sc[toks], win_idx[toks], osz["n_c"], wl.win, wl.ratio, wl.start_pos,
+                          wl.topk, osz["n_a"], tokens=toks)
     assert_idx_sets_equal(idx.cpu().numpy()[toks], oidx, wl.win)
 
 
@@ -395,7 +400,7 @@ def test_forward_no_compressed_rows_yet(orc):
     """start_pos + m < ratio: no compressed row exists, the merged rows are the
     window rows alone."""
     wl = TINY_PREFILL.replace(m=3, start_pos=0, ratio=4)
-    assert wl.n_c == 0
+    assert osizes(orc, wl)["n_c"] == 0 and ds41.step_sizes(wl).n_c == 0
     inp = make_inputs(wl)
     dev = to_dev(inp)
     fc = torch.from_numpy(orc.yarn_freqs_cis(wl.rd, wl.max_pos)).cuda()
@@ -597,7 +602,8 @@ def test_csa_forward_reuse(orc, name):
     src = make_inputs(wl)
     dev_s = to_dev(src)
     out_s = ds41.csa_forward(dev_s, wl, fc)
-    ctopk = wl.K - wl.win
+    sz = ds41.step_sizes(wl)
+    ctopk = sz.ctopk
     cidx = out_s["idx"][:, wl.win:].contiguous() if ctopk else None
     cache = dev_s["cache"]
     lay = make_inputs(wl, seed=4242)
@@ -611,7 +617,7 @@ def test_csa_forward_reuse(orc, name):
     ds41.window_ring_write(dev_c["kv"], dev_c["ring"], win_idx, wl.start_pos, rows_a=rows_a)
     ra = dev_c["kv"] if wl.start_pos == 0 else (dev_c["ring"] if wl.m == 1 else rows_a)
     idx = torch.cat([win_idx, cidx], 1) if ctopk else win_idx
-    o_c = ds41.sparse_attn_sink_fwd(dev_c["q"], ra, cache[: wl.n_c] if ctopk else None, idx,
+    o_c = ds41.sparse_attn_sink_fwd(dev_c["q"], ra, cache[: sz.n_c] if ctopk else None, idx,
                                     dev_c["sink"], wl.scale)
     torch.cuda.synchronize()
     assert ds41.device_status() == 0
@@ -626,10 +632,11 @@ def test_csa_forward_reuse(orc, name):
     _, rows_a_o = orc.window_ring_write(bf16_bits(lay["kv"]), bf16_bits(lay["ring"]), wl.win,
                                         wl.start_pos)
     win_o = orc.window_topk_idxs(wl.win, wl.m, wl.start_pos)[toks]
-    idx_o = np.concatenate([win_o, ref_s["idx"][:, wl.win:]], 1) if ctopk else win_o
+    on_c = ref_s["sizes"]["n_c"]
+    idx_o = np.concatenate([win_o, ref_s["idx"][:, wl.win:]], 1) if on_c else win_o
     o_ref, _, bad = orc.sparse_attn(bf16_bits(lay["q"]), rows_a_o,
-                                    ref_s["cache"][: wl.n_c] if ctopk else None, idx_o,
-                                    lay["sink"].numpy(), wl.scale, tokens=toks)
+                                    ref_s["cache"][:on_c] if on_c else None, idx_o,
+                                    lay["sink"].numpy(), orc.attn_scale(wl.hd), tokens=toks)
     assert bad == 0
     ok, err, worst = attn_close(out_r["o"].float().cpu().numpy()[toks], o_ref)
     assert ok, (name, err, worst)

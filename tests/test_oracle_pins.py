@@ -429,7 +429,7 @@ def test_latent_write_positions_and_rows(orc):
         G = orc.new_groups(m, ratio, sp)
         lat = _bf16_bits_of(rng.standard_normal((max(G, 0), hd)).astype(np.float32))
         cache0 = _bf16_bits_of(np.full((60, hd), 7.0, np.float32))
-        cache, codes, scales = orc.compress_latent_write(lat, fc, cache0, rd, ratio, sp)
+        cache, codes, scales = orc.compress_latent_write(lat, fc, cache0, rd, ratio, sp, m)
         first = sp // ratio
         changed = np.flatnonzero((cache != cache0).any(axis=1))
         assert set(changed.tolist()) <= set(range(first, first + G))
@@ -446,6 +446,72 @@ def test_latent_write_positions_and_rows(orc):
             rb = orc.f32_to_bf16(rot)
             want, _, _ = orc.fp4_quant(rb, 16, True)
             assert np.array_equal(cache[first + g], want[0])
+
+
+def _groups_by_enumeration(m, ratio, sp):
+    """Walk the positions one by one: position p completes a group of
+    ``ratio`` consecutive positions when it is the group's last one
+    ((p + 1) % ratio == 0).  Returns (groups complete after the call, groups
+    completed by this call)."""
+    total = new = 0
+    for p in range(sp + m):
+        if (p + 1) % ratio == 0:
+            total += 1
+            if p >= sp:
+                new += 1
+    return total, new
+
+
+def test_group_counts_by_enumeration(orc):
+    """compress_len (forward.rs / compress.rs: compressed rows that exist after
+    the call) and the groups a call completes, against a walk over every
+    position; plus the row the latent copy starts at (start_pos / ratio =
+    groups complete before the call) and the latent write's own count."""
+    for ratio in (1, 2, 3, 4, 7, 16, 128):
+        for sp in sorted({0, 1, 2, 3, ratio - 1, ratio, ratio + 1, 37, 255, 256, 300}):
+            for m in (1, 2, 3, 4, 5, 8, 13, 64, 129, 300):
+                total, new = _groups_by_enumeration(m, ratio, sp)
+                assert orc.compress_len(m, ratio, sp) == total, (m, ratio, sp)
+                assert orc.new_groups(m, ratio, sp) == new, (m, ratio, sp)
+                before, _ = _groups_by_enumeration(sp, ratio, 0) if sp > 0 else (0, 0)
+                assert total - new == before
+    # the latent write takes exactly its own count of rows
+    fc = orc.yarn_freqs_cis(8, 64)
+    lat = np.zeros((2, 32), np.uint16)
+    with pytest.raises(AssertionError):
+        orc.compress_latent_write(lat, fc, np.zeros((16, 32), np.uint16), 8, 4, 0, 4)
+
+
+def test_merged_row_length(orc):
+    """The merged index row (forward.rs / compress.rs merge: the window indices,
+    then the indexer's ctopk picks, none while no compressed row exists)."""
+    for win in (1, 16, 128):
+        for topk in (1, 8, 512, 2048):
+            for n_c in (0, 1, 7, 512, 520, 32768):
+                want = win + (0 if n_c == 0 else min(topk, n_c))
+                assert orc.merged_len(win, topk, n_c) == want
+
+
+def test_attn_scale(orc):
+    """compress.rs attention_any: scale = head_dim^-0.5 in f32."""
+    assert orc.attn_scale(64) == 0.125 and orc.attn_scale(256) == 0.0625
+    for hd in (128, 512):
+        exact = hd ** -0.5
+        got = orc.attn_scale(hd)
+        assert got == float(np.float32(exact)), (hd, got, exact)
+
+
+def test_workload_sizes_match_oracle(orc):
+    """The generator sizes its tensors with its own shape helpers; they must
+    agree with the row counts the oracle derives, on all five workloads and
+    on ragged variants."""
+    from compressed_sparse_attention_window_gb300.workloads import WORKLOADS, TINY_PREFILL
+    wls = list(WORKLOADS.values()) + [TINY_PREFILL.replace(m=m, start_pos=sp)
+                                      for m in (1, 3, 17) for sp in (0, 5, 15, 16)]
+    for wl in wls:
+        sz = orc.step_sizes(wl.m, wl.win, wl.ratio, wl.start_pos, wl.topk)
+        assert (wl.n_c, wl.G, wl.n_a, wl.K, wl.ctopk) == (
+            sz["n_c"], sz["G"], sz["n_a"], sz["K"], sz["ctopk"]), wl
 
 
 # ---------------------------------------------------------------------------
@@ -606,20 +672,10 @@ def test_one_hot_row_closed_form(orc):
 def _run_pipeline(orc, wl, inp):
     """The oracle's whole forward for one workload (every token)."""
     from compressed_sparse_attention_window_gb300.workloads import bf16_bits
-    kv, ring = bf16_bits(inp["kv"]), bf16_bits(inp["ring"])
-    ring2, rows_a = orc.window_ring_write(kv, ring, wl.win, wl.start_pos)
-    win_idx = orc.window_topk_idxs(wl.win, wl.m, wl.start_pos)
-    fc = orc.yarn_freqs_cis(wl.rd, wl.max_pos)
-    cache, _, _ = orc.compress_latent_write(bf16_bits(inp["latent"]), fc, bf16_bits(inp["cache"]),
-                                            wl.rd, wl.ratio, wl.start_pos)
-    sc, bad = orc.indexer_scores(bf16_bits(inp["q_idx"]), bf16_bits(inp["k_idx"]),
-                                 inp["w"].numpy(), wl.ratio, wl.start_pos)
-    assert bad == 0
-    idx = orc.topk_merge(sc, win_idx, wl.n_c, wl.win, wl.ratio, wl.start_pos, wl.topk, wl.n_a)
-    o, lse, bad = orc.sparse_attn(bf16_bits(inp["q"]), rows_a, cache[: wl.n_c], idx,
-                                  inp["sink"].numpy(), wl.scale)
-    assert bad == 0
-    return dict(rows_a=rows_a, cache=cache, idx=idx, o=o, lse=lse, ring=ring2)
+    b = {k: bf16_bits(inp[k]) for k in ("kv", "ring", "latent", "cache", "q_idx", "k_idx", "q")}
+    return orc.forward(b["kv"], b["ring"], b["latent"], b["cache"], b["q_idx"], b["k_idx"],
+                       inp["w"].numpy(), b["q"], inp["sink"].numpy(), win=wl.win, ratio=wl.ratio,
+                       start_pos=wl.start_pos, topk=wl.topk, rd=wl.rd)
 
 
 @pytest.mark.parametrize("variant", ["prefill", "decode", "chunked"])
@@ -643,13 +699,16 @@ def test_topk_covering_all_rows_is_dense_causal(orc, variant):
     kv = bf16_bits(inp["kv"])
     for t in range(wl.m):
         pos_rows[wl.start_pos + t] = kv[t]
-    comp = r["cache"][: wl.n_c]
+    # compressed rows complete at or before each position: counted here by
+    # walking the positions, not with the oracle's arithmetic
+    n_c, _ = _groups_by_enumeration(wl.m, wl.ratio, wl.start_pos)
+    comp = r["cache"][:n_c]
     qf = orc.bf16_to_f32(bf16_bits(inp["q"])).astype(np.float64)
     sink = inp["sink"].numpy().astype(np.float64)
     for t in range(wl.m):
         p = wl.start_pos + t
         wpos = [q for q in range(max(0, p - wl.win + 1), p + 1)]
-        vis = min(wl.n_c, (p + 1) // wl.ratio)
+        vis, _ = _groups_by_enumeration(1, wl.ratio, p)
         R = np.concatenate([np.stack([pos_rows[q] for q in wpos]), comp[:vis]])
         Rf = orc.bf16_to_f32(R).astype(np.float64)
         for h in range(wl.nh):

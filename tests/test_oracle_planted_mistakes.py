@@ -55,6 +55,15 @@ CASES = {
         "int64_t v = (start_pos + t + 1) / ratio;", "int64_t v = (start_pos + t) / ratio;",
         [PIN.test_latent_write_positions_and_rows, PIN.test_topk_bruteforce_subsets,
          lambda o: PIN.test_topk_covering_all_rows_is_dense_causal(o, "decode")]),
+    "compress_len counts the unfinished group": (
+        "    return (start_pos + m) / ratio;\n}",
+        "    return (start_pos + m + ratio - 1) / ratio;\n}",
+        [PIN.test_group_counts_by_enumeration,
+         lambda o: PIN.test_topk_covering_all_rows_is_dense_causal(o, "chunked")]),
+    "new groups counted as m / ratio": (
+        "return ds41o_compress_len(m, ratio, start_pos) - start_pos / ratio;",
+        "return m / ratio;",
+        [PIN.test_group_counts_by_enumeration, PIN.test_latent_write_positions_and_rows]),
     "sink dropped from the denominator": (
         "double den = exp((double)sink[h] - mx);", "double den = 0.0;",
         [PIN.test_one_hot_row_closed_form,
