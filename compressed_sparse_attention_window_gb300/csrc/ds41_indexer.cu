@@ -982,6 +982,53 @@ extern "C" int ds41_indexer_topk(const ds41_bf16* q_idx, const ds41_bf16* k_idx,
     return launch_topk(sc, win_idx, idx, m, n_c, win, ctopk, ratio, start_pos, offset, false, st);
 }
 
+extern "C" size_t ds41_indexer_mxf4_workspace_bytes(int64_t m, int64_t n_c,
+                                                    int scores_out_given) {
+    if (m < 1 || n_c < 1 || scores_out_given) return 0;
+    return align256((size_t)m * n_c * 2);
+}
+
+extern "C" int ds41_indexer_topk_mxf4(const ds41_bf16* q_idx, const uint8_t* k_codes,
+                                      const uint8_t* k_scales, const float* w,
+                                      const int32_t* win_idx, int32_t* idx, ds41_bf16* scores,
+                                      int64_t m, int64_t Hi, int64_t Di, int64_t n_c, int64_t win,
+                                      int64_t ratio, int64_t start_pos, int64_t topk,
+                                      int64_t offset, void* ws, size_t ws_bytes,
+                                      ds41_stream_t stream) {
+    const char* name = "ds41_indexer_topk_mxf4";
+    DS41_REQUIRE(m >= 1 && m < (int64_t(1) << 25), DS41_E_RANGE, "%s: m=%lld", name,
+                 (long long)m);
+    DS41_REQUIRE(indexer_mxf4_supported(Hi, Di), DS41_E_ARG,
+                 "%s: Hi=%lld Di=%lld; the packed-key path takes 64 heads of dim 128", name,
+                 (long long)Hi, (long long)Di);
+    DS41_REQUIRE(n_c >= 1 && n_c < (int64_t(1) << 31), DS41_E_ARG, "%s: n_c=%lld", name,
+                 (long long)n_c);
+    DS41_REQUIRE(win >= 0 && win <= (int64_t(1) << 20), DS41_E_ARG, "%s: win=%lld", name,
+                 (long long)win);
+    DS41_REQUIRE(ratio >= 1 && start_pos >= 0, DS41_E_ARG, "%s: ratio=%lld start_pos=%lld", name,
+                 (long long)ratio, (long long)start_pos);
+    DS41_REQUIRE(topk >= 1, DS41_E_RANGE, "%s: topk=%lld", name, (long long)topk);
+    DS41_REQUIRE(q_idx && k_codes && k_scales && w && idx && (win == 0 || win_idx), DS41_E_ARG,
+                 "%s: null tensor pointer", name);
+    DS41_REQUIRE(aligned16(q_idx) && aligned16(k_codes) && aligned16(k_scales) && aligned16(w),
+                 DS41_E_ARG, "%s: q_idx/k_codes/k_scales/w must be 16-byte aligned", name);
+    const int64_t ctopk = topk < n_c ? topk : n_c;
+    DS41_REQUIRE(win + ctopk < (int64_t(1) << 30), DS41_E_RANGE, "%s: merged row too long", name);
+    const size_t need = ds41_indexer_mxf4_workspace_bytes(m, n_c, scores != nullptr);
+    DS41_REQUIRE(need == 0 || (ws && ws_bytes >= need), DS41_E_WORKSPACE,
+                 "%s: workspace of %zu bytes needed, %zu given", name, need, ws ? ws_bytes : 0);
+    DS41_REQUIRE(need == 0 || aligned16(ws), DS41_E_ARG, "%s: ws must be 16-byte aligned", name);
+    cudaStream_t st = (cudaStream_t)stream;
+    uint16_t* sc = scores ? scores : static_cast<uint16_t*>(ws);
+    unsigned int* status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    rc = indexer_mxf4_launch(q_idx, k_codes, k_scales, w, sc, m, n_c, ratio, start_pos,
+                             scores != nullptr, status, device_sm_count(), st);
+    if (rc) return rc;
+    return launch_topk(sc, win_idx, idx, m, n_c, win, ctopk, ratio, start_pos, offset, false, st);
+}
+
 // ---------------------------------------------------------------------------
 // Pieces of the fused step (ds41_forward.cu).
 // ---------------------------------------------------------------------------

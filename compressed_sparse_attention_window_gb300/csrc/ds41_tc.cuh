@@ -171,6 +171,10 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 int get_encode(PFN_cuTensorMapEncodeTiled_v12000* out);
 int make_map_bf16(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* ptr,
                   int64_t rows, int64_t cols, int box_cols, int box_rows);
+// A 2-D uint8 map over [rows][cols] (cols a multiple of 16, at most 64) with
+// whole rows as the box width, box_rows rows, and the 64-byte swizzle.
+int make_map_u8_sw64(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* ptr,
+                     int64_t rows, int64_t cols, int box_rows);
 
 }  // namespace tc
 }  // namespace ds41

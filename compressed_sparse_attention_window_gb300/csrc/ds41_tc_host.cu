@@ -39,5 +39,18 @@ int make_map_bf16(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const v
     return DS41_OK;
 }
 
+int make_map_u8_sw64(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* ptr,
+                     int64_t rows, int64_t cols, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {(cuuint32_t)cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DS41_E_CUDA, "cuTensorMapEncodeTiled (u8) failed (%d)", (int)r);
+    return DS41_OK;
+}
+
 }  // namespace tc
 }  // namespace ds41

@@ -42,6 +42,9 @@ SIGNATURES = {
     "ds41_indexer_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64, ctypes.c_int]),
     "ds41_indexer_topk": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                          _I64, _I64, _I64, _P, _SZ, _P]),
+    "ds41_indexer_mxf4_workspace_bytes": (_SZ, [_I64, _I64, ctypes.c_int]),
+    "ds41_indexer_topk_mxf4": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                              _I64, _I64, _I64, _I64, _I64, _P, _SZ, _P]),
     "ds41_sparse_attn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
     "ds41_csa_forward_reuse": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _F, _P, _P, _P,
                                               _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, ctypes.c_size_t,
@@ -238,6 +241,34 @@ def indexer_topk(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor,
           _ptr(w, torch.float32, "w"), _ptr(win_idx, torch.int32, "win_idx"),
           _ptr(idx, torch.int32, "idx"), _ptr(scores, _BF, "scores"), m, Hi, Di, n_c, win, ratio,
           start_pos, topk, offset, _ptr(ws) if need else None, need, _stream())
+    return idx
+
+
+def indexer_topk_mxf4(q_idx: torch.Tensor, k_codes: torch.Tensor, k_scales: torch.Tensor,
+                      w: torch.Tensor, win_idx: torch.Tensor, ratio: int, start_pos: int,
+                      topk: int, offset: int, idx: Optional[torch.Tensor] = None,
+                      scores: Optional[torch.Tensor] = None,
+                      ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """ds41_indexer_topk_mxf4: the indexer top-k on a packed mxf4 key cache
+    (k_codes [n_c, Di/2] and k_scales [n_c, Di/32] uint8, as
+    fp4_quant(..., want_codes=True) writes them).  Returns idx."""
+    m, Hi, Di = q_idx.shape
+    n_c = k_codes.shape[0]
+    if tuple(k_codes.shape) != (n_c, Di // 2) or tuple(k_scales.shape) != (n_c, Di // 32):
+        raise ValueError(f"k_codes/k_scales: expected {(n_c, Di // 2)} / {(n_c, Di // 32)}, got "
+                         f"{tuple(k_codes.shape)} / {tuple(k_scales.shape)}")
+    win = win_idx.shape[1]
+    ctopk = min(topk, n_c)
+    if idx is None:
+        idx = torch.empty(m, win + ctopk, dtype=torch.int32, device=q_idx.device)
+    need = int(load().ds41_indexer_mxf4_workspace_bytes(m, n_c, 1 if scores is not None else 0))
+    if need and (ws is None or ws.numel() < need):
+        ws = torch.empty(need, dtype=torch.uint8, device=q_idx.device)
+    _call("ds41_indexer_topk_mxf4", _ptr(q_idx, _BF, "q_idx"), _ptr(k_codes, torch.uint8, "k_codes"),
+          _ptr(k_scales, torch.uint8, "k_scales"), _ptr(w, torch.float32, "w"),
+          _ptr(win_idx, torch.int32, "win_idx"), _ptr(idx, torch.int32, "idx"),
+          _ptr(scores, _BF, "scores"), m, Hi, Di, n_c, win, ratio, start_pos, topk, offset,
+          _ptr(ws) if need else None, need, _stream())
     return idx
 
 

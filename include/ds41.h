@@ -194,6 +194,34 @@ int ds41_indexer_topk(const ds41_bf16* q_idx, const ds41_bf16* k_idx, const floa
                       int64_t start_pos, int64_t topk, int64_t offset, void* ws, size_t ws_bytes,
                       ds41_stream_t stream);
 
+/* Scratch bytes ds41_indexer_topk_mxf4 needs: the scores of the top-k when
+ * they are not an output (scores_out_given == 0), else 0. */
+size_t ds41_indexer_mxf4_workspace_bytes(int64_t m, int64_t n_c, int scores_out_given);
+
+/* ds41_indexer_topk on a packed mxf4 key cache.  The compress.rs header puts
+ * the indexer's k through the e2m1 round trip with power-of-two scales per
+ * block of 32 (fp4_quant_e8m0_inplace); those values are exactly an e2m1 code
+ * per element and an e8m0 scale per block, which is how this call takes the
+ * keys: 68 bytes per row of 128 instead of 256.  ds41_fp4_quant_e8m0 writes
+ * them (its codes and scales outputs) from bf16 keys.  The scores, picks,
+ * merge and errors are those of ds41_indexer_topk on the bf16 keys the codes
+ * and scales encode (Q8 of those keys gives back the same values), bit for
+ * bit.  The dot products run as block-scaled tensor-core MMAs on the codes;
+ * q is quantised inside the kernel.
+ *   q_idx    [m, Hi, Di] bf16
+ *   k_codes  [n_c, Di/2] uint8: e2m1 codes, element 2j in the low nibble of
+ *            byte j, bit 3 of a code the sign
+ *   k_scales [n_c, Di/32] uint8: biased exponents (e8m0) of the block scales
+ *   w [m, Hi] f32, win_idx [m, win], idx [m, win + ctopk], scores nullable
+ *            [m, n_c] bf16: as ds41_indexer_topk
+ *   Hi == 64 and Di == 128 (DS41_E_ARG otherwise); q_idx, k_codes, k_scales
+ *   and w 16-byte aligned. */
+int ds41_indexer_topk_mxf4(const ds41_bf16* q_idx, const uint8_t* k_codes, const uint8_t* k_scales,
+                           const float* w, const int32_t* win_idx, int32_t* idx, ds41_bf16* scores,
+                           int64_t m, int64_t Hi, int64_t Di, int64_t n_c, int64_t win,
+                           int64_t ratio, int64_t start_pos, int64_t topk, int64_t offset,
+                           void* ws, size_t ws_bytes, ds41_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Step 3: sparse attention with a per-head sink                              */
 /* ------------------------------------------------------------------------ */
