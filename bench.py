@@ -116,6 +116,11 @@ def algorithmic(wl):
             "bytes": (m * wl.Hi * wl.Di * bf + wl.n_c * wl.Di * bf + m * wl.Hi * 4
                       + m * wl.win * 4 + m * K * 4),
             "flops": 2 * wl.Hi * wl.Di * pairs},
+        # the same on the mxf4 key cache: Di/2 code bytes + Di/32 scale bytes per row
+        "indexer_topk_mxf4": {
+            "bytes": (m * wl.Hi * wl.Di * bf + wl.n_c * (wl.Di // 2 + wl.Di // 32) + m * wl.Hi * 4
+                      + m * wl.win * 4 + m * K * 4),
+            "flops": 2 * wl.Hi * wl.Di * pairs},
         "sparse_attn_sink_fwd": {
             "bytes": rows * wl.hd * bf + 2 * m * wl.nh * wl.hd * bf + m * K * 4 + wl.nh * 4,
             "flops": 4 * wl.nh * wl.hd * rows},
@@ -493,18 +498,141 @@ def dominant_roofline(wl, op_ms, args):
     return roof
 
 
+def step_bytes(wl, fp4=False) -> int:
+    """Algorithmic bytes one step touches (the sum of its ops' rows of
+    ``algorithmic``): what has to come from HBM when the step runs L2-cold."""
+    alg = algorithmic(wl)
+    ops = [k for k in OPS if k in alg]
+    if fp4 and "indexer_topk" in alg:
+        ops = [k for k in ops if k != "indexer_topk"] + ["indexer_topk_mxf4"]
+    return sum(alg[k]["bytes"] for k in ops if k in alg)
+
+
+def time_graph_steps(graphs, K, W, world, dev, stream):
+    """W warm-up replays, then K timed replays of the graphs in rotation
+    between a barrier + synchronize on both sides, events on the launching
+    stream, clocks sampled meanwhile.  Returns (max-over-ranks ms, clocks)."""
+    n = len(graphs)
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            graphs[i % n].replay()
+    stream.synchronize()
+    clocks = Clocks(dev.index if dev.index is not None else 0)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(K):
+            graphs[(W + i) % n].replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop()
+    return max_over_ranks(e0.elapsed_time(e1), world), ck
+
+
+def capture_steps(step, slots, stream):
+    """One CUDA graph of ``step(inp, out)`` per layer state."""
+    graphs = []
+    for inp, out in slots:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(inp, out)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    return graphs
+
+
+def fp4_supported(wl) -> bool:
+    return wl.Hi == 64 and wl.Di == 128
+
+
+def add_fp4_caches(wl, slots):
+    """The packed caches of every layer state: the indexer keys as mxf4
+    (codes + e8m0 scales, from the bf16 keys through ds41_fp4_quant_e8m0) and
+    room for the latent rows as e2m1 codes + e4m3 scales."""
+    sz = ds41.step_sizes(wl)
+    for inp, _ in slots:
+        inp["k_codes"], inp["k_scales"] = ds41.pack_keys(inp["k_idx"][: max(1, sz.n_c)].contiguous())
+        rows = inp["cache"].shape[0]
+        inp["cache_codes"] = torch.zeros(rows, wl.hd // 2, dtype=torch.uint8, device=inp["q"].device)
+        inp["cache_scales"] = torch.zeros(rows, wl.hd // 16, dtype=torch.uint8,
+                                          device=inp["q"].device)
+    torch.cuda.synchronize()
+
+
+def time_fp4_variant(wl, slots, fc, K, W, world, dev, stream, args):
+    """The step on packed fp4 caches (ds41_csa_forward_fp4; the step's own
+    results bit for bit, see the tests): per-step time from graph replays over
+    the same rotating layer states, the mxf4 indexer op alone, and the
+    roofline of the variant's dominant op."""
+    add_fp4_caches(wl, slots)
+    outs = [dict(out) for _, out in slots]
+    with torch.cuda.stream(stream):
+        for (inp, _), o in zip(slots, outs):
+            ds41.csa_forward_fp4(inp, wl, fc, o)
+    stream.synchronize()
+    graphs = capture_steps(lambda inp, out: ds41.csa_forward_fp4(inp, wl, fc, out),
+                           list(zip([i for i, _ in slots], outs)), stream)
+    t_ms, ck = time_graph_steps(graphs, K, W, world, dev, stream)
+    del graphs
+    sz = ds41.step_sizes(wl)
+    op_ms = {}
+    if sz.n_c > 0:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for (inp, out), o in zip(slots, outs):
+                ds41.indexer_topk_mxf4(inp["q_idx"], inp["k_codes"], inp["k_scales"], inp["w"],
+                                       out["win_idx"], wl.ratio, wl.start_pos, wl.topk, sz.n_a,
+                                       idx=out["idx"], ws=o.get("ws_fp4"))
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        op_ms["indexer_topk_mxf4"] = e0.elapsed_time(e1) / (5 * len(slots))
+        del g
+    res = {"ms_per_step": t_ms / K, "value": wl.m * K * world / (t_ms / 1e3),
+           "unit": "query-tokens/s", "steps": K, "clocks": ck, "per_op_ms": op_ms,
+           "algorithmic_bytes_per_step": step_bytes(wl, fp4=True),
+           "what": "ds41_csa_forward_fp4: indexer keys as mxf4 (68 B/row), scores by block-scaled "
+                   "tcgen05 MMAs; latent rows also written as e2m1 + e4m3 scales"}
+    if op_ms:
+        alg = algorithmic(wl)["indexer_topk_mxf4"]
+        hbm = load_peaks()[0]
+        ms = op_ms["indexer_topk_mxf4"]
+        ach = alg["bytes"] / (ms / 1e3) / 1e9
+        res["roofline"] = {"kernel": "indexer_topk_mxf4", "bound": "hbm", "achieved": ach,
+                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "ms_per_launch": ms,
+                           "algorithmic_bytes": alg["bytes"], "algorithmic_flops": alg["flops"],
+                           "traffic": recorded_traffic(wl.name, "indexer_topk_mxf4")}
+    return res
+
+
 def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
     """The measurement of one workload: K timed CUDA-graph steps (max over
     ranks), the dominant op's roofline, per-op times, e2e through the host
-    buffer API, the kernel launches in the timed region, clocks, and (with
-    ``extras``) the next rows of the layer."""
+    buffer API, the kernel launches in the timed region, clocks, the step on
+    packed fp4 caches (64 x 128 indexers), and (with ``extras``) the next
+    rows of the layer."""
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
     fc = ds41.yarn_freqs_cis(wl.rd, wl.max_pos, device=dev)
 
+    # Rotate over enough layer states that the bytes the steps of one
+    # rotation touch exceed twice L2 (at most 256 states, 24 GB).
     one = build_slots(wl, 1, dev)
     per = slot_bytes(one[0])
-    n_slots = max(1, min(256, math.ceil(2.2 * l2 / per)))
+    touched = step_bytes(wl, fp4=fp4_supported(wl))
+    n_slots = max(1, min(256, math.ceil(2.2 * l2 / touched), int(24e9 // per)))
     slots = one + (build_slots(wl, n_slots - 1, dev, seed0=2000) if n_slots > 1 else [])
     torch.cuda.synchronize()
 
@@ -515,36 +643,8 @@ def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
     stream.synchronize()
     launches, launches_how = kernel_nodes(wl, slots[0], fc, stream)
 
-    graphs = []
-    for inp, out in slots:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            ds41.csa_forward(inp, wl, fc, out)
-        graphs.append(g)
-    torch.cuda.synchronize()
-
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            graphs[i % n_slots].replay()
-    stream.synchronize()
-
-    clocks = Clocks(dev.index if dev.index is not None else 0)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(K):
-            graphs[(W + i) % n_slots].replay()
-        e1.record(stream)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    barrier(world)
-    ck = clocks.stop()
-    t_ms = e0.elapsed_time(e1)
-    t_max_ms = max_over_ranks(t_ms, world)
+    graphs = capture_steps(lambda inp, out: ds41.csa_forward(inp, wl, fc, out), slots, stream)
+    t_max_ms, ck = time_graph_steps(graphs, K, W, world, dev, stream)
     del graphs
 
     op_ms = time_ops(wl, slots, fc, stream)
@@ -555,9 +655,9 @@ def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
     res = {"value": wl.m * K * world / (t_max_ms / 1e3), "unit": "query-tokens/s",
            "steps": K, "warmup": W, "ms_per_step": t_max_ms / K,
            "workload": workload_desc(wl),
-           "l2": f"inputs larger than L2: {n_slots} rotating layer states x "
-                 f"{per / 2**20:.2f} MiB = {n_slots * per / 2**20:.0f} MiB "
-                 f"(L2 {l2 / 2**20:.0f} MiB)",
+           "l2": f"inputs larger than L2: {n_slots} rotating layer states of {per / 2**20:.2f} MiB "
+                 f"({n_slots * per / 2**20:.0f} MiB); one rotation's steps touch "
+                 f"{n_slots * touched / 2**20:.0f} MiB (L2 {l2 / 2**20:.0f} MiB)",
            "roofline": roof, "per_op_ms": op_ms, "e2e": e2e,
            "gpu_launches": launches * K, "gpu_launches_per_step": launches,
            "gpu_launches_how": launches_how, "clocks": ck}
@@ -567,6 +667,9 @@ def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
         reuse = time_reuse(wl, slots, stream)
         res["next_rows"] = dict({"attn_out_proj": out_proj} if out_proj else {},
                                 csa_forward_reuse=reuse)
+    if fp4_supported(wl):
+        res["variants"] = {"fp4_caches": time_fp4_variant(wl, slots, fc, K, W, world, dev, stream,
+                                                          args)}
     del slots, one
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -598,6 +701,7 @@ def run_ours(args, world, rank, local):
         "roofline": head["roofline"],
         "per_op_ms": head["per_op_ms"],
         "next_rows": head["next_rows"],
+        "variants": head.get("variants", {}),
         "e2e": head["e2e"],
         "gpu_launches": head["gpu_launches"],
         "gpu_launches_how": head["gpu_launches_how"],
@@ -634,6 +738,8 @@ def run_only(args, local):
         for inp, out in slots:
             out["cidx"] = out["idx"][:, wl.win:].contiguous() if sz.ctopk else None
             out["reuse"] = {}
+    elif args.only in ("indexer_topk_mxf4", "step_fp4"):
+        add_fp4_caches(wl, slots)
     torch.cuda.synchronize()
 
     def op(i):
@@ -642,6 +748,12 @@ def run_only(args, local):
             ds41.csa_forward(inp, wl, fc, out)
         elif args.only in OPS:
             call_op(args.only, wl, inp, out, fc)
+        elif args.only == "indexer_topk_mxf4":
+            ds41.indexer_topk_mxf4(inp["q_idx"], inp["k_codes"], inp["k_scales"], inp["w"],
+                                   out["win_idx"], wl.ratio, wl.start_pos, wl.topk, sz.n_a,
+                                   idx=out["idx"])
+        elif args.only == "step_fp4":
+            ds41.csa_forward_fp4(inp, wl, fc, out)
         elif args.only == "attn_out_proj":
             ds41.attn_out_proj(out["o"], fc, wts["wo_a"], wts["wo_b"], wl.rd, P["groups"],
                                wl.start_pos, og=out["og"], out=out["proj"])

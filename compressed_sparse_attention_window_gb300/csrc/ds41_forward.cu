@@ -132,6 +132,129 @@ extern "C" int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf
                     nullptr, 0, true, st, name);
 }
 
+// ---------------------------------------------------------------------------
+// The step on packed fp4 caches: the indexer keys as mxf4 (e2m1 codes + e8m0
+// block-32 scales) read by the block-scaled tensor-core scores, and the latent
+// rows also written as e2m1 codes + e4m3 block-16 scales.
+// ---------------------------------------------------------------------------
+static bool fp4_fused(int64_t m, int64_t nh, int64_t hd, int64_t K, int64_t n_c) {
+    return n_c >= 1 && m <= 8 && attn_is_cluster_path(m, nh, hd, K);
+}
+
+extern "C" size_t ds41_csa_fp4_workspace_bytes(int64_t m, int64_t start_pos, int64_t nh,
+                                               int64_t hd, int64_t win, int64_t ratio,
+                                               int64_t topk) {
+    if (m < 1 || ratio < 1 || win < 1 || start_pos < 0) return 0;
+    const int64_t n_c = (start_pos + m) / ratio;
+    const int64_t K = win + ctopk_of(topk, n_c);
+    const size_t a = n_c > 0 ? ds41_indexer_mxf4_workspace_bytes(m, n_c, 0) : 0;
+    const size_t b = fp4_fused(m, nh, hd, K, n_c) ? 0 : attn_ws_bytes(m, nh, hd, K);
+    return a > b ? a : b;
+}
+
+extern "C" int ds41_csa_forward_fp4(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring,
+                                    ds41_bf16* rows_a, const ds41_bf16* latent,
+                                    const float* freqs_cis, int64_t max_pos, ds41_bf16* cache,
+                                    uint8_t* cache_codes, uint8_t* cache_scales,
+                                    int64_t cache_rows, const ds41_bf16* q_idx,
+                                    const uint8_t* k_codes, const uint8_t* k_scales,
+                                    const float* w, const float* sink, float scale,
+                                    int32_t* win_idx, int32_t* idx, ds41_bf16* o, float* lse,
+                                    int64_t m, int64_t start_pos, int64_t nh, int64_t hd,
+                                    int64_t rd, int64_t win, int64_t ratio, int64_t topk,
+                                    int64_t Hi, int64_t Di, void* ws, size_t ws_bytes,
+                                    ds41_stream_t stream) {
+    const char* name = "ds41_csa_forward_fp4";
+    DS41_REQUIRE(m >= 1 && m < (int64_t(1) << 25), DS41_E_RANGE, "%s: m=%lld", name,
+                 (long long)m);
+    DS41_REQUIRE(start_pos >= 0 && start_pos + m < (int64_t(1) << 31), DS41_E_RANGE,
+                 "%s: start_pos=%lld", name, (long long)start_pos);
+    DS41_REQUIRE(ratio >= 1 && win >= 1 && topk >= 1, DS41_E_ARG,
+                 "%s: ratio=%lld win=%lld topk=%lld", name, (long long)ratio, (long long)win,
+                 (long long)topk);
+    DS41_REQUIRE(indexer_mxf4_supported(Hi, Di), DS41_E_ARG,
+                 "%s: Hi=%lld Di=%lld; the packed-key path takes 64 heads of dim 128", name,
+                 (long long)Hi, (long long)Di);
+    const int64_t n_c = (start_pos + m) / ratio;
+    const int64_t G = n_c - start_pos / ratio;
+    const int64_t ctopk = ctopk_of(topk, n_c);
+    const int64_t K = win + ctopk;
+    const int64_t n_a = ds41_rows_a_len(m, win, start_pos);
+    const size_t need = ds41_csa_fp4_workspace_bytes(m, start_pos, nh, hd, win, ratio, topk);
+    DS41_REQUIRE(need == 0 || (ws && ws_bytes >= need), DS41_E_WORKSPACE,
+                 "%s: workspace of %zu bytes needed, %zu given", name, need, ws ? ws_bytes : 0);
+    DS41_REQUIRE((cache_codes == nullptr) == (cache_scales == nullptr), DS41_E_ARG,
+                 "%s: cache_codes and cache_scales go together", name);
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool chunk = start_pos > 0 && m > 1;
+    const ds41_bf16* rows_a_used = start_pos == 0 ? kv : (m == 1 ? ring : rows_a);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+
+    if (!fp4_fused(m, nh, hd, K, n_c)) {
+        int rc = ds41_window_ring_write(kv, ring, rows_a, win_idx, nullptr, m, hd, win, start_pos,
+                                        stream);
+        if (rc) return rc;
+        if (G > 0) {
+            rc = ds41_compress_latent_write(latent, freqs_cis, max_pos, cache, cache_rows,
+                                            cache_codes, cache_scales, G, hd, rd, ratio,
+                                            start_pos, m, stream);
+            if (rc) return rc;
+        }
+        const int32_t* att_idx = win_idx;
+        if (n_c > 0) {
+            rc = ds41_indexer_topk_mxf4(q_idx, k_codes, k_scales, w, win_idx, idx, nullptr, m, Hi,
+                                        Di, n_c, win, ratio, start_pos, topk, n_a, ws, ws_bytes,
+                                        stream);
+            if (rc) return rc;
+            att_idx = idx;
+        }
+        return ds41_sparse_attn_sink_fwd(q, rows_a_used, n_a, n_c ? cache : nullptr, n_c, att_idx,
+                                         K, sink, scale, o, lse, m, nh, hd, ws, ws_bytes, stream);
+    }
+
+    // ---- few-token fused path: the same checks the separate entry points make
+    DS41_REQUIRE(hd >= 64 && hd <= 512 && (hd & (hd - 1)) == 0 && hd % 16 == 0, DS41_E_ARG,
+                 "%s: hd=%lld must be 64, 128, 256 or 512", name, (long long)hd);
+    DS41_REQUIRE(nh >= 1 && rd > 0 && rd % 2 == 0 && rd <= hd, DS41_E_ARG, "%s: nh=%lld rd=%lld",
+                 name, (long long)nh, (long long)rd);
+    DS41_REQUIRE(n_c <= cache_rows, DS41_E_RANGE, "%s: cache holds %lld rows, need %lld", name,
+                 (long long)cache_rows, (long long)n_c);
+    DS41_REQUIRE(G == 0 || start_pos + m <= max_pos, DS41_E_RANGE,
+                 "%s: RoPE table has %lld rows, need %lld", name, (long long)max_pos,
+                 (long long)(start_pos + m));
+    DS41_REQUIRE(q && kv && ring && cache && q_idx && k_codes && k_scales && w && sink &&
+                     win_idx && idx && o && (G == 0 || (latent && freqs_cis)) && (!chunk || rows_a),
+                 DS41_E_ARG, "%s: null tensor pointer", name);
+    DS41_REQUIRE(aligned16(q) && aligned16(kv) && aligned16(ring) && aligned16(cache) &&
+                     aligned16(q_idx) && aligned16(k_codes) && aligned16(k_scales) &&
+                     aligned16(w) && aligned16(o) &&
+                     (G == 0 || (aligned16(latent) && aligned16(freqs_cis))) &&
+                     (!chunk || aligned16(rows_a)) && aligned16(ws),
+                 DS41_E_ARG, "%s: pointers must be 16-byte aligned", name);
+    RingArgs ra{reinterpret_cast<const uint4*>(kv), reinterpret_cast<uint4*>(ring),
+                reinterpret_cast<uint4*>(rows_a), win_idx, m, hd / 8, win, start_pos, chunk};
+    LatentArgs la{reinterpret_cast<const uint4*>(latent),
+                  reinterpret_cast<const float2*>(freqs_cis), reinterpret_cast<uint4*>(cache),
+                  reinterpret_cast<uint32_t*>(cache_codes), cache_scales, (int)hd, (int)rd, (int)G,
+                  start_pos / ratio, ratio};
+    uint16_t* scores = reinterpret_cast<uint16_t*>(wsb);
+    unsigned int* status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    rc = indexer_mxf4_launch(q_idx, k_codes, k_scales, w, scores, m, n_c, ratio, start_pos, false,
+                             status, device_sm_count(), st, &ra, &la);
+    if (rc) return rc;
+    if (attn_topk_fusable(m, nh, hd, K, n_c)) {
+        const DecTopk tk{scores, win_idx, idx, n_c, ratio, start_pos, n_a, (int)win, (int)ctopk};
+        return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
+                        nullptr, 0, true, st, name, &tk);
+    }
+    rc = launch_topk(scores, win_idx, idx, m, n_c, win, ctopk, ratio, start_pos, n_a, true, st);
+    if (rc) return rc;
+    return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
+                    nullptr, 0, true, st, name);
+}
+
 // The step with its per-step inputs and its output in host memory: one copy
 // per input into the caller's device buffers, the step, and one copy of o
 // back, all on the caller's stream.

@@ -857,7 +857,7 @@ struct IndexerPlan {
     size_t kq_bytes, qq_bytes, sc_bytes;
 };
 
-static int device_sm_count() {
+int device_sm_count() {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

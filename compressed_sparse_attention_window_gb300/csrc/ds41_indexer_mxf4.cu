@@ -37,6 +37,7 @@
 // split over several CTAs.  Every wait is bounded; a timeout raises
 // DS41_E_TIMEOUT and the roles exit.
 #include "ds41_internal.cuh"
+#include "ds41_step1.cuh"
 #include "ds41_tc.cuh"
 
 namespace ds41 {
@@ -123,11 +124,14 @@ struct Params {
     const uint32_t* k_scales;  // [n_c] words: the 4 scale bytes of a key row
     uint16_t* scores;
     int m;
-    int G;   // token groups
-    int ys;  // CTAs per group (1: persistent over groups)
+    int G;          // token groups
+    int ys;         // CTAs per group (1: persistent over groups)
+    int main_ctas;  // CTAs of the score grid; the ones past it do step 1
     int64_t n_c, ratio, start_pos;
     int fill_hidden;
     unsigned int* status;
+    RingArgs ring;    // fused few-token step: ring write + window indices
+    LatentArgs lat;   // ... and the latent groups (lat.G == 0: none)
 };
 
 __device__ __forceinline__ int64_t visible(int64_t t, const Params& p) {
@@ -142,7 +146,7 @@ struct Item {
 };
 __device__ __forceinline__ int n_items(const Params& p) {
     if (p.ys > 1) return 1;
-    return (int)((p.G - (int64_t)blockIdx.x + gridDim.x - 1) / gridDim.x);
+    return (int)((p.G - (int64_t)blockIdx.x + p.main_ctas - 1) / p.main_ctas);
 }
 __device__ __forceinline__ Item item_of(int j, const Params& p) {
     Item it;
@@ -152,7 +156,7 @@ __device__ __forceinline__ Item item_of(int j, const Params& p) {
         it.tile0 = (int)(blockIdx.x / p.G);
         it.tstride = p.ys;
     } else {
-        gi = p.G - 1 - (int)(blockIdx.x + (int64_t)j * gridDim.x);  // later groups see more
+        gi = p.G - 1 - (int)(blockIdx.x + (int64_t)j * p.main_ctas);  // later groups see more
         it.tile0 = 0;
         it.tstride = 1;
     }
@@ -180,6 +184,17 @@ __device__ __forceinline__ void load_sfa(const Params& p, int64_t r0, int lane, 
 __global__ void __launch_bounds__(THREADS, 1)
     indexer_mxf4_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k, const Params p) {
+    pdl_trigger();  // a dependent kernel may start launching (it waits for this one)
+    if ((int)blockIdx.x >= p.main_ctas) {
+        // Fused front of a few-token step: the CTAs past the score grid do
+        // step 1 (ring write + window indices, then the latent groups).
+        const int side = (int)blockIdx.x - p.main_ctas, nside = (int)gridDim.x - p.main_ctas;
+        if (side == 0) ring_write_cta(p.ring);
+        const int hd8 = p.lat.hd / 8;
+        for (int g = side; g < p.lat.G; g += nside)
+            for (int k0 = 0; k0 < hd8; k0 += THREADS) latent_write_item(p.lat, g, k0 + threadIdx.x);
+        return;
+    }
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -500,7 +515,7 @@ bool indexer_mxf4_supported(int64_t Hi, int64_t Di) { return Hi == mx::HI && Di 
 int indexer_mxf4_launch(const uint16_t* q_idx, const uint8_t* k_codes, const uint8_t* k_scales,
                         const float* w, uint16_t* scores, int64_t m, int64_t n_c, int64_t ratio,
                         int64_t start_pos, bool fill_hidden, unsigned int* status, int sms,
-                        cudaStream_t st) {
+                        cudaStream_t st, const RingArgs* ring, const LatentArgs* lat) {
     using namespace mx;
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int rc = get_encode(&enc);
@@ -533,6 +548,10 @@ int indexer_mxf4_launch(const uint16_t* q_idx, const uint8_t* k_codes, const uin
         grid = p.G * p.ys;
         if (p.ys == 1) grid = p.G;
     }
+    p.main_ctas = grid;
+    p.ring = ring ? *ring : RingArgs{};
+    p.lat = lat ? *lat : LatentArgs{};
+    if (ring) grid += (lat && lat->G > 1) ? 2 : 1;  // step-1 CTAs of the fused step
     rc = cuda_check(cudaFuncSetAttribute(indexer_mxf4_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES),

@@ -9,6 +9,8 @@ namespace ds41 {
 struct RingArgs;
 struct LatentArgs;
 
+int device_sm_count();
+
 // few-token fused front: step 1 + indexer scores in one launch
 bool front_fusable(int64_t m, int64_t Hi, int64_t Di, int64_t n_c);
 size_t front_scores_bytes(int64_t m, int64_t n_c);
@@ -54,10 +56,13 @@ int indexer_tc_launch(const uint16_t* qq, const uint16_t* kq, const float* w, ui
 // indexer scores on a packed mxf4 key cache (ds41_indexer_mxf4.cu): q_idx
 // bf16 [m][64][128], k_codes [n_c][64] e2m1 codes, k_scales [n_c][4] e8m0
 bool indexer_mxf4_supported(int64_t Hi, int64_t Di);
+// With ring (and lat), extra CTAs past the score grid do step 1 of the
+// fused few-token step.
 int indexer_mxf4_launch(const uint16_t* q_idx, const uint8_t* k_codes, const uint8_t* k_scales,
                         const float* w, uint16_t* scores, int64_t m, int64_t n_c, int64_t ratio,
                         int64_t start_pos, bool fill_hidden, unsigned int* status, int sms,
-                        cudaStream_t st);
+                        cudaStream_t st, const RingArgs* ring = nullptr,
+                        const LatentArgs* lat = nullptr);
 
 // many-token attention on the tcgen05 tensor cores (ds41_attn_tc.cu)
 bool attn_tc_supported(int64_t m, int64_t nh, int64_t hd, int64_t K, int sms);

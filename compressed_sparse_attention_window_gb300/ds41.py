@@ -54,6 +54,10 @@ SIGNATURES = {
     "ds41_sparse_attn_sink_fwd": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F, _P, _P,
                                                  _I64, _I64, _I64, _P, _SZ, _P]),
     "ds41_csa_workspace_bytes": (_SZ, [_I64] * 9),
+    "ds41_csa_fp4_workspace_bytes": (_SZ, [_I64] * 7),
+    "ds41_csa_forward_fp4": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _I64, _P, _P,
+                                            _P, _P, _P, _F, _P, _P, _P, _P] + [_I64] * 10
+                             + [_P, _SZ, _P]),
     "ds41_csa_forward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _P, _P, _F,
                                         _P, _P, _P, _P] + [_I64] * 10 + [_P, _SZ, _P]),
     "ds41_csa_forward_host": (ctypes.c_int, [_P] * 6 + [_P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P,
@@ -440,6 +444,60 @@ def csa_forward(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
           _ptr(freqs_cis, torch.float32, "freqs_cis"), freqs_cis.shape[0],
           _ptr(inp["cache"], _BF, "cache"), inp["cache"].shape[0], _ptr(inp["q_idx"], _BF, "q_idx"),
           _ptr(inp["k_idx"], _BF, "k_idx"), _ptr(inp["w"], torch.float32, "w"),
+          _ptr(inp["sink"], torch.float32, "sink"), float(wl.scale),
+          _ptr(out["win_idx"], torch.int32, "win_idx"), _ptr(out["idx"], torch.int32, "idx"),
+          _ptr(out["o"], _BF, "o"), _ptr(out.get("lse"), torch.float32, "lse"), m, wl.start_pos,
+          wl.nh, wl.hd, wl.rd, win, wl.ratio, wl.topk, wl.Hi, wl.Di, _ptr(ws) if need else None,
+          need, _stream())
+    if sz.n_c == 0:
+        out["idx"] = out["win_idx"]
+    return out
+
+
+def pack_keys(k_idx: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The mxf4 form of an indexer key cache [n_c, Di] bf16: (codes [n_c, Di/2],
+    scales [n_c, Di/32]) through ds41_fp4_quant_e8m0."""
+    _, codes, scales = fp4_quant(k_idx, e4m3=False, want_codes=True)
+    return codes, scales
+
+
+def csa_fp4_workspace_bytes(wl) -> int:
+    return int(load().ds41_csa_fp4_workspace_bytes(wl.m, wl.start_pos, wl.nh, wl.hd, wl.win,
+                                                   wl.ratio, wl.topk))
+
+
+def csa_forward_fp4(inp: Dict[str, torch.Tensor], wl, freqs_cis: torch.Tensor,
+                    out: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
+    """ds41_csa_forward_fp4: the whole step on packed fp4 caches.  ``inp`` holds
+    the inputs of :func:`csa_forward` with the indexer keys as ``k_codes`` /
+    ``k_scales`` (see :func:`pack_keys`) and, optionally, ``cache_codes`` /
+    ``cache_scales`` for the packed latent rows."""
+    out = {} if out is None else out
+    dev = inp["q"].device
+    m, win = wl.m, wl.win
+    sz = step_sizes(wl)
+    if "win_idx" not in out:
+        out["win_idx"] = torch.empty(m, win, dtype=torch.int32, device=dev)
+    if "idx" not in out:
+        out["idx"] = torch.empty(m, sz.K, dtype=torch.int32, device=dev)
+    if "o" not in out:
+        out["o"] = torch.empty_like(inp["q"])
+    chunk = wl.start_pos > 0 and m > 1
+    if chunk and "rows_a" not in out:
+        out["rows_a"] = torch.empty(win + m, wl.hd, dtype=torch.bfloat16, device=dev)
+    need = csa_fp4_workspace_bytes(wl)
+    ws = out.get("ws_fp4")
+    if need and (ws is None or ws.numel() < need):
+        ws = out["ws_fp4"] = torch.empty(need, dtype=torch.uint8, device=dev)
+    cc, cs = inp.get("cache_codes"), inp.get("cache_scales")
+    _call("ds41_csa_forward_fp4", _ptr(inp["q"], _BF, "q"), _ptr(inp["kv"], _BF, "kv"),
+          _ptr(inp["ring"], _BF, "ring"), _ptr(out.get("rows_a") if chunk else None),
+          _ptr(inp["latent"], _BF, "latent") if sz.G > 0 else None,
+          _ptr(freqs_cis, torch.float32, "freqs_cis"), freqs_cis.shape[0],
+          _ptr(inp["cache"], _BF, "cache"), _ptr(cc, torch.uint8, "cache_codes"),
+          _ptr(cs, torch.uint8, "cache_scales"), inp["cache"].shape[0],
+          _ptr(inp["q_idx"], _BF, "q_idx"), _ptr(inp["k_codes"], torch.uint8, "k_codes"),
+          _ptr(inp["k_scales"], torch.uint8, "k_scales"), _ptr(inp["w"], torch.float32, "w"),
           _ptr(inp["sink"], torch.float32, "sink"), float(wl.scale),
           _ptr(out["win_idx"], torch.int32, "win_idx"), _ptr(out["idx"], torch.int32, "idx"),
           _ptr(out["o"], _BF, "o"), _ptr(out.get("lse"), torch.float32, "lse"), m, wl.start_pos,

@@ -277,6 +277,36 @@ int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring, d
                      int64_t ratio, int64_t topk, int64_t Hi, int64_t Di, void* ws,
                      size_t ws_bytes, ds41_stream_t stream);
 
+/* Scratch bytes ds41_csa_forward_fp4 needs for these sizes. */
+size_t ds41_csa_fp4_workspace_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_t hd,
+                                    int64_t win, int64_t ratio, int64_t topk);
+
+/* ds41_csa_forward on packed fp4 caches (the pages' precision, kept in its
+ * packed form).  The indexer keys are an mxf4 cache, as
+ * ds41_indexer_topk_mxf4 takes them: k_codes [n_c, Di/2] e2m1 codes and
+ * k_scales [n_c, Di/32] e8m0 bytes (68 bytes per row of 128 instead of 256).
+ * The latent write (forward.rs latent branch: fp4_quant with LATENT_BLOCK)
+ * writes the new compressed rows to `cache` (bf16, the values the
+ * attention reads) and, when cache_codes / cache_scales are given, also as
+ * e2m1 codes [cache_rows, hd/2] and e4m3 block-16 scale codes
+ * [cache_rows, hd/16] (288 bytes per row of 512 instead of 1024).  Every
+ * other argument, the results and the errors are those of ds41_csa_forward,
+ * bit for bit (the codes and scales encode the same values).  Hi == 64 and
+ * Di == 128 (DS41_E_ARG otherwise); k_codes, k_scales and w 16-byte
+ * aligned; cache_codes and cache_scales both given or both NULL.  Few-token
+ * calls run in two or three launches chained on the device (the scores
+ * kernel's extra CTAs do the ring and latent writes), larger ones as the
+ * separate calls. */
+int ds41_csa_forward_fp4(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring,
+                         ds41_bf16* rows_a, const ds41_bf16* latent, const float* freqs_cis,
+                         int64_t max_pos, ds41_bf16* cache, uint8_t* cache_codes,
+                         uint8_t* cache_scales, int64_t cache_rows, const ds41_bf16* q_idx,
+                         const uint8_t* k_codes, const uint8_t* k_scales, const float* w,
+                         const float* sink, float scale, int32_t* win_idx, int32_t* idx,
+                         ds41_bf16* o, float* lse, int64_t m, int64_t start_pos, int64_t nh,
+                         int64_t hd, int64_t rd, int64_t win, int64_t ratio, int64_t topk,
+                         int64_t Hi, int64_t Di, void* ws, size_t ws_bytes, ds41_stream_t stream);
+
 /* forward.rs, AttnV41::forward, for a layer that is neither a kv source
  * nor an index source: it writes its own window ring and window indices,
  * takes the compressed rows (rows_b) and the compressed picks of the last

@@ -119,3 +119,77 @@ def test_indexer_mxf4_rejects_other_shapes():
         ds41.indexer_topk_mxf4(inp["q_idx"], codes, scales, inp["w"], win_idx, wl.ratio,
                                wl.start_pos, wl.topk, wl.m)
     assert e.value.code == 1
+
+
+FP4_STEP = ["decode", "long_decode", "chunked_prefill", "prefill"]
+FP4_EXTRA = [DECODE.replace(start_pos=8190), DECODE.replace(m=2, start_pos=5000),
+             DECODE.replace(structure="repeat"), DECODE.replace(start_pos=16399, structure="repeat"),
+             DECODE.replace(m=5, start_pos=4000, topk=16)]
+
+
+@pytest.mark.parametrize("wl", [__import__("compressed_sparse_attention_window_gb300.workloads",
+                                           fromlist=["WORKLOADS"]).WORKLOADS[n] for n in FP4_STEP]
+                         + FP4_EXTRA, ids=lambda w: f"{w.name}-{w.m}-{w.start_pos}")
+def test_csa_forward_fp4_matches_the_bf16_step(orc, wl):
+    """The step on packed caches gives bit for bit the outputs and layer state
+    of ds41_csa_forward on the bf16 caches (fused few-token front with the
+    mxf4 scores kernel's step-1 CTAs, or the separate calls), the packed
+    latent rows equal the oracle's codes and scales, and o matches the
+    oracle."""
+    inp = make_inputs(wl)
+    ora_fc = orc.yarn_freqs_cis(wl.rd, max(wl.max_pos, 1))
+    fc = torch.from_numpy(ora_fc).cuda()
+    d1, d2 = to_dev(inp), to_dev(inp)
+    sz = ds41.step_sizes(wl)
+    d2["k_codes"], d2["k_scales"] = ds41.pack_keys(d2["k_idx"][: sz.n_c].contiguous())
+    rows = d2["cache"].shape[0]
+    d2["cache_codes"] = torch.zeros(rows, wl.hd // 2, dtype=torch.uint8, device="cuda")
+    d2["cache_scales"] = torch.zeros(rows, wl.hd // 16, dtype=torch.uint8, device="cuda")
+    out1 = ds41.csa_forward(d1, wl, fc)
+    out2 = ds41.csa_forward_fp4(d2, wl, fc)
+    torch.cuda.synchronize()
+    assert ds41.device_status() == 0
+    assert torch.equal(d1["ring"], d2["ring"]) and torch.equal(d1["cache"], d2["cache"])
+    assert torch.equal(out1["win_idx"], out2["win_idx"])
+    assert torch.equal(out1["idx"], out2["idx"])
+    assert torch.equal(out1["o"], out2["o"])
+    toks = sample_tokens(wl) if wl.m > 128 else list(range(wl.m))
+    from helpers import attn_close, oracle_forward
+    ref = oracle_forward(orc, wl, inp, tokens=toks, fc=ora_fc)
+    osz = ref["sizes"]
+    first = osz["n_c"] - osz["G"]
+    rows_w = slice(first, osz["n_c"])
+    assert np.array_equal(d2["cache_codes"].cpu().numpy()[rows_w], ref["codes"][rows_w])
+    assert np.array_equal(d2["cache_scales"].cpu().numpy()[rows_w], ref["scales"][rows_w])
+    assert_idx_sets_equal(out2["idx"].cpu().numpy()[toks], ref["idx"], wl.win)
+    ok, err, worst = attn_close(out2["o"].float().cpu().numpy()[toks], ref["o"])
+    assert ok, (wl.name, err, worst)
+
+
+@pytest.mark.parametrize("name", ["decode", "long_decode"])
+def test_csa_forward_fp4_graph_replay_matches_eager(name):
+    from compressed_sparse_attention_window_gb300.workloads import WORKLOADS
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    fc = ds41.yarn_freqs_cis(wl.rd, max(wl.max_pos, 1))
+    sz = ds41.step_sizes(wl)
+
+    def dev():
+        d = to_dev(inp)
+        d["k_codes"], d["k_scales"] = ds41.pack_keys(d["k_idx"][: sz.n_c].contiguous())
+        return d
+    dev_e = dev()
+    out_e = ds41.csa_forward_fp4(dev_e, wl, fc)
+    out_g = {}
+    ds41.csa_forward_fp4(dev(), wl, fc, out_g)
+    dev_g = dev()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ds41.csa_forward_fp4(dev_g, wl, fc, out_g)
+    for k in ("o", "idx"):
+        out_g[k].fill_(0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_e["o"], out_g["o"]) and torch.equal(out_e["idx"], out_g["idx"])
+    assert torch.equal(dev_e["ring"], dev_g["ring"]) and torch.equal(dev_e["cache"], dev_g["cache"])
