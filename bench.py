@@ -438,7 +438,7 @@ def time_out_proj(wl, slots, fc, stream, hbm, bf16, reps=5):
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm}
     roof.update({"ms_per_call": ms, "flops": flops, "algorithmic_bytes": nbytes,
                  "config": f"groups {P['groups']}, o_rank {P['o_rank']}, dim {P['dim']}, "
-                           "synthetic bf16 weights; inverse RoPE kernel + cuBLAS GEMMs"})
+                           "synthetic bf16 weights; inverse RoPE kernel, then a warp per weight row (m <= 16) or tcgen05 tiles"})
     return roof
 
 
@@ -688,8 +688,7 @@ def run_ours(args, world, rank, local):
         for name in CONFIG_ORDER:
             if name == wl.name:
                 continue
-            configs[name] = measure_workload(WORKLOADS[name], K, W, world, dev, stream, args,
-                                             extras=False)
+            configs[name] = measure_workload(WORKLOADS[name], K, W, world, dev, stream, args)
     res = {
         "metric": METRIC, "value": head["value"], "unit": "query-tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": head["ms_per_step"], "higher_is_better": True,

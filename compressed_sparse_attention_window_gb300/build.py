@@ -75,7 +75,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if force or _stale(LIB, objs):
         tmp = LIB + f".{os.getpid()}.tmp"
         cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lcublas",
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart",
                "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
         if verbose:
             print(" ".join(cmd), flush=True)

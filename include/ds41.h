@@ -11,11 +11,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Tensor pointers are DEVICE pointers owned by the caller (for example
- *   torch allocations).  The entry points allocate no device memory, with
- *   one exception: the first ds41_attn_out_proj call creates the library's
- *   cuBLAS handle, which holds cuBLAS's own workspace.  Entry points that
- *   need scratch memory take (ws, ws_bytes); the matching *_workspace_bytes
- *   function says how much.  Host pointers are marked "host".
+ *   torch allocations).  The entry points allocate no device memory.  Entry
+ *   points that need scratch memory take (ws, ws_bytes); the matching
+ *   *_workspace_bytes function says how much.  Host pointers are marked
+ *   "host".
  * - bf16 tensors are passed as uint16_t bit patterns (ds41_bf16).
  * - Layouts are row-major and contiguous; every device pointer must be 16-byte
  *   aligned.
@@ -448,8 +447,12 @@ int ds41_selftest_wait_timeout(uint32_t polls, int arrive, int32_t* result, ds41
  *       the result rounded to bf16 (IN PLACE: o is overwritten)
  *   og[t, g*o_rank + r] = bf16(sum_i o[t, g*gw + i] * wo_a[g*o_rank + r, i])
  *   out[t, j] = sum_k og[t, k] * wo_b[j, k]                           (f32)
- * with f32 accumulation in an unspecified order (cuBLAS), so og can differ
- * from a differently ordered sum by one bf16 step.
+ * with f32 accumulation, so og can differ from a differently ordered sum by
+ * one bf16 step.  Few tokens (m <= 16) run on the CUDA cores, a warp per
+ * weight row (the weight stream from HBM bounds them); more tokens run as
+ * tcgen05 tensor-core tiles of 128 weight rows when o_rank, dim and
+ * groups*o_rank are multiples of 128 and gw of 64 (else the CUDA-core
+ * kernel in chunks of 8 tokens).
  *   o        [m, nh, hd] bf16, in/out (the attention output; rotated back)
  *   freqs_cis [max_pos, rd/2, 2] f32 (cos, sin), as ds41_yarn_freqs_cis
  *   wo_a     [groups*o_rank, gw] bf16;  wo_b [dim, groups*o_rank] bf16
@@ -458,10 +461,8 @@ int ds41_selftest_wait_timeout(uint32_t polls, int arrive, int32_t* result, ds41
  *   and <= hd (rd = 0: no rotation, freqs_cis may be NULL), gw % 8 == 0,
  *   groups*o_rank % 8 == 0, dim % 4 == 0, start_pos + m <= max_pos.
  * Errors: DS41_E_ARG / DS41_E_RANGE before anything is enqueued; DS41_E_CUDA
- * when the rotation's launch or a cuBLAS call fails (the rotation may then
- * have run).  Thread-safe: the library's one cuBLAS handle is used under a
- * lock.  The handle belongs to the device current at the first call, so a
- * process calls this entry point on one device (one process per GPU). */
+ * when a launch fails (the launches before it stay enqueued).  Thread-safe;
+ * the work runs on the current device. */
 int ds41_attn_out_proj(ds41_bf16* o, const float* freqs_cis, int64_t max_pos,
                        const ds41_bf16* wo_a, const ds41_bf16* wo_b, ds41_bf16* og, float* out,
                        int64_t m, int64_t start_pos, int64_t nh, int64_t hd, int64_t rd,

@@ -545,10 +545,17 @@ def _out_proj_check(orc, o_bits, fc, wa, wb, og, out, rd, groups, start_pos, tok
 
 @pytest.mark.parametrize("m,nh,hd,rd,groups,o_rank,dim,start_pos",
                          [(3, 4, 64, 16, 2, 32, 48, 5), (37, 8, 128, 32, 4, 64, 200, 0),
-                          (1, 64, 512, 64, 8, 1024, 7168, 8191)])
+                          (1, 64, 512, 64, 8, 1024, 7168, 8191),
+                          (5, 64, 512, 64, 8, 1024, 7168, 100),
+                          (40, 16, 512, 64, 4, 256, 1024, 7),
+                          (100, 8, 256, 32, 2, 128, 256, 9),
+                          (130, 8, 512, 64, 2, 128, 384, 3)])
 def test_attn_out_proj_matches_oracle(orc, m, nh, hd, rd, groups, o_rank, dim, start_pos):
     """ds41_attn_out_proj against the oracle, every token, from a small case
-    to one decode token at the full sizes."""
+    to one decode token at the full sizes: the few-token kernel (a warp per
+    weight row, tokens in chunks of 1, 2, 4 or 8), the tensor-core kernel with
+    token tiles of 64, 128 and 256 (ragged last tile), and the few-token
+    kernel for more tokens when the row groups are not whole 128-row tiles."""
     g = torch.Generator().manual_seed(m + nh + dim)
     o = torch.randn(m, nh, hd, generator=g).to(torch.bfloat16)
     wts = make_out_proj_weights(nh, hd, groups, o_rank, dim, seed=m)
