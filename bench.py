@@ -11,10 +11,12 @@ decode, chunked prefill) the same way and reports them under ``configs``
 (``--headline-only`` skips them).
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier +
-synchronize on both sides, CUDA events on the launching stream, each step a
-CUDA-graph replay of the whole step.  Steps rotate over independent layer
-states whose total size exceeds twice the L2 cache, so every step reads its
-window ring, latent cache and indexer keys from HBM.  Each workload's entry
+synchronize on both sides, CUDA events on the launching stream, the steps
+replayed from CUDA graphs that each hold up to 8 consecutive steps (as a
+model's forward replays its layers from one graph).  Steps rotate over
+independent layer states, enough of them that the bytes one rotation's steps
+touch exceed twice the L2 cache, so every step reads its window ring, latent
+cache rows and indexer keys from HBM.  Each workload's entry
 adds the roofline of its dominant op (timed again with events around it),
 the end-to-end rate through the public API with host buffers, the number of
 kernel launches in the timed region (the kernel nodes of the captured step),
@@ -91,15 +93,17 @@ def max_over_ranks(x: float, world: int) -> float:
 # ---------------------------------------------------------------------------
 # algorithmic work of one step (bytes / flops the method itself must move)
 # ---------------------------------------------------------------------------
-def attn_valid_rows(wl) -> int:
+def attn_valid_rows(wl, split=False):
     """Valid gathered rows summed over the tokens: window positions that exist
-    plus the visible compressed rows the top-k keeps."""
-    tot = 0
+    plus the visible compressed rows the top-k keeps (with ``split``, the two
+    counts apart)."""
+    win_rows = comp_rows = 0
     for t in range(wl.m):
         p = wl.start_pos + t
         vis = min(wl.n_c, (p + 1) // wl.ratio)
-        tot += min(p + 1, wl.win) + min(wl.topk, vis)
-    return tot
+        win_rows += min(p + 1, wl.win)
+        comp_rows += min(wl.topk, vis)
+    return (win_rows, comp_rows) if split else win_rows + comp_rows
 
 
 def algorithmic(wl):
@@ -125,6 +129,13 @@ def algorithmic(wl):
             "bytes": rows * wl.hd * bf + 2 * m * wl.nh * wl.hd * bf + m * K * 4 + wl.nh * 4,
             "flops": 4 * wl.nh * wl.hd * rows},
     }
+    # the few-token attention on the packed latent rows: hd/2 code bytes +
+    # hd/16 scale bytes per gathered compressed row
+    win_rows, comp_rows = attn_valid_rows(wl, split=True)
+    ops["sparse_attn_sink_fwd_fp4"] = {
+        "bytes": (win_rows * wl.hd * bf + comp_rows * (wl.hd // 2 + wl.hd // 16)
+                  + 2 * m * wl.nh * wl.hd * bf + m * K * 4 + wl.nh * 4),
+        "flops": 4 * wl.nh * wl.hd * rows}
     return ops
 
 
@@ -498,23 +509,40 @@ def dominant_roofline(wl, op_ms, args):
     return roof
 
 
-def step_bytes(wl, fp4=False) -> int:
+def step_bytes(wl, fp4=False, packed_attn=False) -> int:
     """Algorithmic bytes one step touches (the sum of its ops' rows of
-    ``algorithmic``): what has to come from HBM when the step runs L2-cold."""
+    ``algorithmic``): what has to come from HBM when the step runs L2-cold.
+    ``fp4``: the indexer reads the mxf4 keys; ``packed_attn``: the attention
+    gathers packed latent rows."""
     alg = algorithmic(wl)
     ops = [k for k in OPS if k in alg]
-    if fp4 and "indexer_topk" in alg:
+    if fp4:
         ops = [k for k in ops if k != "indexer_topk"] + ["indexer_topk_mxf4"]
+    if packed_attn:
+        ops = [k for k in ops if k != "sparse_attn_sink_fwd"] + ["sparse_attn_sink_fwd_fp4"]
     return sum(alg[k]["bytes"] for k in ops if k in alg)
 
 
-def time_graph_steps(graphs, K, W, world, dev, stream):
-    """W warm-up replays, then K timed replays of the graphs in rotation
-    between a barrier + synchronize on both sides, events on the launching
-    stream, clocks sampled meanwhile.  Returns (max-over-ranks ms, clocks)."""
+def steps_per_graph(K: int, n_slots: int) -> int:
+    """Consecutive steps (layer states) captured in one CUDA graph: the largest
+    divisor of K up to 8 (and up to the number of layer states), so that
+    exactly K steps are timed.  A model's forward likewise replays its layers
+    from one graph; the host launch of a graph is paid once per graph."""
+    for d in range(min(8, n_slots, K), 0, -1):
+        if K % d == 0:
+            return d
+    return 1
+
+
+def time_graph_steps(graphs, spg, K, W, world, dev, stream):
+    """Warm-up replays covering at least W steps, then K timed steps (K / spg
+    replays of graphs of spg steps each, in rotation) between a barrier +
+    synchronize on both sides, events on the launching stream, clocks sampled
+    meanwhile.  Returns (max-over-ranks ms, clocks)."""
     n = len(graphs)
+    wr = (W + spg - 1) // spg
     with torch.cuda.stream(stream):
-        for i in range(W):
+        for i in range(wr):
             graphs[i % n].replay()
     stream.synchronize()
     clocks = Clocks(dev.index if dev.index is not None else 0)
@@ -525,8 +553,8 @@ def time_graph_steps(graphs, K, W, world, dev, stream):
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(K):
-            graphs[(W + i) % n].replay()
+        for i in range(K // spg):
+            graphs[(wr + i) % n].replay()
         e1.record(stream)
     e1.synchronize()
     torch.cuda.synchronize()
@@ -535,13 +563,17 @@ def time_graph_steps(graphs, K, W, world, dev, stream):
     return max_over_ranks(e0.elapsed_time(e1), world), ck
 
 
-def capture_steps(step, slots, stream):
-    """One CUDA graph of ``step(inp, out)`` per layer state."""
+def capture_steps(step, slots, stream, spg=1):
+    """CUDA graphs of ``step(inp, out)``, each holding spg consecutive layer
+    states' steps (wrapping around), covering every layer state."""
     graphs = []
-    for inp, out in slots:
+    n = len(slots)
+    for j in range((n + spg - 1) // spg):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(inp, out)
+            for r in range(spg):
+                inp, out = slots[(j * spg + r) % n]
+                step(inp, out)
         graphs.append(g)
     torch.cuda.synchronize()
     return graphs
@@ -553,32 +585,43 @@ def fp4_supported(wl) -> bool:
 
 def add_fp4_caches(wl, slots):
     """The packed caches of every layer state: the indexer keys as mxf4
-    (codes + e8m0 scales, from the bf16 keys through ds41_fp4_quant_e8m0) and
-    room for the latent rows as e2m1 codes + e4m3 scales."""
+    (codes + e8m0 scales, from the bf16 keys through ds41_fp4_quant_e8m0), and
+    the latent rows as e2m1 codes + e4m3 scales: the drawn rows go through
+    ds41_fp4_quant_e4m3 (the latent write's round trip), whose values replace
+    the bf16 rows, so both forms of the cache hold the same values."""
     sz = ds41.step_sizes(wl)
     for inp, _ in slots:
         inp["k_codes"], inp["k_scales"] = ds41.pack_keys(inp["k_idx"][: max(1, sz.n_c)].contiguous())
-        rows = inp["cache"].shape[0]
-        inp["cache_codes"] = torch.zeros(rows, wl.hd // 2, dtype=torch.uint8, device=inp["q"].device)
-        inp["cache_scales"] = torch.zeros(rows, wl.hd // 16, dtype=torch.uint8,
-                                          device=inp["q"].device)
+        cq, inp["cache_codes"], inp["cache_scales"] = ds41.fp4_quant(inp["cache"], e4m3=True,
+                                                                     want_codes=True)
+        inp["cache"].copy_(cq)
     torch.cuda.synchronize()
 
 
-def time_fp4_variant(wl, slots, fc, K, W, world, dev, stream, args):
+def time_fp4_variant(wl, slots, fc, K, W, world, dev, stream, args, latent_packed=True):
     """The step on packed fp4 caches (ds41_csa_forward_fp4; the step's own
     results bit for bit, see the tests): per-step time from graph replays over
     the same rotating layer states, the mxf4 indexer op alone, and the
-    roofline of the variant's dominant op."""
+    roofline of the variant's dominant op.  With ``latent_packed`` the latent
+    rows are written and (few tokens) gathered packed too; without, only the
+    indexer keys are packed."""
     add_fp4_caches(wl, slots)
+    inps = []
+    for inp, _ in slots:
+        d = dict(inp)
+        if not latent_packed:
+            d.pop("cache_codes", None)
+            d.pop("cache_scales", None)
+        inps.append(d)
     outs = [dict(out) for _, out in slots]
     with torch.cuda.stream(stream):
-        for (inp, _), o in zip(slots, outs):
+        for inp, o in zip(inps, outs):
             ds41.csa_forward_fp4(inp, wl, fc, o)
     stream.synchronize()
+    spg = steps_per_graph(K, len(slots))
     graphs = capture_steps(lambda inp, out: ds41.csa_forward_fp4(inp, wl, fc, out),
-                           list(zip([i for i, _ in slots], outs)), stream)
-    t_ms, ck = time_graph_steps(graphs, K, W, world, dev, stream)
+                           list(zip(inps, outs)), stream, spg)
+    t_ms, ck = time_graph_steps(graphs, spg, K, W, world, dev, stream)
     del graphs
     sz = ds41.step_sizes(wl)
     op_ms = {}
@@ -600,11 +643,15 @@ def time_fp4_variant(wl, slots, fc, K, W, world, dev, stream, args):
         e1.synchronize()
         op_ms["indexer_topk_mxf4"] = e0.elapsed_time(e1) / (5 * len(slots))
         del g
+    packed_attn = latent_packed and wl.m <= 8 and wl.hd == 512
     res = {"ms_per_step": t_ms / K, "value": wl.m * K * world / (t_ms / 1e3),
            "unit": "query-tokens/s", "steps": K, "clocks": ck, "per_op_ms": op_ms,
-           "algorithmic_bytes_per_step": step_bytes(wl, fp4=True),
-           "what": "ds41_csa_forward_fp4: indexer keys as mxf4 (68 B/row), scores by block-scaled "
-                   "tcgen05 MMAs; latent rows also written as e2m1 + e4m3 scales"}
+           "algorithmic_bytes_per_step": step_bytes(wl, fp4=True, packed_attn=packed_attn),
+           "what": ("ds41_csa_forward_fp4: indexer keys as mxf4 (68 B/row), scores by "
+                    "block-scaled tcgen05 MMAs; " +
+                    ("latent rows written and (few tokens) gathered as e2m1 codes + e4m3 "
+                     "block-16 scales (288 B/row), expanded in shared memory" if latent_packed
+                     else "latent cache in bf16"))}
     if op_ms:
         alg = algorithmic(wl)["indexer_topk_mxf4"]
         hbm = load_peaks()[0]
@@ -631,7 +678,8 @@ def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
     # rotation touch exceed twice L2 (at most 256 states, 24 GB).
     one = build_slots(wl, 1, dev)
     per = slot_bytes(one[0])
-    touched = step_bytes(wl, fp4=fp4_supported(wl))
+    touched = step_bytes(wl, fp4=fp4_supported(wl),
+                         packed_attn=fp4_supported(wl) and wl.m <= 8 and wl.hd == 512)
     n_slots = max(1, min(256, math.ceil(2.2 * l2 / touched), int(24e9 // per)))
     slots = one + (build_slots(wl, n_slots - 1, dev, seed0=2000) if n_slots > 1 else [])
     torch.cuda.synchronize()
@@ -643,8 +691,10 @@ def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
     stream.synchronize()
     launches, launches_how = kernel_nodes(wl, slots[0], fc, stream)
 
-    graphs = capture_steps(lambda inp, out: ds41.csa_forward(inp, wl, fc, out), slots, stream)
-    t_max_ms, ck = time_graph_steps(graphs, K, W, world, dev, stream)
+    spg = steps_per_graph(K, n_slots)
+    graphs = capture_steps(lambda inp, out: ds41.csa_forward(inp, wl, fc, out), slots, stream,
+                           spg)
+    t_max_ms, ck = time_graph_steps(graphs, spg, K, W, world, dev, stream)
     del graphs
 
     op_ms = time_ops(wl, slots, fc, stream)
@@ -658,6 +708,8 @@ def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
            "l2": f"inputs larger than L2: {n_slots} rotating layer states of {per / 2**20:.2f} MiB "
                  f"({n_slots * per / 2**20:.0f} MiB); one rotation's steps touch "
                  f"{n_slots * touched / 2**20:.0f} MiB (L2 {l2 / 2**20:.0f} MiB)",
+           "timing": f"CUDA graphs of {spg} consecutive steps (layer states), "
+                     f"{K // spg} replays, events on the launching stream",
            "roofline": roof, "per_op_ms": op_ms, "e2e": e2e,
            "gpu_launches": launches * K, "gpu_launches_per_step": launches,
            "gpu_launches_how": launches_how, "clocks": ck}
@@ -668,8 +720,10 @@ def measure_workload(wl, K, W, world, dev, stream, args, extras=True):
         res["next_rows"] = dict({"attn_out_proj": out_proj} if out_proj else {},
                                 csa_forward_reuse=reuse)
     if fp4_supported(wl):
-        res["variants"] = {"fp4_caches": time_fp4_variant(wl, slots, fc, K, W, world, dev, stream,
-                                                          args)}
+        res["variants"] = {
+            "fp4_keys": time_fp4_variant(wl, slots, fc, K, W, world, dev, stream, args,
+                                         latent_packed=False),
+            "fp4_caches": time_fp4_variant(wl, slots, fc, K, W, world, dev, stream, args)}
     del slots, one
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -696,7 +750,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": head["workload"],
                    "global_batch": wl.m * world, "parallelism": f"replicas{world}",
                    "l2": head["l2"],
-                   "timing": "CUDA-graph replay per step, CUDA events on the launching stream"},
+                   "timing": head["timing"]},
         "roofline": head["roofline"],
         "per_op_ms": head["per_op_ms"],
         "next_rows": head["next_rows"],

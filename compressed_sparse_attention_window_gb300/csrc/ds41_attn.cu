@@ -735,7 +735,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ rows_a, int64_t n_a,
     const uint16_t* __restrict__ rows_b, int64_t n_c, const int32_t* __restrict__ idx, int K,
     const float* __restrict__ sink, float scale_log2, uint16_t* __restrict__ o,
-    float* __restrict__ lse, int nh, unsigned int* status, DecTopk tk) {
+    float* __restrict__ lse, int nh, unsigned int* status, DecTopk tk, PackedRows pk) {
     namespace cg = cooperative_groups;
     using SM = DecSmem<HD>;
     constexpr int NW = dec_warps<HD>();
@@ -744,6 +744,12 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     constexpr int QW = HD / NW;      // head-dim columns per warp
     constexpr int NT = QW / 8;       // output n-tiles per warp
     constexpr uint32_t ROWB = HD * 2;  // bytes of one row
+    // A packed compressed row (e2m1 codes + e4m3 block-16 scale codes) lands
+    // at the tail of its padded row buffer and is expanded in place.
+    constexpr uint32_t PKB = HD / 2 + HD / 16;
+    constexpr uint32_t PKO = ((uint32_t)RS * 2 - PKB) & ~15u;
+    static_assert(PKO + PKB <= (uint32_t)RS * 2 && PKO % 16 == 0, "packed row placement");
+    const bool packed = HD == 512 && pk.codes != nullptr;
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* qs = reinterpret_cast<uint16_t*>(smem);
     uint16_t* kvs = reinterpret_cast<uint16_t*>(smem + SM::q_bytes);
@@ -809,7 +815,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     auto load_chunk = [&](int chunk, int buf) {
         int64_t vr[RPL];
         bool okr[RPL];
-        uint32_t nok = 0;
+        uint32_t nok = 0, npk = 0;
 #pragma unroll
         for (int i = 0; i < RPL; i++) {
             const int r = lane + 32 * i;
@@ -820,27 +826,78 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
             const bool ok = v >= 0 && v < n_rows;
             if (in && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
             nok += __popc(__ballot_sync(0xffffffffu, ok));
+            npk += __popc(__ballot_sync(0xffffffffu, ok && packed && v >= n_a));
             vr[i] = v;
             okr[i] = ok;
         }
         // order this buffer's earlier generic-proxy writes before the copies
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        if (lane == 0) mbar_arrive_expect_tx(&bars[1 + buf], nok * ROWB);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[1 + buf], (nok - npk) * ROWB + npk * PKB);
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < RPL; i++) {
             const int r = lane + 32 * i;
             if (r >= DEC_NC) continue;
             uint16_t* dst = kvs + buf * (DEC_NC * RS) + r * RS;
+            int flag = 0;
             if (okr[i]) {
                 const int64_t v = vr[i];
-                const uint16_t* src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
-                bulk_g2s(dst, src, ROWB, &bars[1 + buf]);
+                if (packed && v >= n_a) {
+                    uint8_t* d8 = reinterpret_cast<uint8_t*>(dst) + PKO;
+                    bulk_g2s(d8, pk.codes + (v - n_a) * (HD / 2), HD / 2, &bars[1 + buf]);
+                    bulk_g2s(d8 + HD / 2, pk.scales + (v - n_a) * (HD / 16), HD / 16, &bars[1 + buf]);
+                    flag = 2;
+                } else {
+                    const uint16_t* src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
+                    bulk_g2s(dst, src, ROWB, &bars[1 + buf]);
+                    flag = 1;
+                }
             } else {
                 for (int c = 0; c < HD / 8; c++) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
             }
-            vflag[buf * DEC_NC + r] = okr[i] ? 1 : 0;
+            vflag[buf * DEC_NC + r] = flag;
         }
+    };
+    // Packed rows of a landed chunk -> bf16 in place, a warp per row: lane b
+    // holds block b (16 values: 8 code bytes, one scale byte) in registers
+    // before any lane writes, then writes bf16(e2m1 * scale), the exact value
+    // the latent write stored in the bf16 cache.
+    auto expand_chunk = [&](int buf) {
+        uint16_t* kvb = kvs + buf * (DEC_NC * RS);
+        for (int r = warp; r < DEC_NC; r += NW) {
+            if (vflag[buf * DEC_NC + r] != 2) continue;  // the same for the whole warp
+            uint8_t* row = reinterpret_cast<uint8_t*>(kvb + r * RS);
+            uint2 cb[(HD / 16 + 31) / 32];
+            uint32_t sb[(HD / 16 + 31) / 32];
+#pragma unroll
+            for (int u = 0; u < (HD / 16 + 31) / 32; u++) {
+                const int b = lane + 32 * u;
+                if (b < HD / 16) {
+                    cb[u] = *reinterpret_cast<const uint2*>(row + PKO + 8 * b);
+                    sb[u] = row[PKO + HD / 2 + b];
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < (HD / 16 + 31) / 32; u++) {
+                const int b = lane + 32 * u;
+                if (b >= HD / 16) continue;
+                const float s = e4m3_to_f32(sb[u]);
+                uint32_t w[8];
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const uint32_t byte = ((k < 4 ? cb[u].x : cb[u].y) >> (8 * (k & 3))) & 0xffu;
+                    const float2 g = e2m1x2_to_float2(byte);
+                    w[k] = (uint32_t)f2bf(__fmul_rn(g.x, s)) | ((uint32_t)f2bf(__fmul_rn(g.y, s)) << 16);
+                }
+                uint4* out = reinterpret_cast<uint4*>(row + 32 * b);
+                out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+        }
+        // these generic writes come before later bulk copies into the buffer
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        __syncthreads();
     };
     constexpr int NCT = DEC_NC / 8;   // n-tiles of 8 rows per chunk
     constexpr int NKS = DEC_NC / 16;  // k-steps of 16 rows per chunk in P*V
@@ -860,6 +917,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         if (chunk == 0 && !mbar_wait(&bars[0], 0, kWaitPolls)) failed = true;
         if (!mbar_wait(&bars[1 + buf], (chunk >> 1) & 1, kWaitPolls)) failed = true;
         __syncthreads();  // zero-filled rows and flags of warp 0 are visible
+        if (packed) expand_chunk(buf);
         const uint16_t* kv = kvs + buf * (DEC_NC * RS);
         float sacc[NCT][4];
 #pragma unroll
@@ -1141,10 +1199,11 @@ static int launch_attn_decode(const AttnPlan& p, const uint16_t* q, const uint16
                               const int32_t* idx, int64_t K, const float* sink, float scale,
                               uint16_t* o, float* lse, int64_t m, int64_t nh,
                               unsigned int* status, cudaStream_t st, bool pdl,
-                              const DecTopk* tk = nullptr) {
+                              const DecTopk* tk = nullptr, const PackedRows* pk = nullptr) {
     const size_t smem = tk ? DecSmem<HD>::fused_total : DecSmem<HD>::total;
     auto kern = tk ? sparse_attn_decode_kernel<HD, true> : sparse_attn_decode_kernel<HD, false>;
     const DecTopk tkv = tk ? *tk : DecTopk{};
+    const PackedRows pkv = (pk && HD == 512) ? *pk : PackedRows{nullptr, nullptr};
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (p.cluster > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
@@ -1162,7 +1221,8 @@ static int launch_attn_decode(const AttnPlan& p, const uint16_t* q, const uint16
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
     int rc = cuda_check(cudaLaunchKernelEx(&cfg, kern, q, rows_a, n_a, rows_b, n_c, idx, (int)K,
-                                           sink, scale * LOG2E, o, lse, (int)nh, status, tkv),
+                                           sink, scale * LOG2E, o, lse, (int)nh, status, tkv,
+                                           pkv),
                         "ds41_sparse_attn_sink_fwd: decode kernel");
     if (rc) return rc;
     return launch_check("ds41_sparse_attn_sink_fwd: decode kernel");
@@ -1173,10 +1233,11 @@ static int launch_attn(const AttnPlan& p, const uint16_t* q, const uint16_t* row
                        const uint16_t* rows_b, int64_t n_c, const int32_t* idx, int64_t K,
                        const float* sink, float scale, uint16_t* o, float* lse, int64_t m,
                        int64_t nh, uint8_t* ws, unsigned int* status, cudaStream_t st,
-                       bool pdl = false, const DecTopk* tk = nullptr) {
+                       bool pdl = false, const DecTopk* tk = nullptr,
+                       const PackedRows* pk = nullptr) {
     if (p.cluster > 0)
         return launch_attn_decode<HD>(p, q, rows_a, n_a, rows_b, n_c, idx, K, sink, scale, o, lse,
-                                      m, nh, status, st, pdl, tk);
+                                      m, nh, status, st, pdl, tk, pk);
     if constexpr (HD == 512) {
         if (p.tc > 0)
             return attn_tc_launch(q, rows_a, n_a, rows_b, n_c, idx, K, sink, scale, o, lse, m, nh,
@@ -1264,7 +1325,8 @@ size_t attn_ws_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K) {
 int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint16_t* rows_b,
              int64_t n_c, const int32_t* idx, int64_t K, const float* sink, float scale,
              uint16_t* o, float* lse, int64_t m, int64_t nh, int64_t hd, uint8_t* ws,
-             size_t ws_bytes, bool pdl, cudaStream_t st, const char* name, const DecTopk* tk) {
+             size_t ws_bytes, bool pdl, cudaStream_t st, const char* name, const DecTopk* tk,
+             const PackedRows* pk) {
     unsigned int* status = nullptr;
     int rc = status_word(&status);
     if (rc) return rc;
@@ -1278,7 +1340,7 @@ int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint1
         case 64: return launch_attn<64>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk);
         case 128: return launch_attn<128>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk);
         case 256: return launch_attn<256>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk);
-        default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk);
+        default: return launch_attn<512>(p, q, ra, n_a, rb, n_c, idx, K, sink, scale, o, lse, m, nh, ws, status, st, pdl, tk, pk);
     }
 }
 

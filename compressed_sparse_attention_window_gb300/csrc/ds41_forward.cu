@@ -228,6 +228,7 @@ extern "C" int ds41_csa_forward_fp4(const ds41_bf16* q, const ds41_bf16* kv, ds4
     DS41_REQUIRE(aligned16(q) && aligned16(kv) && aligned16(ring) && aligned16(cache) &&
                      aligned16(q_idx) && aligned16(k_codes) && aligned16(k_scales) &&
                      aligned16(w) && aligned16(o) &&
+                     (!cache_codes || (aligned16(cache_codes) && aligned16(cache_scales))) &&
                      (G == 0 || (aligned16(latent) && aligned16(freqs_cis))) &&
                      (!chunk || aligned16(rows_a)) && aligned16(ws),
                  DS41_E_ARG, "%s: pointers must be 16-byte aligned", name);
@@ -244,15 +245,18 @@ extern "C" int ds41_csa_forward_fp4(const ds41_bf16* q, const ds41_bf16* kv, ds4
     rc = indexer_mxf4_launch(q_idx, k_codes, k_scales, w, scores, m, n_c, ratio, start_pos, false,
                              status, device_sm_count(), st, &ra, &la);
     if (rc) return rc;
+    // with the packed latent rows given, the attention gathers them packed
+    const PackedRows pk{cache_codes, cache_scales};
+    const PackedRows* pkp = (cache_codes && hd == 512) ? &pk : nullptr;
     if (attn_topk_fusable(m, nh, hd, K, n_c)) {
         const DecTopk tk{scores, win_idx, idx, n_c, ratio, start_pos, n_a, (int)win, (int)ctopk};
         return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
-                        nullptr, 0, true, st, name, &tk);
+                        nullptr, 0, true, st, name, &tk, pkp);
     }
     rc = launch_topk(scores, win_idx, idx, m, n_c, win, ctopk, ratio, start_pos, n_a, true, st);
     if (rc) return rc;
     return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
-                    nullptr, 0, true, st, name);
+                    nullptr, 0, true, st, name, nullptr, pkp);
 }
 
 // The step with its per-step inputs and its output in host memory: one copy

@@ -33,14 +33,23 @@ struct DecTopk {
     int win, ctopk;
 };
 
+// The compressed rows (rows_b) in their packed form: e2m1 codes [n_c][hd/2]
+// and e4m3 block-16 scale codes [n_c][hd/16], as the latent write stores them.
+struct PackedRows {
+    const uint8_t* codes;
+    const uint8_t* scales;
+};
+
 // sparse attention with an explicit plan choice; pdl launches the few-token
 // kernel with programmatic stream serialization; tk (few-token cluster path
-// only) makes the attention select its rows from the scores first
+// only) makes the attention select its rows from the scores first; pk
+// (few-token cluster path, hd 512 only) makes it gather the compressed rows
+// packed and expand them in shared memory
 int attn_run(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const uint16_t* rows_b,
              int64_t n_c, const int32_t* idx, int64_t K, const float* sink, float scale,
              uint16_t* o, float* lse, int64_t m, int64_t nh, int64_t hd, uint8_t* ws,
              size_t ws_bytes, bool pdl, cudaStream_t st, const char* name,
-             const DecTopk* tk = nullptr);
+             const DecTopk* tk = nullptr, const PackedRows* pk = nullptr);
 // whether the few-token attention can select its own rows for these sizes
 bool attn_topk_fusable(int64_t m, int64_t nh, int64_t hd, int64_t K, int64_t n_c);
 size_t attn_ws_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K);

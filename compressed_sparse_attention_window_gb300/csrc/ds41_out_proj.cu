@@ -170,6 +170,8 @@ struct Params {
     unsigned int* status;
 };
 
+// One CTA per SM walks its tiles: D[128 weight rows][BN tokens] in tensor
+// memory (two accumulators), the K steps through STAGES shared-memory stages.
 template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     proj_tc_kernel(const __grid_constant__ CUtensorMap map_w,

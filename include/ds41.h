@@ -285,13 +285,17 @@ size_t ds41_csa_fp4_workspace_bytes(int64_t m, int64_t start_pos, int64_t nh, in
  * ds41_indexer_topk_mxf4 takes them: k_codes [n_c, Di/2] e2m1 codes and
  * k_scales [n_c, Di/32] e8m0 bytes (68 bytes per row of 128 instead of 256).
  * The latent write (forward.rs latent branch: fp4_quant with LATENT_BLOCK)
- * writes the new compressed rows to `cache` (bf16, the values the
- * attention reads) and, when cache_codes / cache_scales are given, also as
- * e2m1 codes [cache_rows, hd/2] and e4m3 block-16 scale codes
- * [cache_rows, hd/16] (288 bytes per row of 512 instead of 1024).  Every
- * other argument, the results and the errors are those of ds41_csa_forward,
- * bit for bit (the codes and scales encode the same values).  Hi == 64 and
- * Di == 128 (DS41_E_ARG otherwise); k_codes, k_scales and w 16-byte
+ * writes the new compressed rows to `cache` (bf16) and, when cache_codes /
+ * cache_scales are given, also as e2m1 codes [cache_rows, hd/2] and e4m3
+ * block-16 scale codes [cache_rows, hd/16] (288 bytes per row of 512
+ * instead of 1024).  With them given, few-token calls at hd 512 gather the
+ * compressed rows in that packed form and expand them in shared memory to
+ * exactly the bf16 values (so cache_codes / cache_scales must hold the packed
+ * form of every row below n_c that the call does not write itself);
+ * many-token calls read the bf16 cache.  Every other argument, the results
+ * and the errors are those of ds41_csa_forward, bit for bit (the codes and
+ * scales encode the same values).  Hi == 64 and Di == 128 (DS41_E_ARG
+ * otherwise); k_codes, k_scales, w, cache_codes and cache_scales 16-byte
  * aligned; cache_codes and cache_scales both given or both NULL.  Few-token
  * calls run in two or three launches chained on the device (the scores
  * kernel's extra CTAs do the ring and latent writes), larger ones as the

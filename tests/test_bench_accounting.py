@@ -59,3 +59,16 @@ def test_recorded_traffic_only_for_matching_sources(tmp_path, monkeypatch):
     other.write_text(text.replace(head[0], "csrc 0000000000000000"))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(other))
     assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") is None
+
+
+def test_packed_cache_bytes_closed_form():
+    """Decode on packed caches: the attention gathers 128 window rows of
+    1024 B and 512 compressed rows of 256 code bytes + 32 scale bytes, plus q
+    and o (2 x 64 x 512 x 2 B), 640 indices and 64 sinks:
+    131072 + 147456 + 131072 + 2560 + 256 = 412416 B (789248 B on the bf16
+    cache).  The mxf4 indexer reads 2048 key rows of 64 + 4 B instead of 256 B:
+    16384 (q) + 139264 + 256 (w) + 512 (window indices) + 2560 (idx)."""
+    alg = bench.algorithmic(WORKLOADS["decode"])
+    assert alg["sparse_attn_sink_fwd"]["bytes"] == 789248
+    assert alg["sparse_attn_sink_fwd_fp4"]["bytes"] == 412416
+    assert alg["indexer_topk_mxf4"]["bytes"] == 16384 + 2048 * 68 + 256 + 512 + 2560

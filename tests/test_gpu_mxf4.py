@@ -133,18 +133,26 @@ FP4_EXTRA = [DECODE.replace(start_pos=8190), DECODE.replace(m=2, start_pos=5000)
 def test_csa_forward_fp4_matches_the_bf16_step(orc, wl):
     """The step on packed caches gives bit for bit the outputs and layer state
     of ds41_csa_forward on the bf16 caches (fused few-token front with the
-    mxf4 scores kernel's step-1 CTAs, or the separate calls), the packed
-    latent rows equal the oracle's codes and scales, and o matches the
-    oracle."""
+    mxf4 scores kernel's step-1 CTAs and the attention gathering the packed
+    latent rows, or the separate calls), its packed latent rows equal the
+    oracle's codes and scales, and o matches the oracle.  The prior cache rows
+    are method output: each side quantises the drawn rows with its own
+    e4m3 quantiser."""
+    from compressed_sparse_attention_window_gb300.workloads import from_bits
+    from helpers import attn_close, oracle_forward
     inp = make_inputs(wl)
+    # the oracle's prior cache: its own fp4 round trip of the drawn rows
+    ocq, occ, ocs = orc.fp4_quant(bf16_bits(inp["cache"]), 16, True)
+    oinp = dict(inp)
+    oinp["cache"] = from_bits(ocq)
     ora_fc = orc.yarn_freqs_cis(wl.rd, max(wl.max_pos, 1))
     fc = torch.from_numpy(ora_fc).cuda()
     d1, d2 = to_dev(inp), to_dev(inp)
+    cq, cc, cs = ds41.fp4_quant(d1["cache"], e4m3=True, want_codes=True)
+    d1["cache"], d2["cache"] = cq.clone(), cq.clone()
+    d2["cache_codes"], d2["cache_scales"] = cc, cs
     sz = ds41.step_sizes(wl)
     d2["k_codes"], d2["k_scales"] = ds41.pack_keys(d2["k_idx"][: sz.n_c].contiguous())
-    rows = d2["cache"].shape[0]
-    d2["cache_codes"] = torch.zeros(rows, wl.hd // 2, dtype=torch.uint8, device="cuda")
-    d2["cache_scales"] = torch.zeros(rows, wl.hd // 16, dtype=torch.uint8, device="cuda")
     out1 = ds41.csa_forward(d1, wl, fc)
     out2 = ds41.csa_forward_fp4(d2, wl, fc)
     torch.cuda.synchronize()
@@ -154,13 +162,16 @@ def test_csa_forward_fp4_matches_the_bf16_step(orc, wl):
     assert torch.equal(out1["idx"], out2["idx"])
     assert torch.equal(out1["o"], out2["o"])
     toks = sample_tokens(wl) if wl.m > 128 else list(range(wl.m))
-    from helpers import attn_close, oracle_forward
-    ref = oracle_forward(orc, wl, inp, tokens=toks, fc=ora_fc)
+    ref = oracle_forward(orc, wl, oinp, tokens=toks, fc=ora_fc)
     osz = ref["sizes"]
     first = osz["n_c"] - osz["G"]
-    rows_w = slice(first, osz["n_c"])
-    assert np.array_equal(d2["cache_codes"].cpu().numpy()[rows_w], ref["codes"][rows_w])
-    assert np.array_equal(d2["cache_scales"].cpu().numpy()[rows_w], ref["scales"][rows_w])
+    # the rows this call wrote: the oracle's latent codes; the rows before it:
+    # the oracle's round trip of the drawn rows
+    gcc, gcs = d2["cache_codes"].cpu().numpy(), d2["cache_scales"].cpu().numpy()
+    assert np.array_equal(gcc[first:osz["n_c"]], ref["codes"][first:osz["n_c"]])
+    assert np.array_equal(gcs[first:osz["n_c"]], ref["scales"][first:osz["n_c"]])
+    assert np.array_equal(gcc[:first], occ[:first]) and np.array_equal(gcs[:first], ocs[:first])
+    assert np.array_equal(bf16_bits(d2["cache"]), ref["cache"])
     assert_idx_sets_equal(out2["idx"].cpu().numpy()[toks], ref["idx"], wl.win)
     ok, err, worst = attn_close(out2["o"].float().cpu().numpy()[toks], ref["o"])
     assert ok, (wl.name, err, worst)
