@@ -142,40 +142,52 @@ def algorithmic(wl):
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
-def csrc_digest() -> str:
-    """sha256 (first 16 hex digits) over the CUDA sources, by sorted name: the
-    kernels that a set of ncu counters describes."""
+CSRC = os.path.join(ROOT, "compressed_sparse_attention_window_gb300", "csrc")
+# The sources each op's kernels are built from: a recorded traffic figure
+# stands while these files are unchanged.
+_SHARED = ["ds41_common.cuh", "ds41_tc.cuh", "ds41_step1.cuh", "ds41_topk.cuh"]
+OP_SOURCES = {
+    "window_ring_write": ["ds41_window.cu"],
+    "compress_latent_write": ["ds41_window.cu"],
+    "indexer_topk": ["ds41_indexer.cu", "ds41_indexer_tc.cu", "ds41_quant.cu"],
+    "indexer_topk_mxf4": ["ds41_indexer.cu", "ds41_indexer_mxf4.cu"],
+    "sparse_attn_sink_fwd": ["ds41_attn.cu", "ds41_attn_tc.cu"],
+}
+
+
+def csrc_digest(op=None) -> str:
+    """sha256 (first 16 hex digits) over CUDA sources by sorted name: those of
+    ``op``'s kernels (with the shared headers), or every source when op is
+    None."""
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "compressed_sparse_attention_window_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    if op is None:
+        names = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh")))
+    else:
+        names = sorted(set(OP_SOURCES[op] + _SHARED))
+    for f in names:
+        h.update(f.encode())
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str, op: str):
     """DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per call of
     `op` on `workload`, from profiles/dram_traffic.txt, when they were taken on
-    the current kernel sources; None otherwise."""
+    the current sources of that op's kernels (the line's digest); None
+    otherwise."""
     try:
         with open(TRAFFIC_FILE) as fh:
             lines = fh.read().splitlines()
     except OSError:
         return None
-    digest, table = None, {}
     for line in lines:
         f = line.split()
-        if not f or f[0].startswith("#"):
+        if len(f) < 6 or f[0].startswith("#") or f[0] != workload or f[1] != op:
             continue
-        if f[0] == "csrc" and len(f) >= 2:
-            digest = f[1]
-        elif len(f) >= 3:
-            table[(f[0], f[1])] = float(f[2])
-    if digest != csrc_digest():
-        return None
-    return table.get((workload, op))
+        if op in OP_SOURCES and f[-1] == csrc_digest(op):
+            return float(f[2])
+    return None
 
 
 def load_peaks():

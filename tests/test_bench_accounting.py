@@ -42,23 +42,31 @@ def test_indexer_pairs_closed_form():
 
 
 def test_recorded_traffic_only_for_matching_sources(tmp_path, monkeypatch):
-    """The traffic table gives its numbers only while its digest matches the
-    current CUDA sources: the committed table parses, the same table under
-    the current digest gives numbers, under another digest none."""
-    with open(bench.TRAFFIC_FILE) as f:
-        text = f.read()
-    lines = text.splitlines()
-    head = [ln for ln in lines if ln.startswith("csrc ")]
-    assert len(head) == 1
-    cur = tmp_path / "cur.txt"
-    cur.write_text(text.replace(head[0], "csrc " + bench.csrc_digest()))
-    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(cur))
-    assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") is not None
+    """A traffic line gives its number only while the digest at its end
+    matches the current sources of that op's kernels."""
+    cur = bench.csrc_digest("sparse_attn_sink_fwd")
+    assert cur != bench.csrc_digest("indexer_topk_mxf4")
+    table = tmp_path / "t.txt"
+    table.write_text("# workload op bytes time kernels digest\n"
+                     f"prefill sparse_attn_sink_fwd 5e8 600.0 k {cur}\n"
+                     "prefill indexer_topk 1e8 90.0 k 0000000000000000\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(table))
+    assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") == 5e8
+    assert bench.recorded_traffic("prefill", "indexer_topk") is None
     assert bench.recorded_traffic("prefill", "no_such_op") is None
-    other = tmp_path / "other.txt"
-    other.write_text(text.replace(head[0], "csrc 0000000000000000"))
-    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(other))
-    assert bench.recorded_traffic("prefill", "sparse_attn_sink_fwd") is None
+    assert bench.recorded_traffic("decode", "sparse_attn_sink_fwd") is None
+
+
+def test_committed_traffic_table_parses():
+    """Every line of the committed table names a known op and carries bytes,
+    a time and a 16-digit digest."""
+    for line in open(bench.TRAFFIC_FILE).read().splitlines():
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        assert f[1] in bench.OP_SOURCES, line
+        float(f[2]), float(f[3])
+        assert len(f[-1]) == 16, line
 
 
 def test_packed_cache_bytes_closed_form():
