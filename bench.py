@@ -31,6 +31,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -143,31 +144,49 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
 CSRC = os.path.join(ROOT, "compressed_sparse_attention_window_gb300", "csrc")
-# The sources each op's kernels are built from: a recorded traffic figure
-# stands while these files are unchanged.
-_SHARED = ["ds41_common.cuh", "ds41_tc.cuh", "ds41_step1.cuh", "ds41_topk.cuh"]
+INCLUDE_DIR = os.path.join(ROOT, "include")
+# The translation units each op's kernels (and their tensor maps) come from; a
+# recorded traffic figure stands while these files and the headers they
+# include are unchanged.
 OP_SOURCES = {
     "window_ring_write": ["ds41_window.cu"],
     "compress_latent_write": ["ds41_window.cu"],
-    "indexer_topk": ["ds41_indexer.cu", "ds41_indexer_tc.cu", "ds41_quant.cu"],
-    "indexer_topk_mxf4": ["ds41_indexer.cu", "ds41_indexer_mxf4.cu"],
-    "sparse_attn_sink_fwd": ["ds41_attn.cu", "ds41_attn_tc.cu"],
+    "indexer_topk": ["ds41_indexer.cu", "ds41_indexer_tc.cu", "ds41_quant.cu", "ds41_tc_host.cu"],
+    "indexer_topk_mxf4": ["ds41_indexer.cu", "ds41_indexer_mxf4.cu", "ds41_tc_host.cu"],
+    "sparse_attn_sink_fwd": ["ds41_attn.cu", "ds41_attn_tc.cu", "ds41_tc_host.cu"],
 }
+_INCLUDE_RE = re.compile(r'^\s*#\s*include\s+"([^"]+)"', re.M)
+
+
+def _source_closure(names):
+    """The files ``names`` and every local header they include, transitively."""
+    seen, todo = {}, list(names)
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        path = os.path.join(CSRC, f)
+        if not os.path.exists(path):
+            path = os.path.join(INCLUDE_DIR, f)
+        with open(path, "rb") as fh:
+            seen[f] = fh.read()
+        todo.extend(_INCLUDE_RE.findall(seen[f].decode(errors="replace")))
+    return seen
 
 
 def csrc_digest(op=None) -> str:
     """sha256 (first 16 hex digits) over CUDA sources by sorted name: those of
-    ``op``'s kernels (with the shared headers), or every source when op is
+    ``op``'s kernels with the headers they include, or every source when op is
     None."""
     h = hashlib.sha256()
     if op is None:
         names = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh")))
+        files = {f: open(os.path.join(CSRC, f), "rb").read() for f in names}
     else:
-        names = sorted(set(OP_SOURCES[op] + _SHARED))
-    for f in names:
+        files = _source_closure(OP_SOURCES[op])
+    for f in sorted(files):
         h.update(f.encode())
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(fh.read())
+        h.update(files[f])
     return h.hexdigest()[:16]
 
 

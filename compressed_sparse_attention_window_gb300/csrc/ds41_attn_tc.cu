@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&bars[B_INVL + b], 4);
             mbar_init(&bars[B_INVLFREE + b], 4);
             mbar_init(&bars[B_PLANFULL + b], 1);
-            mbar_init(&bars[B_PLANEMPTY + b], 6);  // producer, 4 softmax warps, correction
+            mbar_init(&bars[B_PLANEMPTY + b], 10);  // producer, MMA issuer, 4 softmax, 4 correction
         }
         mbar_init(&bars[B_ODONE], 1);
         mbar_init(&bars[B_OFREE], 4);
@@ -478,10 +478,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             // let every copy this CTA started land before the CTA exits: the
             // last chunk's block pairs land after every earlier chunk's (a pair
             // is loaded only once the PV of the chunk before has read it)
-            if (q_armed) wait_bar(&bars[B_QFULL], (q_armed - 1) & 1, abort_f, p.status);
+            if (q_armed) drain_bar(&bars[B_QFULL], (q_armed - 1) & 1, p.status);
             if (g >= 1)
                 for (int kp = 0; kp < NKP; kp++)
-                    wait_bar(&bars[B_RFULL + kp], (g - 1) & 1, abort_f, p.status);
+                    drain_bar(&bars[B_RFULL + kp], (g - 1) & 1, p.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
@@ -538,6 +538,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         s_n = *reinterpret_cast<const int*>(sm + PLAN_OFF +
                                                             (s_tok & 1) * PLAN_BYTES + PLAN_N);
                         nring = (nring & ~(0xffu << (8 * (s_tok & 3)))) | ((uint32_t)s_n << (8 * (s_tok & 3)));
+                        mbar_arrive(&bars[B_PLANEMPTY + (s_tok & 1)]);  // done with the plan
                     }
                     if (s_n > 0) {
                         const bool ok =
@@ -587,7 +588,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // every MMA issued so far completes before tensor memory is freed
             tc_commit(&bars[B_FINAL]);
-            wait_bar(&bars[B_FINAL], 0, abort_f, p.status);
+            drain_bar(&bars[B_FINAL], 0, p.status);
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------------
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int nch =
                 *reinterpret_cast<const int*>(sm + PLAN_OFF + slot * PLAN_BYTES + PLAN_N);
             __syncwarp();
-            if (warp == 8 && lane == 0) mbar_arrive(&bars[B_PLANEMPTY + slot]);
+            if (lane == 0) mbar_arrive(&bars[B_PLANEMPTY + slot]);  // each warp read nch
             bool bad = false;
             for (int i = 0; i < nch; i++, g++) {
                 if (!wait_bar(&bars[B_CORR], g & 1, abort_f, p.status)) {

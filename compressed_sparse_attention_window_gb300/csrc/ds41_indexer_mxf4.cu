@@ -281,11 +281,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // let every copy this CTA started land before the CTA exits
             for (int b = 0; b < 2; b++) {
-                if (q_armed[b]) wait_bar(&bars[B_QFULL + b], (q_armed[b] - 1) & 1, abort_f, p.status);
-                if (w_armed[b]) wait_bar(&bars[B_WFULL + b], (w_armed[b] - 1) & 1, abort_f, p.status);
+                if (q_armed[b]) drain_bar(&bars[B_QFULL + b], (q_armed[b] - 1) & 1, p.status);
+                if (w_armed[b]) drain_bar(&bars[B_WFULL + b], (w_armed[b] - 1) & 1, p.status);
             }
             for (int s = 0; s < KST; s++)
-                if (k_armed[s]) wait_bar(&bars[B_KFULL + s], (k_armed[s] - 1) & 1, abort_f, p.status);
+                if (k_armed[s]) drain_bar(&bars[B_KFULL + s], (k_armed[s] - 1) & 1, p.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 jq++;
             }
             tc_commit(&bars[B_FINAL]);
-            wait_bar(&bars[B_FINAL], 0, abort_f, p.status);
+            drain_bar(&bars[B_FINAL], 0, p.status);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------------

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             for (int s = 0; s < STAGES; s++)
-                if (armed[s]) wait_bar(&bars[B_FULL + s], (armed[s] - 1) & 1, abort_f, p.status);
+                if (armed[s]) drain_bar(&bars[B_FULL + s], (armed[s] - 1) & 1, p.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (ok) tc_commit(&bars[B_AFULL + ab]);
             }
             tc_commit(&bars[B_FINAL]);
-            wait_bar(&bars[B_FINAL], 0, abort_f, p.status);
+            drain_bar(&bars[B_FINAL], 0, p.status);
         }
     } else if (warp >= 4) {
         const int q = warp & 3;

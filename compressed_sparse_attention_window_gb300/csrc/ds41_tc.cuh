@@ -165,6 +165,26 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     return false;
 }
 
+// A bounded wait for this CTA's own work in flight (its copies landing, its
+// MMAs completing) before it frees tensor memory or exits.  Unlike wait_bar it
+// ignores the abort flag: a role that gave up still lets what it started
+// finish.  After `polls` polls it raises DS41_E_TIMEOUT and returns false.
+__device__ __forceinline__ bool drain_bar(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          uint32_t polls = kWaitPolls) {
+    for (uint32_t i = 0; i < polls; i++) {
+        uint32_t done;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    raise_status(status, DS41_E_TIMEOUT);
+    return false;
+}
+
 // Host: the driver's tensor-map encoder (looked up once) and a 2-D bf16 map
 // over [rows][cols] with a box of box_cols x box_rows and the 128-byte
 // swizzle; elements outside the tensor read as zero.
