@@ -319,10 +319,14 @@ __device__ void plan_item(const Params& p, int t, uint8_t* plan, uint32_t* bm, i
             pos += __popc(bal);
         }
     }
+    // consecutive-row chunks first, then listed ones: the copy engine's loads
+    // of an item then all precede its gathers, so the producer's wait for the
+    // chunk before each of its loads never runs ahead of the barrier's phase
     int nch = 0;
 #pragma unroll
-    for (int s = 0; s < 2; s++) {
-        if (cnt[s] == 0) continue;
+    for (int k = 0; k < 4; k++) {
+        const int s = k & 1;
+        if (cnt[s] == 0 || dense[s] != (k < 2)) continue;
         const uint32_t sbit = (uint32_t)s << 30;
         if (dense[s]) {
             const int nck = (range[s] + RC - 1) / RC;

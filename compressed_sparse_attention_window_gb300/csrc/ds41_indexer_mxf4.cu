@@ -28,10 +28,12 @@
 //
 // Roles (384 threads): warp 0 issues the TMA copies (the group's q rows in
 // bf16, the weights, the key-code tiles through 6 stages); warp 1 owns tensor
-// memory and (one lane) issues the MMAs into two D buffers; warps 4..11 first
-// quantise the group's q into codes + scale bytes in shared memory (warps
-// 4..7 also write the scale factors into tensor memory), then run the head
-// chains: warp 4 + 4 p + q holds lane quarter q of D and token p of the group.
+// memory and (one lane) issues the MMAs into two D buffers; warps 2..3
+// quantise the q of the CTA's next group into codes + scale bytes in shared
+// memory while warps 4..11 run the head chains of this one (the CTA's first
+// group they quantise themselves); warps 4..7 write the scale factors into
+// tensor memory, and warp 4 + 4 p + q holds lane quarter q of D and token p
+// of the group for the head chains.
 // Groups of 2 tokens go to persistent CTAs (heaviest first) when there are at
 // least as many groups as SMs; otherwise the row tiles of each group are
 // split over several CTAs.  Every wait is bounded; a timeout raises
@@ -75,7 +77,8 @@ enum {
     B_QFULL, B_QEMPTY = B_QFULL + 2, B_QREADY = B_QEMPTY + 2, B_QPEMPTY = B_QREADY + 2,
     B_WFULL = B_QPEMPTY + 2, B_WEMPTY = B_WFULL + 2, B_KFULL = B_WEMPTY + 2,
     B_KEMPTY = B_KFULL + KST, B_SFFULL = B_KEMPTY + KST, B_SFEMPTY = B_SFFULL + 2,
-    B_DFULL = B_SFEMPTY + 2, B_DEMPTY = B_DFULL + 2, B_FINAL = B_DEMPTY + 2, NBAR
+    B_DFULL = B_SFEMPTY + 2, B_DEMPTY = B_DFULL + 2, B_QPFULL = B_DEMPTY + 2,
+    B_EPI = B_QPFULL + 2, B_QW, B_FINAL, NBAR
 };
 static_assert(NBAR * 8 + 8 <= 512, "barrier area");
 
@@ -115,8 +118,64 @@ __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint32_t (&r)[4]) {
                  : "memory");
 }
 
-__device__ __forceinline__ void epi_sync() {
-    asm volatile("bar.sync 1, %0;\n" ::"n"(EPI_THREADS) : "memory");
+constexpr int QW_THREADS = 64;     // warps 2..3: q of the next group
+
+// A barrier of whole warps on an mbarrier whose count is their number: each
+// warp arrives once, then every thread waits (bounded) for the phase; `ph`
+// counts this thread's uses.  Unlike a named barrier it cannot hang when a
+// warp has left after a failed wait: the others give up with it.
+__device__ __forceinline__ bool warps_sync(uint64_t* bar, uint32_t& ph, volatile int* abort_f,
+                                           unsigned int* status) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = wait_bar(bar, ph & 1, abort_f, status);
+    ph++;
+    return ok;
+}
+
+// A group's q, N bf16 rows of 128 (two 64-column blocks with the 128-byte
+// swizzle, as the tiled copy lands them) -> e2m1 codes (rows of 64 bytes with
+// the 64-byte swizzle) and one e8m0 scale byte per block of 32, exactly as
+// fp4_quant_e8m0: s = 2^ceil(log2(max(amax, 6 * 2^-126) / 6)), codes =
+// e2m1(x / s).  Thread `tid` of `nthr` takes blocks tid, tid + nthr, ...
+__device__ __forceinline__ void quant_group(const uint8_t* qsrc, uint8_t* qdst, uint8_t* sfq, int N,
+                                            int tid, int nthr) {
+#pragma unroll 1
+    for (int id = tid; id < N * 4; id += nthr) {
+        const int n = id >> 2, kb = id & 3;
+        const uint8_t* row = qsrc + (kb >> 1) * QBLK + n * 128;
+        float v[32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; c4++) {
+            const int c = (kb & 1) * 4 + c4;
+            const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ (n & 7)) << 4));
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                v[c4 * 8 + 2 * e] = __uint_as_float(w4[e] << 16);
+                v[c4 * 8 + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e++) amax = fmaxf(amax, fabsf(v[e]));
+        amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
+        const float sc = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
+        const float rs = __frcp_rn(sc);  // exact: sc is a power of two
+        uint32_t cw[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int k = 0; k < 8; k += 2)
+                c |= cvt_e2m1x2(__fmul_rn(v[8 * e + k], rs), __fmul_rn(v[8 * e + k + 1], rs))
+                     << (4 * k);
+            cw[e] = c;
+        }
+        *reinterpret_cast<uint4*>(qdst + n * 64 + ((kb ^ ((n >> 1) & 3)) << 4)) =
+            make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        sfq[n * 4 + kb] = (uint8_t)(__float_as_uint(sc) >> 23);
+    }
 }
 
 struct Params {
@@ -218,11 +277,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&bars[B_SFEMPTY + b], 1);
             mbar_init(&bars[B_DFULL + b], 1);
             mbar_init(&bars[B_DEMPTY + b], 8);
+            mbar_init(&bars[B_QPFULL + b], 1);
         }
         for (int s = 0; s < KST; s++) {
             mbar_init(&bars[B_KFULL + s], 1);
             mbar_init(&bars[B_KEMPTY + s], 1);
         }
+        mbar_init(&bars[B_EPI], EPI_THREADS / 32);
+        mbar_init(&bars[B_QW], QW_THREADS / 32);
         mbar_init(&bars[B_FINAL], 1);
         *abort_f = 0;
         mbar_init_fence();
@@ -328,6 +390,34 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_commit(&bars[B_FINAL]);
             drain_bar(&bars[B_FINAL], 0, p.status);
         }
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------------------------
+        // q of the CTA's second and later groups, one group ahead of the head
+        // chains (the first group's q is quantised by the epilogue warps)
+        // ------------------------------------------------------------------
+        const int qt = threadIdx.x - 64;
+        uint32_t jq = 0, qw_ph = 0;
+        for (int j = 0; j < nit; j++) {
+            const Item it = item_of(j, p);
+            if (item_tiles(it) == 0) continue;
+            const int qs = jq & 1;
+            if (jq >= 1) {
+                // the packed buffer is free once the MMAs of group jq - 2 are done
+                if ((jq >= 2 && !wait_bar(&bars[B_QPEMPTY + qs], ((jq - 2) >> 1) & 1, abort_f,
+                                          p.status)) ||
+                    !wait_bar(&bars[B_QFULL + qs], (jq >> 1) & 1, abort_f, p.status))
+                    break;
+                quant_group(sm + Q_OFF + qs * Q_BYTES, sm + QP_OFF + qs * QP_BYTES,
+                            sm + SFQ_OFF + qs * SFQ_BYTES, it.tcount * HI, qt, QW_THREADS);
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                if (!warps_sync(&bars[B_QW], qw_ph, abort_f, p.status)) break;
+                if (qt == 0) {
+                    mbar_arrive(&bars[B_QPFULL + ((jq - 1) & 1)]);
+                    mbar_arrive(&bars[B_QEMPTY + qs]);
+                }
+            }
+            jq++;
+        }
     } else if (warp >= 4) {
         // ------------------------------------------------------------------
         // q quantisation, scale factors, head chains: thread = compressed
@@ -337,7 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool sfw = pr == 0;  // warps 4..7 write the scale factors
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const int64_t all_tiles = (p.n_c + ROWS - 1) / ROWS;
-        uint32_t jq = 0, kt = 0;
+        uint32_t jq = 0, kt = 0, epi_ph = 0;
         bool ok = true;
         for (int j = 0; j < nit && ok; j++) {
             const Item it = item_of(j, p);
@@ -349,56 +439,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                     load_sfa(p, (int64_t)it.tile0 * ROWS, lane, sfa_next);
                     if (nt > 1) load_sfa(p, (int64_t)(it.tile0 + it.tstride) * ROWS, lane, sfa_after);
                 }
-                // (1) the group's q: bf16 rows (token tt, head h) -> e2m1 codes
-                // and e8m0 scale bytes, exactly as fp4_quant_e8m0
-                if ((jq >= 2 && !wait_bar(&bars[B_QPEMPTY + qs], ((jq - 2) >> 1) & 1, abort_f,
-                                          p.status)) ||
-                    !wait_bar(&bars[B_QFULL + qs], (jq >> 1) & 1, abort_f, p.status)) {
+                // (1) the group's q as e2m1 codes + e8m0 scale bytes: the first
+                // group here, every later one by warps 2..3 while this group's
+                // predecessor ran its head chains
+                const int N = it.tcount * HI;
+                uint8_t* sfq = sm + SFQ_OFF + qs * SFQ_BYTES;
+                if (jq == 0) {
+                    if (!wait_bar(&bars[B_QFULL + qs], 0, abort_f, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    quant_group(sm + Q_OFF + qs * Q_BYTES, sm + QP_OFF + qs * QP_BYTES, sfq, N, etid,
+                                EPI_THREADS);
+                    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                    if (!warps_sync(&bars[B_EPI], epi_ph, abort_f, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                } else if (!wait_bar(&bars[B_QPFULL + ((jq - 1) & 1)], ((jq - 1) >> 1) & 1, abort_f,
+                                     p.status)) {
                     ok = false;
                     break;
                 }
-                const int N = it.tcount * HI;
-                const uint8_t* qsrc = sm + Q_OFF + qs * Q_BYTES;
-                uint8_t* qdst = sm + QP_OFF + qs * QP_BYTES;
-                uint8_t* sfq = sm + SFQ_OFF + qs * SFQ_BYTES;
-#pragma unroll 1
-                for (int id = etid; id < N * 4; id += EPI_THREADS) {
-                    const int n = id >> 2, kb = id & 3;
-                    const uint8_t* row = qsrc + (kb >> 1) * QBLK + n * 128;
-                    float v[32];
-                    float amax = 0.0f;
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; c4++) {
-                        const int c = (kb & 1) * 4 + c4;
-                        const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ (n & 7)) << 4));
-                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            v[c4 * 8 + 2 * e] = __uint_as_float(w4[e] << 16);
-                            v[c4 * 8 + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 32; e++) amax = fmaxf(amax, fabsf(v[e]));
-                    amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
-                    const float s = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
-                    const float rs = __frcp_rn(s);  // exact: s is a power of two
-                    uint32_t cw[4];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        uint32_t c = 0;
-#pragma unroll
-                        for (int k = 0; k < 8; k += 2)
-                            c |= cvt_e2m1x2(__fmul_rn(v[8 * e + k], rs), __fmul_rn(v[8 * e + k + 1], rs))
-                                 << (4 * k);
-                        cw[e] = c;
-                    }
-                    *reinterpret_cast<uint4*>(qdst + n * 64 + ((kb ^ ((n >> 1) & 3)) << 4)) =
-                        make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                    sfq[n * 4 + kb] = (uint8_t)(__float_as_uint(s) >> 23);
-                }
-                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-                epi_sync();
                 if (sfw) {
                     // query scale factors: lane r, column j = row r + 32 j
                     const uint32_t* sw = reinterpret_cast<const uint32_t*>(sfq);
@@ -412,10 +474,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_wait_st();
                 }
                 tc_fence_before();
-                epi_sync();
+                if (!warps_sync(&bars[B_EPI], epi_ph, abort_f, p.status)) {
+                    ok = false;
+                    break;
+                }
                 if (etid == 0) {
                     mbar_arrive(&bars[B_QREADY + qs]);
-                    mbar_arrive(&bars[B_QEMPTY + qs]);
+                    if (jq == 0) mbar_arrive(&bars[B_QEMPTY + qs]);
                 }
                 if (!wait_bar(&bars[B_WFULL + qs], (jq >> 1) & 1, abort_f, p.status)) {
                     ok = false;

@@ -275,10 +275,12 @@ def _tc_index_rows(m, n_a, n_c, K, rng):
     """Index rows that exercise every chunk form of the many-token kernel:
     compact ranges of both sources (consecutive-row chunks with masks),
     scattered rows and sparse ranges (listed rows), repeated rows, rows with
-    no or one valid index, and padding with -1."""
+    no or one valid index, padding with -1, and scattered rows_a beside a
+    compact range of rows_b (listed chunks of the first source with
+    consecutive-row chunks of the second)."""
     idx = np.full((m, K), -1, np.int32)
     for t in range(m):
-        kind = t % 6
+        kind = t % 7
         if kind == 0:   # a window-like run of rows_a + most of a range of rows_b,
             #             the range rounded up to whole 128-row chunks (kept as
             #             consecutive-row chunks with holes in their masks)
@@ -299,6 +301,11 @@ def _tc_index_rows(m, n_a, n_c, K, rng):
             n = K - 3
             b0 = rng.integers(0, n_c - n + 1)
             row = n_a + b0 + rng.integers(0, n, n)
+        elif kind == 6:  # scattered rows_a + a compact range of rows_b
+            na = min(K // 4, n_a)
+            nb = min(K - na, n_c)
+            b0 = rng.integers(0, n_c - nb + 1)
+            row = np.concatenate([rng.permutation(n_a)[:na], n_a + b0 + np.arange(nb)])
         elif kind == 3:  # a few valid rows among -1
             row = rng.permutation(n_a + n_c)[: max(1, K // 9)]
         else:            # rows_b only, ascending, every third row
