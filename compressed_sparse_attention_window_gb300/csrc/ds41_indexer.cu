@@ -853,8 +853,8 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct IndexerPlan {
     int hpad, TT, groups;
     bool prequant;  // keys quantised once into the workspace
-    bool tc;        // many tokens: q quantised too, scores on the tcgen05 tensor cores
-    size_t kq_bytes, qq_bytes, sc_bytes;
+    bool tc;        // many tokens: scores on the tcgen05 tensor cores (q quantised in the kernel)
+    size_t kq_bytes, sc_bytes;
 };
 
 int device_sm_count() {
@@ -864,7 +864,7 @@ int device_sm_count() {
     return sms;
 }
 
-// Workspace: [quantised keys | quantised queries | scores], each 256-byte aligned.
+// Workspace: [quantised keys | scores], each 256-byte aligned.
 static IndexerPlan plan_indexer(int64_t m, int64_t Hi, int64_t Di, int64_t n_c, bool scores_given) {
     IndexerPlan p;
     p.hpad = (int)((Hi + 7) / 8 * 8);
@@ -874,7 +874,6 @@ static IndexerPlan plan_indexer(int64_t m, int64_t Hi, int64_t Di, int64_t n_c, 
     p.prequant = p.groups > 4;
     p.tc = p.prequant && indexer_tc_supported(m, Hi, Di, device_sm_count());
     p.kq_bytes = p.prequant ? align256((size_t)n_c * Di * 2) : 0;
-    p.qq_bytes = p.tc ? align256((size_t)m * Hi * Di * 2) : 0;
     p.sc_bytes = scores_given ? 0 : align256((size_t)m * n_c * 2);
     return p;
 }
@@ -918,7 +917,7 @@ extern "C" size_t ds41_indexer_workspace_bytes(int64_t m, int64_t Hi, int64_t Di
                                                int scores_out_given) {
     if (m < 1 || Hi < 1 || Di < 1 || n_c < 1) return 0;
     IndexerPlan p = plan_indexer(m, Hi, Di, n_c, scores_out_given != 0);
-    return p.kq_bytes + p.qq_bytes + p.sc_bytes;
+    return p.kq_bytes + p.sc_bytes;
 }
 
 extern "C" int ds41_indexer_topk(const ds41_bf16* q_idx, const ds41_bf16* k_idx, const float* w,
@@ -947,15 +946,14 @@ extern "C" int ds41_indexer_topk(const ds41_bf16* q_idx, const ds41_bf16* k_idx,
     const int64_t ctopk = topk < n_c ? topk : n_c;
     DS41_REQUIRE(win + ctopk < (int64_t(1) << 30), DS41_E_RANGE, "%s: merged row too long", name);
     IndexerPlan p = plan_indexer(m, Hi, Di, n_c, scores != nullptr);
-    const size_t need = p.kq_bytes + p.qq_bytes + p.sc_bytes;
+    const size_t need = p.kq_bytes + p.sc_bytes;
     DS41_REQUIRE(need == 0 || (ws && ws_bytes >= need), DS41_E_WORKSPACE,
                  "%s: workspace of %zu bytes needed, %zu given", name, need, ws ? ws_bytes : 0);
     DS41_REQUIRE(need == 0 || aligned16(ws), DS41_E_ARG, "%s: ws must be 16-byte aligned", name);
     cudaStream_t st = (cudaStream_t)stream;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     uint16_t* kq = p.prequant ? reinterpret_cast<uint16_t*>(wsb) : nullptr;
-    uint16_t* qq = p.tc ? reinterpret_cast<uint16_t*>(wsb + p.kq_bytes) : nullptr;
-    uint16_t* sc = scores ? scores : reinterpret_cast<uint16_t*>(wsb + p.kq_bytes + p.qq_bytes);
+    uint16_t* sc = scores ? scores : reinterpret_cast<uint16_t*>(wsb + p.kq_bytes);
     int rc;
     if (p.prequant) {
         rc = ds41_fp4_quant_e8m0(k_idx, kq, nullptr, nullptr, n_c, Di, stream);
@@ -964,13 +962,11 @@ extern "C" int ds41_indexer_topk(const ds41_bf16* q_idx, const ds41_bf16* k_idx,
     const uint16_t* ksrc = p.prequant ? kq : k_idx;
     const bool fill = scores != nullptr;
     if (p.tc && aligned16(w)) {
-        // q through the same quantiser, then the scores on the tensor cores
-        rc = ds41_fp4_quant_e8m0(q_idx, qq, nullptr, nullptr, m * Hi, Di, stream);
-        if (rc) return rc;
+        // the scores on the tensor cores, q quantised in the kernel
         unsigned int* status = nullptr;
         rc = status_word(&status);
         if (rc) return rc;
-        rc = indexer_tc_launch(qq, kq, w, sc, m, n_c, ratio, start_pos, fill, status,
+        rc = indexer_tc_launch(q_idx, kq, w, sc, m, n_c, ratio, start_pos, fill, status,
                                device_sm_count(), st);
     } else switch (Di) {
         case 32: rc = launch_scores<32>(p, q_idx, ksrc, w, sc, m, Hi, n_c, ratio, start_pos, fill, st); break;

@@ -120,18 +120,6 @@ __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint32_t (&r)[4]) {
 
 constexpr int QW_THREADS = 64;     // warps 2..3: q of the next group
 
-// A barrier of whole warps on an mbarrier whose count is their number: each
-// warp arrives once, then every thread waits (bounded) for the phase; `ph`
-// counts this thread's uses.  Unlike a named barrier it cannot hang when a
-// warp has left after a failed wait: the others give up with it.
-__device__ __forceinline__ bool warps_sync(uint64_t* bar, uint32_t& ph, volatile int* abort_f,
-                                           unsigned int* status) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = wait_bar(bar, ph & 1, abort_f, status);
-    ph++;
-    return ok;
-}
 
 // A group's q, N bf16 rows of 128 (two 64-column blocks with the 128-byte
 // swizzle, as the tiled copy lands them) -> e2m1 codes (rows of 64 bytes with

@@ -9,9 +9,10 @@
 //   acc = 0; for h in 0..63: acc = fma(w[t,h], max(<qh[t,h], kh[s]>, 0), acc)
 //   score = bf16(acc)          (-0 -> +0; rows not visible yet score -inf)
 //
-// The quantised q and k arrive as bf16 values (each fp4 value times its
-// power-of-two scale is exact in bf16), so one bf16 MMA gives the dot
-// products; they are exact in f32, so any summation order gives the same
+// The quantised k arrives as bf16 values, q as it is: the kernel takes each
+// group's q through the same round trip in shared memory (each fp4 value
+// times its power-of-two scale is exact in bf16), so one bf16 MMA gives the
+// dot products; they are exact in f32, so any summation order gives the same
 // bits.  A tile is 128 compressed rows x 4 tokens:
 //
 //   D = Kh Qh^T    M = 128 rows, N = 256 (4 tokens x 64 heads), K = 128
@@ -23,9 +24,10 @@
 // first); per group the row tiles run over the rows its last token can see.
 // Warp 0 issues the TMA copies (the group's 256 q rows and 4 x 64 weights,
 // then the row tiles through two stages), warp 1 owns tensor memory and (one
-// lane) issues the MMAs into two D buffers, warps 4..11 run the head chains
-// (warp 4 + 4p + q: lane quarter q, tokens 2p and 2p + 1).  Every wait is
-// bounded; a timeout raises DS41_E_TIMEOUT and the roles exit.
+// lane) issues the MMAs into two D buffers, warps 4..11 quantise each
+// group's q in place and then run its head chains (warp 4 + 4p + q: lane
+// quarter q, tokens 2p and 2p + 1).  Every wait is bounded; a timeout raises
+// DS41_E_TIMEOUT and the roles exit.
 #include "ds41_internal.cuh"
 #include "ds41_tc.cuh"
 
@@ -56,11 +58,13 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 enum {
     B_QFULL, B_QEMPTY = B_QFULL + 2, B_WFULL = B_QEMPTY + 2, B_WEMPTY = B_WFULL + 2,
     B_KFULL = B_WEMPTY + 2, B_KEMPTY = B_KFULL + 2, B_DFULL = B_KEMPTY + 2,
-    B_DEMPTY = B_DFULL + 2, B_FINAL = B_DEMPTY + 2, NBAR
+    B_DEMPTY = B_DFULL + 2, B_QREADY = B_DEMPTY + 2,  // 2: the group's q quantised in place
+    B_EPI = B_QREADY + 2, B_FINAL, NBAR
 };
 static_assert(NBAR * 8 + 8 <= 256, "barrier area");
 
 constexpr uint32_t TM_COLS = 512;  // two D buffers of 256 columns
+constexpr int EPI_THREADS = 256;   // warps 4..11
 constexpr uint32_t IDESC = idesc_bf16(128, TT * HI, 0, 0);
 
 struct Params {
@@ -88,6 +92,48 @@ __device__ __forceinline__ void group_of(int j, const Params& p, int& t0, int& t
     ntile = (int)((vis + ROWS - 1) / ROWS);
 }
 
+// A group's q in place: the q stage holds 256 bf16 rows of 128 as two
+// 64-column blocks with the 128-byte swizzle (as the tiled copy lands them);
+// every block of 32 values becomes bf16(e2m1(v / s) * s) with
+// s = 2^ceil(log2(max(amax, 6 * 2^-126) / 6)), exactly as fp4_quant_e8m0.
+// Thread `tid` of `nthr` takes blocks tid, tid + nthr, ... of the first `rows`
+// rows (rows past the group's tokens are zero-filled and stay zero).
+__device__ __forceinline__ void quant_q_inplace(uint8_t* qst, int rows, int tid, int nthr) {
+#pragma unroll 1
+    for (int id = tid; id < rows * 4; id += nthr) {
+        const int n = id >> 2, j = id & 3;
+        uint8_t* row = qst + (j >> 1) * QBLK + n * 128;
+        uint4 u[4];
+        float v[32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; c4++) {
+            const int c = (j & 1) * 4 + c4;
+            u[c4] = *reinterpret_cast<const uint4*>(row + ((c ^ (n & 7)) << 4));
+            const uint32_t w4[4] = {u[c4].x, u[c4].y, u[c4].z, u[c4].w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                v[c4 * 8 + 2 * e] = __uint_as_float(w4[e] << 16);
+                v[c4 * 8 + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e++) amax = fmaxf(amax, fabsf(v[e]));
+        amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
+        const float sc = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
+        const float rs = __frcp_rn(sc);  // exact: sc is a power of two
+#pragma unroll
+        for (int c4 = 0; c4 < 4; c4++) {
+            float t[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) t[e] = __fmul_rn(v[c4 * 8 + e], rs);
+            uint32_t codes;
+            const int c = (j & 1) * 4 + c4;
+            *reinterpret_cast<uint4*>(row + ((c ^ (n & 7)) << 4)) = e2m1_round8(t, sc, &codes);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k, const Params p) {
@@ -113,7 +159,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&bars[B_KEMPTY + b], 1);
             mbar_init(&bars[B_DFULL + b], 1);
             mbar_init(&bars[B_DEMPTY + b], 8);
+            mbar_init(&bars[B_QREADY + b], 1);
         }
+        mbar_init(&bars[B_EPI], EPI_THREADS / 32);
         mbar_init(&bars[B_FINAL], 1);
         *abort_f = 0;
         mbar_init_fence();
@@ -190,7 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 group_of(j, p, t0, tcount, ntile);
                 if (ntile == 0) continue;
                 const int qs = jq & 1;
-                if (!wait_bar(&bars[B_QFULL + qs], (jq >> 1) & 1, abort_f, p.status)) break;
+                if (!wait_bar(&bars[B_QREADY + qs], (jq >> 1) & 1, abort_f, p.status)) break;
                 const uint64_t qd = sdesc(sbase + Q_OFF + qs * Q_BYTES, 16, 1024);
                 for (int i = 0; i < ntile; i++, kt++) {
                     const int ks = kt & 1, db = kt & 1;
@@ -224,13 +272,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------------
         const int q = warp & 3, pr = (warp - 4) >> 2;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        uint32_t jq = 0, kt = 0;
+        uint32_t jq = 0, kt = 0, epi_ph = 0;
         for (int j = 0; j < ngroups; j++) {
             int t0, tcount, ntile;
             group_of(j, p, t0, tcount, ntile);
             const int64_t all_tiles = (p.n_c + ROWS - 1) / ROWS;
             if (ntile > 0) {
                 const int ws = jq & 1;
+                {
+                    // the group's q quantised in place, before its head chains
+                    if (!wait_bar(&bars[B_QFULL + ws], (jq >> 1) & 1, abort_f, p.status)) break;
+                    quant_q_inplace(sm + Q_OFF + ws * Q_BYTES, tcount * HI, threadIdx.x - 128,
+                                    EPI_THREADS);
+                    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                    if (!warps_sync(&bars[B_EPI], epi_ph, abort_f, p.status)) break;
+                    if (threadIdx.x == 128) mbar_arrive(&bars[B_QREADY + ws]);
+                }
                 if (!wait_bar(&bars[B_WFULL + ws], (jq >> 1) & 1, abort_f, p.status)) break;
                 const float* wsm = reinterpret_cast<const float*>(sm + W_OFF + ws * W_BYTES);
                 bool ok = true;
@@ -304,7 +361,7 @@ bool indexer_tc_supported(int64_t m, int64_t Hi, int64_t Di, int sms) {
            m * Hi < (int64_t(1) << 31);
 }
 
-int indexer_tc_launch(const uint16_t* qq, const uint16_t* kq, const float* w, uint16_t* scores,
+int indexer_tc_launch(const uint16_t* q_idx, const uint16_t* kq, const float* w, uint16_t* scores,
                       int64_t m, int64_t n_c, int64_t ratio, int64_t start_pos, bool fill_hidden,
                       unsigned int* status, int sms, cudaStream_t st) {
     using namespace tci;
@@ -312,7 +369,7 @@ int indexer_tc_launch(const uint16_t* qq, const uint16_t* kq, const float* w, ui
     int rc = get_encode(&enc);
     if (rc) return rc;
     CUtensorMap mq, mk;
-    if ((rc = make_map_bf16(enc, &mq, qq, m * HI, DI, 64, TT * HI))) return rc;
+    if ((rc = make_map_bf16(enc, &mq, q_idx, m * HI, DI, 64, TT * HI))) return rc;
     if ((rc = make_map_bf16(enc, &mk, kq, n_c, DI, 64, ROWS))) return rc;
     Params p;
     p.w = w;

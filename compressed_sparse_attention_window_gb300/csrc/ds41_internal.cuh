@@ -56,9 +56,10 @@ size_t attn_ws_bytes(int64_t m, int64_t nh, int64_t hd, int64_t K);
 bool attn_is_cluster_path(int64_t m, int64_t nh, int64_t hd, int64_t K);
 
 // many-token indexer scores on the tcgen05 tensor cores (ds41_indexer_tc.cu):
-// qq [m*64][128] and kq [n_c][128] hold the fp4 round-trip values in bf16
+// q_idx [m*64][128] as given (the kernel takes it through the fp4 round trip),
+// kq [n_c][128] the keys' fp4 round-trip values in bf16
 bool indexer_tc_supported(int64_t m, int64_t Hi, int64_t Di, int sms);
-int indexer_tc_launch(const uint16_t* qq, const uint16_t* kq, const float* w, uint16_t* scores,
+int indexer_tc_launch(const uint16_t* q_idx, const uint16_t* kq, const float* w, uint16_t* scores,
                       int64_t m, int64_t n_c, int64_t ratio, int64_t start_pos, bool fill_hidden,
                       unsigned int* status, int sms, cudaStream_t st);
 

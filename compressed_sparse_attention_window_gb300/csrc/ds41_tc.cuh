@@ -185,6 +185,19 @@ __device__ __forceinline__ bool drain_bar(uint64_t* bar, uint32_t parity, unsign
     return false;
 }
 
+// A barrier of whole warps on an mbarrier whose count is their number: each
+// warp arrives once, then every thread waits (bounded) for the phase; `ph`
+// counts this thread's uses.  Unlike a named barrier it cannot hang when a
+// warp has left after a failed wait: the others give up with it.
+__device__ __forceinline__ bool warps_sync(uint64_t* bar, uint32_t& ph, volatile int* abort_f,
+                                           unsigned int* status) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = wait_bar(bar, ph & 1, abort_f, status);
+    ph++;
+    return ok;
+}
+
 // Host: the driver's tensor-map encoder (looked up once) and a 2-D bf16 map
 // over [rows][cols] with a box of box_cols x box_rows and the 128-byte
 // swizzle; elements outside the tensor read as zero.
