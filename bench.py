@@ -144,7 +144,6 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
 CSRC = os.path.join(ROOT, "compressed_sparse_attention_window_gb300", "csrc")
-INCLUDE_DIR = os.path.join(ROOT, "include")
 # The translation units each op's kernels (and their tensor maps) come from; a
 # recorded traffic figure stands while these files and the headers they
 # include are unchanged.
@@ -159,7 +158,8 @@ _INCLUDE_RE = re.compile(r'^\s*#\s*include\s+"([^"]+)"', re.M)
 
 
 def _source_closure(names):
-    """The files ``names`` and every local header they include, transitively."""
+    """The files ``names`` and every header of the CUDA sources they include,
+    transitively (the public C header, declarations only, is left out)."""
     seen, todo = {}, list(names)
     while todo:
         f = todo.pop()
@@ -167,7 +167,7 @@ def _source_closure(names):
             continue
         path = os.path.join(CSRC, f)
         if not os.path.exists(path):
-            path = os.path.join(INCLUDE_DIR, f)
+            continue
         with open(path, "rb") as fh:
             seen[f] = fh.read()
         todo.extend(_INCLUDE_RE.findall(seen[f].decode(errors="replace")))
@@ -861,12 +861,13 @@ def run_only(args, local):
 
 
 def run_e2e(wl, slots, fc, stream, K, W, n_slots, world=1):
-    """The same metric through ds41_csa_forward_host, the C-ABI call for
-    host-resident step data, prepared once per layer state (ds41.HostStep):
-    every step copies that step's inputs from page-locked host memory into
-    the device buffers (laid out back to back on both sides, so in one copy),
-    runs the step and copies o back to host memory, on one stream; the layer
-    states stay resident."""
+    """The same metric through the C-ABI calls for host-resident step data:
+    per layer state, ds41_host_step_create records once what
+    ds41_csa_forward_host_packed enqueues (ds41.HostStep, graph=True), and
+    every step is one ds41_host_step_launch: it copies that step's inputs from
+    page-locked host memory into the device buffers (laid out back to back on
+    both sides, so in one copy), runs the step and copies o back to host
+    memory, on one stream; the layer states stay resident."""
     names = ds41.STEP_INPUTS
     o_host = torch.empty(slots[0][1]["o"].shape, dtype=torch.bfloat16).pin_memory()
     steps = []
@@ -878,7 +879,7 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots, world=1):
             host_in[k].copy_(inp[k].cpu())
         e_inp = dict(inp)
         e_inp.update(dev_in)
-        steps.append(ds41.HostStep(host_in, e_inp, wl, fc, out, h_o=o_host))
+        steps.append(ds41.HostStep(host_in, e_inp, wl, fc, out, h_o=o_host, graph=True))
     h2d = sum(t.numel() * t.element_size() for t in steps[0]._keep[0].values())
     d2h = o_host.numel() * o_host.element_size()
     sid = stream.cuda_stream
@@ -901,8 +902,9 @@ def run_e2e(wl, slots, fc, stream, K, W, n_slots, world=1):
     ms = max_over_ranks(max(e0.elapsed_time(e1), wall * 1e3), world)
     return {"value": wl.m * K * world / (ms / 1e3), "unit": "query-tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "how": "ds41_csa_forward_host per step (prepared call): one pinned H2D of "
-                   "q/kv/latent/q_idx/w, the step, D2H of o, one stream"}
+            "how": "ds41_host_step_launch per step (the packed host step recorded once "
+                   "per layer state as a CUDA graph): one pinned H2D of q/kv/latent/q_idx/w, "
+                   "the step, D2H of o, one stream"}
 
 
 # ---------------------------------------------------------------------------

@@ -16,6 +16,7 @@
 // sequence.
 #include "ds41_internal.cuh"
 #include "ds41_step1.cuh"
+#include "ds41_tc.cuh"
 
 using namespace ds41;
 
@@ -262,6 +263,53 @@ extern "C" int ds41_csa_forward_fp4(const ds41_bf16* q, const ds41_bf16* kv, ds4
 // The step with its per-step inputs and its output in host memory: one copy
 // per input into the caller's device buffers, the step, and one copy of o
 // back, all on the caller's stream.
+// ---------------------------------------------------------------------------
+// Copies between host buffers and device buffers for the host entry points.
+// When the host side is device-mapped page-locked memory (cudaHostAlloc,
+// cudaHostRegister) and the copy is small, a kernel moves the bytes with
+// 16-byte loads and stores through the mapping: for the tens of KB of a
+// decode step this finishes sooner than a copy-engine transfer, whose
+// start-up dominates at that size.  Everything else goes through
+// cudaMemcpyAsync.
+// ---------------------------------------------------------------------------
+__global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n16) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+constexpr size_t kKernelCopyMax = size_t(4) << 20;  // larger copies use the copy engines
+
+static int host_copy(void* dst, const void* src, size_t bytes, bool h2d, cudaStream_t st,
+                     const char* what) {
+    if (bytes == 0) return DS41_OK;
+    const void* host = h2d ? src : dst;
+    void* mapped = nullptr;
+    cudaPointerAttributes a;
+    int dev = -1;
+    if (bytes <= kKernelCopyMax && bytes % 16 == 0 && cudaGetDevice(&dev) == cudaSuccess) {
+        // page-locked memory of this device's context, mapped into its address space
+        if (cudaPointerGetAttributes(&a, host) == cudaSuccess && a.type == cudaMemoryTypeHost &&
+            a.device == dev)
+            mapped = a.devicePointer;
+        else
+            cudaGetLastError();  // not registered with CUDA: clear the query's error
+    }
+    const void* s = h2d ? mapped : src;
+    void* d = h2d ? dst : mapped;
+    if (mapped && ((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d)) & 15u) == 0) {
+        const int64_t n16 = (int64_t)(bytes / 16);
+        const int64_t cap = 4 * (int64_t)device_sm_count();
+        const int64_t blocks = (n16 + 255) / 256;
+        copy16_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, st>>>(
+            static_cast<const uint4*>(s), static_cast<uint4*>(d), n16);
+        return launch_check(what);
+    }
+    return cuda_check(cudaMemcpyAsync(dst, src, bytes,
+                                      h2d ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost, st),
+                      what);
+}
+
 extern "C" int ds41_csa_forward_host(
     const ds41_bf16* h_q, const ds41_bf16* h_kv, const ds41_bf16* h_latent, const ds41_bf16* h_q_idx,
     const float* h_w, ds41_bf16* h_o, ds41_bf16* q, ds41_bf16* kv, ds41_bf16* ring, ds41_bf16* rows_a,
@@ -292,16 +340,14 @@ extern "C" int ds41_csa_forward_host(
                         {w, h_w, (size_t)(m * Hi) * 4}};
     for (const Copy& c : in) {
         if (c.bytes == 0) continue;
-        const int rc = cuda_check(cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st),
-                                  "ds41_csa_forward_host: input copy");
+        const int rc = host_copy(c.dst, c.src, c.bytes, true, st, "ds41_csa_forward_host: input copy");
         if (rc) return rc;
     }
     const int rc = ds41_csa_forward(q, kv, ring, rows_a, latent, freqs_cis, max_pos, cache, cache_rows,
                                     q_idx, k_idx, w, sink, scale, win_idx, idx, o, lse, m, start_pos,
                                     nh, hd, rd, win, ratio, topk, Hi, Di, ws, ws_bytes, stream);
     if (rc) return rc;
-    return cuda_check(cudaMemcpyAsync(h_o, o, (size_t)(m * nh * hd) * 2, cudaMemcpyDeviceToHost, st),
-                      "ds41_csa_forward_host: output copy");
+    return host_copy(h_o, o, (size_t)(m * nh * hd) * 2, false, st, "ds41_csa_forward_host: output copy");
 }
 
 extern "C" size_t ds41_step_inputs_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_t hd,
@@ -331,15 +377,87 @@ extern "C" int ds41_csa_forward_host_packed(
     ds41_bf16* q_idx = latent + G * hd;
     float* w = reinterpret_cast<float*>(q_idx + m * Hi * Di);
     cudaStream_t st = (cudaStream_t)stream;
-    int rc = cuda_check(cudaMemcpyAsync(d_in, h_in, bytes, cudaMemcpyHostToDevice, st),
-                        "ds41_csa_forward_host_packed: input copy");
+    int rc = host_copy(d_in, h_in, bytes, true, st, "ds41_csa_forward_host_packed: input copy");
     if (rc) return rc;
     rc = ds41_csa_forward(q, kv, ring, rows_a, G > 0 ? latent : nullptr, freqs_cis, max_pos, cache,
                           cache_rows, q_idx, k_idx, w, sink, scale, win_idx, idx, o, lse, m,
                           start_pos, nh, hd, rd, win, ratio, topk, Hi, Di, ws, ws_bytes, stream);
     if (rc) return rc;
-    return cuda_check(cudaMemcpyAsync(h_o, o, (size_t)(m * nh * hd) * 2, cudaMemcpyDeviceToHost, st),
-                      "ds41_csa_forward_host_packed: output copy");
+    return host_copy(h_o, o, (size_t)(m * nh * hd) * 2, false, st,
+                     "ds41_csa_forward_host_packed: output copy");
+}
+
+// ---------------------------------------------------------------------------
+// A prepared host step: the packed host step recorded once into a CUDA graph
+// ---------------------------------------------------------------------------
+struct ds41_host_step {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+extern "C" int ds41_host_step_create(
+    ds41_host_step** out, const void* h_in, void* d_in, ds41_bf16* h_o, ds41_bf16* ring,
+    ds41_bf16* rows_a, const float* freqs_cis, int64_t max_pos, ds41_bf16* cache,
+    int64_t cache_rows, const ds41_bf16* k_idx, const float* sink, float scale, int32_t* win_idx,
+    int32_t* idx, ds41_bf16* o, float* lse, int64_t m, int64_t start_pos, int64_t nh, int64_t hd,
+    int64_t rd, int64_t win, int64_t ratio, int64_t topk, int64_t Hi, int64_t Di, void* ws,
+    size_t ws_bytes) {
+    const char* name = "ds41_host_step_create";
+    DS41_REQUIRE(out, DS41_E_ARG, "%s: out is NULL", name);
+    *out = nullptr;
+    DS41_REQUIRE(ds41_step_inputs_bytes(m, start_pos, nh, hd, ratio, Hi, Di) > 0 && h_in && d_in &&
+                     h_o && o,
+                 DS41_E_ARG, "%s: m=%lld, null pointer", name, (long long)m);
+    // resources the step looks up on first use, outside the recording
+    unsigned int* status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    if ((rc = tc::get_encode(&enc))) return rc;
+    cudaStream_t cs;
+    if ((rc = cuda_check(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking),
+                         "ds41_host_step_create: stream")))
+        return rc;
+    rc = cuda_check(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal),
+                    "ds41_host_step_create: begin capture");
+    if (rc) {
+        cudaStreamDestroy(cs);
+        return rc;
+    }
+    const int step_rc = ds41_csa_forward_host_packed(
+        h_in, d_in, h_o, ring, rows_a, freqs_cis, max_pos, cache, cache_rows, k_idx, sink, scale,
+        win_idx, idx, o, lse, m, start_pos, nh, hd, rd, win, ratio, topk, Hi, Di, ws, ws_bytes,
+        (ds41_stream_t)cs);
+    cudaGraph_t g = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (step_rc || ce != cudaSuccess || !g) {
+        if (g) cudaGraphDestroy(g);
+        if (step_rc) return step_rc;  // its message stands
+        cudaGetLastError();
+        return fail(DS41_E_CUDA, "%s: capture failed: %s", name, cudaGetErrorString(ce));
+    }
+    cudaGraphExec_t ex = nullptr;
+    rc = cuda_check(cudaGraphInstantiate(&ex, g, 0), "ds41_host_step_create: instantiate");
+    if (rc) {
+        cudaGraphDestroy(g);
+        return rc;
+    }
+    *out = new ds41_host_step{g, ex};
+    return DS41_OK;
+}
+
+extern "C" int ds41_host_step_launch(ds41_host_step* h, ds41_stream_t stream) {
+    DS41_REQUIRE(h, DS41_E_ARG, "ds41_host_step_launch: handle is NULL");
+    return cuda_check(cudaGraphLaunch(h->exec, (cudaStream_t)stream), "ds41_host_step_launch");
+}
+
+extern "C" int ds41_host_step_destroy(ds41_host_step* h) {
+    if (!h) return DS41_OK;
+    cudaGraphExecDestroy(h->exec);
+    cudaGraphDestroy(h->graph);
+    delete h;
+    return DS41_OK;
 }
 
 // ---------------------------------------------------------------------------

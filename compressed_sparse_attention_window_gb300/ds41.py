@@ -65,6 +65,11 @@ SIGNATURES = {
     "ds41_step_inputs_bytes": (_SZ, [_I64] * 7),
     "ds41_csa_forward_host_packed": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P, _P, _F,
                                                     _P, _P, _P, _P] + [_I64] * 10 + [_P, _SZ, _P]),
+    "ds41_host_step_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), _P, _P, _P, _P, _P, _P, _I64,
+                                             _P, _I64, _P, _P, _F, _P, _P, _P, _P] + [_I64] * 10
+                              + [_P, _SZ]),
+    "ds41_host_step_launch": (ctypes.c_int, [_P, _P]),
+    "ds41_host_step_destroy": (ctypes.c_int, [_P]),
     "ds41_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, ctypes.c_int, _P, _P]),
     "ds41_sparse_attn_noalloc_capacity": (_SZ, []),
     "ds41_sparse_attn_sink_fwd_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _I64, _P, _F,
@@ -561,11 +566,13 @@ class HostStep:
     step on the stream and returns ``h_o``, which holds the result once the
     stream has reached the copy.  When both sides hold the inputs as one block
     (step_input_buffers), the call is ds41_csa_forward_host_packed: one copy
-    in instead of five."""
+    in instead of five.  With ``graph=True`` (packed blocks only) the call is
+    recorded once into a CUDA graph by ds41_host_step_create and every call is
+    one ds41_host_step_launch."""
 
     def __init__(self, host: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], wl,
                  freqs_cis: torch.Tensor, out: Optional[Dict[str, torch.Tensor]] = None,
-                 h_o: Optional[torch.Tensor] = None):
+                 h_o: Optional[torch.Tensor] = None, graph: bool = False):
         out = {} if out is None else out
         dev = inp["q"].device
         m, win = wl.m, wl.win
@@ -628,6 +635,17 @@ class HostStep:
         self._keep = (host, inp, out, freqs_cis)  # the buffers stay alive with the call
         self._fn = getattr(load(), self._name)
         self.h_o = h_o
+        self._handle = None
+        if graph:
+            if not self.packed:
+                raise ValueError("HostStep: graph=True needs the packed input blocks "
+                                 "(step_input_buffers on both sides)")
+            h = ctypes.c_void_p()
+            _call("ds41_host_step_create", ctypes.byref(h), *self._args)
+            self._handle = h
+            self._name = "ds41_host_step_launch"
+            self._fn = load().ds41_host_step_launch
+            self._args = (h,)
         if sz.n_c == 0:
             out["idx"] = out["win_idx"]
 
@@ -637,6 +655,19 @@ class HostStep:
             raise DS41Error(self._name, rc,
                             load().ds41_last_error().decode(errors="replace"))
         return self.h_o
+
+    def close(self) -> None:
+        """Frees the recorded graph (graph mode); launches still pending
+        complete first."""
+        if self._handle is not None:
+            load().ds41_host_step_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def csa_forward_host(host: Dict[str, torch.Tensor], inp: Dict[str, torch.Tensor], wl,

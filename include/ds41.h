@@ -347,7 +347,11 @@ int ds41_csa_forward_reuse(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* r
  * once the stream has reached that point (cudaStreamSynchronize).  The copies
  * are asynchronous only for page-locked host memory (cudaHostAlloc /
  * cudaHostRegister); pageable buffers work but the copies then block the
- * calling thread.  The host buffers must stay valid and unmodified until the
+ * calling thread.  A copy of at most 4 MiB, a multiple of 16 bytes, between
+ * 16-byte aligned device memory and page-locked memory mapped for the current
+ * device runs as a small kernel on the stream that moves the bytes through
+ * the mapping (for a decode step's tens of KB this ends sooner than a
+ * copy-engine transfer); other copies use cudaMemcpyAsync.  The host buffers must stay valid and unmodified until the
  * stream has passed the copies.  Errors: ds41_csa_forward's, DS41_E_ARG for a
  * NULL pointer, DS41_E_CUDA when a copy cannot be enqueued (the copies
  * enqueued before stay enqueued). */
@@ -382,6 +386,45 @@ int ds41_csa_forward_host_packed(const void* h_in, void* d_in, ds41_bf16* h_o, d
                                  int64_t nh, int64_t hd, int64_t rd, int64_t win, int64_t ratio,
                                  int64_t topk, int64_t Hi, int64_t Di, void* ws, size_t ws_bytes,
                                  ds41_stream_t stream);
+
+/* A prepared host step: what one ds41_csa_forward_host_packed call enqueues
+ * (the input copy, the step's kernels, the output copy), recorded once into a
+ * CUDA graph for fixed buffers, as a serving loop runs a layer's step again
+ * and again.  Each ds41_host_step_launch then enqueues the whole step with one
+ * graph launch instead of a copy, two kernel launches and a copy, which takes
+ * less host time per step and leaves fewer gaps between the operations on the
+ * GPU.  No counterpart on the pages (their runtime launches the kernels
+ * directly).  The handle is opaque and owned by the caller. */
+typedef struct ds41_host_step ds41_host_step;
+
+/* Records the step into *out.  Arguments as ds41_csa_forward_host_packed,
+ * minus the stream; every pointer and size is fixed in the recording, so the
+ * buffers must outlive the handle and each launch reads whatever h_in holds
+ * when the copy runs.  Nothing runs at creation (the recording is made on a
+ * private stream in capture mode).  Errors: those of
+ * ds41_csa_forward_host_packed's argument checks (nothing is recorded then),
+ * DS41_E_ARG for a NULL out, DS41_E_CUDA when the capture or the graph's
+ * instantiation fails; *out is NULL on any error. */
+int ds41_host_step_create(ds41_host_step** out, const void* h_in, void* d_in, ds41_bf16* h_o,
+                          ds41_bf16* ring, ds41_bf16* rows_a, const float* freqs_cis,
+                          int64_t max_pos, ds41_bf16* cache, int64_t cache_rows,
+                          const ds41_bf16* k_idx, const float* sink, float scale,
+                          int32_t* win_idx, int32_t* idx, ds41_bf16* o, float* lse, int64_t m,
+                          int64_t start_pos, int64_t nh, int64_t hd, int64_t rd, int64_t win,
+                          int64_t ratio, int64_t topk, int64_t Hi, int64_t Di, void* ws,
+                          size_t ws_bytes);
+
+/* Enqueues the recorded step on `stream` (one graph launch); returns without
+ * waiting, and h_o holds the result once the stream has passed the step.
+ * Launches of one handle run one after another.  Results are the same bits
+ * as ds41_csa_forward_host_packed with the same arguments.  Errors: DS41_E_ARG
+ * for a NULL handle, DS41_E_CUDA when the launch fails. */
+int ds41_host_step_launch(ds41_host_step* h, ds41_stream_t stream);
+
+/* Frees the recording (NULL is a no-op).  Launches still pending complete
+ * first: the driver frees an executable graph that is in flight once it has
+ * finished.  Returns DS41_OK. */
+int ds41_host_step_destroy(ds41_host_step* h);
 
 /* ------------------------------------------------------------------------ */
 /* Step 3 without caller-provided scratch                                     */

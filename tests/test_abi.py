@@ -144,6 +144,30 @@ def test_host_buffer_entry_points_check_arguments(lib):
     assert rc == 1 and "null pointer" in _err(lib)
 
 
+def test_host_step_checks_arguments(lib):
+    """ds41_host_step_create rejects a missing handle slot, sizes and buffers
+    on the host (leaving the handle NULL); launching a NULL handle is an
+    argument error and destroying one a no-op."""
+    f = ctypes.c_float(0.04)
+    sizes = (8191, 64, 512, 64, 128, 4, 512, 64, 128)  # start_pos nh hd rd win ratio topk Hi Di
+    h = ctypes.c_void_p(0x1234)
+
+    def create(out, h_in, m):
+        # out | h_in d_in h_o ring rows_a freqs_cis max_pos cache cache_rows k_idx sink scale
+        # win_idx idx o lse | m, sizes | ws ws_bytes
+        return lib.ds41_host_step_create(out, h_in, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, FAKE,
+                                         1 << 20, FAKE, FAKE, f, FAKE, FAKE, FAKE, None, m, *sizes,
+                                         None, 0)
+
+    assert create(None, FAKE, 1) == 1 and "out is NULL" in _err(lib)
+    assert create(ctypes.byref(h), None, 1) == 1 and "null pointer" in _err(lib)
+    assert h.value is None
+    h = ctypes.c_void_p(0x1234)
+    assert create(ctypes.byref(h), FAKE, 0) == 1 and h.value is None  # no token
+    assert lib.ds41_host_step_launch(None, None) == 1 and "NULL" in _err(lib)
+    assert lib.ds41_host_step_destroy(None) == 0
+
+
 def test_attn_out_proj_checks_arguments(lib):
     """ds41_attn_out_proj rejects bad sizes and pointers on the host, before
     anything is enqueued (no GPU needed)."""

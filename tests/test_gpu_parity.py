@@ -520,6 +520,21 @@ def test_csa_forward_host_buffers(wl, packed):
         again()
         torch.cuda.synchronize()
         assert torch.equal(h_o, ref["o"].cpu())
+    if packed:
+        # the same call recorded once into a CUDA graph (ds41_host_step_create),
+        # launched twice from the same starting state: the same bits
+        rec = ds41.HostStep(host, dev, wl, fc, out, h_o=h_o, graph=True)
+        for _ in range(2):
+            h_o.zero_()
+            dev["ring"].copy_(start["ring"])
+            dev["cache"].copy_(start["cache"])
+            rec()
+            torch.cuda.synchronize()
+            assert torch.equal(h_o, ref["o"].cpu())
+            assert torch.equal(out["idx"], ref["idx"])
+            assert torch.equal(dev["ring"], dev_ref["ring"])
+            assert torch.equal(dev["cache"], dev_ref["cache"])
+        rec.close()
 
 
 # --------------------------------------------------------------------------
