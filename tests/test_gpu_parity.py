@@ -537,6 +537,36 @@ def test_csa_forward_host_buffers(wl, packed):
         rec.close()
 
 
+@pytest.mark.parametrize("wl", [WORKLOADS["decode"], WORKLOADS["tiny_prefill"]],
+                         ids=lambda w: w.name)
+@pytest.mark.parametrize("packed", [False, True])
+def test_csa_forward_host_pageable(wl, packed):
+    """Pageable host buffers (not page-locked, so not mapped for the device)
+    go through the copy engines rather than the copy kernel, and give the
+    same bits as the device-tensor step."""
+    inp = make_inputs(wl)
+    fc = ds41.yarn_freqs_cis(wl.rd, max(wl.max_pos, 1))
+    dev_ref = to_dev(inp)
+    ref = ds41.csa_forward(dev_ref, wl, fc)
+    dev = to_dev(inp)
+    step = ds41.STEP_INPUTS
+    if packed:
+        dev.update(ds41.step_input_buffers(wl, "cuda"))
+        host = ds41.step_input_buffers(wl, "cpu", pinned=False)
+        for k in step:
+            host[k].copy_(inp[k])
+    else:
+        host = {k: inp[k].contiguous().clone() for k in step}
+    assert not any(host[k].is_pinned() for k in step)
+    h_o = torch.empty(tuple(inp["q"].shape), dtype=torch.bfloat16)  # pageable too
+    out = {}
+    got = ds41.csa_forward_host(host, dev, wl, fc, out, h_o=h_o)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref["o"].cpu())
+    assert torch.equal(out["idx"], ref["idx"])
+    assert torch.equal(dev["ring"], dev_ref["ring"]) and torch.equal(dev["cache"], dev_ref["cache"])
+
+
 # --------------------------------------------------------------------------
 # The output side of the layer: inverse RoPE, grouped wo_a, wo_b
 # --------------------------------------------------------------------------
