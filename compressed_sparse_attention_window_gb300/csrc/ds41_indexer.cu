@@ -90,8 +90,8 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     }
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* qs = reinterpret_cast<uint16_t*>(smem);                 // [IDX_N][DI]
-    uint16_t* ks = qs + IDX_N * DI;                                    // [IDX_ROWS][DI]
-    float* cs = reinterpret_cast<float*>(ks + IDX_ROWS * DI);         // [IDX_ROWS][IDX_N + 1]
+    uint16_t* ksb = qs + IDX_N * DI;                                   // 2 x [IDX_ROWS][DI]
+    float* cs = reinterpret_cast<float*>(ksb + 2 * IDX_ROWS * DI);    // [IDX_ROWS][IDX_N + 1]
     float* wsm = cs + IDX_ROWS * (IDX_N + 1);                          // [IDX_N]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -115,9 +115,11 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     // group can see yet are written as -inf too.
     const int64_t tiles = fill_hidden ? (n_c + IDX_ROWS - 1) / IDX_ROWS : tiles_vis;
     cp_async_commit();  // group of q
-    // The first key tile is fetched together with q, so the two loads overlap,
-    // and q is quantised while the tile is still in flight.
-    auto fetch_k = [&](int64_t tile) {
+    // Key tiles go through two buffers: the CTA's first two tiles are fetched
+    // together with q, so the three loads overlap (a decode CTA takes one or
+    // two tiles), and q is quantised while they are in flight; each later
+    // tile is fetched as soon as the tile two before it is done.
+    auto fetch_k = [&](int64_t tile, uint16_t* ks) {
         const int64_t r0 = tile * IDX_ROWS;
         for (int id = tid; id < IDX_ROWS * CPR; id += IDX_THREADS) {
             const int r = id / CPR, c = id % CPR;
@@ -127,14 +129,16 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
                        k_src + (live ? row : 0) * DI + c * 8, live);
         }
     };
-    const bool prefetched = (int64_t)blockIdx.y < tiles_vis;
-    if (prefetched) fetch_k(blockIdx.y);
-    cp_async_commit();  // group of the first key tile (empty when not prefetched)
+    for (int b = 0; b < 2; b++) {
+        const int64_t tile = (int64_t)blockIdx.y + (int64_t)b * ymain;
+        if (tile < tiles_vis) fetch_k(tile, ksb + b * IDX_ROWS * DI);
+        cp_async_commit();  // one group per buffer (empty when there is no such tile)
+    }
     for (int n = tid; n < IDX_N; n += IDX_THREADS) {
         const int tt = n / hpad, h = n % hpad;
         wsm[n] = (tt < tcount && h < Hi) ? w[(int64_t)(t0 + tt) * Hi + h] : 0.0f;
     }
-    cp_async_wait<1>();  // this thread's q copies have landed
+    cp_async_wait<2>();  // this thread's q copies have landed
     __syncthreads();
     // only the live rows (tokens of the group x Hi heads), rounded up to whole
     // passes of the block: q8_chunk shuffles over the full warp, and the
@@ -148,8 +152,8 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
         uint4* p = reinterpret_cast<uint4*>(qs + n * DI + swz<CPR>(n, c) * 8);
         *p = q8_chunk(*p, true);
     }
-    cp_async_wait<0>();  // the first key tile (its readers sync below)
 
+    int it = 0;  // this CTA's visible tiles so far: tile it uses buffer it & 1
     for (int64_t tile = blockIdx.y; tile < tiles; tile += ymain) {
         const int64_t r0 = tile * IDX_ROWS;
         if (tile >= tiles_vis) {
@@ -159,13 +163,9 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             }
             continue;
         }
-        __syncthreads();  // previous tile's readers are done with ks / cs
-        if (!(prefetched && tile == (int64_t)blockIdx.y)) {
-            fetch_k(tile);
-            cp_async_commit();
-            cp_async_wait<0>();
-            __syncthreads();
-        }
+        uint16_t* ks = ksb + (it & 1) * IDX_ROWS * DI;
+        cp_async_wait<1>();  // this thread's copies of this tile (the next may be in flight)
+        __syncthreads();     // everyone's copies; previous tile's readers are done with cs
         if (KQ_INLINE) {
             // raw keys -> fp4 round trip, in place (rows past n_c are zero)
 #pragma unroll 1
@@ -211,7 +211,13 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             cs[(r + 8) * (IDX_N + 1) + col] = acc[j][2];
             cs[(r + 8) * (IDX_N + 1) + col + 1] = acc[j][3];
         }
-        __syncthreads();
+        __syncthreads();  // cs written; every warp is done reading ks
+        {
+            // refill this buffer with the tile two after this one
+            const int64_t next = tile + 2 * (int64_t)ymain;
+            if (next < tiles_vis) fetch_k(next, ks);
+            cp_async_commit();
+        }
 
         for (int p = tid; p < IDX_ROWS * tcount; p += IDX_THREADS) {
             const int tt = p / IDX_ROWS, r = p % IDX_ROWS;
@@ -224,13 +230,21 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
                 const float* col = cs + r * (IDX_N + 1) + tt * hpad;
                 const float* wt = wsm + tt * hpad;
                 float a = 0.0f;
-                for (int h = 0; h < Hi; h++) a = __fmaf_rn(wt[h], fmaxf(col[h], 0.0f), a);
+                if (Hi == 64) {
+                    // the same chain unrolled: its loads no longer wait in turn
+#pragma unroll
+                    for (int h = 0; h < 64; h++) a = __fmaf_rn(wt[h], fmaxf(col[h], 0.0f), a);
+                } else {
+                    for (int h = 0; h < Hi; h++) a = __fmaf_rn(wt[h], fmaxf(col[h], 0.0f), a);
+                }
                 out = f2bf(a);
                 if (out == 0x8000u) out = 0u;
             }
             scores[(int64_t)t * n_c + s] = out;
         }
+        it++;
     }
+    cp_async_wait<0>();  // no copy of this CTA outlives it
 }
 
 // ---------------------------------------------------------------------------
@@ -883,7 +897,7 @@ static int launch_scores(const IndexerPlan& p, const uint16_t* q, const uint16_t
                          uint16_t* scores, int64_t m, int64_t Hi, int64_t n_c, int64_t ratio,
                          int64_t start_pos, bool fill_hidden, cudaStream_t st,
                          const RingArgs* ring = nullptr, const LatentArgs* lat = nullptr) {
-    const size_t smem = (size_t)IDX_N * DI * 2 + (size_t)IDX_ROWS * DI * 2 +
+    const size_t smem = (size_t)IDX_N * DI * 2 + 2 * (size_t)IDX_ROWS * DI * 2 +
                         (size_t)IDX_ROWS * (IDX_N + 1) * 4 + IDX_N * 4;
     // Row-tile splits: enough CTAs to cover the GPU when there are few tokens.
     const int64_t tiles = (n_c + IDX_ROWS - 1) / IDX_ROWS;
