@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
 }
 
 // ---------------------------------------------------------------------------
-constexpr int TKD_CAP = 4096;  // score keys of one CTA's slice in the fused decode step
+constexpr int TKD_CAP = 4096;  // most score keys one CTA ranks in the fused decode step
 constexpr int TKD_WHIST = 10752;  // per-warp histograms of the local selection, in its area
 
 // Split halves of a cluster barrier: every CTA arrives once it has started,
@@ -458,30 +458,15 @@ __device__ void dec_topk_local(const DecTopk& tk, int64_t t, int vis, int kk, in
 
 // Fill sidx[0 .. j1 - j0) with slice [j0, j1) of the merged index row
 // [window indices | the min(ctopk, visible) best compressed rows in ascending
-// order | -1].  Up to TKD_CAP visible scores every CTA ranks them all itself
-// (dec_topk_local).  Beyond, the CL CTAs of the cluster each take one slice
-// of the visible scores (in registers, as there), sum their two 8-bit
-// histograms over the cluster (every CTA derives the same threshold; the
-// lowest-numbered ties are taken), take the counts of the earlier slices from
-// their pushed histograms and above-bucket counts, and store each pick
-// straight into the index slice of the CTA that owns its position: three
-// cluster barriers.  Returns whether it waited on the cluster barrier's first
-// phase.
+// order | -1].  Every CTA ranks the visible scores itself (dec_topk_local):
+// the host fuses the selection into the attention only while they fit one
+// CTA's registers (n_c <= TKD_CAP); longer score rows go through the
+// separate top-k kernel, which measured faster than any selection split over
+// the attention's cluster.
 template <int NTH>
-__device__ bool dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, int j1, int* sidx,
-                         uint8_t* area, int* hpush, bool write_idx, unsigned int* status) {
-    namespace cg = cooperative_groups;
-    cg::cluster_group cl = cg::this_cluster();
-    const int CL = (int)cl.num_blocks(), r = (int)cl.block_rank();
-    int* hist = reinterpret_cast<int*>(area + 8192);  // this slice's histogram
-    int* ghist = hist + 256;                          // the cluster's
-    int* wsum = ghist + 256;
-    int* sel = wsum + 64;
-    int* tpush = sel + 8;                             // [16]: each slice's keys above bucket hb
-    int* hpush1 = hpush;                              // [16][256] histograms of the slices
-    int* hpush2 = hpush + 16 * 256;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int NW = NTH / 32;
+__device__ void dec_topk(const DecTopk& tk, int64_t t, int K, int j0, int j1, int* sidx,
+                         uint8_t* area, bool write_idx, unsigned int* status) {
+    const int tid = threadIdx.x;
     const int win = tk.win;
     int64_t vis = (tk.start_pos + t + 1) / tk.ratio;
     if (vis > tk.n_c) vis = tk.n_c;
@@ -497,175 +482,17 @@ __device__ bool dec_topk(const DecTopk& tk, int64_t t, int K, int per, int j0, i
         } else if (vis <= tk.ctopk) {
             v = (int)(tk.offset + (j - win));
         } else {
-            continue;  // a pick: stored by the CTA that holds its score
+            continue;  // a pick: stored by the ranking below
         }
         sidx[j - j0] = v;
         if (write_idx) orow[j] = v;
     }
-    if (vis <= tk.ctopk) return false;  // the same branch in every CTA of the cluster
-    if (vis <= TKD_CAP) {
-        dec_topk_local<NTH>(tk, t, (int)vis, kk, win, j0, j1, sidx, area, orow, write_idx);
-        return false;
+    if (vis <= tk.ctopk) return;  // the same branch in every CTA of the cluster
+    if (vis > TKD_CAP) {
+        raise_status(status, DS41_E_RANGE);  // excluded by the host plan
+        return;
     }
-    cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
-
-    const int64_t kseg = ((vis + CL - 1) / CL + 7) & ~int64_t(7);
-    const int64_t klo = min(vis, (int64_t)r * kseg);
-    const int n = (int)(min(vis, klo + kseg) - klo);
-    if (n > TKD_CAP) raise_status(status, DS41_E_RANGE);  // excluded by the host plan
-    const int nk = min(n, TKD_CAP);
-    // this slice's keys in registers: thread tid holds the run of kpt
-    // consecutive scores from kpt * tid, so index order is warp, lane, register
-    constexpr int KMAX = TKD_CAP / NTH;
-    int* whist = reinterpret_cast<int*>(area + TKD_WHIST);  // [NW][256]
-    const int kpt = (nk + NTH - 1) / NTH;
-    const int i0 = kpt * tid;
-    const uint16_t* sc = tk.scores + t * tk.n_c + klo;
-    uint32_t key[KMAX];
-    const bool vec = (kpt & 7) == 0 && ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0);
-#pragma unroll
-    for (int v = 0; v < KMAX / 8; v++) {
-        const int b0 = i0 + 8 * v;
-        if (8 * v >= kpt || b0 >= nk) continue;
-        if (vec && b0 + 8 <= nk) {  // whole groups of eight only: nothing past the slice is read
-            uint4 u = __ldg(reinterpret_cast<const uint4*>(sc + b0));
-            const uint16_t* h = reinterpret_cast<const uint16_t*>(&u);
-#pragma unroll
-            for (int e = 0; e < 8; e++) key[8 * v + e] = order_key(h[e]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; e++)
-                if (8 * v + e < kpt && b0 + e < nk) key[8 * v + e] = order_key(sc[b0 + e]);
-        }
-    }
-    const int n_mine = max(0, min(kpt, nk - i0));
-    int* wh = whist + warp * 256;
-#pragma unroll
-    for (int e = 0; e < 8; e++) wh[lane + 32 * e] = 0;
-    __syncwarp();
-#pragma unroll
-    for (int e = 0; e < KMAX; e++)
-        if (e < n_mine) atomicAdd(&wh[key[e] >> 8], 1);
-    __syncthreads();
-    // this slice's top-byte histogram: kept here, and pushed into every CTA
-    // (four bins a thread, 16-byte remote stores)
-    if (tid < 64) {
-        int4 v = make_int4(0, 0, 0, 0);
-#pragma unroll
-        for (int w = 0; w < NW; w++) {
-            int4* h = reinterpret_cast<int4*>(whist + w * 256 + 4 * tid);
-            const int4 x = *h;
-            v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
-            *h = make_int4(0, 0, 0, 0);
-        }
-        *reinterpret_cast<int4*>(hist + 4 * tid) = v;
-        for (int q = 0; q < CL; q++) reinterpret_cast<int4*>(cl.map_shared_rank(hpush1 + r * 256, q))[tid] = v;
-    }
-    cl.sync();
-    for (int b = tid; b < 256; b += NTH) {
-        int v = 0;
-        for (int q = 0; q < CL; q++) v += hpush1[q * 256 + b];
-        ghist[b] = v;
-    }
-    __syncthreads();
-    if (tid < 32) find_bucket(ghist, kk, 0, &sel[0], &sel[1]);
-    __syncthreads();
-    const uint32_t hb = (uint32_t)sel[0];
-    const int above1 = sel[1];
-#pragma unroll
-    for (int e = 0; e < KMAX; e++)
-        if (e < n_mine && (key[e] >> 8) == hb) atomicAdd(&wh[key[e] & 0xffu], 1);
-    if (warp == 0) {
-        // keys of this slice in buckets above hb, for the other slices' prefixes
-        int a = 0;
-        for (int b = (int)hb + 1 + lane; b < 256; b += 32) a += hist[b];
-        a = __reduce_add_sync(0xffffffffu, a);
-        if (lane < CL) cl.map_shared_rank(tpush, lane)[r] = a;
-    }
-    __syncthreads();
-    // this slice's low-byte histogram of bucket hb, pushed into every CTA; with
-    // the above counts it gives every slice's count of keys above and at the
-    // threshold, so no further exchange is needed before the picks
-    if (tid < 64) {
-        int4 v = make_int4(0, 0, 0, 0);
-#pragma unroll
-        for (int w = 0; w < NW; w++) {
-            const int4 x = *reinterpret_cast<const int4*>(whist + w * 256 + 4 * tid);
-            v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
-        }
-        for (int q = 0; q < CL; q++) reinterpret_cast<int4*>(cl.map_shared_rank(hpush2 + r * 256, q))[tid] = v;
-    }
-    cl.sync();
-    for (int b = tid; b < 256; b += NTH) {
-        int v = 0;
-        for (int q = 0; q < CL; q++) v += hpush2[q * 256 + b];
-        ghist[b] = v;
-    }
-    __syncthreads();
-    if (tid < 32) find_bucket(ghist, kk, above1, &sel[2], &sel[3]);
-    __syncthreads();
-    const uint32_t T = (hb << 8) | (uint32_t)sel[2];
-    const int need_eq = kk - sel[3];
-    if (warp == 0) {
-        // keys above and at the threshold in the slices before this one
-        const int tl = sel[2];
-        int g = 0, e = 0;
-        for (int q = 0; q < r; q++) {
-            int a = 0;
-            for (int b = tl + 1 + lane; b < 256; b += 32) a += hpush2[q * 256 + b];
-            g += __reduce_add_sync(0xffffffffu, a) + tpush[q];
-            e += hpush2[q * 256 + tl];
-        }
-        if (lane == 0) {
-            sel[4] = g;
-            sel[5] = e;
-        }
-    }
-    int n_gt = 0, n_eq = 0;
-#pragma unroll
-    for (int e = 0; e < KMAX; e++) {
-        if (e < n_mine) {
-            n_gt += key[e] > T ? 1 : 0;
-            n_eq += key[e] == T ? 1 : 0;
-        }
-    }
-    int x_gt = n_gt, x_eq = n_eq;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, x_gt, off);
-        const int b = __shfl_up_sync(0xffffffffu, x_eq, off);
-        if (lane >= off) {
-            x_gt += a;
-            x_eq += b;
-        }
-    }
-    if (lane == 31) {
-        wsum[warp] = x_gt;
-        wsum[32 + warp] = x_eq;
-    }
-    __syncthreads();
-    int gt = sel[4] + x_gt - n_gt, eq = sel[5] + x_eq - n_eq;
-    for (int w = 0; w < warp; w++) {
-        gt += wsum[w];
-        eq += wsum[32 + w];
-    }
-#pragma unroll
-    for (int e = 0; e < KMAX; e++) {
-        if (e < n_mine) {
-            const bool is_eq = key[e] == T;
-            if (key[e] > T || (is_eq && eq < need_eq)) {
-                const int j = win + gt + min(eq, need_eq);  // position in the merged row
-                const int owner = j / per;
-                const int v = (int)(tk.offset + klo + i0 + e);
-                cl.map_shared_rank(sidx, owner)[j - owner * per] = v;
-                if (write_idx) orow[j] = v;
-            }
-            gt += key[e] > T ? 1 : 0;
-            eq += is_eq ? 1 : 0;
-        }
-    }
-    cl.sync();  // every index slice is complete
-    return true;
+    dec_topk_local<NTH>(tk, t, (int)vis, kk, win, j0, j1, sidx, area, orow, write_idx);
 }
 
 // Few-token (decode) path.  A cluster of CL CTAs shares one (token, group of
@@ -729,7 +556,8 @@ struct DecSmem {
 // slices of its unnormalised O into the CTAs that reduce them (distributed
 // shared memory); CTA r reduces the r-th slice of the columns over the
 // cluster, adds the sink and writes o.  No scratch memory and no second
-// launch.  In the fused step the cluster first selects the rows itself.
+// launch.  In the fused step every CTA first ranks the scores itself (up to
+// TKD_CAP of them) and keeps the picks of its own slice.
 template <int HD, bool FUSED>
 __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ rows_a, int64_t n_a,
@@ -780,7 +608,6 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     }
     __syncthreads();
     cluster_arrive_relaxed();  // this CTA has started (waited on before any remote store)
-    bool cl_waited = false;
     // q rows of this head group (rows past nh are zero); q is an input, so it
     // is read before waiting for the previous kernel.
     if (warp == 0) {
@@ -802,8 +629,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     const int nst = max(0, min(j1 - j0, DEC_STAGE));
     if constexpr (FUSED) {
         // select this query's rows here (the scores come from the kernel before)
-        cl_waited = dec_topk<NTH>(tk, t, K, per, j0, j1, sidx, smem + SM::tk_off,
-                                  reinterpret_cast<int*>(smem + SM::xch_off), blockIdx.y == 0, status);
+        dec_topk<NTH>(tk, t, K, j0, j1, sidx, smem + SM::tk_off, blockIdx.y == 0, status);
     } else {
         for (int j = tid; j < nst; j += NTH) sidx[j] = irow[j0 + j];
     }
@@ -1061,7 +887,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         dst[rb * (cols / 2) + cc] = pack_bf16x2(oacc[j][2], oacc[j][3]);
     }
     __syncthreads();
-    if (!cl_waited) cluster_wait();
+    cluster_wait();
     {
         const int per_q = 2 * cols;  // 16-byte pieces of one receiver's block
         for (int c = tid; c < CL * per_q; c += NTH) {
@@ -1352,8 +1178,7 @@ bool attn_topk_fusable(int64_t m, int64_t nh, int64_t hd, int64_t K, int64_t n_c
     const AttnPlan p = plan_attn(m, nh, hd, K, device_sms());
     if (p.cluster < 4) return false;
     const int64_t per = (K + p.cluster - 1) / p.cluster;
-    const int64_t kseg = ((n_c + p.cluster - 1) / p.cluster + 7) / 8 * 8;
-    return per <= DEC_STAGE && kseg <= TKD_CAP;
+    return per <= DEC_STAGE && n_c <= TKD_CAP;
 }
 
 }  // namespace ds41
