@@ -557,8 +557,12 @@ struct DecSmem {
 // shared memory); CTA r reduces the r-th slice of the columns over the
 // cluster, adds the sink and writes o.  No scratch memory and no second
 // launch.  In the fused step every CTA first ranks the scores itself (up to
-// TKD_CAP of them) and keeps the picks of its own slice.
-template <int HD, bool FUSED>
+// TKD_CAP of them) and keeps the picks of its own slice.  PACKED: the
+// compressed rows may arrive packed (e2m1 codes + e4m3 scales) and are
+// expanded in shared memory; a separate instantiation, so that the code runs
+// only where packed rows are possible (the kernel's time goes largely to
+// fetching its instructions: it runs once per launch on each SM).
+template <int HD, bool FUSED, bool PACKED>
 __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ rows_a, int64_t n_a,
     const uint16_t* __restrict__ rows_b, int64_t n_c, const int32_t* __restrict__ idx, int K,
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     constexpr uint32_t PKB = HD / 2 + HD / 16;
     constexpr uint32_t PKO = ((uint32_t)RS * 2 - PKB) & ~15u;
     static_assert(PKO + PKB <= (uint32_t)RS * 2 && PKO % 16 == 0, "packed row placement");
-    const bool packed = HD == 512 && pk.codes != nullptr;
+    const bool packed = PACKED && HD == 512 && pk.codes != nullptr;
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* qs = reinterpret_cast<uint16_t*>(smem);
     uint16_t* kvs = reinterpret_cast<uint16_t*>(smem + SM::q_bytes);
@@ -1027,9 +1031,16 @@ static int launch_attn_decode(const AttnPlan& p, const uint16_t* q, const uint16
                               unsigned int* status, cudaStream_t st, bool pdl,
                               const DecTopk* tk = nullptr, const PackedRows* pk = nullptr) {
     const size_t smem = tk ? DecSmem<HD>::fused_total : DecSmem<HD>::total;
-    auto kern = tk ? sparse_attn_decode_kernel<HD, true> : sparse_attn_decode_kernel<HD, false>;
+    auto kern = tk ? sparse_attn_decode_kernel<HD, true, false>
+                   : sparse_attn_decode_kernel<HD, false, false>;
+    const bool packed = pk && HD == 512 && pk->codes != nullptr;
+    if constexpr (HD == 512) {
+        if (packed)
+            kern = tk ? sparse_attn_decode_kernel<HD, true, true>
+                      : sparse_attn_decode_kernel<HD, false, true>;
+    }
     const DecTopk tkv = tk ? *tk : DecTopk{};
-    const PackedRows pkv = (pk && HD == 512) ? *pk : PackedRows{nullptr, nullptr};
+    const PackedRows pkv = packed ? *pk : PackedRows{nullptr, nullptr};
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (p.cluster > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
