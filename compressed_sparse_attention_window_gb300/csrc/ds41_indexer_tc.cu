@@ -299,32 +299,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const int64_t s = (int64_t)i * ROWS + 32 * q + lane;
-#pragma unroll 1
+                    // both tokens' 64 head dots, then the buffer goes back to
+                    // the MMA issuer before the chains run
+                    uint32_t dv[2][64];
+#pragma unroll
+                    for (int u = 0; u < 2; u++) {
+                        const uint32_t col = tmem + lane_off + 256 * db + 64 * (2 * pr + u);
+                        tc_ld32(col, *reinterpret_cast<uint32_t(*)[32]>(dv[u]));
+                        tc_ld32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(dv[u] + 32));
+                    }
+                    tc_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[B_DEMPTY + db]);
+                    // the two tokens' chains side by side, each in head order
+                    const float* w0 = wsm + (2 * pr) * HI;
+                    const float* w1 = w0 + HI;
+                    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+                    for (int h = 0; h < HI; h++) {
+                        a0 = __fmaf_rn(w0[h], fmaxf(__uint_as_float(dv[0][h]), 0.0f), a0);
+                        a1 = __fmaf_rn(w1[h], fmaxf(__uint_as_float(dv[1][h]), 0.0f), a1);
+                    }
+#pragma unroll
                     for (int u = 0; u < 2; u++) {
                         const int tt = 2 * pr + u;
-                        uint32_t dv[64];
-                        tc_ld32(tmem + lane_off + 256 * db + 64 * tt,
-                                *reinterpret_cast<uint32_t(*)[32]>(dv));
-                        tc_ld32(tmem + lane_off + 256 * db + 64 * tt + 32,
-                                *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
-                        tc_wait_ld();
                         if (tt >= tcount || s >= p.n_c) continue;
                         const int64_t t = t0 + tt;
                         uint16_t out = 0xff80u;  // -inf: not visible yet
                         if (s < visible(t, p)) {
-                            const float* wt = wsm + tt * HI;
-                            float a = 0.0f;
-#pragma unroll
-                            for (int h = 0; h < HI; h++)
-                                a = __fmaf_rn(wt[h], fmaxf(__uint_as_float(dv[h]), 0.0f), a);
-                            out = f2bf(a);
+                            out = f2bf(u == 0 ? a0 : a1);
                             if (out == 0x8000u) out = 0u;
                         }
                         p.scores[t * p.n_c + s] = out;
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[B_DEMPTY + db]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_WEMPTY + ws]);
