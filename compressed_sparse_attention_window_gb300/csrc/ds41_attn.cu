@@ -606,6 +606,9 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     const int j1 = min(K, j0 + per);
     const int nchunks = j1 > j0 ? (j1 - j0 + DEC_NC - 1) / DEC_NC : 0;
 
+    // the next kernel (the following step's front) may start launching; it
+    // waits for this one to complete before it touches memory
+    pdl_trigger();
     if (tid == 0) {
         for (int i = 0; i < 3; i++) mbar_init(&bars[i], 1);
         mbar_init_fence();

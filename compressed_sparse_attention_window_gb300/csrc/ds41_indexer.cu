@@ -77,6 +77,12 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     LatentArgs lat) {
     constexpr int CPR = DI / 8;  // 16-byte chunks per row
     pdl_trigger();  // the next kernel may start launching (it waits for this one)
+    // Every input (and the ring and cache this kernel writes) may belong to the
+    // kernel before, e.g. the previous step's attention reading the ring: this
+    // kernel is launched with programmatic stream serialization, so it waits
+    // for that kernel here, before its first memory access, and only its
+    // launch overlaps it.
+    pdl_wait();
     if ((int)blockIdx.y >= ymain) {
         // Fused front of a few-token step: the CTAs past the score grid do
         // step 1 (ring write + window indices, then the latent groups).
@@ -918,8 +924,23 @@ static int launch_scores(const IndexerPlan& p, const uint16_t* q, const uint16_t
                            : (narrow ? indexer_scores_kernel<DI, true, true>
                                      : indexer_scores_kernel<DI, true, false>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<grid, IDX_THREADS, smem, st>>>(q, k, w, scores, (int)m, (int)Hi, p.hpad, p.TT, n_c,
-                                          ratio, start_pos, fill_hidden, (int)ysplit, ra, la);
+    // programmatic stream serialization: the kernel may launch while the one
+    // before it runs (it waits for it before touching memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(IDX_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int rc = cuda_check(cudaLaunchKernelEx(&cfg, kern, q, k, w, scores, (int)m, (int)Hi, p.hpad,
+                                           p.TT, n_c, ratio, start_pos, fill_hidden, (int)ysplit,
+                                           ra, la),
+                        "ds41_indexer_topk: scores kernel");
+    if (rc) return rc;
     return launch_check("ds41_indexer_topk: scores kernel");
 }
 

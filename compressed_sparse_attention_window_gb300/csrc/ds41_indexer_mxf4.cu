@@ -232,6 +232,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     indexer_mxf4_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k, const Params p) {
     pdl_trigger();  // a dependent kernel may start launching (it waits for this one)
+    // launched with programmatic stream serialization: the kernel before (the
+    // previous step's attention, which reads the ring this kernel writes) is
+    // waited for here, before the first memory access
+    pdl_wait();
     if ((int)blockIdx.x >= p.main_ctas) {
         // Fused front of a few-token step: the CTAs past the score grid do
         // step 1 (ring write + window indices, then the latent groups).
@@ -610,7 +614,19 @@ int indexer_mxf4_launch(const uint16_t* q_idx, const uint8_t* k_codes, const uin
                                          (int)SMEM_BYTES),
                     "indexer mxf4 kernel attributes");
     if (rc) return rc;
-    indexer_mxf4_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(mq, mk, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    rc = cuda_check(cudaLaunchKernelEx(&cfg, indexer_mxf4_kernel, mq, mk, p),
+                    "ds41_indexer_topk_mxf4: scores kernel");
+    if (rc) return rc;
     return launch_check("ds41_indexer_topk_mxf4: scores kernel");
 }
 
