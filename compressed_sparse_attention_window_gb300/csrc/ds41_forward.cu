@@ -273,6 +273,12 @@ extern "C" int ds41_csa_forward_fp4(const ds41_bf16* q, const ds41_bf16* kv, ds4
 // cudaMemcpyAsync.
 // ---------------------------------------------------------------------------
 __global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n16) {
+    // launched with programmatic stream serialization: the kernel after this
+    // one may start launching now, and this one waits for the kernel before
+    // it (whose output it may read, or whose inputs it may overwrite) before
+    // its first memory access
+    pdl_trigger();
+    pdl_wait();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
          i += (int64_t)gridDim.x * blockDim.x)
         dst[i] = src[i];
@@ -301,8 +307,20 @@ static int host_copy(void* dst, const void* src, size_t bytes, bool h2d, cudaStr
         const int64_t n16 = (int64_t)(bytes / 16);
         const int64_t cap = 4 * (int64_t)device_sm_count();
         const int64_t blocks = (n16 + 255) / 256;
-        copy16_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, st>>>(
-            static_cast<const uint4*>(s), static_cast<uint4*>(d), n16);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(blocks < cap ? blocks : cap));
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const int rc = cuda_check(cudaLaunchKernelEx(&cfg, copy16_kernel,
+                                                     static_cast<const uint4*>(s),
+                                                     static_cast<uint4*>(d), n16),
+                                  what);
+        if (rc) return rc;
         return launch_check(what);
     }
     return cuda_check(cudaMemcpyAsync(dst, src, bytes,
