@@ -76,13 +76,15 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     int64_t n_c, int64_t ratio, int64_t start_pos, bool fill_hidden, int ymain, RingArgs ring,
     LatentArgs lat) {
     constexpr int CPR = DI / 8;  // 16-byte chunks per row
-    pdl_trigger();  // the next kernel may start launching (it waits for this one)
     // Every input (and the ring and cache this kernel writes) may belong to the
     // kernel before, e.g. the previous step's attention reading the ring: this
     // kernel is launched with programmatic stream serialization, so it waits
     // for that kernel here, before its first memory access, and only its
-    // launch overlaps it.
+    // launch overlaps it.  Only then may the next kernel start launching: the
+    // decode attention reads q (an input of the step) before its own wait, so
+    // everything before this kernel must be complete when it launches.
     pdl_wait();
+    pdl_trigger();
     if ((int)blockIdx.y >= ymain) {
         // Fused front of a few-token step: the CTAs past the score grid do
         // step 1 (ring write + window indices, then the latent groups).

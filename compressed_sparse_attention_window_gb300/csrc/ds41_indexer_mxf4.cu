@@ -231,11 +231,13 @@ __device__ __forceinline__ void load_sfa(const Params& p, int64_t r0, int lane, 
 __global__ void __launch_bounds__(THREADS, 1)
     indexer_mxf4_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k, const Params p) {
-    pdl_trigger();  // a dependent kernel may start launching (it waits for this one)
     // launched with programmatic stream serialization: the kernel before (the
     // previous step's attention, which reads the ring this kernel writes) is
-    // waited for here, before the first memory access
+    // waited for here, before the first memory access; only then may a
+    // dependent kernel start launching (the decode attention reads q before
+    // its own wait, so everything before this kernel must be complete)
     pdl_wait();
+    pdl_trigger();
     if ((int)blockIdx.x >= p.main_ctas) {
         // Fused front of a few-token step: the CTAs past the score grid do
         // step 1 (ring write + window indices, then the latent groups).
