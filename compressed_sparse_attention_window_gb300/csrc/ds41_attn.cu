@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) sparse_attn_kernel(
     const float* __restrict__ sink, float scale_log2, uint16_t* __restrict__ o,
     float* __restrict__ lse, int nh, int chunks_per_split, float* __restrict__ part_o,
     float2* __restrict__ part_ml, unsigned int* status) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
+    pdl_trigger();
     using SM = AttnSmem<HD>;
     constexpr int CPR = SM::CPR;
     constexpr int HALF = HD / 2;
@@ -289,6 +291,8 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict
                                                          uint16_t* __restrict__ o,
                                                          float* __restrict__ lse, int nh,
                                                          int splits) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
+    pdl_trigger();
     const int64_t t = blockIdx.x;
     const int h = blockIdx.y;
     const float sk = sink[h] * LOG2E;
@@ -1089,14 +1093,14 @@ static int launch_attn(const AttnPlan& p, const uint16_t* q, const uint16_t* row
     float* part_o = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
     float2* part_ml = p.splits > 1 ? reinterpret_cast<float2*>(ws + p.part_o_bytes) : nullptr;
     dim3 grid((unsigned)m, (unsigned)p.splits, (unsigned)p.head_groups);
-    kern<<<grid, ATT_THREADS, smem, st>>>(q, rows_a, n_a, rows_b, n_c, idx, (int)K, sink,
-                                          scale * LOG2E, o, lse, (int)nh, p.chunks_per_split,
-                                          part_o, part_ml, status);
-    int rc = launch_check("ds41_sparse_attn_sink_fwd: attention kernel");
+    int rc = launch_pdl(kern, grid, dim3(ATT_THREADS), smem, st,
+                        "ds41_sparse_attn_sink_fwd: attention kernel", q, rows_a, n_a, rows_b, n_c,
+                        idx, (int)K, sink, scale * LOG2E, o, lse, (int)nh, p.chunks_per_split,
+                        part_o, part_ml, status);
     if (rc || p.splits == 1) return rc;
-    attn_merge_kernel<HD><<<dim3((unsigned)m, (unsigned)nh), 128, 0, st>>>(
-        part_o, part_ml, sink, o, lse, (int)nh, p.splits);
-    return launch_check("ds41_sparse_attn_sink_fwd: merge kernel");
+    return launch_pdl(attn_merge_kernel<HD>, dim3((unsigned)m, (unsigned)nh), dim3(128), 0, st,
+                      "ds41_sparse_attn_sink_fwd: merge kernel", (const float*)part_o,
+                      (const float2*)part_ml, sink, o, lse, (int)nh, p.splits);
 }
 
 }  // namespace ds41

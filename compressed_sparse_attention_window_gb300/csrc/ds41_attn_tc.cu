@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap map_ad,
                    const __grid_constant__ CUtensorMap map_bd,
                    const Params p) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -957,6 +958,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    // a long persistent kernel: its dependents may start launching once this
+    // CTA's work is done (an early trigger would keep their CTAs resident and
+    // waiting beside this kernel for its whole run)
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1012,6 +1017,10 @@ int attn_tc_launch(const uint16_t* q, const uint16_t* rows_a, int64_t n_a, const
                                          (int)SMEM_BYTES),
                     "ds41_sparse_attn_sink_fwd: tensor-core kernel attributes");
     if (rc) return rc;
+    // A plain launch: launched programmatically behind the top-k kernel, its
+    // CTAs (a whole SM's shared memory each) wait resident beside that kernel,
+    // and the step measured slower (prefill 704 -> 724 us, chunked prefill
+    // 234 -> 255 us).  Its own trigger still lets the next kernel launch early.
     kern<<<grid, THREADS, SMEM_BYTES, st>>>(mq, mad, mbd, p);
     return launch_check("ds41_sparse_attn_sink_fwd: tensor-core kernel");
 }

@@ -484,6 +484,8 @@ extern "C" int ds41_host_step_destroy(ds41_host_step* h) {
 // idx row t = the window indices of t, then the shared picks of t.
 __global__ void merge_shared_kernel(const int32_t* win_idx, const int32_t* cidx, int32_t* idx,
                                     int64_t m, int win, int ctopk) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
+    pdl_trigger();
     const int K = win + ctopk;
     const int64_t total = m * K;
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
@@ -534,10 +536,11 @@ extern "C" int ds41_csa_forward_reuse(const ds41_bf16* q, const ds41_bf16* kv, d
         const int64_t total = m * (win + ctopk);
         const int threads = 256;
         const int64_t blocks = (total + threads - 1) / threads;
-        merge_shared_kernel<<<(unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0,
-                              (cudaStream_t)stream>>>(win_idx, cidx, idx, m, (int)win,
-                                                      (int)ctopk);
-        if ((rc = launch_check(name))) return rc;
+        if ((rc = launch_pdl(merge_shared_kernel,
+                             dim3((unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16)),
+                             dim3(threads), 0, (cudaStream_t)stream, name,
+                             (const int32_t*)win_idx, cidx, idx, m, (int)win, (int)ctopk)))
+            return rc;
         att_idx = idx;
     }
     const ds41_bf16* rows_a_used = start_pos == 0 ? kv : (m == 1 ? ring : rows_a);

@@ -237,7 +237,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // dependent kernel start launching (the decode attention reads q before
     // its own wait, so everything before this kernel must be complete)
     pdl_wait();
-    pdl_trigger();
+    const bool front = p.ring.ring != nullptr;  // the fused few-token step: a short kernel
+    if (front) pdl_trigger();
     if ((int)blockIdx.x >= p.main_ctas) {
         // Fused front of a few-token step: the CTAs past the score grid do
         // step 1 (ring write + window indices, then the latent groups).
@@ -558,6 +559,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    // many tokens: a long persistent kernel, whose dependents may start
+    // launching once this CTA's work is done
+    if (!front) pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

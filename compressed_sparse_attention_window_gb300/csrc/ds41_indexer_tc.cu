@@ -137,6 +137,7 @@ __device__ __forceinline__ void quant_q_inplace(uint8_t* qst, int rows, int tid,
 __global__ void __launch_bounds__(THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k, const Params p) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -353,6 +354,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    // a long persistent kernel: its dependents may start launching once this
+    // CTA's work is done (an early trigger would keep their CTAs resident and
+    // waiting beside this kernel for its whole run)
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -395,8 +400,8 @@ int indexer_tc_launch(const uint16_t* q_idx, const uint16_t* kq, const float* w,
                                          (int)SMEM_BYTES),
                     "ds41_indexer_topk: tensor-core kernel attributes");
     if (rc) return rc;
-    indexer_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(mq, mk, p);
-    return launch_check("ds41_indexer_topk: tensor-core scores kernel");
+    return launch_pdl(indexer_tc_kernel, dim3((unsigned)grid), dim3(THREADS), SMEM_BYTES, st,
+                      "ds41_indexer_topk: tensor-core scores kernel", mq, mk, p);
 }
 
 }  // namespace ds41

@@ -35,6 +35,8 @@ namespace ds41 {
 // start_pos + t with the angle negated.
 __global__ void inv_rope_kernel(uint16_t* o, const float2* fc, int64_t m, int nh, int hd, int rd,
                                 int64_t start_pos) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
+    pdl_trigger();
     const int half = rd / 2;
     const int64_t total = m * nh * half;
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
@@ -89,6 +91,8 @@ __device__ __forceinline__ void dot8(float& acc, uint4 w, uint4 x) {
 
 template <int MT>
 __global__ void __launch_bounds__(GEMV_THREADS) proj_gemv_kernel(Lin a, int t0) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * GEMV_THREADS + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * GEMV_THREADS) >> 5;
@@ -176,6 +180,7 @@ template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     proj_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                    const __grid_constant__ CUtensorMap map_x, const Params p) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -304,6 +309,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    // a long persistent kernel: its dependents may start launching once this
+    // CTA's work is done (an early trigger would keep their CTAs resident and
+    // waiting beside this kernel for its whole run)
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -332,8 +341,8 @@ int launch_tc(const Lin& a, int sms, unsigned int* status, cudaStream_t st) {
                                          (int)Cfg<BN>::SMEM),
                     "ds41_attn_out_proj: tensor-core kernel attributes");
     if (rc) return rc;
-    proj_tc_kernel<BN><<<grid, THREADS, Cfg<BN>::SMEM, st>>>(mw, mx, p);
-    return launch_check("ds41_attn_out_proj: tensor-core projection");
+    return launch_pdl(proj_tc_kernel<BN>, dim3((unsigned)grid), dim3(THREADS), Cfg<BN>::SMEM, st,
+                      "ds41_attn_out_proj: tensor-core projection", mw, mx, p);
 }
 
 }  // namespace pj
@@ -366,11 +375,13 @@ static int run_lin(const Lin& a, cudaStream_t st) {
     // tokens in chunks of up to 8: the smallest kernel that covers the chunk
     for (int t0 = 0; t0 < a.m; t0 += 8) {
         const int rem = a.m - t0;
-        if (rem > 4) proj_gemv_kernel<8><<<(unsigned)blocks, GEMV_THREADS, 0, st>>>(a, t0);
-        else if (rem > 2) proj_gemv_kernel<4><<<(unsigned)blocks, GEMV_THREADS, 0, st>>>(a, t0);
-        else if (rem > 1) proj_gemv_kernel<2><<<(unsigned)blocks, GEMV_THREADS, 0, st>>>(a, t0);
-        else proj_gemv_kernel<1><<<(unsigned)blocks, GEMV_THREADS, 0, st>>>(a, t0);
-        if (int rc = launch_check("ds41_attn_out_proj: projection")) return rc;
+        auto kern = rem > 4 ? proj_gemv_kernel<8>
+                    : rem > 2 ? proj_gemv_kernel<4>
+                    : rem > 1 ? proj_gemv_kernel<2>
+                              : proj_gemv_kernel<1>;
+        if (int rc = launch_pdl(kern, dim3((unsigned)blocks), dim3(GEMV_THREADS), 0, st,
+                                "ds41_attn_out_proj: projection", a, t0))
+            return rc;
     }
     return DS41_OK;
 }
@@ -411,10 +422,12 @@ extern "C" int ds41_attn_out_proj(ds41_bf16* o, const float* freqs_cis, int64_t 
         const int64_t pairs = m * nh * (rd / 2);
         const int threads = 256;
         const int64_t blocks = (pairs + threads - 1) / threads;
-        inv_rope_kernel<<<(unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16), threads, 0, st>>>(
-            reinterpret_cast<uint16_t*>(o), reinterpret_cast<const float2*>(freqs_cis), m, (int)nh,
-            (int)hd, (int)rd, start_pos);
-        if (int rc = launch_check(name)) return rc;
+        if (int rc = launch_pdl(inv_rope_kernel,
+                                dim3((unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16)),
+                                dim3(threads), 0, st, name, reinterpret_cast<uint16_t*>(o),
+                                reinterpret_cast<const float2*>(freqs_cis), m, (int)nh, (int)hd,
+                                (int)rd, start_pos))
+            return rc;
     }
     const int gw = (int)((nh * hd) / groups), gr = (int)(groups * o_rank);
     // og[t, g*o_rank + r] = bf16(sum_i o[t, g*gw + i] wo_a[g*o_rank + r, i])

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) fp4_quant_kernel(const uint4* __restrict_
                                                         uint32_t* __restrict__ codes,
                                                         uint8_t* __restrict__ scales,
                                                         int64_t n8) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
+    pdl_trigger();
     constexpr int LANES = BLOCK / 8;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     // Threads past the end still take part in the shuffles (n8 is a multiple
@@ -73,10 +75,9 @@ static int quant_launch(const ds41_bf16* x, ds41_bf16* y, uint8_t* codes, uint8_
     if (n8 == 0) return DS41_OK;
     const int threads = 256;
     const int64_t blocks = (n8 + threads - 1) / threads;
-    fp4_quant_kernel<BLOCK, E4M3><<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
-        reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(y),
-        reinterpret_cast<uint32_t*>(codes), scales, n8);
-    return launch_check(name);
+    return launch_pdl(fp4_quant_kernel<BLOCK, E4M3>, dim3((unsigned)blocks), dim3(threads), 0,
+                      (cudaStream_t)stream, name, reinterpret_cast<const uint4*>(x),
+                      reinterpret_cast<uint4*>(y), reinterpret_cast<uint32_t*>(codes), scales, n8);
 }
 
 // ---------------------------------------------------------------------------

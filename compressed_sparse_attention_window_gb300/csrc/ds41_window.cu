@@ -11,12 +11,16 @@ namespace ds41 {
 
 // One thread per work item (see ring_write_item).
 __global__ void __launch_bounds__(256) ring_write_kernel(RingArgs a) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
+    pdl_trigger();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < a.total()) ring_write_item(a, i);
 }
 
 // One CTA per completed group, one lane per 8 dims (whole warps).
 __global__ void latent_write_kernel(LatentArgs a) {
+    pdl_wait();     // the kernel before may still be running (programmatic launch)
+    pdl_trigger();
     latent_write_item(a, blockIdx.x, threadIdx.x);
 }
 
@@ -72,9 +76,8 @@ extern "C" int ds41_window_ring_write(const ds41_bf16* kv, ds41_bf16* ring, ds41
                 reinterpret_cast<uint4*>(rows_a), win_idx, m, hd / 8, win, start_pos, chunk};
     const int64_t total = ra.total();
     const int threads = 256;
-    ring_write_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0,
-                        (cudaStream_t)stream>>>(ra);
-    return launch_check(name);
+    return launch_pdl(ring_write_kernel, dim3((unsigned)((total + threads - 1) / threads)),
+                      dim3(threads), 0, (cudaStream_t)stream, name, ra);
 }
 
 extern "C" int ds41_compress_latent_write(const ds41_bf16* latent, const float* freqs_cis,
@@ -111,6 +114,6 @@ extern "C" int ds41_compress_latent_write(const ds41_bf16* latent, const float* 
     LatentArgs la{reinterpret_cast<const uint4*>(latent), reinterpret_cast<const float2*>(freqs_cis),
                   reinterpret_cast<uint4*>(cache), reinterpret_cast<uint32_t*>(cache_codes),
                   cache_scales, (int)hd, (int)rd, (int)G, start_pos / ratio, ratio};
-    latent_write_kernel<<<(unsigned)G, threads, 0, (cudaStream_t)stream>>>(la);
-    return launch_check(name);
+    return launch_pdl(latent_write_kernel, dim3((unsigned)G), dim3(threads), 0,
+                      (cudaStream_t)stream, name, la);
 }
