@@ -332,6 +332,23 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
 }
+// The shared::cluster address of `p` (this CTA's shared memory) in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+// One bulk copy of `bytes` (a multiple of 16, both ends 16-byte aligned) from
+// this CTA's shared memory into another CTA's, completing `bytes`
+// transactions on the mbarrier at cluster address `bar` (in the receiver).
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];\n" ::"r"(dst),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
 
 // The selection of dec_topk when every visible score fits in registers
 // (vis <= TKD_CAP, at most TKD_CAP / NTH per thread): each CTA ranks all of
@@ -590,7 +607,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     uint16_t* qs = reinterpret_cast<uint16_t*>(smem);
     uint16_t* kvs = reinterpret_cast<uint16_t*>(smem + SM::q_bytes);
     float* sp = reinterpret_cast<float*>(smem + SM::q_bytes + 2 * SM::kv_bytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bar_off);  // q, kv0, kv1
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bar_off);  // q, kv0, kv1, exchange
     int* vflag = reinterpret_cast<int*>(smem + SM::bar_off + 4 * 8);
     float* stat = reinterpret_cast<float*>(vflag + 2 * DEC_NC);  // [2][16]: m then l
     int* sidx = reinterpret_cast<int*>(stat + 2 * DEC_HEADS);      // [DEC_STAGE]
@@ -614,7 +631,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     // waits for this one to complete before it touches memory
     pdl_trigger();
     if (tid == 0) {
-        for (int i = 0; i < 3; i++) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 4; i++) mbar_init(&bars[i], 1);  // q, kv0, kv1, cluster exchange
         mbar_init_fence();
     }
     __syncthreads();
@@ -874,15 +891,19 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     // Push this CTA's (m, l) into every CTA of the cluster and each slice of
     // its unnormalised O, as bf16 pairs (half the exchanged bytes; the same
     // relative rounding as the bf16 output), into the CTA that reduces those
-    // columns; after one barrier every read is local.  Both are staged in this
-    // CTA's shared memory first ((m, l) in stat, the O slices in sp, laid out
-    // as the receivers' blocks) so that every remote store moves 16 bytes.
+    // columns; every read afterwards is local.  Both are staged in this CTA's
+    // shared memory first ((m, l) in stat, the O slices in sp, laid out as the
+    // receivers' blocks) and moved by bulk copies, two per receiver, that
+    // complete on the receiver's exchange barrier: each CTA waits only for the
+    // bytes it receives.  A sender cannot see when its copies have read the
+    // staging, so sp and stat stay untouched until the closing cluster barrier,
+    // which every CTA passes only once all copies have landed.
     const int cols = HD / CL;
     float* spush = reinterpret_cast<float*>(smem + SM::spush_off);    // [16 ranks][2][16]
     uint32_t* opush = reinterpret_cast<uint32_t*>(smem + SM::xch_off);  // [CL ranks][16][cols/2]
     uint32_t* ostage = reinterpret_cast<uint32_t*>(sp);                 // [CL][16][cols/2]
     static_assert((size_t)DEC_HEADS * HD * 2 <= SM::sp_bytes && (SM::bar_off + 32 + 2 * DEC_NC * 4) % 16 == 0,
-                  "O staging; (m, l) staging read as 16-byte pieces");
+                  "O staging; (m, l) staging moved as 16-byte multiples");
     if (warp == 0 && (lane & 3) == 0) {
         stat[ra] = mrow[0];
         stat[rb] = mrow[1];
@@ -897,28 +918,26 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         dst[ra * (cols / 2) + cc] = pack_bf16x2(oacc[j][0], oacc[j][1]);
         dst[rb * (cols / 2) + cc] = pack_bf16x2(oacc[j][2], oacc[j][3]);
     }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // staged bytes, for the copies
     __syncthreads();
-    cluster_wait();
-    {
-        const int per_q = 2 * cols;  // 16-byte pieces of one receiver's block
-        for (int c = tid; c < CL * per_q; c += NTH) {
-            const int qd = c / per_q;
-            uint4* dst = reinterpret_cast<uint4*>(cluster.map_shared_rank(opush, qd)) +
-                         rank * per_q + (c - qd * per_q);
-            *dst = reinterpret_cast<const uint4*>(ostage)[c];
-        }
-        for (int c = tid; c < CL * 8; c += NTH) {
-            const int qd = c >> 3;
-            uint4* dst = reinterpret_cast<uint4*>(cluster.map_shared_rank(spush, qd) + rank * 2 * DEC_HEADS) +
-                         (c & 7);
-            *dst = reinterpret_cast<const uint4*>(stat)[c & 7];
+    cluster_wait();  // every CTA of the cluster has started: its exchange barrier is initialised
+    if (tid == 0) {
+        const uint32_t oblk = (uint32_t)DEC_HEADS * (cols / 2) * 4;  // one receiver's O block
+        const uint32_t mlb = 2 * DEC_HEADS * 4;                      // (m, l) of one sender
+        mbar_arrive_expect_tx(&bars[3], (uint32_t)CL * (oblk + mlb));
+        for (int qd = 0; qd < CL; qd++) {
+            const uint32_t rbar = cluster_addr(&bars[3], qd);
+            bulk_s2cluster(cluster_addr(opush, qd) + (uint32_t)rank * oblk, ostage + qd * (oblk / 4),
+                           oblk, rbar);
+            bulk_s2cluster(cluster_addr(spush, qd) + (uint32_t)rank * mlb, stat, mlb, rbar);
         }
     }
-    cluster.sync();
+    if (!mbar_wait(&bars[3], 0, kWaitPolls)) raise_status(status, DS41_E_TIMEOUT);
+    cluster_arrive_relaxed();  // every block this CTA receives has landed
 
     // Weights e^{m_r - M} / L for every (head, rank): one thread per pair,
     // the max and the sum over the ranks by shuffles within 16-lane groups.
-    float* wts = sp;  // [16 ranks][16 heads]
+    float* wts = reinterpret_cast<float*>(kvs);  // [16 ranks][16 heads]; the row buffers are idle now
     for (int pidx = tid; pidx < DEC_HEADS * 16; pidx += NTH) {
         const int hh = pidx >> 4, r = pidx & 15;
         const int h = h0 + hh;
@@ -966,8 +985,9 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
             *reinterpret_cast<uint2*>(o + (t * nh + h) * (int64_t)HD + c0 + cl4) = packed;
         }
     }
-    // no CTA reads another's shared memory after the barrier above, so each
-    // may exit on its own
+    // no CTA leaves while a copy into or out of its shared memory may be in
+    // flight: each has arrived once its own blocks landed
+    cluster_wait();
 }
 
 struct AttnPlan {
