@@ -631,7 +631,10 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     // waits for this one to complete before it touches memory
     pdl_trigger();
     if (tid == 0) {
-        for (int i = 0; i < 4; i++) mbar_init(&bars[i], 1);  // q, kv0, kv1, cluster exchange
+        mbar_init(&bars[0], 1);   // q
+        mbar_init(&bars[1], NW);  // kv buffer 0: one arrival a warp (load_chunk)
+        mbar_init(&bars[2], NW);  // kv buffer 1
+        mbar_init(&bars[3], 1);   // cluster exchange
         mbar_init_fence();
     }
     __syncthreads();
@@ -662,55 +665,49 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
         for (int j = tid; j < nst; j += NTH) sidx[j] = irow[j0 + j];
     }
     __syncthreads();
-    // warp 0: one bulk copy per valid row of the chunk (row r by lane r % 32);
-    // invalid rows are zeroed (their scores are masked, and 0 * row must stay
-    // finite in P*V)
-    constexpr int RPL = (DEC_NC + 31) / 32;  // rows per lane
+    // Every warp copies its own share of the chunk's rows, one bulk copy per
+    // valid row (rows w * RPW .. w * RPW + RPW - 1 of the chunk, one a lane):
+    // a warp issues its copies one after another (a microbenchmark: about
+    // 40 ns apart), so spreading them over the warps lands the chunk sooner.
+    // The chunk's barrier takes one arrival a warp, each carrying that warp's
+    // byte count, so it cannot complete before every warp has announced its
+    // bytes.  Invalid rows are zeroed (their scores are masked, and 0 * row
+    // must stay finite in P*V).
+    constexpr int RPW = (DEC_NC + NW - 1) / NW;  // rows per warp
+    static_assert(RPW <= 32, "one row a lane");
     auto load_chunk = [&](int chunk, int buf) {
-        int64_t vr[RPL];
-        bool okr[RPL];
-        uint32_t nok = 0, npk = 0;
-#pragma unroll
-        for (int i = 0; i < RPL; i++) {
-            const int r = lane + 32 * i;
-            const int j = j0 + chunk * DEC_NC + r;
-            const bool in = r < DEC_NC && j < j1;
-            int64_t v = -1;
-            if (in) v = (j - j0 < nst) ? sidx[j - j0] : irow[j];
-            const bool ok = v >= 0 && v < n_rows;
-            if (in && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
-            nok += __popc(__ballot_sync(0xffffffffu, ok));
-            npk += __popc(__ballot_sync(0xffffffffu, ok && packed && v >= n_a));
-            vr[i] = v;
-            okr[i] = ok;
-        }
+        const int r = warp * RPW + lane;
+        const bool mine = lane < RPW && r < DEC_NC;
+        const int j = j0 + chunk * DEC_NC + r;
+        const bool in = mine && j < j1;
+        int64_t v = -1;
+        if (in) v = (j - j0 < nst) ? sidx[j - j0] : irow[j];
+        const bool ok = v >= 0 && v < n_rows;
+        if (in && (v < -1 || v >= n_rows)) raise_status(status, DS41_E_INDEX);
+        const uint32_t nok = __popc(__ballot_sync(0xffffffffu, ok));
+        const uint32_t npk = __popc(__ballot_sync(0xffffffffu, ok && packed && v >= n_a));
         // order this buffer's earlier generic-proxy writes before the copies
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         if (lane == 0) mbar_arrive_expect_tx(&bars[1 + buf], (nok - npk) * ROWB + npk * PKB);
         __syncwarp();
-#pragma unroll
-        for (int i = 0; i < RPL; i++) {
-            const int r = lane + 32 * i;
-            if (r >= DEC_NC) continue;
-            uint16_t* dst = kvs + buf * (DEC_NC * RS) + r * RS;
-            int flag = 0;
-            if (okr[i]) {
-                const int64_t v = vr[i];
-                if (packed && v >= n_a) {
-                    uint8_t* d8 = reinterpret_cast<uint8_t*>(dst) + PKO;
-                    bulk_g2s(d8, pk.codes + (v - n_a) * (HD / 2), HD / 2, &bars[1 + buf]);
-                    bulk_g2s(d8 + HD / 2, pk.scales + (v - n_a) * (HD / 16), HD / 16, &bars[1 + buf]);
-                    flag = 2;
-                } else {
-                    const uint16_t* src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
-                    bulk_g2s(dst, src, ROWB, &bars[1 + buf]);
-                    flag = 1;
-                }
+        if (!mine) return;
+        uint16_t* dst = kvs + buf * (DEC_NC * RS) + r * RS;
+        int flag = 0;
+        if (ok) {
+            if (packed && v >= n_a) {
+                uint8_t* d8 = reinterpret_cast<uint8_t*>(dst) + PKO;
+                bulk_g2s(d8, pk.codes + (v - n_a) * (HD / 2), HD / 2, &bars[1 + buf]);
+                bulk_g2s(d8 + HD / 2, pk.scales + (v - n_a) * (HD / 16), HD / 16, &bars[1 + buf]);
+                flag = 2;
             } else {
-                for (int c = 0; c < HD / 8; c++) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+                const uint16_t* src = (v < n_a) ? rows_a + v * HD : rows_b + (v - n_a) * HD;
+                bulk_g2s(dst, src, ROWB, &bars[1 + buf]);
+                flag = 1;
             }
-            vflag[buf * DEC_NC + r] = flag;
+        } else {
+            for (int c = 0; c < HD / 8; c++) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
         }
+        vflag[buf * DEC_NC + r] = flag;
     };
     // Packed rows of a landed chunk -> bf16 in place, a warp per row: lane b
     // holds block b (16 values: 8 code bytes, one scale byte) in registers
@@ -764,10 +761,10 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
     const int ra = lane >> 2, rb = ra + 8;
     bool failed = false;
 
-    if (warp == 0 && nchunks > 0) load_chunk(0, 0);
+    if (nchunks > 0) load_chunk(0, 0);
     for (int chunk = 0; chunk < nchunks; chunk++) {
         const int buf = chunk & 1;
-        if (warp == 0 && chunk + 1 < nchunks) load_chunk(chunk + 1, buf ^ 1);
+        if (chunk + 1 < nchunks) load_chunk(chunk + 1, buf ^ 1);
         if (chunk == 0 && !mbar_wait(&bars[0], 0, kWaitPolls)) failed = true;
         if (!mbar_wait(&bars[1 + buf], (chunk >> 1) & 1, kWaitPolls)) failed = true;
         __syncthreads();  // zero-filled rows and flags of warp 0 are visible
