@@ -516,15 +516,8 @@ __device__ void dec_topk(const DecTopk& tk, int64_t t, int K, int j0, int j1, in
     dec_topk_local<NTH>(tk, t, (int)vis, kk, win, j0, j1, sidx, area, orow, write_idx);
 }
 
-// Few-token (decode) path.  A cluster of CL CTAs shares one (token, group of
-// 16 heads); CTA r of the cluster takes slice r of the index row.  Four warps
-// split the head dim: for S each warp reduces over its quarter of hd and the
-// four partials are summed in a fixed order by every warp, so all warps hold
-// bit-identical scores and softmax statistics; for P*V each warp owns a
-// quarter of the output columns.  At the end the CTAs exchange (m, l) and
-// their unnormalised O through distributed shared memory; CTA r reduces the
-// r-th slice of the columns over the cluster, adds the sink and writes o.
-// No scratch memory and no second launch.
+// Few-token (decode) path: constants and the shared memory map of
+// sparse_attn_decode_kernel below.
 // ---------------------------------------------------------------------------
 constexpr int DEC_HEADS = 16;
 constexpr int DEC_NC = 48;  // gathered rows per chunk: a 16-CTA slice of 640 rows (40) in one chunk
@@ -567,17 +560,18 @@ struct DecSmem {
 };
 
 // Few-token (decode) path.  A cluster of CL CTAs shares one (token, group of
-// 16 heads); CTA r of the cluster takes slice r of the index row.  Warp 0
-// moves data with TMA bulk copies (one per 1 KiB row) completing on
-// mbarriers: the 16 q rows, then chunks of 32 gathered rows, double-buffered.
-// The warps split the head dim: for S each warp reduces over its slice and the
-// partials are summed in a fixed order by every warp, so all warps hold
-// bit-identical scores and softmax statistics; for P*V each warp owns a slice
-// of the output columns.  At the end each CTA pushes its (m, l) and the
-// slices of its unnormalised O into the CTAs that reduce them (distributed
-// shared memory); CTA r reduces the r-th slice of the columns over the
-// cluster, adds the sink and writes o.  No scratch memory and no second
-// launch.  In the fused step every CTA first ranks the scores itself (up to
+// 16 heads); CTA r of the cluster takes slice r of the index row.  Rows move
+// by TMA bulk copies (one per 1 KiB row) completing on mbarriers: the 16 q
+// rows, then chunks of DEC_NC gathered rows, double-buffered, each warp
+// copying its own share of a chunk.  The warps split the head dim for S (each
+// reduces over its slice of hd); every score is then summed once over the
+// partials in a fixed order, so all warps read the same scores and derive the
+// same softmax statistics; for P*V each warp owns a slice of the output
+// columns.  At the end each CTA pushes its (m, l) and the slices of its
+// unnormalised O into the CTAs that reduce them (bulk copies into
+// distributed shared memory); CTA r reduces the r-th slice of the columns
+// over the cluster, adds the sink and writes o.  No scratch memory and no
+// second launch.  In the fused step every CTA first ranks the scores itself (up to
 // TKD_CAP of them) and keeps the picks of its own slice.  PACKED: the
 // compressed rows may arrive packed (e2m1 codes + e4m3 scales) and are
 // expanded in shared memory; a separate instantiation, so that the code runs
@@ -791,7 +785,7 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
                 mma_bf16(sacc[2 * jj + 1], a0, a1, a2, a3, b2, b3);
             }
         }
-        // partial scores of the NW slices of hd, summed in a fixed order by all
+        // partial scores of the NW slices of hd, one block a warp
         float* mine = sp + warp * (DEC_HEADS * DEC_SPS);
 #pragma unroll
         for (int j = 0; j < NCT; j++) {
@@ -800,24 +794,28 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
             *reinterpret_cast<float2*>(mine + rb * DEC_SPS + col) = make_float2(sacc[j][2], sacc[j][3]);
         }
         __syncthreads();
+        // every score summed once over the warps' partials, in the warps'
+        // order, then scaled (or masked) in place of warp 0's block; every
+        // warp then reads the same final scores (each warp summing all the
+        // partials itself read eight times the bytes)
+        for (int e = tid; e < DEC_HEADS * DEC_NC; e += NTH) {
+            const int h = e / DEC_NC, c = e - h * DEC_NC;
+            float x = sp[h * DEC_SPS + c];
+#pragma unroll
+            for (int w = 1; w < NW; w++) x += sp[w * DEC_HEADS * DEC_SPS + h * DEC_SPS + c];
+            sp[h * DEC_SPS + c] = vflag[buf * DEC_NC + c] != 0 ? x * scale_log2 : -INFINITY;
+        }
+        __syncthreads();
         float sv[NCT][4];
 #pragma unroll
         for (int j = 0; j < NCT; j++) {
             const int col = j * 8 + 2 * (lane & 3);
-            float2 xa = *reinterpret_cast<const float2*>(sp + ra * DEC_SPS + col);
-            float2 xb = *reinterpret_cast<const float2*>(sp + rb * DEC_SPS + col);
-#pragma unroll
-            for (int w = 1; w < NW; w++) {
-                const float2 ya = *reinterpret_cast<const float2*>(sp + w * DEC_HEADS * DEC_SPS + ra * DEC_SPS + col);
-                const float2 yb = *reinterpret_cast<const float2*>(sp + w * DEC_HEADS * DEC_SPS + rb * DEC_SPS + col);
-                xa.x += ya.x; xa.y += ya.y; xb.x += yb.x; xb.y += yb.y;
-            }
-            const bool v0 = vflag[buf * DEC_NC + col] != 0;
-            const bool v1 = vflag[buf * DEC_NC + col + 1] != 0;
-            sv[j][0] = v0 ? xa.x * scale_log2 : -INFINITY;
-            sv[j][1] = v1 ? xa.y * scale_log2 : -INFINITY;
-            sv[j][2] = v0 ? xb.x * scale_log2 : -INFINITY;
-            sv[j][3] = v1 ? xb.y * scale_log2 : -INFINITY;
+            const float2 xa = *reinterpret_cast<const float2*>(sp + ra * DEC_SPS + col);
+            const float2 xb = *reinterpret_cast<const float2*>(sp + rb * DEC_SPS + col);
+            sv[j][0] = xa.x;
+            sv[j][1] = xa.y;
+            sv[j][2] = xb.x;
+            sv[j][3] = xb.y;
         }
         float mx[2] = {mrow[0], mrow[1]};
 #pragma unroll
