@@ -332,23 +332,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
 }
-// The shared::cluster address of `p` (this CTA's shared memory) in CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, int rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-// One bulk copy of `bytes` (a multiple of 16, both ends 16-byte aligned) from
-// this CTA's shared memory into another CTA's, completing `bytes`
-// transactions on the mbarrier at cluster address `bar` (in the receiver).
-__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes,
-                                               uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-        "[%3];\n" ::"r"(dst),
-        "r"(smem_u32(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
 
 // The selection of dec_topk when every visible score fits in registers
 // (vis <= TKD_CAP, at most TKD_CAP / NTH per thread): each CTA ranks all of

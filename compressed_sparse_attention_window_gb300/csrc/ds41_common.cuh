@@ -288,6 +288,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 }
 constexpr uint32_t kWaitPolls = 1u << 22;  // bound of every mbarrier wait (~1 s)
 
+// The shared::cluster address of `p` (this CTA's shared memory) in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+// One bulk copy of `bytes` (a multiple of 16, both ends 16-byte aligned) from
+// this CTA's shared memory into another CTA's, completing `bytes`
+// transactions on the mbarrier at cluster address `bar` (in the receiver).
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];\n" ::"r"(dst),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // Raise a DS41_E_* code in the device status word (first error wins).
 __device__ __forceinline__ void raise_status(unsigned int* status, unsigned int code) {
     if (status) atomicCAS(status, 0u, code);

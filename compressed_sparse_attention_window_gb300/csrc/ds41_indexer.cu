@@ -687,19 +687,28 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_kernel(
 __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
     const uint16_t* __restrict__ scores, const int32_t* __restrict__ win_idx,
     int32_t* __restrict__ idx, int64_t n_c, int win, int ctopk, int64_t ratio, int64_t start_pos,
-    int64_t offset) {
+    int64_t offset, unsigned int* status) {
     namespace cg = cooperative_groups;
     constexpr int NW = TK_THREADS / 32;
+    constexpr uint32_t HB1 = 256 * 4;  // bytes a slice pushes in round 1 (its histogram)
+    constexpr uint32_t HB2 = 260 * 4;  // round 2: its histogram, then its count above bucket hb
     constexpr int KMAX = TK_SLICE_CAP / TK_THREADS;
     cg::cluster_group cl = cg::this_cluster();
     __shared__ __align__(16) int whist[NW][256];      // per-warp histograms
-    __shared__ __align__(16) int hist[256];           // this slice's pass-1 histogram
+    __shared__ __align__(16) int hist[256];           // this slice's pass-1 histogram (round 1's bytes)
     __shared__ __align__(16) int hpush1[TK_CL][256];  // every slice's pass-1 histogram (pushed)
-    __shared__ __align__(16) int hpush2[TK_CL][256];  // every slice's pass-2 histogram (pushed)
-    __shared__ int above[TK_CL];               // every slice's keys above bucket hb (pushed)
+    __shared__ __align__(16) int stage2[260];         // round 2's bytes: histogram, count above hb
+    __shared__ __align__(16) int hpush2[TK_CL][260];  // every slice's round-2 bytes (pushed)
+    __shared__ __align__(8) uint64_t xbar[2];         // the two exchange rounds
     __shared__ int ghist[256];
     __shared__ int wsum[64];
     __shared__ int sel[8];
+    if (threadIdx.x == 0) {
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
     asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");  // this CTA has started
     pdl_wait();  // the scores (and window indices) come from the previous kernel
     pdl_trigger();
@@ -754,7 +763,10 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
         if (e < n_mine) atomicAdd(&wh[key[e] >> 8], 1);
     __syncthreads();
     asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");  // every CTA has started
-    // sums of four bins a thread, pushed as 16-byte remote stores
+    // Sums of four bins a thread; the slice's histogram then goes to every
+    // CTA of the cluster by bulk copies that complete on the receiver's own
+    // round barrier, so each CTA waits only for the bytes it receives.  The
+    // staged bytes (hist, stage2) stay untouched until the closing barrier.
     if (tid < 64) {
         int4 v = make_int4(0, 0, 0, 0);
 #pragma unroll
@@ -765,10 +777,15 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
             *h = make_int4(0, 0, 0, 0);
         }
         *reinterpret_cast<int4*>(&hist[4 * tid]) = v;
-        for (int q = 0; q < TK_CL; q++)
-            reinterpret_cast<int4*>(cl.map_shared_rank(&hpush1[r][0], q))[tid] = v;
     }
-    cl.sync();  // every slice's histogram is in every CTA
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&xbar[0], TK_CL * HB1);
+        for (int q = 0; q < TK_CL; q++)
+            bulk_s2cluster(cluster_addr(&hpush1[r][0], q), hist, HB1, cluster_addr(&xbar[0], q));
+    }
+    if (!mbar_wait(&xbar[0], 0, kWaitPolls)) raise_status(status, DS41_E_TIMEOUT);
     for (int b = tid; b < 256; b += TK_THREADS) {
         int v = 0;
 #pragma unroll
@@ -788,7 +805,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
         int a = 0;
         for (int b = (int)hb + 1 + lane; b < 256; b += 32) a += hist[b];
         a = __reduce_add_sync(0xffffffffu, a);
-        if (lane < TK_CL) cl.map_shared_rank(above, lane)[r] = a;
+        if (lane == 0) *reinterpret_cast<int4*>(&stage2[256]) = make_int4(a, 0, 0, 0);
     }
     __syncthreads();
     if (tid < 64) {
@@ -798,10 +815,18 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
             const int4 x = *reinterpret_cast<const int4*>(&whist[w][4 * tid]);
             v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
         }
-        for (int q = 0; q < TK_CL; q++)
-            reinterpret_cast<int4*>(cl.map_shared_rank(&hpush2[r][0], q))[tid] = v;
+        *reinterpret_cast<int4*>(&stage2[4 * tid]) = v;
     }
-    cl.sync();  // every slice's low-byte histogram and above count are in every CTA
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&xbar[1], TK_CL * HB2);
+        for (int q = 0; q < TK_CL; q++)
+            bulk_s2cluster(cluster_addr(&hpush2[r][0], q), stage2, HB2, cluster_addr(&xbar[1], q));
+    }
+    if (!mbar_wait(&xbar[1], 0, kWaitPolls)) raise_status(status, DS41_E_TIMEOUT);
+    // every block this CTA receives has landed; no CTA leaves before all have
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
     for (int b = tid; b < 256; b += TK_THREADS) {
         int v = 0;
 #pragma unroll
@@ -820,7 +845,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
         for (int q = 0; q < r; q++) {
             int a = 0;
             for (int b = tl + 1 + lane; b < 256; b += 32) a += hpush2[q][b];
-            g += __reduce_add_sync(0xffffffffu, a) + above[q];
+            g += __reduce_add_sync(0xffffffffu, a) + hpush2[q][256];
             e += hpush2[q][tl];
         }
         if (lane == 0) {
@@ -868,6 +893,8 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
     }
     if (r == 0)
         for (int j = kk + tid; j < ctopk; j += TK_THREADS) out[win + j] = -1;
+    // no CTA leaves while a copy into or out of its shared memory may be in flight
+    asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1131,10 +1158,18 @@ int launch_topk(const uint16_t* scores, const int32_t* win_idx, int32_t* idx, in
         cfg.attrs = attr;
         cfg.numAttrs = na;
         const bool big = n_c > (int64_t)TK_CL * TK_SMALL;
-        rc = cuda_check(cudaLaunchKernelEx(&cfg, big ? topk_cluster_big_kernel : topk_cluster_kernel,
-                                           scores, win_idx, idx, n_c,
-                                           (int)win, (int)ctopk, ratio, start_pos, offset),
-                        "top-k cluster kernel");
+        if (big) {
+            unsigned int* status = nullptr;
+            if ((rc = status_word(&status))) return rc;
+            rc = cuda_check(cudaLaunchKernelEx(&cfg, topk_cluster_big_kernel, scores, win_idx, idx,
+                                               n_c, (int)win, (int)ctopk, ratio, start_pos, offset,
+                                               status),
+                            "top-k cluster kernel");
+        } else {
+            rc = cuda_check(cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, win_idx, idx, n_c,
+                                               (int)win, (int)ctopk, ratio, start_pos, offset),
+                            "top-k cluster kernel");
+        }
         if (rc) return rc;
         return launch_check("top-k cluster kernel");
     }
