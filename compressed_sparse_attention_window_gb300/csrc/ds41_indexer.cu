@@ -73,9 +73,11 @@ template <int DI, bool KQ_INLINE, bool NARROW>
 __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_src,
     const float* __restrict__ w, uint16_t* __restrict__ scores, int m, int Hi, int hpad, int TT,
-    int64_t n_c, int64_t ratio, int64_t start_pos, bool fill_hidden, int ymain, RingArgs ring,
-    LatentArgs lat) {
+    int64_t n_c, int64_t ratio, int64_t start_pos, bool fill_hidden, int ymain, int nkb,
+    RingArgs ring, LatentArgs lat) {
     constexpr int CPR = DI / 8;  // 16-byte chunks per row
+    // q rows and score columns held: the narrow form holds only the live half
+    constexpr int QN = NARROW ? IDX_N / 2 : IDX_N;
     // Every input (and the ring and cache this kernel writes) may belong to the
     // kernel before, e.g. the previous step's attention reading the ring: this
     // kernel is launched with programmatic stream serialization, so it waits
@@ -97,10 +99,12 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
         return;
     }
     extern __shared__ __align__(128) uint8_t smem[];
-    uint16_t* qs = reinterpret_cast<uint16_t*>(smem);                 // [IDX_N][DI]
-    uint16_t* ksb = qs + IDX_N * DI;                                   // 2 x [IDX_ROWS][DI]
-    float* cs = reinterpret_cast<float*>(ksb + 2 * IDX_ROWS * DI);    // [IDX_ROWS][IDX_N + 1]
-    float* wsm = cs + IDX_ROWS * (IDX_N + 1);                          // [IDX_N]
+    // nkb key buffers: 2, or 1 when every CTA takes at most one tile (the
+    // host launches a CTA per tile then, so more CTAs fit an SM)
+    uint16_t* qs = reinterpret_cast<uint16_t*>(smem);                 // [QN][DI]
+    uint16_t* ksb = qs + QN * DI;                                      // nkb x [IDX_ROWS][DI]
+    float* cs = reinterpret_cast<float*>(ksb + nkb * IDX_ROWS * DI);  // [IDX_ROWS][QN + 1]
+    float* wsm = cs + IDX_ROWS * (QN + 1);                             // [QN]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.x * TT;
@@ -110,7 +114,7 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     // cp.async (padding rows zero-filled), then quantised in place.  The
     // quantisation loop stays rolled: a decode call runs this code once per
     // SM, so compact code (fewer instruction-cache misses) beats unrolling.
-    for (int id = tid; id < IDX_N * CPR; id += IDX_THREADS) {
+    for (int id = tid; id < QN * CPR; id += IDX_THREADS) {
         const int n = id / CPR, c = id % CPR;
         const int tt = n / hpad, h = n % hpad;
         const bool live = tt < tcount && h < Hi;
@@ -139,10 +143,10 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     };
     for (int b = 0; b < 2; b++) {
         const int64_t tile = (int64_t)blockIdx.y + (int64_t)b * ymain;
-        if (tile < tiles_vis) fetch_k(tile, ksb + b * IDX_ROWS * DI);
+        if (b < nkb && tile < tiles_vis) fetch_k(tile, ksb + b * IDX_ROWS * DI);
         cp_async_commit();  // one group per buffer (empty when there is no such tile)
     }
-    for (int n = tid; n < IDX_N; n += IDX_THREADS) {
+    for (int n = tid; n < QN; n += IDX_THREADS) {
         const int tt = n / hpad, h = n % hpad;
         wsm[n] = (tt < tcount && h < Hi) ? w[(int64_t)(t0 + tt) * Hi + h] : 0.0f;
     }
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     // passes of the block: q8_chunk shuffles over the full warp, and the
     // padding rows past the live ones are zero (they stay zero)
     const int live_rows = (tcount - 1) * hpad + Hi;
-    const int q_iters = min(IDX_N * CPR,
+    const int q_iters = min(QN * CPR,
                             (live_rows * CPR + IDX_THREADS - 1) / IDX_THREADS * IDX_THREADS);
 #pragma unroll 1
     for (int id = tid; id < q_iters; id += IDX_THREADS) {
@@ -171,6 +175,7 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             }
             continue;
         }
+        if (it >= nkb && nkb == 1) break;  // one buffer: one tile a CTA (the host plan)
         uint16_t* ks = ksb + (it & 1) * IDX_ROWS * DI;
         cp_async_wait<1>();  // this thread's copies of this tile (the next may be in flight)
         __syncthreads();     // everyone's copies; previous tile's readers are done with cs
@@ -214,16 +219,16 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
         for (int j = 0; j < WN / 8; j++) {
             const int r = wr + (lane >> 2);
             const int col = wc + j * 8 + 2 * (lane & 3);
-            cs[r * (IDX_N + 1) + col] = acc[j][0];
-            cs[r * (IDX_N + 1) + col + 1] = acc[j][1];
-            cs[(r + 8) * (IDX_N + 1) + col] = acc[j][2];
-            cs[(r + 8) * (IDX_N + 1) + col + 1] = acc[j][3];
+            cs[r * (QN + 1) + col] = acc[j][0];
+            cs[r * (QN + 1) + col + 1] = acc[j][1];
+            cs[(r + 8) * (QN + 1) + col] = acc[j][2];
+            cs[(r + 8) * (QN + 1) + col + 1] = acc[j][3];
         }
         __syncthreads();  // cs written; every warp is done reading ks
         {
             // refill this buffer with the tile two after this one
             const int64_t next = tile + 2 * (int64_t)ymain;
-            if (next < tiles_vis) fetch_k(next, ks);
+            if (nkb == 2 && next < tiles_vis) fetch_k(next, ks);
             cp_async_commit();
         }
 
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
             uint16_t out = 0xff80u;  // -inf: not visible yet
             if (s < vis) {
-                const float* col = cs + r * (IDX_N + 1) + tt * hpad;
+                const float* col = cs + r * (QN + 1) + tt * hpad;
                 const float* wt = wsm + tt * hpad;
                 float a = 0.0f;
                 if (Hi == 64) {
@@ -932,22 +937,30 @@ static int launch_scores(const IndexerPlan& p, const uint16_t* q, const uint16_t
                          uint16_t* scores, int64_t m, int64_t Hi, int64_t n_c, int64_t ratio,
                          int64_t start_pos, bool fill_hidden, cudaStream_t st,
                          const RingArgs* ring = nullptr, const LatentArgs* lat = nullptr) {
-    const size_t smem = (size_t)IDX_N * DI * 2 + 2 * (size_t)IDX_ROWS * DI * 2 +
-                        (size_t)IDX_ROWS * (IDX_N + 1) * 4 + IDX_N * 4;
     // Row-tile splits: enough CTAs to cover the GPU when there are few tokens.
     const int64_t tiles = (n_c + IDX_ROWS - 1) / IDX_ROWS;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // every group's live columns fit in half the tile: one token of <= 64 heads
+    const bool narrow = (int64_t)p.hpad * (m < p.TT ? m : p.TT) <= IDX_N / 2;
+    const int qn = narrow ? IDX_N / 2 : IDX_N;
     int64_t ysplit = (2 * (int64_t)sms + p.groups - 1) / p.groups;
+    int nkb = 2;
+    if (narrow && p.groups * tiles <= 4 * (int64_t)sms) {
+        // a CTA per tile and one key buffer: four CTAs fit an SM, and no CTA
+        // runs two tiles in turn (long decode: 512 tiles)
+        ysplit = tiles;
+        nkb = 1;
+    }
     if (ysplit > tiles) ysplit = tiles;
     if (ysplit < 1) ysplit = 1;
+    const size_t smem = (size_t)qn * DI * 2 + (size_t)nkb * IDX_ROWS * DI * 2 +
+                        (size_t)IDX_ROWS * (qn + 1) * 4 + qn * 4;
     const bool side = ring != nullptr;
     const RingArgs ra = side ? *ring : RingArgs{};
     const LatentArgs la = side ? *lat : LatentArgs{};
     dim3 grid((unsigned)p.groups, (unsigned)(ysplit + (side ? 1 : 0)));
-    // every group's live columns fit in half the tile: one token of <= 64 heads
-    const bool narrow = (int64_t)p.hpad * (m < p.TT ? m : p.TT) <= IDX_N / 2;
     auto kern = p.prequant ? (narrow ? indexer_scores_kernel<DI, false, true>
                                      : indexer_scores_kernel<DI, false, false>)
                            : (narrow ? indexer_scores_kernel<DI, true, true>
@@ -967,7 +980,7 @@ static int launch_scores(const IndexerPlan& p, const uint16_t* q, const uint16_t
     cfg.numAttrs = 1;
     int rc = cuda_check(cudaLaunchKernelEx(&cfg, kern, q, k, w, scores, (int)m, (int)Hi, p.hpad,
                                            p.TT, n_c, ratio, start_pos, fill_hidden, (int)ysplit,
-                                           ra, la),
+                                           nkb, ra, la),
                         "ds41_indexer_topk: scores kernel");
     if (rc) return rc;
     return launch_check("ds41_indexer_topk: scores kernel");
