@@ -80,6 +80,26 @@ __device__ __forceinline__ float pow2_ceil_pos(float x) {
     return __uint_as_float((u & 0x7f800000u) + 0x00800000u);
 }
 
+// The power-of-two block scale s = pow2_ceil(amax / 6) (the quotient
+// correctly rounded) and rs = 1/s, both exact, for an amax that is a bf16
+// magnitude or the floor 6 * 2^-126 (at most 8 significant bits, normal).
+// Writing amax = M 2^E with 1 <= M < 2: amax / 6 = (M / 1.5) 2^(E-2), so s is
+// 2^(E-2) when M <= 1.5 and 2^(E-1) when M > 1.5; the rounded quotient never
+// crosses the power of two, since M - 1.5 >= 2^-7 whenever it is positive.
+// This holds for every positive finite bf16 magnitude (checked against the
+// divide for all of them); an infinite amax takes the divide.
+__device__ __forceinline__ float e8m0_scale_bf16(float amax, float* rs) {
+    const uint32_t u = __float_as_uint(amax);
+    if (u >= 0x7f800000u) {
+        const float s = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
+        *rs = __frcp_rn(s);
+        return s;
+    }
+    const uint32_t e = (u >> 23) - 2u + ((u & 0x007fffffu) > 0x00400000u ? 1u : 0u);
+    *rs = __uint_as_float((254u - e) << 23);
+    return __uint_as_float(e << 23);
+}
+
 // f32 -> e4m3 (OCP "fn") with round-to-nearest-even and saturation at the
 // largest finite value (448), via the hardware conversion.  Returns the byte.
 __device__ __forceinline__ uint32_t f32_to_e4m3_sat(float x) {
@@ -151,7 +171,8 @@ __device__ __forceinline__ uint4 e2m1_round8(const float t[8], float s, uint32_t
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
         const float2 g = e2m1x2_to_float2(c >> (4 * k));
-        o[k / 2] = (uint32_t)f2bf(__fmul_rn(g.x, s)) | ((uint32_t)f2bf(__fmul_rn(g.y, s)) << 16);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(g.x, s), __fmul_rn(g.y, s));
+        o[k / 2] = *reinterpret_cast<const uint32_t*>(&b2);
     }
     *codes = c;
     return out;

@@ -47,8 +47,8 @@ __device__ __forceinline__ uint4 q8_chunk(uint4 raw, bool live) {
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
-    const float s = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
-    const float rs = __frcp_rn(s);  // exact: s is a power of two
+    float rs;
+    const float s = e8m0_scale_bf16(amax, &rs);  // amax: a bf16 magnitude or the floor
 #pragma unroll
     for (int k = 0; k < 8; k++) v[k] = __fmul_rn(v[k], rs);
     uint32_t codes;
@@ -121,6 +121,10 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
         const uint16_t* src = q_idx + ((int64_t)(t0 + (live ? tt : 0)) * Hi + (live ? h : 0)) * DI;
         cp_async16(smem_u32(qs + n * DI + swz<CPR>(n, c) * 8), src + c * 8, live);
     }
+    // rows each token of the group can see: one 64-bit division per token
+    __shared__ int64_t vis_s[IDX_N];
+    for (int tt = tid; tt < tcount; tt += IDX_THREADS)
+        vis_s[tt] = visible_rows(t0 + tt, start_pos, ratio, n_c);
     const int64_t vis_last = visible_rows(t0 + tcount - 1, start_pos, ratio, n_c);
     const int64_t tiles_vis = (vis_last + IDX_ROWS - 1) / IDX_ROWS;
     // When the scores are a caller-visible output, rows no query of this
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
             const int64_t s = r0 + r;
             if (s >= n_c) continue;
             const int t = t0 + tt;
-            const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
+            const int64_t vis = vis_s[tt];
             uint16_t out = 0xff80u;  // -inf: not visible yet
             if (s < vis) {
                 const float* col = cs + r * (QN + 1) + tt * hpad;

@@ -148,8 +148,8 @@ __device__ __forceinline__ void quant_group(const uint8_t* qsrc, uint8_t* qdst, 
 #pragma unroll
         for (int e = 0; e < 32; e++) amax = fmaxf(amax, fabsf(v[e]));
         amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
-        const float sc = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
-        const float rs = __frcp_rn(sc);  // exact: sc is a power of two
+        float rs;
+        const float sc = e8m0_scale_bf16(amax, &rs);  // amax: a bf16 magnitude or the floor
         uint32_t cw[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) {

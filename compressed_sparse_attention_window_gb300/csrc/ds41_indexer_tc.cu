@@ -24,9 +24,9 @@
 // first); per group the row tiles run over the rows its last token can see.
 // Warp 0 issues the TMA copies (the group's 256 q rows and 4 x 64 weights,
 // then the row tiles through two stages), warp 1 owns tensor memory and (one
-// lane) issues the MMAs into two D buffers, warps 4..11 quantise each
-// group's q in place and then run its head chains (warp 4 + 4p + q: lane
-// quarter q, tokens 2p and 2p + 1).  Every wait is bounded; a timeout raises
+// lane) issues the MMAs into two D buffers, warps 4..11 quantise each group's
+// q in place and then run its head chains (warp 4 + 4p + q: lane quarter q,
+// tokens 2p and 2p + 1).  Every wait is bounded; a timeout raises
 // DS41_E_TIMEOUT and the roles exit.
 #include "ds41_internal.cuh"
 #include "ds41_tc.cuh"
@@ -47,9 +47,10 @@ constexpr uint32_t QBLK = TT * HI * 64 * 2;            // [256 q rows][64 dims]:
 constexpr uint32_t Q_BYTES = 2 * QBLK;                 // one group's q (2 blocks of 64 dims)
 constexpr uint32_t KBLK = ROWS * 64 * 2;               // [128 rows][64 dims]: 16 KiB
 constexpr uint32_t K_BYTES = 2 * KBLK;                 // one row tile
+constexpr int KST = 2;                                 // row-tile stages
 constexpr uint32_t Q_OFF = 0;                          // 2 q stages
-constexpr uint32_t K_OFF = 2 * Q_BYTES;                // 2 row-tile stages
-constexpr uint32_t W_OFF = K_OFF + 2 * K_BYTES;        // 2 x [4][64] f32 weights
+constexpr uint32_t K_OFF = 2 * Q_BYTES;                // KST row-tile stages
+constexpr uint32_t W_OFF = K_OFF + KST * K_BYTES;      // 2 x [4][64] f32 weights
 constexpr uint32_t W_BYTES = TT * HI * 4;
 constexpr uint32_t BAR_OFF = W_OFF + 2 * W_BYTES;
 constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;  // + alignment slack
@@ -57,7 +58,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 enum {
     B_QFULL, B_QEMPTY = B_QFULL + 2, B_WFULL = B_QEMPTY + 2, B_WEMPTY = B_WFULL + 2,
-    B_KFULL = B_WEMPTY + 2, B_KEMPTY = B_KFULL + 2, B_DFULL = B_KEMPTY + 2,
+    B_KFULL = B_WEMPTY + 2, B_KEMPTY = B_KFULL + KST, B_DFULL = B_KEMPTY + KST,
     B_DEMPTY = B_DFULL + 2, B_QREADY = B_DEMPTY + 2,  // 2: the group's q quantised in place
     B_EPI = B_QREADY + 2, B_FINAL, NBAR
 };
@@ -97,39 +98,61 @@ __device__ __forceinline__ void group_of(int j, const Params& p, int& t0, int& t
 // every block of 32 values becomes bf16(e2m1(v / s) * s) with
 // s = 2^ceil(log2(max(amax, 6 * 2^-126) / 6)), exactly as fp4_quant_e8m0.
 // Thread `tid` of `nthr` takes blocks tid, tid + nthr, ... of the first `rows`
-// rows (rows past the group's tokens are zero-filled and stay zero).
+// rows (rows past the group's tokens are zero-filled and stay zero), two at a
+// time so that their dependent steps interleave; the maximum is a tree (the
+// maximum of a set does not depend on the order).
 __device__ __forceinline__ void quant_q_inplace(uint8_t* qst, int rows, int tid, int nthr) {
+    const int nb = rows * 4;
 #pragma unroll 1
-    for (int id = tid; id < rows * 4; id += nthr) {
-        const int n = id >> 2, j = id & 3;
-        uint8_t* row = qst + (j >> 1) * QBLK + n * 128;
-        uint4 u[4];
-        float v[32];
-        float amax = 0.0f;
+    for (int id0 = tid; id0 < nb; id0 += 2 * nthr) {
+        float v[2][32];
+        uint8_t* rowp[2];
+        int nn[2], cb[2];
+        bool live[2];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; c4++) {
-            const int c = (j & 1) * 4 + c4;
-            u[c4] = *reinterpret_cast<const uint4*>(row + ((c ^ (n & 7)) << 4));
-            const uint32_t w4[4] = {u[c4].x, u[c4].y, u[c4].z, u[c4].w};
+        for (int b = 0; b < 2; b++) {
+            const int id = id0 + b * nthr;
+            live[b] = id < nb;
+            // a second block past the end reads this thread's first block
+            // again (before this thread stores it) and is never stored
+            const int idc = live[b] ? id : id0;
+            const int n = idc >> 2, j = idc & 3;
+            nn[b] = n;
+            cb[b] = (j & 1) * 4;
+            rowp[b] = qst + (j >> 1) * QBLK + n * 128;
 #pragma unroll
-            for (int e = 0; e < 4; e++) {
-                v[c4 * 8 + 2 * e] = __uint_as_float(w4[e] << 16);
-                v[c4 * 8 + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+            for (int c4 = 0; c4 < 4; c4++) {
+                const uint4 u = *reinterpret_cast<const uint4*>(rowp[b] + (((cb[b] + c4) ^ (n & 7)) << 4));
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    v[b][c4 * 8 + 2 * e] = __uint_as_float(w4[e] << 16);
+                    v[b][c4 * 8 + 2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+                }
             }
         }
 #pragma unroll
-        for (int e = 0; e < 32; e++) amax = fmaxf(amax, fabsf(v[e]));
-        amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
-        const float sc = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
-        const float rs = __frcp_rn(sc);  // exact: sc is a power of two
+        for (int b = 0; b < 2; b++) {
+            float mx[16];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; c4++) {
-            float t[8];
+            for (int e = 0; e < 16; e++) mx[e] = fmaxf(fabsf(v[b][2 * e]), fabsf(v[b][2 * e + 1]));
 #pragma unroll
-            for (int e = 0; e < 8; e++) t[e] = __fmul_rn(v[c4 * 8 + e], rs);
-            uint32_t codes;
-            const int c = (j & 1) * 4 + c4;
-            *reinterpret_cast<uint4*>(row + ((c ^ (n & 7)) << 4)) = e2m1_round8(t, sc, &codes);
+            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                for (int e = 0; e < w; e++) mx[e] = fmaxf(mx[e], mx[e + w]);
+            const float amax = fmaxf(mx[0], __uint_as_float(0x01c00000u));  // 6 * 2^-126
+            float rs;
+            const float sc = e8m0_scale_bf16(amax, &rs);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; c4++) {
+                float t[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) t[e] = __fmul_rn(v[b][c4 * 8 + e], rs);
+                uint32_t codes;
+                const uint4 o = e2m1_round8(t, sc, &codes);
+                if (live[b])
+                    *reinterpret_cast<uint4*>(rowp[b] + (((cb[b] + c4) ^ (nn[b] & 7)) << 4)) = o;
+            }
         }
     }
 }
@@ -155,12 +178,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&bars[B_QFULL + b], 1);
             mbar_init(&bars[B_QEMPTY + b], 1);
             mbar_init(&bars[B_WFULL + b], 1);
-            mbar_init(&bars[B_WEMPTY + b], 8);
+            mbar_init(&bars[B_WEMPTY + b], EPI_THREADS / 32);
+            mbar_init(&bars[B_DFULL + b], 1);
+            mbar_init(&bars[B_DEMPTY + b], EPI_THREADS / 32);
+            mbar_init(&bars[B_QREADY + b], 1);
+        }
+        for (int b = 0; b < KST; b++) {
             mbar_init(&bars[B_KFULL + b], 1);
             mbar_init(&bars[B_KEMPTY + b], 1);
-            mbar_init(&bars[B_DFULL + b], 1);
-            mbar_init(&bars[B_DEMPTY + b], 8);
-            mbar_init(&bars[B_QREADY + b], 1);
         }
         mbar_init(&bars[B_EPI], EPI_THREADS / 32);
         mbar_init(&bars[B_FINAL], 1);
@@ -185,15 +210,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         // TMA producer (one lane)
         // ------------------------------------------------------------------
         if (lane == 0) {
-            uint32_t jq = 0, kt = 0, q_armed[2] = {0, 0}, w_armed[2] = {0, 0}, k_armed[2] = {0, 0};
+            uint32_t kt = 0, q_armed[2] = {0, 0}, w_armed[2] = {0, 0}, k_armed[KST] = {};
             bool ok = true;
+            int jq = 0;  // groups with tiles so far
             for (int j = 0; j < ngroups && ok; j++) {
                 int t0, tcount, ntile;
                 group_of(j, p, t0, tcount, ntile);
                 if (ntile == 0) continue;
                 const int qs = jq & 1;
-                if (jq >= 2 && !(wait_bar(&bars[B_QEMPTY + qs], ((jq - 2) >> 1) & 1, abort_f, p.status) &&
-                                 wait_bar(&bars[B_WEMPTY + qs], ((jq - 2) >> 1) & 1, abort_f, p.status)))
+                if (jq >= 2 &&
+                    !(wait_bar(&bars[B_QEMPTY + qs], ((jq - 2) >> 1) & 1, abort_f, p.status) &&
+                      wait_bar(&bars[B_WEMPTY + qs], ((jq - 2) >> 1) & 1, abort_f, p.status)))
                     break;
                 mbar_arrive_expect_tx(&bars[B_QFULL + qs], Q_BYTES);
                 q_armed[qs]++;
@@ -206,9 +233,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 bulk_g2s(sm + W_OFF + qs * W_BYTES, p.w + (int64_t)t0 * HI, wbytes,
                          &bars[B_WFULL + qs]);
                 for (int i = 0; i < ntile; i++, kt++) {
-                    const int ks = kt & 1;
-                    if (kt >= 2 && !wait_bar(&bars[B_KEMPTY + ks], ((kt - 2) >> 1) & 1, abort_f,
-                                             p.status)) {
+                    const int ks = kt % KST;
+                    if (kt >= KST && !wait_bar(&bars[B_KEMPTY + ks], ((kt - KST) / KST) & 1, abort_f,
+                                               p.status)) {
                         ok = false;
                         break;
                     }
@@ -224,8 +251,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int b = 0; b < 2; b++) {
                 if (q_armed[b]) drain_bar(&bars[B_QFULL + b], (q_armed[b] - 1) & 1, p.status);
                 if (w_armed[b]) drain_bar(&bars[B_WFULL + b], (w_armed[b] - 1) & 1, p.status);
-                if (k_armed[b]) drain_bar(&bars[B_KFULL + b], (k_armed[b] - 1) & 1, p.status);
             }
+            for (int b = 0; b < KST; b++)
+                if (k_armed[b]) drain_bar(&bars[B_KFULL + b], (k_armed[b] - 1) & 1, p.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
@@ -242,8 +270,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!wait_bar(&bars[B_QREADY + qs], (jq >> 1) & 1, abort_f, p.status)) break;
                 const uint64_t qd = sdesc(sbase + Q_OFF + qs * Q_BYTES, 16, 1024);
                 for (int i = 0; i < ntile; i++, kt++) {
-                    const int ks = kt & 1, db = kt & 1;
-                    if (!wait_bar(&bars[B_KFULL + ks], (kt >> 1) & 1, abort_f, p.status) ||
+                    const int ks = kt % KST, db = kt & 1;
+                    if (!wait_bar(&bars[B_KFULL + ks], (kt / KST) & 1, abort_f, p.status) ||
                         (kt >= 2 &&
                          !wait_bar(&bars[B_DEMPTY + db], ((kt - 2) >> 1) & 1, abort_f, p.status))) {
                         ok = false;
@@ -269,9 +297,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------------------------
         // Head chains: thread = compressed row 32 q + lane of the tile,
-        // tokens 2 pr and 2 pr + 1 of the group
+        // tokens 2 pr and 2 pr + 1 of the group.  The same warps quantise
+        // each group's q first.  (Quantising the next group's q while a
+        // group's tiles run measured slower: the quantisation then took about
+        // twice as long, beside the MMAs reading their operands from shared
+        // memory.)
         // ------------------------------------------------------------------
         const int q = warp & 3, pr = (warp - 4) >> 2;
+        const int etid = threadIdx.x - 128;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t jq = 0, kt = 0, epi_ph = 0;
         for (int j = 0; j < ngroups; j++) {
@@ -283,14 +316,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 {
                     // the group's q quantised in place, before its head chains
                     if (!wait_bar(&bars[B_QFULL + ws], (jq >> 1) & 1, abort_f, p.status)) break;
-                    quant_q_inplace(sm + Q_OFF + ws * Q_BYTES, tcount * HI, threadIdx.x - 128,
-                                    EPI_THREADS);
+                    quant_q_inplace(sm + Q_OFF + ws * Q_BYTES, tcount * HI, etid, EPI_THREADS);
                     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
                     if (!warps_sync(&bars[B_EPI], epi_ph, abort_f, p.status)) break;
-                    if (threadIdx.x == 128) mbar_arrive(&bars[B_QREADY + ws]);
+                    if (etid == 0) mbar_arrive(&bars[B_QREADY + ws]);
                 }
                 if (!wait_bar(&bars[B_WFULL + ws], (jq >> 1) & 1, abort_f, p.status)) break;
                 const float* wsm = reinterpret_cast<const float*>(sm + W_OFF + ws * W_BYTES);
+                // rows each of this thread's two tokens can see (one 64-bit
+                // division per token and group, not per score)
+                int64_t vis_u[2];
+#pragma unroll
+                for (int u = 0; u < 2; u++)
+                    vis_u[u] = 2 * pr + u < tcount ? visible(t0 + 2 * pr + u, p) : 0;
                 bool ok = true;
                 for (int i = 0; i < ntile; i++, kt++) {
                     const int db = kt & 1;
@@ -313,26 +351,33 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[B_DEMPTY + db]);
-                    // the two tokens' chains side by side, each in head order
-                    const float* w0 = wsm + (2 * pr) * HI;
-                    const float* w1 = w0 + HI;
+                    // the two tokens' chains side by side, each in head order;
+                    // the weights come four heads per 16-byte load
+                    const float4* w0 = reinterpret_cast<const float4*>(wsm + (2 * pr) * HI);
+                    const float4* w1 = w0 + HI / 4;
                     float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-                    for (int h = 0; h < HI; h++) {
-                        a0 = __fmaf_rn(w0[h], fmaxf(__uint_as_float(dv[0][h]), 0.0f), a0);
-                        a1 = __fmaf_rn(w1[h], fmaxf(__uint_as_float(dv[1][h]), 0.0f), a1);
+                    for (int h4 = 0; h4 < HI / 4; h4++) {
+                        const float4 x0 = w0[h4], x1 = w1[h4];
+                        const float c0[4] = {x0.x, x0.y, x0.z, x0.w};
+                        const float c1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const int h = 4 * h4 + e;
+                            a0 = __fmaf_rn(c0[e], fmaxf(__uint_as_float(dv[0][h]), 0.0f), a0);
+                            a1 = __fmaf_rn(c1[e], fmaxf(__uint_as_float(dv[1][h]), 0.0f), a1);
+                        }
                     }
 #pragma unroll
                     for (int u = 0; u < 2; u++) {
                         const int tt = 2 * pr + u;
                         if (tt >= tcount || s >= p.n_c) continue;
-                        const int64_t t = t0 + tt;
                         uint16_t out = 0xff80u;  // -inf: not visible yet
-                        if (s < visible(t, p)) {
+                        if (s < vis_u[u]) {
                             out = f2bf(u == 0 ? a0 : a1);
                             if (out == 0x8000u) out = 0u;
                         }
-                        p.scores[t * p.n_c + s] = out;
+                        p.scores[(int64_t)(t0 + tt) * p.n_c + s] = out;
                     }
                 }
                 __syncwarp();

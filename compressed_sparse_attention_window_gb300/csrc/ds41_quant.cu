@@ -45,8 +45,7 @@ __global__ void __launch_bounds__(256) fp4_quant_kernel(const uint4* __restrict_
         s = e4m3_to_f32(sbyte);
     } else {
         amax = fmaxf(amax, __uint_as_float(0x01c00000u));  // 6 * 2^-126
-        s = pow2_ceil_pos(__fdiv_rn(amax, 6.0f));
-        rs = __frcp_rn(s);
+        s = e8m0_scale_bf16(amax, &rs);  // amax: a bf16 magnitude or the floor
         sbyte = (__float_as_uint(s) >> 23) & 0xffu;  // biased exponent = e8m0
     }
     if (!live) return;
