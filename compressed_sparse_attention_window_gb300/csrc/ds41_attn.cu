@@ -468,12 +468,10 @@ __device__ void dec_topk_local(const DecTopk& tk, int64_t t, int vis, int kk, in
 // separate top-k kernel, which measured faster than any selection split over
 // the attention's cluster.
 template <int NTH>
-__device__ void dec_topk(const DecTopk& tk, int64_t t, int K, int j0, int j1, int* sidx,
+__device__ void dec_topk(const DecTopk& tk, int64_t t, int64_t vis, int K, int j0, int j1, int* sidx,
                          uint8_t* area, bool write_idx, unsigned int* status) {
     const int tid = threadIdx.x;
     const int win = tk.win;
-    int64_t vis = (tk.start_pos + t + 1) / tk.ratio;
-    if (vis > tk.n_c) vis = tk.n_c;
     const int kk = (int)(vis < tk.ctopk ? vis : tk.ctopk);
     int32_t* orow = tk.idx_out + t * (int64_t)K;
     // window entries, the picks when every visible row is kept, and padding
@@ -631,13 +629,19 @@ __global__ void __launch_bounds__(32 * dec_warps<HD>(), 1) sparse_attn_decode_ke
             }
         }
     }
-    // The indices, the ring and the cache may come from the kernels just
-    // before this one.
+    // The rows the query can see (a 64-bit division, from the arguments
+    // alone) while the kernel before finishes; the indices, the ring and the
+    // cache may come from it.
+    int64_t vis = 0;
+    if constexpr (FUSED) {
+        vis = (tk.start_pos + t + 1) / tk.ratio;
+        if (vis > tk.n_c) vis = tk.n_c;
+    }
     pdl_wait();
     const int nst = max(0, min(j1 - j0, DEC_STAGE));
     if constexpr (FUSED) {
         // select this query's rows here (the scores come from the kernel before)
-        dec_topk<NTH>(tk, t, K, j0, j1, sidx, smem + SM::tk_off, blockIdx.y == 0, status);
+        dec_topk<NTH>(tk, t, vis, K, j0, j1, sidx, smem + SM::tk_off, blockIdx.y == 0, status);
     } else {
         for (int j = tid; j < nst; j += NTH) sidx[j] = irow[j0 + j];
     }

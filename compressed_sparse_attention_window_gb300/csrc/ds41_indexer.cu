@@ -85,6 +85,15 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     // launch overlaps it.  Only then may the next kernel start launching: the
     // decode attention reads q (an input of the step) before its own wait, so
     // everything before this kernel must be complete when it launches.
+    // The rows each token of the group can see (one 64-bit division per
+    // token, from the arguments alone) are worked out while it waits.
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = blockIdx.x * TT;
+    const int tcount = min(TT, m - t0);
+    __shared__ int64_t vis_s[IDX_N];
+    for (int tt = tid; tt < tcount; tt += IDX_THREADS)
+        vis_s[tt] = visible_rows(t0 + tt, start_pos, ratio, n_c);
+    const int64_t vis_last = visible_rows(t0 + tcount - 1, start_pos, ratio, n_c);
     pdl_wait();
     pdl_trigger();
     if ((int)blockIdx.y >= ymain) {
@@ -106,9 +115,6 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
     float* cs = reinterpret_cast<float*>(ksb + nkb * IDX_ROWS * DI);  // [IDX_ROWS][QN + 1]
     float* wsm = cs + IDX_ROWS * (QN + 1);                             // [QN]
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * TT;
-    const int tcount = min(TT, m - t0);
 
     // q of this CTA's tokens as rows n = tt * hpad + h: staged raw with
     // cp.async (padding rows zero-filled), then quantised in place.  The
@@ -121,11 +127,6 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
         const uint16_t* src = q_idx + ((int64_t)(t0 + (live ? tt : 0)) * Hi + (live ? h : 0)) * DI;
         cp_async16(smem_u32(qs + n * DI + swz<CPR>(n, c) * 8), src + c * 8, live);
     }
-    // rows each token of the group can see: one 64-bit division per token
-    __shared__ int64_t vis_s[IDX_N];
-    for (int tt = tid; tt < tcount; tt += IDX_THREADS)
-        vis_s[tt] = visible_rows(t0 + tt, start_pos, ratio, n_c);
-    const int64_t vis_last = visible_rows(t0 + tcount - 1, start_pos, ratio, n_c);
     const int64_t tiles_vis = (vis_last + IDX_ROWS - 1) / IDX_ROWS;
     // When the scores are a caller-visible output, rows no query of this
     // group can see yet are written as -inf too.
