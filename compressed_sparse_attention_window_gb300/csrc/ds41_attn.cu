@@ -478,7 +478,9 @@ __device__ void dec_topk(const DecTopk& tk, int64_t t, int64_t vis, int K, int j
     for (int j = j0 + tid; j < j1; j += NTH) {
         int v;
         if (j < win) {
-            v = tk.win_idx[t * win + j];
+            // the same entry the front writes to win_idx, worked out here
+            // rather than read back
+            v = window_index(tk.start_pos, tk.m, win, t, j);
         } else if (j - win >= kk) {
             v = -1;
         } else if (vis <= tk.ctopk) {

@@ -80,6 +80,25 @@ __device__ __forceinline__ float pow2_ceil_pos(float x) {
     return __uint_as_float((u & 0x7f800000u) + 0x00800000u);
 }
 
+// Entry j of the window part of query token t's index row, for a call of m
+// tokens from start_pos (window win): the row that holds position
+// q = start_pos + t - win + 1 + j, or -1 before position 0.  With no earlier
+// positions the rows are the call's own kv rows (q); a single token reads the
+// ring (slot q mod win); a chunk reads rows_a, the ring's old contents
+// (slot q mod win) followed by the chunk's kv rows (win + q - start_pos).
+__device__ __forceinline__ int32_t window_index(int64_t start_pos, int64_t m, int64_t win,
+                                                int64_t t, int64_t j) {
+    const int64_t q = start_pos + t - win + 1 + j;
+    if (q < 0) return -1;
+    if (start_pos == 0) return (int32_t)q;
+    if (m == 1 || q < start_pos) {
+        // q mod win, by a 32-bit division when both fit
+        if (((q | win) >> 31) == 0) return (int32_t)((uint32_t)q % (uint32_t)win);
+        return (int32_t)(q % win);
+    }
+    return (int32_t)(win + (q - start_pos));
+}
+
 // The power-of-two block scale s = pow2_ceil(amax / 6) (the quotient
 // correctly rounded) and rs = 1/s, both exact, for an amax that is a bf16
 // magnitude or the floor 6 * 2^-126 (at most 8 significant bits, normal).

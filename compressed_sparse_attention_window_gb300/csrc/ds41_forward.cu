@@ -123,7 +123,7 @@ extern "C" int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf
     if (rc) return rc;
     if (attn_topk_fusable(m, nh, hd, K, n_c)) {
         // the attention clusters select their rows from the scores themselves
-        const DecTopk tk{scores, win_idx, idx, n_c, ratio, start_pos, n_a, (int)win, (int)ctopk};
+        const DecTopk tk{scores, win_idx, idx, n_c, ratio, start_pos, n_a, (int)win, (int)ctopk, m};
         return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
                         nullptr, 0, true, st, name, &tk);
     }
@@ -250,7 +250,7 @@ extern "C" int ds41_csa_forward_fp4(const ds41_bf16* q, const ds41_bf16* kv, ds4
     const PackedRows pk{cache_codes, cache_scales};
     const PackedRows* pkp = (cache_codes && hd == 512) ? &pk : nullptr;
     if (attn_topk_fusable(m, nh, hd, K, n_c)) {
-        const DecTopk tk{scores, win_idx, idx, n_c, ratio, start_pos, n_a, (int)win, (int)ctopk};
+        const DecTopk tk{scores, win_idx, idx, n_c, ratio, start_pos, n_a, (int)win, (int)ctopk, m};
         return attn_run(q, rows_a_used, n_a, cache, n_c, idx, K, sink, scale, o, lse, m, nh, hd,
                         nullptr, 0, true, st, name, &tk, pkp);
     }

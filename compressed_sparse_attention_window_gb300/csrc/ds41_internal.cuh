@@ -31,6 +31,7 @@ struct DecTopk {
     int32_t* idx_out;         // [m][K] merged index rows (written by head group 0)
     int64_t n_c, ratio, start_pos, offset;
     int win, ctopk;
+    int64_t m;                // tokens of the call (the window entries follow from it)
 };
 
 // The compressed rows (rows_b) in their packed form: e2m1 codes [n_c][hd/2]

@@ -58,15 +58,7 @@ __device__ __forceinline__ void ring_write_item(const RingArgs& a, int64_t i) {
     i -= nB;
     if (i < nC) {
         const int64_t t = i / a.win, j = i % a.win;
-        const int64_t p = a.start_pos + t;
-        const int64_t q = p - a.win + 1 + j;
-        int64_t v;
-        if (q < 0) v = -1;
-        else if (a.start_pos == 0) v = q;
-        else if (a.m == 1) v = q % a.win;
-        else if (q < a.start_pos) v = q % a.win;
-        else v = a.win + (q - a.start_pos);
-        a.win_idx[i] = (int32_t)v;
+        a.win_idx[i] = window_index(a.start_pos, a.m, a.win, t, j);
     }
 }
 
@@ -93,15 +85,7 @@ __device__ __forceinline__ void ring_write_cta(const RingArgs& a) {
     }
     for (int i = tid; i < m * win; i += nt) {
         const int t = i / win, j = i - t * win;
-        const int64_t p = a.start_pos + t;
-        const int64_t q = p - a.win + 1 + j;
-        int64_t v;
-        if (q < 0) v = -1;
-        else if (a.start_pos == 0) v = q;
-        else if (a.m == 1) v = q % a.win;
-        else if (q < a.start_pos) v = q % a.win;
-        else v = a.win + (q - a.start_pos);
-        a.win_idx[i] = (int32_t)v;
+        a.win_idx[i] = window_index(a.start_pos, a.m, a.win, t, j);
     }
 }
 
