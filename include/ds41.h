@@ -342,7 +342,10 @@ int ds41_csa_forward_reuse(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* r
  * may be NULL otherwise), h_q_idx [m, Hi, Di] and h_w [m, Hi] are copied into
  * the device buffers q, kv, latent, q_idx and w (caller-owned, same shapes),
  * ds41_csa_forward runs on them, and o is copied into h_o [m, nh, hd]; the
- * other arguments are ds41_csa_forward's.  Everything is enqueued on `stream`
+ * other arguments are ds41_csa_forward's.  When h_o is page-locked memory
+ * mapped for the current device, m <= 16 and o takes at most 4 MiB (a
+ * multiple of 16 bytes), the step writes o straight into h_o through the
+ * mapping instead and the device buffer o is left unwritten.  Everything is enqueued on `stream`
  * in that order; the call returns without waiting, and h_o holds the result
  * once the stream has reached that point (cudaStreamSynchronize).  The copies
  * are asynchronous only for page-locked host memory (cudaHostAlloc /
