@@ -412,14 +412,15 @@ __device__ void dec_topk_local(const DecTopk& tk, int64_t t, int vis, int kk, in
     __syncthreads();
     const uint32_t T = (hb << 8) | (uint32_t)sel[2];
     const int need_eq = kk - sel[3];
-    int n_gt = 0, n_eq = 0;
+    // this thread's keys above and at the threshold as bit masks (bit e:
+    // key e), so that every key's rank among them is one population count
+    uint32_t gm = 0, qm = 0;
 #pragma unroll
     for (int e = 0; e < KMAX; e++) {
-        if (e < n_mine) {
-            n_gt += key[e] > T ? 1 : 0;
-            n_eq += key[e] == T ? 1 : 0;
-        }
+        gm |= (e < n_mine && key[e] > T) ? (1u << e) : 0u;
+        qm |= (e < n_mine && key[e] == T) ? (1u << e) : 0u;
     }
+    const int n_gt = __popc(gm), n_eq = __popc(qm);
     // exclusive prefixes over the lanes of the warp, then over the warps
     int x_gt = n_gt, x_eq = n_eq;
 #pragma unroll
@@ -441,21 +442,16 @@ __device__ void dec_topk_local(const DecTopk& tk, int64_t t, int vis, int kk, in
         gt += wsum[w];
         eq += wsum[32 + w];
     }
+    const int v0 = (int)(tk.offset + i0);
 #pragma unroll
     for (int e = 0; e < KMAX; e++) {
-        if (e < n_mine) {
-            const bool is_eq = key[e] == T;
-            const bool take = key[e] > T || (is_eq && eq < need_eq);
-            if (take) {
-                const int j = win + gt + min(eq, need_eq);  // position in the merged row
-                if (j >= j0 && j < j1) {
-                    const int v = (int)(tk.offset + i0 + e);
-                    sidx[j - j0] = v;
-                    if (write_idx) orow[j] = v;
-                }
-            }
-            gt += key[e] > T ? 1 : 0;
-            eq += is_eq ? 1 : 0;
+        const uint32_t below = (1u << e) - 1u;
+        const int eqb = eq + __popc(qm & below);  // keys at T before this one
+        const bool take = ((gm >> e) & 1u) || (((qm >> e) & 1u) && eqb < need_eq);
+        const int j = win + gt + __popc(gm & below) + min(eqb, need_eq);  // merged-row position
+        if (take && j >= j0 && j < j1) {
+            sidx[j - j0] = v0 + e;
+            if (write_idx) orow[j] = v0 + e;
         }
     }
 }

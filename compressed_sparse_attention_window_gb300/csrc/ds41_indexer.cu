@@ -289,10 +289,13 @@ __global__ void __launch_bounds__(32 * TKW_WARPS) topk_warp_kernel(
     int64_t start_pos, int64_t offset) {
     __shared__ __align__(16) int hist_all[TKW_WARPS][256];
     __shared__ int sel_all[TKW_WARPS][4];
-    pdl_wait();     // the scores (and window indices) come from the previous kernel
-    pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = (int64_t)blockIdx.x * TKW_WARPS + warp;
+    // the rows this query can see (a 64-bit division, from the arguments
+    // alone) while the kernel before finishes
+    const int64_t vis64 = t < m ? visible_rows(t, start_pos, ratio, n_c) : 0;
+    pdl_wait();     // the scores (and window indices) come from the previous kernel
+    pdl_trigger();
     if (t >= m) return;  // whole warps only: the rest of the CTA syncs nothing with it
     int* hist = hist_all[warp];
     int* sel = sel_all[warp];
@@ -300,7 +303,6 @@ __global__ void __launch_bounds__(32 * TKW_WARPS) topk_warp_kernel(
     int32_t* out = idx + t * K;
     const uint16_t* sc = scores + t * n_c;
     for (int j = lane; j < win; j += 32) out[j] = win_idx[t * win + j];
-    const int64_t vis64 = visible_rows(t, start_pos, ratio, n_c);
     const int vis = (int)vis64;  // <= TKW_MAX (host plan)
     const int kk = vis < ctopk ? vis : ctopk;
     if (vis <= ctopk) {
@@ -349,14 +351,15 @@ __global__ void __launch_bounds__(32 * TKW_WARPS) topk_warp_kernel(
     __syncwarp();
     const uint32_t T = (hb << 8) | (uint32_t)sel[2];
     const int need_eq = kk - sel[3];
-    int n_gt = 0, n_eq = 0;
+    // this lane's keys above and at the threshold as bit masks (bit e: key
+    // e), so that every key's rank among them is one population count
+    uint32_t gm = 0, qm = 0;
 #pragma unroll
     for (int e = 0; e < TKW_KPL; e++) {
-        if (e < n_mine) {
-            n_gt += key[e] > T ? 1 : 0;
-            n_eq += key[e] == T ? 1 : 0;
-        }
+        gm |= (e < n_mine && key[e] > T) ? (1u << e) : 0u;
+        qm |= (e < n_mine && key[e] == T) ? (1u << e) : 0u;
     }
+    const int n_gt = __popc(gm), n_eq = __popc(qm);
     int x_gt = n_gt, x_eq = n_eq;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -367,16 +370,14 @@ __global__ void __launch_bounds__(32 * TKW_WARPS) topk_warp_kernel(
             x_eq += b;
         }
     }
-    int gt = x_gt - n_gt, eq = x_eq - n_eq;
+    const int gt = x_gt - n_gt, eq = x_eq - n_eq;
+    const int32_t v0 = (int32_t)(offset + i0);
 #pragma unroll
     for (int e = 0; e < TKW_KPL; e++) {
-        if (e < n_mine) {
-            const bool is_eq = key[e] == T;
-            if (key[e] > T || (is_eq && eq < need_eq))
-                out[win + gt + min(eq, need_eq)] = (int32_t)(offset + i0 + e);
-            gt += key[e] > T ? 1 : 0;
-            eq += is_eq ? 1 : 0;
-        }
+        const uint32_t below = (1u << e) - 1u;  // bits 0 .. e-1
+        const int eqb = eq + __popc(qm & below);
+        if (((gm >> e) & 1u) || (((qm >> e) & 1u) && eqb < need_eq))
+            out[win + gt + __popc(gm & below) + min(eqb, need_eq)] = v0 + e;
     }
     for (int j = kk + lane; j < ctopk; j += 32) out[win + j] = -1;
 }
@@ -863,14 +864,16 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
             sel[5] = e;
         }
     }
-    int n_gt = 0, n_eq = 0;
+    // this thread's keys above and at the threshold as bit masks (bit e:
+    // key e), so that every key's rank among them is one population count
+    static_assert(KMAX <= 32, "one mask word");
+    uint32_t gm = 0, qm = 0;
 #pragma unroll
     for (int e = 0; e < KMAX; e++) {
-        if (e < n_mine) {
-            n_gt += key[e] > T ? 1 : 0;
-            n_eq += key[e] == T ? 1 : 0;
-        }
+        gm |= (e < n_mine && key[e] > T) ? (1u << e) : 0u;
+        qm |= (e < n_mine && key[e] == T) ? (1u << e) : 0u;
     }
+    const int n_gt = __popc(gm), n_eq = __popc(qm);
     int x_gt = n_gt, x_eq = n_eq;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -891,15 +894,13 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
         gt += wsum[w];
         eq += wsum[32 + w];
     }
+    const int32_t v0 = (int32_t)(offset + lo + i0);
 #pragma unroll
     for (int e = 0; e < KMAX; e++) {
-        if (e < n_mine) {
-            const bool is_eq = key[e] == T;
-            if (key[e] > T || (is_eq && eq < need_eq))
-                out[win + gt + min(eq, need_eq)] = (int32_t)(offset + lo + i0 + e);
-            gt += key[e] > T ? 1 : 0;
-            eq += is_eq ? 1 : 0;
-        }
+        const uint32_t below = (1u << e) - 1u;  // bits 0 .. e-1
+        const int eqb = eq + __popc(qm & below);
+        if (((gm >> e) & 1u) || (((qm >> e) & 1u) && eqb < need_eq))
+            out[win + gt + __popc(gm & below) + min(eqb, need_eq)] = v0 + e;
     }
     if (r == 0)
         for (int j = kk + tid; j < ctopk; j += TK_THREADS) out[win + j] = -1;
