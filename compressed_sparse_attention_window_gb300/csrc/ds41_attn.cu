@@ -45,13 +45,24 @@ struct AttnSmem {
 
 __device__ __forceinline__ int aswz(int row, int c) { return c ^ (row & 7); }
 
-template <int HD>
+// SEL: the CTA builds its token's merged index row itself, from the
+// indexer scores of the kernel before (tk; one split, K <= ATT_STAGE, at most
+// WTK_MAX visible scores): the window entries, then warp 0 ranks the visible
+// scores (warp_topk), and head group 0 writes the row to tk.idx_out.
+template <int HD, bool SEL>
 __global__ void __launch_bounds__(ATT_THREADS, 1) sparse_attn_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ rows_a, int64_t n_a,
     const uint16_t* __restrict__ rows_b, int64_t n_c, const int32_t* __restrict__ idx, int K,
     const float* __restrict__ sink, float scale_log2, uint16_t* __restrict__ o,
     float* __restrict__ lse, int nh, int chunks_per_split, float* __restrict__ part_o,
-    float2* __restrict__ part_ml, unsigned int* status) {
+    float2* __restrict__ part_ml, unsigned int* status, DecTopk tk) {
+    // the rows the query can see (a 64-bit division, from the arguments
+    // alone) while the kernel before finishes
+    int64_t vis = 0;
+    if constexpr (SEL) {
+        vis = (tk.start_pos + (int64_t)blockIdx.x + 1) / tk.ratio;
+        if (vis > tk.n_c) vis = tk.n_c;
+    }
     pdl_wait();     // the kernel before may still be running (programmatic launch)
     pdl_trigger();
     using SM = AttnSmem<HD>;
@@ -91,7 +102,27 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) sparse_attn_kernel(
     // pass, so the gathers below do not wait on a global load per row.
     const int jr0 = c_begin * ATT_NC;
     const int nst = max(0, min(min(K, c_end * ATT_NC) - jr0, ATT_STAGE));
-    for (int j = tid; j < nst; j += ATT_THREADS) sidx[j] = irow[jr0 + j];
+    if constexpr (SEL) {
+        // [window entries | the kk best visible rows, ascending | -1] (one
+        // split: jr0 = 0 and nst = K)
+        const int win = tk.win;
+        const int kk = (int)(vis < tk.ctopk ? vis : tk.ctopk);
+        for (int j = tid; j < K; j += ATT_THREADS) {
+            if (j < win) sidx[j] = window_index(tk.start_pos, tk.m, win, t, j);
+            else if (j - win >= kk) sidx[j] = -1;
+            else if (vis <= tk.ctopk) sidx[j] = (int)(tk.offset + (j - win));
+        }
+        if (vis > tk.ctopk && warp == 0) {
+            int* hist = reinterpret_cast<int*>(sx);  // free until the chunks below
+            warp_topk(tk.scores + t * tk.n_c, (int)vis, kk, hist, hist + 256,
+                      [&](int pos, int r) { sidx[win + pos] = (int)(tk.offset + r); });
+        }
+        __syncthreads();
+        if (blockIdx.z == 0)
+            for (int j = tid; j < K; j += ATT_THREADS) tk.idx_out[t * (int64_t)K + j] = sidx[j];
+    } else {
+        for (int j = tid; j < nst; j += ATT_THREADS) sidx[j] = irow[jr0 + j];
+    }
     __syncthreads();
     auto load_chunk = [&](int chunk, int buf) {
         uint16_t* dst = kvs + buf * (ATT_NC * HD);
@@ -1088,7 +1119,10 @@ static int launch_attn(const AttnPlan& p, const uint16_t* q, const uint16_t* row
                                   status, p.tc, st);
     }
     const size_t smem = AttnSmem<HD>::total;
-    auto kern = sparse_attn_kernel<HD>;
+    // with tk (one split only, see attn_topk_fusable) the kernel selects the
+    // rows itself and writes the index rows to tk->idx_out
+    auto kern = tk ? sparse_attn_kernel<HD, true> : sparse_attn_kernel<HD, false>;
+    const DecTopk tkv = tk ? *tk : DecTopk{};
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     float* part_o = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
     float2* part_ml = p.splits > 1 ? reinterpret_cast<float2*>(ws + p.part_o_bytes) : nullptr;
@@ -1096,7 +1130,7 @@ static int launch_attn(const AttnPlan& p, const uint16_t* q, const uint16_t* row
     int rc = launch_pdl(kern, grid, dim3(ATT_THREADS), smem, st,
                         "ds41_sparse_attn_sink_fwd: attention kernel", q, rows_a, n_a, rows_b, n_c,
                         idx, (int)K, sink, scale * LOG2E, o, lse, (int)nh, p.chunks_per_split,
-                        part_o, part_ml, status);
+                        part_o, part_ml, status, tkv);
     if (rc || p.splits == 1) return rc;
     return launch_pdl(attn_merge_kernel<HD>, dim3((unsigned)m, (unsigned)nh), dim3(128), 0, st,
                       "ds41_sparse_attn_sink_fwd: merge kernel", (const float*)part_o,
@@ -1193,10 +1227,16 @@ bool attn_is_cluster_path(int64_t m, int64_t nh, int64_t hd, int64_t K) {
 }
 
 bool attn_topk_fusable(int64_t m, int64_t nh, int64_t hd, int64_t K, int64_t n_c) {
-    const AttnPlan p = plan_attn(m, nh, hd, K, device_sms());
-    if (p.cluster < 4) return false;
-    const int64_t per = (K + p.cluster - 1) / p.cluster;
-    return per <= DEC_STAGE && n_c <= TKD_CAP;
+    const int sms = device_sms();
+    const AttnPlan p = plan_attn(m, nh, hd, K, sms);
+    if (p.cluster >= 4) {
+        const int64_t per = (K + p.cluster - 1) / p.cluster;
+        return per <= DEC_STAGE && n_c <= TKD_CAP;
+    }
+    // the generic kernel in one wave of CTAs, one split each: every CTA ranks
+    // its token's scores with one warp (SEL)
+    return p.cluster == 0 && p.tc == 0 && p.splits == 1 && m * p.head_groups <= sms &&
+           K <= ATT_STAGE && n_c <= WTK_MAX;
 }
 
 }  // namespace ds41

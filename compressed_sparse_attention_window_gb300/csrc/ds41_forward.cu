@@ -27,7 +27,10 @@ static bool use_fused(int64_t m, int64_t start_pos, int64_t nh, int64_t hd, int6
     const int64_t n_c = (start_pos + m) / ratio;
     if (n_c < 1) return false;
     const int64_t K = win + ctopk_of(topk, n_c);
-    return front_fusable(m, Hi, Di, n_c) && attn_is_cluster_path(m, nh, hd, K);
+    // the fused front feeds the few-token cluster attention, or the generic
+    // attention when its CTAs select their rows themselves
+    return front_fusable(m, Hi, Di, n_c) &&
+           (attn_is_cluster_path(m, nh, hd, K) || attn_topk_fusable(m, nh, hd, K, n_c));
 }
 
 extern "C" size_t ds41_csa_workspace_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_t hd,

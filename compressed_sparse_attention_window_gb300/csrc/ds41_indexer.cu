@@ -280,8 +280,7 @@ __global__ void __launch_bounds__(IDX_THREADS) indexer_scores_kernel(
 // (the lowest-numbered ties first), merged after the window indices.
 // ---------------------------------------------------------------------------
 constexpr int TKW_WARPS = 8;
-constexpr int TKW_KPL = 32;               // keys per lane at most
-constexpr int TKW_MAX = 32 * TKW_KPL;     // 1024 visible scores
+constexpr int TKW_MAX = WTK_MAX;          // 1024 visible scores
 
 __global__ void __launch_bounds__(32 * TKW_WARPS) topk_warp_kernel(
     const uint16_t* __restrict__ scores, const int32_t* __restrict__ win_idx,
@@ -297,11 +296,8 @@ __global__ void __launch_bounds__(32 * TKW_WARPS) topk_warp_kernel(
     pdl_wait();     // the scores (and window indices) come from the previous kernel
     pdl_trigger();
     if (t >= m) return;  // whole warps only: the rest of the CTA syncs nothing with it
-    int* hist = hist_all[warp];
-    int* sel = sel_all[warp];
     const int K = win + ctopk;
     int32_t* out = idx + t * K;
-    const uint16_t* sc = scores + t * n_c;
     for (int j = lane; j < win; j += 32) out[j] = win_idx[t * win + j];
     const int vis = (int)vis64;  // <= TKW_MAX (host plan)
     const int kk = vis < ctopk ? vis : ctopk;
@@ -309,76 +305,8 @@ __global__ void __launch_bounds__(32 * TKW_WARPS) topk_warp_kernel(
         for (int j = lane; j < ctopk; j += 32) out[win + j] = (j < vis) ? (int32_t)(offset + j) : -1;
         return;
     }
-    const int kpl = (vis + 31) / 32;
-    const int i0 = kpl * lane;
-    const int n_mine = max(0, min(kpl, vis - i0));
-    uint32_t key[TKW_KPL];
-    const bool vec = (kpl & 7) == 0 && ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0);
-#pragma unroll
-    for (int v = 0; v < TKW_KPL / 8; v++) {
-        const int b0 = i0 + 8 * v;
-        if (8 * v >= n_mine) continue;
-        if (vec && 8 * v + 8 <= n_mine) {  // whole groups of eight only
-            uint4 u = __ldg(reinterpret_cast<const uint4*>(sc + b0));
-            const uint16_t* h = reinterpret_cast<const uint16_t*>(&u);
-#pragma unroll
-            for (int e = 0; e < 8; e++) key[8 * v + e] = order_key(h[e]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; e++)
-                if (8 * v + e < n_mine) key[8 * v + e] = order_key(__ldg(sc + b0 + e));
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 8; e++) hist[lane + 32 * e] = 0;
-    __syncwarp();
-#pragma unroll
-    for (int e = 0; e < TKW_KPL; e++)
-        if (e < n_mine) atomicAdd(&hist[key[e] >> 8], 1);
-    __syncwarp();
-    find_bucket(hist, kk, 0, &sel[0], &sel[1]);
-    __syncwarp();
-    const uint32_t hb = (uint32_t)sel[0];
-    const int above1 = sel[1];
-#pragma unroll
-    for (int e = 0; e < 8; e++) hist[lane + 32 * e] = 0;
-    __syncwarp();
-#pragma unroll
-    for (int e = 0; e < TKW_KPL; e++)
-        if (e < n_mine && (key[e] >> 8) == hb) atomicAdd(&hist[key[e] & 0xffu], 1);
-    __syncwarp();
-    find_bucket(hist, kk, above1, &sel[2], &sel[3]);
-    __syncwarp();
-    const uint32_t T = (hb << 8) | (uint32_t)sel[2];
-    const int need_eq = kk - sel[3];
-    // this lane's keys above and at the threshold as bit masks (bit e: key
-    // e), so that every key's rank among them is one population count
-    uint32_t gm = 0, qm = 0;
-#pragma unroll
-    for (int e = 0; e < TKW_KPL; e++) {
-        gm |= (e < n_mine && key[e] > T) ? (1u << e) : 0u;
-        qm |= (e < n_mine && key[e] == T) ? (1u << e) : 0u;
-    }
-    const int n_gt = __popc(gm), n_eq = __popc(qm);
-    int x_gt = n_gt, x_eq = n_eq;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, x_gt, off);
-        const int b = __shfl_up_sync(0xffffffffu, x_eq, off);
-        if (lane >= off) {
-            x_gt += a;
-            x_eq += b;
-        }
-    }
-    const int gt = x_gt - n_gt, eq = x_eq - n_eq;
-    const int32_t v0 = (int32_t)(offset + i0);
-#pragma unroll
-    for (int e = 0; e < TKW_KPL; e++) {
-        const uint32_t below = (1u << e) - 1u;  // bits 0 .. e-1
-        const int eqb = eq + __popc(qm & below);
-        if (((gm >> e) & 1u) || (((qm >> e) & 1u) && eqb < need_eq))
-            out[win + gt + __popc(gm & below) + min(eqb, need_eq)] = v0 + e;
-    }
+    warp_topk(scores + t * n_c, vis, kk, hist_all[warp], sel_all[warp],
+              [&](int pos, int r) { out[win + pos] = (int32_t)(offset + r); });
     for (int j = kk + lane; j < ctopk; j += 32) out[win + j] = -1;
 }
 

@@ -25,6 +25,7 @@ CASES = [
     DECODE.replace(start_pos=1001),             # the same, where some steps complete a group
     TINY_PREFILL.replace(m=3, start_pos=37),    # chunks of three tokens
     CHUNKED.replace(m=2, start_pos=70000),      # chunks past a heavily compressed prefix
+    TINY_PREFILL,                               # 64-token chunks: the generic attention selecting its rows
 ]
 
 

@@ -424,7 +424,14 @@ CSA_EXTRA = [TINY_PREFILL.replace(m=1, start_pos=43), TINY_PREFILL.replace(m=3, 
              # tied scores: every CTA ranks all 2048 (or 546) visible rows itself ...
              DECODE.replace(structure="repeat"), CHUNKED.replace(m=1, start_pos=70000),
              # ... or, past 4096 visible rows, the cluster splits them
-             DECODE.replace(start_pos=16399, structure="repeat")]
+             DECODE.replace(start_pos=16399, structure="repeat"),
+             # the generic attention selecting its own rows after the fused
+             # front (one wave of CTAs): a chunk with tied scores, two head
+             # groups, and past 1024 visible rows the separate top-k again
+             TINY_PREFILL.replace(start_pos=200, structure="repeat"),
+             TINY_PREFILL.replace(m=100, start_pos=1000),
+             TINY_PREFILL.replace(m=40, nh=80, start_pos=300),
+             TINY_PREFILL.replace(start_pos=5000)]
 
 
 @pytest.mark.parametrize("wl", [WORKLOADS[n] for n in CSA_CASES] + CSA_EXTRA,
