@@ -327,14 +327,16 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(
     __shared__ int hist[256];
     __shared__ int wsum[64];
     __shared__ int sel[4];
+    const int t = blockIdx.x;
+    // the rows this query can see (a 64-bit division, from the arguments
+    // alone) while the kernel before finishes
+    const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
     pdl_wait();     // the scores (and window indices) come from the previous kernel
     pdl_trigger();
-    const int t = blockIdx.x;
     const int K = win + ctopk;
     int32_t* out = idx + (int64_t)t * K;
     const uint16_t* sc = scores + (int64_t)t * n_c;
     for (int j = threadIdx.x; j < win; j += blockDim.x) out[j] = win_idx[(int64_t)t * win + j];
-    const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
     const int kk = (int)(vis < ctopk ? vis : ctopk);
     if (vis <= ctopk) {
         for (int j = threadIdx.x; j < ctopk; j += blockDim.x)
@@ -476,17 +478,19 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_kernel(
     __shared__ int wsum[64];
     __shared__ int sel[4];
     __shared__ int tot[2];
+    const int t = blockIdx.x / TK_CL;
+    // the rows this query can see (a 64-bit division, from the arguments
+    // alone) while the kernel before finishes
+    const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
     pdl_wait();  // the scores (and window indices) come from the previous kernel
     pdl_trigger();
     const int r = (int)cl.block_rank();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const int t = blockIdx.x / TK_CL;
     const int K = win + ctopk;
     int32_t* out = idx + (int64_t)t * K;
     const uint16_t* sc = scores + (int64_t)t * n_c;
     if (r == 0)
         for (int j = threadIdx.x; j < win; j += blockDim.x) out[j] = win_idx[(int64_t)t * win + j];
-    const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
     const int kk = (int)(vis < ctopk ? vis : ctopk);
     if (vis <= ctopk) {  // the same branch in every CTA of the cluster
         if (r == 0)
@@ -649,17 +653,19 @@ __global__ void __launch_bounds__(TK_THREADS) topk_cluster_big_kernel(
     }
     __syncthreads();
     asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");  // this CTA has started
+    const int t = blockIdx.x / TK_CL;
+    // the rows this query can see (a 64-bit division, from the arguments
+    // alone) while the kernel before finishes
+    const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
     pdl_wait();  // the scores (and window indices) come from the previous kernel
     pdl_trigger();
     const int r = (int)cl.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t = blockIdx.x / TK_CL;
     const int K = win + ctopk;
     int32_t* out = idx + (int64_t)t * K;
     const uint16_t* sc = scores + (int64_t)t * n_c;
     if (r == 0)
         for (int j = tid; j < win; j += TK_THREADS) out[j] = win_idx[(int64_t)t * win + j];
-    const int64_t vis = visible_rows(t, start_pos, ratio, n_c);
     const int kk = (int)(vis < ctopk ? vis : ctopk);
     if (vis <= ctopk) {  // the same branch in every CTA of the cluster
         if (r == 0)
