@@ -17,7 +17,9 @@
 // each then accumulates P*V for its half of the output columns.  Rows are
 // gathered with cp.async (double-buffered); tensor-core MMAs are bf16 with f32
 // accumulation.  With several splits the unnormalised (m, l, O) of each split
-// goes to the workspace and a merge kernel adds the sink once.
+// goes to the workspace and a merge kernel adds the sink once.  In the whole
+// step, when the CTAs fit one wave with one split each, every CTA builds its
+// token's index row itself from the indexer scores (SEL).
 #include <cooperative_groups.h>
 
 #include <mutex>
