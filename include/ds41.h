@@ -265,8 +265,10 @@ size_t ds41_csa_workspace_bytes(int64_t m, int64_t start_pos, int64_t nh, int64_
  * needed only for a chunk of m > 1 tokens past position 0; latent /
  * freqs_cis only when the call completes a group; lse is nullable.  idx is
  * [m, win + min(topk, n_c)] with n_c = (start_pos + m)/ratio (unused when
- * n_c == 0).  Few-token calls run in two or three launches chained on the device
- * (programmatic dependent launch), larger ones as the four calls. */
+ * n_c == 0).  Few-token calls, and calls whose attention runs in one wave of
+ * CTAs with one split (each CTA then selects its token's rows from the scores
+ * itself), run in two or three launches chained on the device (programmatic
+ * dependent launch), larger ones as the four calls. */
 int ds41_csa_forward(const ds41_bf16* q, const ds41_bf16* kv, ds41_bf16* ring, ds41_bf16* rows_a,
                      const ds41_bf16* latent, const float* freqs_cis, int64_t max_pos,
                      ds41_bf16* cache, int64_t cache_rows, const ds41_bf16* q_idx,
